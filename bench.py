@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked KDA forward on GB300.
+
+One step = one pass of the hot path over one batch of the Kimi-Linear-shaped
+bf16 workload (B=4, T=8192, H=32, d_k=d_v=128; gate activation, base-2 decay,
+beta sigmoid and Q/K L2 norm in kernel):
+  gather the 4 initial states from a [512, 32, 128, 128] fp32 state pool,
+  kda_chunk_fwd (preprocess, intra-chunk, inter-chunk chain, output),
+  scatter the 4 final states back to the pool.
+The segment path (summary -> prefix scan -> segment finish) is timed on the
+long-sequence workload (T = 2^20, H = 8, 16 segments) and reported beside it.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "chunk-KDA fwd tokens/s and TFLOP/s on 1 GB300 (% of bf16 tensor peak)"
+WORKLOAD = "kimi_bf16"
+# Algorithmic work per token-head at d_k = d_v = d, BT = 64 (lower triangles
+# counted once): 6 d_k d_v + BT (3 d_k + 2 d_v) flop; bytes: q, k, v, o in bf16
+# (2 d each), the raw gate in fp32 (4 d_k), beta in fp32 (4).
+def alg_flops_per_token_head(dk, dv, bt=64):
+    return 6 * dk * dv + bt * (3 * dk + 2 * dv)
+
+
+def alg_bytes_per_token_head(dk, dv):
+    return 2 * dk * 2 + 2 * dv * 2 + 4 * dk + 4
+
+
+def intra_alg_bytes_per_token_head(dk, dv):   # inputs the intra-chunk stage must read
+    return 2 * dk * 2 + 2 * dv + 4 * dk + 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        load = [x for x in sm if smax and x > 0.3 * smax] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def cpu_oracle_sample(cfg, inp_cpu, units, ntokens, nthreads=0):
+    """Times the fp64 oracle on `units` (b, h) pairs over the first `ntokens`
+    tokens.  Returns (seconds, token_heads, threads)."""
+    import numpy as np
+    import oracle
+    from chunked_kimi_delta_gb300.inputs import oracle_kwargs
+    b = units[0][0]
+    heads = [h for (_, h) in units]
+    q = inp_cpu["q"][b:b + 1, :ntokens][:, :, heads]
+    k = inp_cpu["k"][b:b + 1, :ntokens][:, :, heads]
+    v = inp_cpu["v"][b:b + 1, :ntokens][:, :, heads]
+    g = inp_cpu["g"][b:b + 1, :ntokens][:, :, heads]
+    be = inp_cpu["beta"][b:b + 1, :ntokens][:, :, heads]
+    H = len(heads)
+    p = oracle.Problem(q.reshape(ntokens, H, -1), k.reshape(ntokens, H, -1),
+                       v.reshape(ntokens, H, -1), g.reshape(ntokens, H, -1),
+                       be.reshape(ntokens, H), cu_seqlens=[0, ntokens],
+                       scale=float(np.float32(cfg.dk ** -0.5)), a_log=inp_cpu["a_log"][heads],
+                       dt_bias=inp_cpu["dt_bias"][heads], **oracle_kwargs(cfg))
+    S0 = inp_cpu["initial_state"][b:b + 1][:, heads] if inp_cpu["initial_state"] is not None else None
+    threads = oracle.max_threads(nthreads)
+    t = time.perf_counter()
+    oracle.chunk_fwd(p, S0, nthreads=nthreads)
+    return time.perf_counter() - t, ntokens * H, threads
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    import torch
+    from chunked_kimi_delta_gb300.inputs import CONFIGS, make_inputs
+    cfg = CONFIGS[WORKLOAD]
+    small = cfg.replace(T=2048)
+    inp = make_inputs(small, device="cpu")
+    units = [(0, h) for h in range(8)]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(small, inp, units[:2], 256)
+    secs, th, threads = 0.0, 0, 1
+    for _ in range(args.steps):
+        s, n, threads = cpu_oracle_sample(small, inp, units, 2048)
+        secs += s
+        th += n
+    tok_s = th / secs / cfg.H   # tokens/s of the full 32-head workload
+    tflops = th * alg_flops_per_token_head(cfg.dk, cfg.dv) / secs / 1e12
+    sample = (f"fp64 oracle, {len(units)} heads x 2048 tokens of batch row 0 per step "
+              f"(token-heads/s divided by H={cfg.H})")
+    line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_desc(cfg), "tflops": tflops,
+            "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_desc(cfg):
+    return {"workload": (f"{cfg.name}: B={cfg.B} T={cfg.T} H={cfg.H} d_k={cfg.dk} d_v={cfg.dv} "
+                         f"bf16 q/k/v/o, fp32 gate/beta/state, gate+exp2+sigmoid+L2 in kernel, "
+                         f"initial states gathered from a 512-row fp32 pool, final states "
+                         f"scattered back"),
+            "B": cfg.B, "T": cfg.T, "H": cfg.H, "dk": cfg.dk, "dv": cfg.dv, "chunk": 64,
+            "l2_policy": "inputs (1.35 GB) larger than L2 (129 MB); no flush"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-segment", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import torch.distributed as dist
+    import chunked_kimi_delta_gb300 as kda
+    from chunked_kimi_delta_gb300.inputs import CONFIGS, make_inputs
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lib = kda.load_library()
+    dev = torch.device("cuda", local)
+    hbm_peak, tc_peak, tc_sus, peak_src = load_peaks()
+
+    cfg = CONFIGS[WORKLOAD]
+    inp = make_inputs(cfg, device=dev, seed=rank)
+    H, K, V = cfg.H, cfg.dk, cfg.dv
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    pool = torch.randn(512, H, K, V, generator=gen, device=dev) * 0.1
+    idx = torch.randperm(512, generator=gen, device=dev)[:cfg.B].to(torch.int32)
+    S0 = torch.empty(cfg.B, H, K, V, device=dev)
+    scale = float(K ** -0.5)
+    fa, out, fin, ws = kda.prepare_chunk_fwd(
+        inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=scale, a_log=inp["a_log"],
+        dt_bias=inp["dt_bias"], initial_state=S0, l2norm_qk=True, beta_sigmoid=True,
+        gate_in_kernel=True, use_exp2=True)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    stages = kda.kda_chunk_fwd_stages(fa)
+    # one event set per timed step, read after the timed region
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+               for _ in range(args.steps)]
+    for es in ev_sets:
+        for e in es:
+            e.record(stream)
+
+    def step(events=None):
+        kda.kda_state_gather(pool, idx, packed=S0, stream=stream)
+        if events is not None:
+            kda.kda_chunk_fwd_profiled(fa, events, stream=stream)
+        else:
+            st = lib.kda_chunk_fwd(ctypes.byref(fa), sp)
+            if st:
+                raise kda.KdaError(st, "kda_chunk_fwd")
+        kda.kda_state_scatter(pool, idx, fin, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = kda.kda_get_device_status(ws)
+    if status:
+        raise kda.KdaError(status, "device status after warm-up")
+
+    # timed region: whole steps, CUDA events on the launching stream; the
+    # per-stage events of each forward give each kernel's duration
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(ev_sets[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    tokens = cfg.B * cfg.T
+    token_heads = tokens * H
+    value = tokens * world * args.steps / (ms / 1e3)
+    tflops = token_heads * world * args.steps * alg_flops_per_token_head(K, V) / (ms / 1e3) / 1e12
+    stage_avg = [sum(es[j].elapsed_time(es[j + 1]) for es in ev_sets) / args.steps
+                 for j in range(len(stages))]
+    status = kda.kda_get_device_status(ws)
+    if status:
+        raise kda.KdaError(status, "device status after timed region")
+
+    # dominant kernel: its algorithmic bytes per launch / its average duration
+    dom = max(range(len(stages)), key=lambda i: stage_avg[i])
+    dom_name = stages[dom]
+    state_bytes = 2 * 4 * K * V * cfg.B * H          # initial + final state
+    if dom_name.startswith("intra"):
+        dom_bytes = intra_alg_bytes_per_token_head(K, V) * token_heads
+    elif dom_name.startswith("inter"):
+        dom_bytes = 2 * V * token_heads + state_bytes  # the output o and the states
+    else:
+        dom_bytes = alg_bytes_per_token_head(K, V) * token_heads + state_bytes
+    achieved = dom_bytes / (stage_avg[dom] / 1e3) / 1e9
+    fwd_ms = sum(stage_avg)
+    fwd_bytes = alg_bytes_per_token_head(K, V) * token_heads + state_bytes
+    traffic = load_traffic(dom_name)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": config_desc(cfg),
+        "tflops": tflops, "tensor_peak_frac": tflops / tc_peak,
+        "hbm_frac_fwd": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,
+        "peaks": {"hbm_gbs": hbm_peak, "bf16_tflops": tc_peak, "source": peak_src},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": stage_avg[dom],
+                     "peak_source": peak_src},
+        "stages_ms": dict(zip(stages, stage_avg)),
+        "gpu_launches": args.steps * (len(stages) + 2),
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_segment:
+        result["segment_mode"] = bench_segment(kda, dev, stream)
+    if not args.no_e2e:
+        result["e2e"] = bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        inp_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        secs, th, threads = cpu_oracle_sample(cfg, inp_cpu, [(0, h) for h in range(H)], 8192)
+        result["cpu_baseline"] = {
+            "value": th / secs / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle on batch row 0, all {H} heads x 8192 tokens "
+                      f"({th} token-heads, {secs:.1f} s); tokens/s = token-heads/s / H"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when no capture of the current kernel exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(kernel)
+    except Exception:
+        return None
+
+
+def bench_segment(kda, dev, stream, steps=3, warmup=2):
+    """Segment mode on the long-sequence workload: summary -> scan -> finish."""
+    import torch
+    from chunked_kimi_delta_gb300.inputs import CONFIGS, make_inputs
+    cfg = CONFIGS["long_segment_bf16"]
+    inp = make_inputs(cfg, device=dev)
+    T, H, K, V = cfg.T, cfg.H, cfg.dk, cfg.dv
+    S = cfg.num_segments
+    sb = inp["seg_bounds"]
+    kw = dict(scale=float(K ** -0.5), a_log=inp["a_log"], dt_bias=inp["dt_bias"], l2norm_qk=True,
+              beta_sigmoid=True, gate_in_kernel=True, use_exp2=True)
+    M = torch.empty(S, H, K, K, device=dev)
+    St = torch.empty(S, H, K, V, device=dev)
+    S_in = torch.empty(S, H, K, V, device=dev)
+    S_fin = torch.empty(H, K, V, device=dev)
+    flat = lambda x: x.reshape(T, *x.shape[2:])
+    q, k, v, g, be = (flat(inp[n]) for n in ("q", "k", "v", "g", "beta"))
+    fa, out, fin, ws = kda.prepare_chunk_fwd(q, k, v, g, be, cu_seqlens=sb, initial_state=S_in, **kw)
+    sa, _, _, ws_sum = kda.prepare_segment_summary(q, k, v, g, be, sb, M=M, S_tilde=St, **kw)
+    lib = kda.load_library()
+    sp = stream.cuda_stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def one(rec):
+        if rec:
+            ev[0].record(stream)
+        st = lib.kda_segment_summary(ctypes.byref(sa), sb.data_ptr(), S, M.data_ptr(), St.data_ptr(), sp)
+        if st:
+            raise kda.KdaError(st, "kda_segment_summary")
+        if rec:
+            ev[1].record(stream)
+        kda.kda_state_prefix_scan(M, St, None, S_in=S_in, S_final=S_fin, stream=stream)
+        if rec:
+            ev[2].record(stream)
+        st = lib.kda_chunk_fwd(ctypes.byref(fa), sp)
+        if st:
+            raise kda.KdaError(st, "segment finish")
+        if rec:
+            ev[3].record(stream)
+
+    for _ in range(warmup):
+        one(False)
+    torch.cuda.synchronize()
+    parts = [0.0, 0.0, 0.0]
+    for _ in range(steps):
+        one(True)
+        ev[3].synchronize()
+        for i in range(3):
+            parts[i] += ev[i].elapsed_time(ev[i + 1])
+    parts = [x / steps for x in parts]
+    total = sum(parts)
+    return {"workload": f"long_segment_bf16: B=1 T={T} H={H} d={K} bf16, {S} segments",
+            "tokens_per_s": T / (total / 1e3), "ms_per_pass": total,
+            "summary_ms": parts[0], "scan_ms": parts[1], "finish_ms": parts[2],
+            "tflops_alg": T * H * alg_flops_per_token_head(K, V) / (total / 1e3) / 1e12}
+
+
+def bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world, steps=3):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: H2D of q, k, v, gate, beta, then the step, then D2H of o."""
+    import torch
+    names = ["q", "k", "v", "g", "beta"]
+    host = {n: torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True) for n in names}
+    for n in names:
+        host[n].copy_(inp[n])
+    o_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev_in = {n: inp[n] for n in names}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def step():
+        for n in names:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        kda.kda_state_gather(pool, idx, packed=S0, stream=stream)
+        st = lib.kda_chunk_fwd(ctypes.byref(fa), stream.cuda_stream)
+        if st:
+            raise kda.KdaError(st, "kda_chunk_fwd")
+        kda.kda_state_scatter(pool, idx, fin, stream=stream)
+        o_host.copy_(out, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": cfg.B * cfg.T * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    main()

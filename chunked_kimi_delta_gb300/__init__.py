@@ -1,0 +1,358 @@
+"""Chunked Kimi Delta Attention (KDA) forward for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``include/kda.h`` (``libkda.so``,
+built in-tree by :mod:`chunked_kimi_delta_gb300.build`).  The Python
+functions carry the C names and only marshal arguments: every step of the
+computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and the current stream.  There is no fallback: when the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libkda.so")
+
+# include/kda.h constants
+KDA_OK = 0
+KDA_F32, KDA_BF16 = 0, 1
+KDA_I32, KDA_I64 = 0, 1
+KDA_L2NORM_QK = 1 << 0
+KDA_BETA_SIGMOID = 1 << 1
+KDA_GATE_IN_KERNEL = 1 << 2
+KDA_USE_EXP2 = 1 << 3
+KDA_SAFE_GATE = 1 << 8
+KDA_ALLOW_NEG_EIGVAL = 1 << 9
+KDA_STATE_V_FIRST = 1 << 10
+CHUNK = 64
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class kda_fwd_args(ctypes.Structure):
+    """Mirror of ``kda_fwd_args`` in include/kda.h."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
+        ("qkv_dtype", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p),
+        ("scale", ctypes.c_float), ("eps", ctypes.c_float),
+        ("initial_state", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+        ("num_seqs", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("out", ctypes.c_void_p), ("final_state", ctypes.c_void_p),
+        ("h_out", ctypes.c_void_p), ("v_new_out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libkda.so (raises when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libkda.so not built ({path}); run "
+                          "`python -m chunked_kimi_delta_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(kda_fwd_args)
+    sigs = {
+        "kda_chunk_fwd_workspace_size": ([P], ctypes.c_size_t),
+        "kda_chunk_fwd": ([P, vp], ctypes.c_int),
+        "kda_segment_summary_workspace_size": ([P, i32], ctypes.c_size_t),
+        "kda_segment_summary": ([P, vp, i32, vp, vp, vp], ctypes.c_int),
+        "kda_state_prefix_scan": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp], ctypes.c_int),
+        "kda_state_gather": ([vp, ctypes.c_int, i64, i64, i64, vp, ctypes.c_int, vp, i64, vp, vp],
+                             ctypes.c_int),
+        "kda_state_scatter": ([vp, ctypes.c_int, i64, i64, i64, vp, ctypes.c_int, vp, ctypes.c_int,
+                               i64, vp], ctypes.c_int),
+        "kda_get_device_status": ([vp, vp], ctypes.c_int),
+        "kda_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "kda_chunk_fwd_stages": ([P, ctypes.POINTER(ctypes.c_char_p), i32], i32),
+        "kda_chunk_fwd_profiled": ([P, vp, ctypes.POINTER(vp), i32], ctypes.c_int),
+    }
+    for name, (argt, rest) in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = argt
+        f.restype = rest
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().kda_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != KDA_OK:
+        raise KdaError(status, what)
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias=None,
+                  initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
+                  gate_in_kernel=False, use_exp2=False, extra_flags=0, out=None,
+                  final_state=None, h_out=None, v_new_out=None) -> kda_fwd_args:
+    """Fills a ``kda_fwd_args`` from tensors (BSND [B,T,H,D], or TND [T,H,D]
+    with ``cu_seqlens``)."""
+    _contig(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state,
+            h_out, v_new_out)
+    a = kda_fwd_args()
+    if q.dim() == 3:    # TND: one token axis
+        a.B, a.T = 1, q.shape[0]
+    elif q.dim() == 4:  # BSND
+        a.B, a.T = q.shape[0], q.shape[1]
+    else:
+        raise ValueError("q/k/v are [B, T, H, D] or [T_total, H, D]")
+    if cu_seqlens is not None:
+        if q.dim() != 3:
+            raise ValueError("with cu_seqlens, q/k/v are [T_total, H, D]")
+        a.num_seqs = cu_seqlens.numel() - 1
+        a.cu_seqlens = _ptr(cu_seqlens)
+    a.H, a.dk, a.dv, a.chunk = q.shape[-2], q.shape[-1], v.shape[-1], CHUNK
+    a.qkv_dtype = _dtype_code(q)
+    a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
+    a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
+    a.scale = float(q.shape[-1] ** -0.5 if scale is None else scale)
+    a.eps = float(eps)
+    a.initial_state = _ptr(initial_state)
+    a.flags = ((KDA_L2NORM_QK if l2norm_qk else 0) | (KDA_BETA_SIGMOID if beta_sigmoid else 0)
+               | (KDA_GATE_IN_KERNEL if gate_in_kernel else 0) | (KDA_USE_EXP2 if use_exp2 else 0)
+               | extra_flags)
+    a.out, a.final_state = _ptr(out), _ptr(final_state)
+    a.h_out, a.v_new_out = _ptr(h_out), _ptr(v_new_out)
+    return a
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias=None,
+                  initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
+                  gate_in_kernel=False, use_exp2=False, output_final_state=True, out=None,
+                  final_state=None, h_out=None, v_new_out=None, workspace=None, stream=None,
+                  extra_flags=0):
+    """Chunked KDA forward.  Returns ``(out, final_state)`` (final_state is
+    None unless requested).  See ``kda_chunk_fwd`` in include/kda.h."""
+    torch = _torch()
+    lib = load_library()
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if q.dim() == 3 else q.shape[0]
+    if out is None:
+        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty(N, q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+                                  device=q.device)
+    a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
+                      initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
+                      beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
+                      extra_flags=extra_flags, out=out, final_state=final_state, h_out=h_out,
+                      v_new_out=v_new_out)
+    ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib.kda_chunk_fwd(ctypes.byref(a), _stream(stream)), "kda_chunk_fwd")
+    return out, final_state
+
+
+def prepare_chunk_fwd(q, k, v, g, beta, *, output_final_state=True, workspace=None, **kw):
+    """Builds the ``kda_fwd_args`` of a forward once (outputs and workspace
+    allocated), for callers that launch the same problem repeatedly through
+    ``load_library().kda_chunk_fwd``.  Returns (args, out, final_state, ws)."""
+    torch = _torch()
+    lib = load_library()
+    cu = kw.get("cu_seqlens")
+    N = (cu.numel() - 1) if cu is not None else (1 if q.dim() == 3 else q.shape[0])
+    out = kw.pop("out", None)
+    if out is None:
+        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+    fin = kw.pop("final_state", None)
+    if output_final_state and fin is None:
+        fin = torch.empty(N, q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+                          device=q.device)
+    a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
+    ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    return a, out, fin, ws
+
+
+def prepare_segment_summary(q, k, v, g, beta, seg_bounds, *, M=None, S_tilde=None,
+                            workspace=None, **kw):
+    """Builds the ``kda_fwd_args`` of a segment summary once (outputs and
+    workspace allocated).  Returns (args, M, S_tilde, ws)."""
+    torch = _torch()
+    lib = load_library()
+    S = seg_bounds.numel() - 1
+    H, K, V = q.shape[-2], q.shape[-1], v.shape[-1]
+    if M is None:
+        M = torch.empty(S, H, K, K, dtype=torch.float32, device=q.device)
+    if S_tilde is None:
+        S_tilde = torch.empty(S, H, K, V, dtype=torch.float32, device=q.device)
+    a = make_fwd_args(q, k, v, g, beta, **kw)
+    ws = _workspace(lib.kda_segment_summary_workspace_size(ctypes.byref(a), S), q.device, workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    return a, M, S_tilde, ws
+
+
+def kda_chunk_fwd_stages(args: kda_fwd_args) -> list:
+    """Names of the kernels kda_chunk_fwd launches for ``args``, in order."""
+    lib = load_library()
+    names = (ctypes.c_char_p * 8)()
+    n = lib.kda_chunk_fwd_stages(ctypes.byref(args), names, 8)
+    return [names[i].decode() for i in range(n)]
+
+
+def kda_chunk_fwd_profiled(args: kda_fwd_args, events, stream=None):
+    """kda_chunk_fwd with ``events[i]`` (torch.cuda.Event, already recorded
+    once so that they exist) recorded before stage i and after the last."""
+    lib = load_library()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib.kda_chunk_fwd_profiled(ctypes.byref(args), _stream(stream), arr, len(events)),
+           "kda_chunk_fwd_profiled")
+
+
+def kda_segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_log=None,
+                        dt_bias=None, l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
+                        use_exp2=False, M=None, S_tilde=None, workspace=None, stream=None):
+    """Segment affine summary.  ``seg_bounds``: int32 device tensor [S+1] of
+    token offsets on the flattened token axis.  Returns ``(M, S_tilde)``."""
+    torch = _torch()
+    lib = load_library()
+    S = seg_bounds.numel() - 1
+    H, K, V = q.shape[-2], q.shape[-1], v.shape[-1]
+    if M is None:
+        M = torch.empty(S, H, K, K, dtype=torch.float32, device=q.device)
+    if S_tilde is None:
+        S_tilde = torch.empty(S, H, K, V, dtype=torch.float32, device=q.device)
+    _contig(seg_bounds, M, S_tilde)
+    a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
+                      l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid,
+                      gate_in_kernel=gate_in_kernel, use_exp2=use_exp2)
+    ws = _workspace(lib.kda_segment_summary_workspace_size(ctypes.byref(a), S), q.device, workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib.kda_segment_summary(ctypes.byref(a), seg_bounds.data_ptr(), S, M.data_ptr(),
+                                   S_tilde.data_ptr(), _stream(stream)), "kda_segment_summary")
+    return M, S_tilde
+
+
+def kda_state_prefix_scan(M, S_tilde, S0=None, *, S_in=None, S_final=None, stream=None):
+    """Ordered prefix scan.  M [C,S,H,K,K] or [S,H,K,K]; S_tilde likewise with
+    V; S0 [C,H,K,V] / [H,K,V] or None.  Returns ``(S_in, S_final)``."""
+    torch = _torch()
+    lib = load_library()
+    one = M.dim() == 4
+    C = 1 if one else M.shape[0]
+    S, H, K = M.shape[-4], M.shape[-3], M.shape[-1]
+    V = S_tilde.shape[-1]
+    if S_in is None:
+        S_in = torch.empty(S_tilde.shape, dtype=torch.float32, device=M.device)
+    if S_final is None:
+        S_final = torch.empty(*(() if one else (C,)), H, K, V, dtype=torch.float32, device=M.device)
+    _contig(M, S_tilde, S0, S_in, S_final)
+    _check(lib.kda_state_prefix_scan(_ptr(M), _ptr(S_tilde), _ptr(S0), C, S, H, K, V, _ptr(S_in),
+                                     _ptr(S_final), _stream(stream)), "kda_state_prefix_scan")
+    return S_in, S_final
+
+
+def _rows(cache):
+    """(num_rows, row_stride_elems, payload_elems) of a pool whose dim 0 indexes
+    rows and whose remaining dims are dense."""
+    payload = 1
+    for d in cache.shape[1:]:
+        payload *= d
+    inner = cache[0] if cache.shape[0] > 0 else cache
+    if cache.dim() > 1 and not inner.is_contiguous():
+        raise ValueError("the payload of a cache row must be dense")
+    return cache.shape[0], cache.stride(0), payload
+
+
+def _idx_code(idx) -> int:
+    torch = _torch()
+    if idx.dtype == torch.int32:
+        return KDA_I32
+    if idx.dtype == torch.int64:
+        return KDA_I64
+    raise TypeError("indices must be int32 or int64")
+
+
+def kda_state_gather(cache, idx, flags=None, *, packed=None, stream=None):
+    """packed[i] = cache[idx[i]] (zeros for invalid idx or false flag)."""
+    torch = _torch()
+    lib = load_library()
+    n_rows, stride, payload = _rows(cache)
+    n = idx.numel()
+    if packed is None:
+        packed = torch.empty(n, *cache.shape[1:], dtype=cache.dtype, device=cache.device)
+    _contig(idx, flags, packed)
+    if flags is not None and flags.dtype != torch.bool:
+        raise TypeError("flags must be bool")
+    _check(lib.kda_state_gather(_ptr(cache), _dtype_code(cache), n_rows, stride, payload, _ptr(idx),
+                                _idx_code(idx), _ptr(flags), n, _ptr(packed), _stream(stream)),
+           "kda_state_gather")
+    return packed
+
+
+def kda_state_scatter(cache, idx, packed, *, stream=None):
+    """cache[idx[i]] = packed[i] (converted to the cache dtype) for valid idx."""
+    lib = load_library()
+    n_rows, stride, payload = _rows(cache)
+    _contig(idx, packed)
+    _check(lib.kda_state_scatter(_ptr(cache), _dtype_code(cache), n_rows, stride, payload,
+                                 _ptr(idx), _idx_code(idx), _ptr(packed), _dtype_code(packed),
+                                 idx.numel(), _stream(stream)), "kda_state_scatter")
+    return cache
+
+
+def kda_get_device_status(workspace, stream=None) -> int:
+    """Reads and clears the device error word of a workspace; returns the status."""
+    return load_library().kda_get_device_status(workspace.data_ptr(), _stream(stream))

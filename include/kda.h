@@ -1,0 +1,223 @@
+/*
+ * kda.h - C ABI of the GB300 (sm_103a) chunked Kimi Delta Attention library.
+ *
+ * The library computes, on one GPU, the forward pass of KDA, the per-channel
+ * gated delta rule
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,          alpha_t = exp(g_t) per key channel,
+ * in chunks of 64 tokens, together with the segment affine summary (M, S~)
+ * of a token range, the ordered prefix scan S <- M_j S + S~_j that composes
+ * summaries, and the gather/scatter of per-request states between a cache
+ * pool and packed rows.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers unless a comment says "host".
+ *    The caller allocates and owns every buffer; the library allocates no
+ *    device memory, keeps no pointer after a call returns, and holds no
+ *    global state besides a lazily filled per-process table of driver entry
+ *    points.
+ *  - Calls are asynchronous on the given stream (NULL = legacy default
+ *    stream).  Argument checks run on the host before anything is launched;
+ *    a failed check returns an error code and launches nothing.  A launch
+ *    failure returns KDA_ERR_CUDA.  No call aborts, traps or prints.
+ *  - Tensors are dense and row-major ("contiguous") in the shapes given.
+ *    Every tensor pointer must be 16-byte aligned (KDA_ERR_ALIGNMENT).
+ *  - Recurrent states are fp32 and K-first: state[..., c, j] with c a key
+ *    channel (d_k) and j a value channel (d_v).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdbool.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same handle type), spelled without CUDA headers. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,    /* null required pointer, bad size or shape      */
+  KDA_ERR_UNSUPPORTED = 2,    /* a valid request this library does not compute */
+  KDA_ERR_ALIGNMENT = 3,      /* a tensor pointer is not 16-byte aligned       */
+  KDA_ERR_WORKSPACE = 4,      /* workspace missing or smaller than required    */
+  KDA_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed          */
+  KDA_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait gave up            */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+typedef enum { KDA_I32 = 0, KDA_I64 = 1 } kda_index_dtype;
+
+/* Flags of kda_fwd_args.flags.  The first four follow the keyword arguments
+ * use_qk_l2norm_in_kernel, use_beta_sigmoid_in_kernel, use_gate_in_kernel and
+ * use_exp2 of npu_chunk_kda ("Hyper-Parallel Chunk KDA current implementation
+ * design", section 4 and 4.1). */
+enum {
+  KDA_L2NORM_QK = 1u << 0,      /* q^ = q (sum q^2 + eps)^-1/2, same for k       */
+  KDA_BETA_SIGMOID = 1u << 1,   /* beta = 1 / (1 + exp(-b)) of the given logits  */
+  KDA_GATE_IN_KERNEL = 1u << 2, /* g = -exp(a_log[h]) softplus(x + dt_bias[h,c]) */
+  KDA_USE_EXP2 = 1u << 3,       /* work in base 2 internally; same result        */
+  /* Named on the pages without a formula (safe_gate/lower_bound,
+   * allow_neg_eigval) or a layout this library does not take (V-first
+   * state): always rejected with KDA_ERR_UNSUPPORTED. */
+  KDA_SAFE_GATE = 1u << 8,
+  KDA_ALLOW_NEG_EIGVAL = 1u << 9,
+  KDA_STATE_V_FIRST = 1u << 10
+};
+
+/*
+ * Arguments of the chunked forward ("Hyper-Parallel Chunk KDA current
+ * implementation design", section 4, npu_chunk_kda; "KDA Chunk Backward -
+ * TPU/Pallas Kernel Design", section 1 and 1.2 for the chunk formulas).
+ *
+ * Layout: tokens are BSND [B, T, H, D] when cu_seqlens is NULL, or TND
+ * [T_total, H, D] packed sequences when cu_seqlens is given (then B must be
+ * 1 and T = T_total).  q and k have d_k channels, v and out d_v channels.
+ * Every sequence starts from its own initial state (section 6.5 of the same
+ * design); chunks restart at every sequence start, the last one may be
+ * partial.
+ */
+typedef struct {
+  int32_t B, T, H;          /* batch, tokens per sequence (or T_total), heads    */
+  int32_t dk, dv;           /* head dims; each must be 64 or 128                 */
+  int32_t chunk;            /* chunk length; must be 64                          */
+  kda_dtype qkv_dtype;      /* dtype of q, k, v and out                          */
+  const void *q, *k;        /* [B,T,H,dk] or [T_total,H,dk], qkv_dtype           */
+  const void *v;            /* [B,T,H,dv] or [T_total,H,dv], qkv_dtype           */
+  const float *g;           /* [.., H, dk] fp32: raw gate input x when           */
+                            /* KDA_GATE_IN_KERNEL, else natural-log decay g <= 0 */
+  const float *a_log;       /* [H] fp32; required with KDA_GATE_IN_KERNEL        */
+  const float *dt_bias;     /* [H, dk] fp32 or NULL (= zeros)                    */
+  const float *beta;        /* [.., H] fp32: logits with KDA_BETA_SIGMOID        */
+  float scale;              /* output scale, usually dk^-1/2                     */
+  float eps;                /* L2-norm epsilon, usually 1e-6                     */
+  const float *initial_state; /* [N, H, dk, dv] fp32 or NULL (= zeros)           */
+  const int32_t *cu_seqlens;  /* device [num_seqs+1] token offsets or NULL;      */
+                              /* caller precondition: 0 = cu[0] <= .. <= cu[N] = T */
+  int32_t num_seqs;         /* N when cu_seqlens is given; ignored otherwise     */
+  uint32_t flags;           /* KDA_* flags above                                 */
+  void *out;                /* [.., H, dv] qkv_dtype, written                    */
+  float *final_state;       /* [N, H, dk, dv] fp32 or NULL (not written)         */
+  float *h_out;             /* [num_chunks, H, dk, dv] fp32 state entering each  */
+                            /* chunk (chunks numbered sequence by sequence), or  */
+                            /* NULL; num_chunks = sum over sequences of ceil(len/64) */
+  float *v_new_out;         /* [.., H, dv] fp32 corrected values u - w h, or NULL */
+  void *workspace;          /* device scratch, >= kda_chunk_fwd_workspace_size   */
+  size_t workspace_bytes;   /* and 256-byte aligned                              */
+} kda_fwd_args;
+
+/* Bytes of workspace kda_chunk_fwd needs for these arguments (0 when the
+ * arguments are invalid).  Depends only on sizes, dtype, flags and which
+ * optional outputs are requested. */
+size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
+
+/* The chunked KDA forward: out, and final_state / h_out / v_new_out when
+ * given.  N = B without cu_seqlens, num_seqs with it.
+ * With no tokens (B*T == 0, or only empty sequences) the final state is the
+ * initial state; q/k/v/g/beta/out may then be NULL.
+ * Errors: KDA_ERR_INVALID_ARG (null q/k/v/g/beta/out with tokens, B or H < 1,
+ * T < 0, a_log
+ * missing with KDA_GATE_IN_KERNEL, cu_seqlens with B != 1), KDA_ERR_UNSUPPORTED
+ * (dk or dv not 64/128, chunk != 64, KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL /
+ * KDA_STATE_V_FIRST), KDA_ERR_ALIGNMENT, KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
+kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
+
+/* Bytes of workspace kda_segment_summary needs. */
+size_t kda_segment_summary_workspace_size(const kda_fwd_args *args, int32_t num_segments);
+
+/*
+ * Segment affine summary ("Hyper-Parallel Chunk KDA current implementation
+ * design", section 5.1, PreProcessFwd: H_out = M @ H_in + E; "KDA Context
+ * Parallelism (KCP)", "Les notations").  Segment s covers the tokens
+ * [seg_bounds[s], seg_bounds[s+1]) of the token axis (b*T + t for BSND, the
+ * packed index for TND); each segment must lie inside one sequence (caller
+ * precondition).  For each segment and head:
+ *   M[s,h]       = M_b ... M_{a+1}, M_t = (I - beta_t k_t k_t^T) Diag(alpha_t),
+ *                  later tokens on the left              [S, H, dk, dk] fp32
+ *   S_tilde[s,h] = the state after the segment started from zero
+ *                                                        [S, H, dk, dv] fp32
+ * so that the state leaving a segment is M S_in + S_tilde.  Uses q, k, v, g,
+ * a_log, dt_bias, beta, flags, sizes and workspace of args (q is not needed
+ * by the math but is validated); ignores initial_state, cu_seqlens,
+ * num_seqs, out, final_state, h_out, v_new_out.
+ * seg_bounds: device int32 [num_segments+1], strictly increasing, within
+ * [0, tokens].  Errors as kda_chunk_fwd, plus KDA_ERR_INVALID_ARG for
+ * num_segments < 1 or a null M / S_tilde / seg_bounds. */
+kda_status kda_segment_summary(const kda_fwd_args *args, const int32_t *seg_bounds,
+                               int32_t num_segments, float *M, float *S_tilde,
+                               kda_stream_t stream);
+
+/*
+ * Ordered prefix scan of segment summaries ("KDA Context Parallelism (KCP)",
+ * "L'algorithme"; "Hyper-Parallel Chunk KDA current implementation design",
+ * sections 5.3 and 6.3: forward summaries compose in time order).
+ * For every chain c and head h, with S = S0[c,h] (zeros when S0 is NULL):
+ *   for j in 0..num_segments-1:  S_in[c,j,h] = S;  S = M[c,j,h] S + S_tilde[c,j,h]
+ *   S_final[c,h] = S   (when S_final is not NULL)
+ * M: [C, S, H, dk, dk]; S_tilde, S_in: [C, S, H, dk, dv]; S0, S_final:
+ * [C, H, dk, dv]; all fp32.  Computed in fp32 on CUDA cores (no tensor-core
+ * rounding).  S_in must not alias the inputs.
+ * Errors: KDA_ERR_INVALID_ARG (null M / S_tilde / S_in, sizes < 1),
+ * KDA_ERR_UNSUPPORTED (dk, dv not 64/128), KDA_ERR_ALIGNMENT, KDA_ERR_CUDA. */
+kda_status kda_state_prefix_scan(const float *M, const float *S_tilde, const float *S0,
+                                 int32_t num_chains, int32_t num_segments, int32_t H,
+                                 int32_t dk, int32_t dv, float *S_in, float *S_final,
+                                 kda_stream_t stream);
+
+/*
+ * State gather, cache pool -> packed rows (vllm-ascend KDA prefill state copy
+ * article, section "数值契约", numerical contract).
+ * The cache holds num_rows rows, row_stride_elems elements apart; the first
+ * payload_elems elements of each row are the state, the rest of the row is a
+ * gap that is never read or written.  For i in [0, n_sel):
+ *   packed[i, :] = cache_row[idx[i]]  if 0 <= idx[i] < num_rows and (flags is
+ *                                      NULL or flags[i])
+ *                = 0                  otherwise.
+ * Duplicate indices are legal.  Every packed row is written.  Addresses are
+ * computed in 64 bits (rows may lie more than 4 GiB apart).  n_sel == 0
+ * returns KDA_OK and launches nothing.
+ * cache: [num_rows, row_stride_elems] of cache_dtype; idx: [n_sel] int32 or
+ * int64; flags: [n_sel] bool (one byte each) or NULL; packed: [n_sel,
+ * payload_elems] of cache_dtype.
+ * Errors: KDA_ERR_INVALID_ARG (null pointers with n_sel > 0, num_rows < 1,
+ * payload_elems < 1, row_stride_elems < payload_elems, n_sel < 0),
+ * KDA_ERR_CUDA. */
+kda_status kda_state_gather(const void *cache, kda_dtype cache_dtype, int64_t num_rows,
+                            int64_t row_stride_elems, int64_t payload_elems, const void *idx,
+                            kda_index_dtype idx_dtype, const bool *flags, int64_t n_sel,
+                            void *packed, kda_stream_t stream);
+
+/*
+ * State scatter, packed rows -> cache pool (same contract).  For i in
+ * [0, n_sel) with 0 <= idx[i] < num_rows:
+ *   cache_row[idx[i]] = convert(packed[i, :])    (fp32 -> bf16 rounds to
+ *                                                 nearest even)
+ * Out-of-range indices are skipped.  There are no flags: a flag describes
+ * only an initial state and never suppresses a final write.  Valid targets
+ * must be unique (caller precondition, not checked).  packed: [n_sel,
+ * payload_elems] of packed_dtype.  The gap of each row is untouched.
+ * n_sel == 0 returns KDA_OK and launches nothing.  Errors as gather. */
+kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_rows,
+                             int64_t row_stride_elems, int64_t payload_elems, const void *idx,
+                             kda_index_dtype idx_dtype, const void *packed,
+                             kda_dtype packed_dtype, int64_t n_sel, kda_stream_t stream);
+
+/* Reads and clears the device error word kept at the start of a forward or
+ * summary workspace: synchronises the stream, returns KDA_OK or
+ * KDA_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up.  Every
+ * kda_chunk_fwd / kda_segment_summary clears the word when it starts, so the
+ * status describes the most recent such call on this workspace. */
+kda_status kda_get_device_status(void *workspace, kda_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *kda_status_string(kda_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

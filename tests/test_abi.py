@@ -1,0 +1,129 @@
+"""The C ABI on the host, without a GPU: the library builds and loads, exports
+every entry point include/kda.h declares, and rejects bad arguments with the
+documented status codes before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_kimi_delta_gb300 as kda
+from chunked_kimi_delta_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load_library()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "kda_chunk_fwd" in names and "kda_state_scatter" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARG"), (2, "KDA_ERR_UNSUPPORTED"),
+                       (3, "KDA_ERR_ALIGNMENT"), (4, "KDA_ERR_WORKSPACE"), (5, "KDA_ERR_CUDA"),
+                       (6, "KDA_ERR_DEVICE_TIMEOUT")]:
+        assert kda.status_string(code) == name
+
+
+def _args(**kw):
+    a = kda.kda_fwd_args()
+    a.B, a.T, a.H, a.dk, a.dv, a.chunk = 2, 100, 4, 128, 128, 64
+    a.qkv_dtype = kda.KDA_BF16
+    base = 1 << 20
+    a.q, a.k, a.v, a.g, a.beta, a.out = (base * (i + 1) for i in range(6))
+    a.scale, a.eps = 0.088, 1e-6
+    for key, val in kw.items():
+        setattr(a, key, val)
+    return a
+
+
+def test_fwd_argument_checks(lib):
+    f = lambda a: lib.kda_chunk_fwd(ctypes.byref(a), None)
+    assert f(_args(q=None)) == 1
+    assert f(_args(out=None)) == 1
+    assert f(_args(B=0)) == 1
+    assert f(_args(dk=96)) == 2
+    assert f(_args(dv=256)) == 2
+    assert f(_args(chunk=32)) == 2
+    assert f(_args(flags=kda.KDA_SAFE_GATE)) == 2
+    assert f(_args(flags=kda.KDA_ALLOW_NEG_EIGVAL)) == 2
+    assert f(_args(flags=kda.KDA_STATE_V_FIRST)) == 2
+    assert f(_args(flags=1 << 20)) == 1
+    assert f(_args(flags=kda.KDA_GATE_IN_KERNEL)) == 1          # a_log missing
+    assert f(_args(q=(1 << 20) + 8)) == 3                        # misaligned
+    assert f(_args(cu_seqlens=1 << 24, num_seqs=3)) == 1         # cu_seqlens needs B = 1
+    assert f(_args()) == 4                                       # no workspace
+    a = _args()
+    need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(a))
+    assert need > 0
+    a.workspace, a.workspace_bytes = 1 << 30, need - 1
+    assert f(a) == 4
+    a.workspace, a.workspace_bytes = (1 << 30) + 16, need
+    assert f(a) == 3                                             # workspace not 256-aligned
+    assert lib.kda_chunk_fwd(None, None) == 1
+
+
+def test_workspace_grows_with_tokens(lib):
+    small = lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args(T=64)))
+    big = lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args(T=6400)))
+    assert 0 < small < big
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args(dk=80))) == 0
+
+
+def test_summary_and_scan_checks(lib):
+    a = _args()
+    assert lib.kda_segment_summary(ctypes.byref(a), None, 4, 1 << 20, 1 << 21, None) == 1
+    assert lib.kda_segment_summary(ctypes.byref(a), 1 << 20, 0, 1 << 20, 1 << 21, None) == 1
+    assert lib.kda_segment_summary_workspace_size(ctypes.byref(a), 0) == 0
+    assert lib.kda_segment_summary_workspace_size(ctypes.byref(a), 4) > 0
+    s = lib.kda_state_prefix_scan
+    assert s(None, 1 << 20, None, 1, 4, 8, 128, 128, 1 << 21, None, None) == 1
+    assert s(1 << 20, 1 << 20, None, 1, 0, 8, 128, 128, 1 << 21, None, None) == 1
+    assert s(1 << 20, 1 << 20, None, 1, 4, 8, 96, 128, 1 << 21, None, None) == 2
+    assert s(1 << 20, 1 << 20, None, 1, 4, 8, 128, 128, (1 << 21) + 4, None, None) == 3
+
+
+def test_state_copy_checks(lib):
+    g = lib.kda_state_gather
+    # empty selection: OK, nothing launched (null pointers allowed)
+    assert g(None, kda.KDA_F32, 4, 10, 10, None, kda.KDA_I32, None, 0, None, None) == 0
+    assert g(1 << 20, kda.KDA_F32, 4, 5, 10, 1 << 21, kda.KDA_I32, None, 3, 1 << 22, None) == 1
+    assert g(1 << 20, kda.KDA_F32, 0, 10, 10, 1 << 21, kda.KDA_I32, None, 3, 1 << 22, None) == 1
+    assert g(1 << 20, kda.KDA_F32, 4, 10, 10, None, kda.KDA_I32, None, 3, 1 << 22, None) == 1
+    assert g(1 << 20, kda.KDA_F32, 4, 10, 10, 1 << 21, kda.KDA_I32, None, -1, 1 << 22, None) == 1
+    sc = lib.kda_state_scatter
+    assert sc(None, kda.KDA_BF16, 4, 10, 10, None, kda.KDA_I64, None, kda.KDA_F32, 0, None) == 0
+    assert sc(1 << 20, kda.KDA_BF16, 4, 10, 10, 1 << 21, 7, 1 << 22, kda.KDA_F32, 2, None) == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(ImportError):
+        kda.load_library.__wrapped__(str(tmp_path / "nope.so")) if hasattr(kda.load_library, "__wrapped__") \
+            else _load_fresh(str(tmp_path / "nope.so"))
+
+
+def _load_fresh(path):
+    saved = kda._lib
+    kda._lib = None
+    try:
+        return kda.load_library(path)
+    finally:
+        kda._lib = saved
