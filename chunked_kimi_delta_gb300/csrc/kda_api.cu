@@ -9,6 +9,7 @@
 
 #include "../../include/kda_profile.h"
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 using namespace kda;
 
@@ -63,8 +64,31 @@ FwdPlan summary_plan(const kda_fwd_args *a, int32_t num_segments) {
   return make_plan(T_tot, num_segments, true, a->T, a->H, a->dk, a->dv);
 }
 
+// The tensor-core path takes bf16 inputs with d_k = d_v = 128; every other
+// case runs on the CUDA-core path.
+bool use_tc(const kda_fwd_args *a) {
+  return a->qkv_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128 && (int64_t)a->B * a->T > 0;
+}
+
+// Tensor-core workspace: error word, chunk offsets, one package per (chunk, head).
+struct TcPlan {
+  size_t off_chunk_off, off_pkg, total;
+};
+TcPlan tc_plan(const FwdPlan &p) {
+  TcPlan t{};
+  size_t o = 256;
+  t.off_chunk_off = o; o = align256(o + sizeof(int32_t) * (size_t)(p.N + 1));
+  t.off_pkg = o; o = align256(o + (size_t)p.nchunks * p.H * tcp::PK_BYTES);
+  t.total = o;
+  return t;
+}
+
+size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p) {
+  return use_tc(a) ? tc_plan(p).total : p.total;
+}
+
 kda_status check_workspace(const kda_fwd_args *a, const FwdPlan &p) {
-  if (!a->workspace || a->workspace_bytes < p.total) return KDA_ERR_WORKSPACE;
+  if (!a->workspace || a->workspace_bytes < plan_bytes(a, p)) return KDA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
   return KDA_OK;
 }
@@ -100,12 +124,12 @@ const char *kda_status_string(kda_status s) {
 
 size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *a) {
   if (check_fwd(a) != KDA_OK) return 0;
-  return fwd_plan(a).total;
+  return plan_bytes(a, fwd_plan(a));
 }
 
 size_t kda_segment_summary_workspace_size(const kda_fwd_args *a, int32_t num_segments) {
   if (check_common(a) != KDA_OK || num_segments < 1) return 0;
-  return summary_plan(a, num_segments).total;
+  return plan_bytes(a, summary_plan(a, num_segments));
 }
 
 // Launch sequence of the forward.  When events are given, events[i] is
@@ -132,23 +156,49 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
     ++stage;
     return r;
   };
+  const bool tc = use_tc(a);
+  const size_t off_co = tc ? tc_plan(p).off_chunk_off : p.off_chunk_off;
+  si.chunk_off = reinterpret_cast<int32_t *>(ws + off_co);
+  tcp::TcMaps maps;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, maps)) return KDA_ERR_CUDA;
+
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);  // device error word
   if (e == cudaSuccess && si.bounds) {
     e = mark();
-    if (e == cudaSuccess) e = launch_chunk_map(si, reinterpret_cast<int32_t *>(ws + p.off_chunk_off), st);
+    if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
   }
-  if (e == cudaSuccess) e = mark();
-  if (e == cudaSuccess)
-    e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);
-  if (e == cudaSuccess) e = mark();
-  if (e == cudaSuccess) {
-    InterOut io{};
-    io.out = a->out;
-    io.final_state = a->final_state;
-    io.h_out = a->h_out;
-    io.v_new_out = a->v_new_out;
-    io.initial_state = a->initial_state;
-    e = launch_generic_inter(a->qkv_dtype, false, io, si, p, ws, st);
+  if (tc) {
+    char *pkg = ws + tc_plan(p).off_pkg;
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws);
+    if (e == cudaSuccess) e = mark();
+    if (e == cudaSuccess)
+      e = tcp::launch_tc_prep(maps, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
+    if (e == cudaSuccess) e = mark();
+    if (e == cudaSuccess) {
+      tcp::ChainArgs ca{};
+      ca.pkg = pkg;
+      ca.out = a->out;
+      ca.initial_state = a->initial_state;
+      ca.final_state = a->final_state;
+      ca.h_out = a->h_out;
+      ca.v_new_out = a->v_new_out;
+      ca.err = err;
+      e = tcp::launch_tc_chain(tcp::CHAIN_FWD, ca, si, a->H, st);
+    }
+  } else {
+    if (e == cudaSuccess) e = mark();
+    if (e == cudaSuccess)
+      e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);
+    if (e == cudaSuccess) e = mark();
+    if (e == cudaSuccess) {
+      InterOut io{};
+      io.out = a->out;
+      io.final_state = a->final_state;
+      io.h_out = a->h_out;
+      io.v_new_out = a->v_new_out;
+      io.initial_state = a->initial_state;
+      e = launch_generic_inter(a->qkv_dtype, false, io, si, p, ws, st);
+    }
   }
   if (e == cudaSuccess) e = mark();
   return cuda_status(e);
@@ -163,8 +213,13 @@ int32_t kda_chunk_fwd_stages(const kda_fwd_args *a, const char **names, int32_t 
   const char *list[3];
   int32_t n = 0;
   if (a->cu_seqlens) list[n++] = "chunk_map";
-  list[n++] = "intra_generic";
-  list[n++] = "inter_generic";
+  if (use_tc(a)) {
+    list[n++] = "tc_prep";
+    list[n++] = "tc_chain";
+  } else {
+    list[n++] = "intra_generic";
+    list[n++] = "inter_generic";
+  }
   for (int32_t i = 0; names && i < n && i < max_names; ++i) names[i] = list[i];
   return n;
 }
@@ -194,20 +249,38 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
 
   SeqInfo si{};
   si.bounds = seg_bounds;
-  si.chunk_off = reinterpret_cast<int32_t *>(ws + p.off_chunk_off);
   si.T_tot = p.T_tot;
   si.T = a->T;
   si.N = num_segments;
+  const bool tc = use_tc(a);
+  si.chunk_off = reinterpret_cast<int32_t *>(ws + (tc ? tc_plan(p).off_chunk_off : p.off_chunk_off));
+  tcp::TcMaps maps;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, maps)) return KDA_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
-  if (e == cudaSuccess) e = launch_chunk_map(si, reinterpret_cast<int32_t *>(ws + p.off_chunk_off), st);
-  if (e == cudaSuccess)
-    e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);
-  if (e == cudaSuccess) {
-    InterOut io{};
-    io.S_tilde = S_tilde;
-    io.M = M;
-    e = launch_generic_inter(a->qkv_dtype, true, io, si, p, ws, st);
+  if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
+  if (tc) {
+    char *pkg = ws + tc_plan(p).off_pkg;
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws);
+    if (e == cudaSuccess)
+      e = tcp::launch_tc_prep(maps, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
+    if (e == cudaSuccess) {
+      tcp::ChainArgs ca{};
+      ca.pkg = pkg;
+      ca.S_tilde = S_tilde;
+      ca.M = M;
+      ca.err = err;
+      e = tcp::launch_tc_chain(tcp::CHAIN_SUMMARY, ca, si, a->H, st);
+    }
+  } else {
+    if (e == cudaSuccess)
+      e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);
+    if (e == cudaSuccess) {
+      InterOut io{};
+      io.S_tilde = S_tilde;
+      io.M = M;
+      e = launch_generic_inter(a->qkv_dtype, true, io, si, p, ws, st);
+    }
   }
   return cuda_status(e);
 }

@@ -1,0 +1,147 @@
+// kda_tc.cuh - shared definitions of the tensor-core (tcgen05) forward path
+// for bf16 inputs with d_k = d_v = 128.
+//
+// The path has two kernels:
+//   prep  (kda_tc_prep.cu): per (chunk, head) - gate, cumulative decay, L2
+//         norms, the decay-weighted A_kk / A_qk products, the triangular
+//         inverse and the WY products w = A (k.beta.e^G), u = A (v.beta);
+//   chain (kda_tc_chain.cu): per (sequence, head) - the sequential state
+//         recurrence v_new = u - w h, o = qg h + Aqk v_new,
+//         h' = e^{G_C} h + kg^T v_new.
+// prep hands each chunk to chain as a "package": a byte image of the shared
+// memory tiles chain feeds to the tensor cores, so chain moves it with one
+// bulk copy and no re-layout.
+#pragma once
+
+#include <cuda.h>
+
+#include "kda_internal.cuh"
+#include "tc_primitives.cuh"
+
+namespace kda {
+namespace tcp {
+
+constexpr int K = 128, V = 128;
+
+// Package of one (chunk, head), byte offsets.  All tiles are bf16 SW128 except
+// U (fp32, 16-byte chunks of row r permuted by XOR with r % 32) and GC (fp32).
+//   WQ : [qg (rows 0-63); w (rows 64-127)] x 128 channels, K-major, two
+//        64-channel panels of 128 rows           -> A operand of [qg; w] h
+//   KG : kg = k^ e^{G_C - G} as [token][channel], MN-major, two 64-channel
+//        panels of 64 token rows                  -> A operand of kg^T v_new
+//   AQK: Aqk [64 rows][64 tokens], K-major        -> A operand of Aqk v_new
+//   U  : u [64 tokens][128] fp32
+//   GC : e^{G_C} [128] fp32 (decay of the whole chunk per key channel)
+constexpr uint32_t PK_WQ = 0;
+constexpr uint32_t PK_KG = 32768;
+constexpr uint32_t PK_AQK = 49152;
+constexpr uint32_t PK_U = 57344;
+constexpr uint32_t PK_GC = 90112;
+constexpr uint32_t PK_BYTES = 90624;
+
+__host__ __device__ __forceinline__ uint32_t u_offset(uint32_t row, uint32_t col) {
+  // fp32 element (row, col) of the U tile
+  const uint32_t chunk = (col >> 2) ^ (row & 31u);
+  return row * 512u + chunk * 16u + (col & 3u) * 4u;
+}
+
+// K-major SW128 tile with `rows` rows per 64-element K panel: byte offset of
+// bf16 element (row, k).
+__host__ __device__ __forceinline__ uint32_t kmaj_off(uint32_t rows, uint32_t row, uint32_t k) {
+  return (k >> 6) * rows * 128u + tc::sw128_offset(row, (k & 63u) * 2u);
+}
+// MN-major SW128 tile with `krows` K rows per 64-element MN panel: byte offset
+// of bf16 element (k, mn).
+__host__ __device__ __forceinline__ uint32_t mnmaj_off(uint32_t krows, uint32_t k, uint32_t mn) {
+  return (mn >> 6) * krows * 128u + tc::sw128_offset(k, (mn & 63u) * 2u);
+}
+
+// Bounded waits: give up after this many nanoseconds.
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for an mbarrier phase; on timeout record the device error word and
+// return false.
+__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, uint32_t *err) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 256; ++i)
+      if (tc::mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      atomicOr(err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used when a CTA winds down after a timeout: lets copies or
+// MMAs it started finish before it releases its memory; ignores the result.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!tc::mbar_try_wait(bar, parity) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+  }
+}
+
+// 3-D TMA load (coordinates: channel, head, token).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(tc::smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+         "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(tc::smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+         "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Host side --------------------------------------------------------------------
+struct TcMaps {
+  CUtensorMap q, k, v, x;
+};
+
+// Encodes the four input tensor maps; false when the driver entry point is
+// unavailable or a map is rejected.
+bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
+                     int H, TcMaps &maps);
+
+cudaError_t launch_tc_prep(const TcMaps &maps, const float *beta, const GateParams &gp,
+                           const SeqInfo &s, int64_t nchunks, int H, char *pkg, uint32_t *err,
+                           cudaStream_t st);
+
+enum ChainMode { CHAIN_FWD = 0, CHAIN_SUMMARY = 1 };
+
+struct ChainArgs {
+  const char *pkg;
+  void *out;                    // bf16 [T_tot, H, V]
+  const float *initial_state;   // [N, H, K, V] or null
+  float *final_state;           // [N, H, K, V] or null
+  float *h_out;                 // [nchunks, H, K, V] or null
+  float *v_new_out;             // [T_tot, H, V] or null
+  float *S_tilde, *M;           // summary outputs
+  uint32_t *err;
+};
+
+cudaError_t launch_tc_chain(ChainMode mode, const ChainArgs &a, const SeqInfo &s, int H,
+                            cudaStream_t st);
+
+}  // namespace tcp
+}  // namespace kda
