@@ -7,7 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
-#include "../../include/kda_profile.h"
+#include "kda_profile.h"
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -172,7 +172,7 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess) e = mark();
     if (e == cudaSuccess)
-      e = tcp::launch_tc_prep(maps, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
     if (e == cudaSuccess) e = mark();
     if (e == cudaSuccess) {
       tcp::ChainArgs ca{};
@@ -263,7 +263,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     char *pkg = ws + tc_plan(p).off_pkg;
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess)
-      e = tcp::launch_tc_prep(maps, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
     if (e == cudaSuccess) {
       tcp::ChainArgs ca{};
       ca.pkg = pkg;

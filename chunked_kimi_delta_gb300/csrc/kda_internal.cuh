@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kda.h"
+#include "kda.h"
 
 namespace kda {
 

@@ -99,6 +99,33 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// Prefetch a 3-D TMA box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t x, int32_t y,
+                                                   int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
+}
+
+// Bulk copy shared -> global (16-byte aligned, size multiple of 16), tracked
+// by the issuing thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(tc::smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the shared-memory sources of all committed bulk stores have
+// been read (the smem may then be rewritten).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until all committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Plain bulk copy global -> shared (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile(
@@ -123,9 +150,9 @@ struct TcMaps {
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
                      int H, TcMaps &maps);
 
-cudaError_t launch_tc_prep(const TcMaps &maps, const float *beta, const GateParams &gp,
-                           const SeqInfo &s, int64_t nchunks, int H, char *pkg, uint32_t *err,
-                           cudaStream_t st);
+cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
+                           const float *beta, const GateParams &gp, const SeqInfo &s,
+                           int64_t nchunks, int H, char *pkg, uint32_t *err, cudaStream_t st);
 
 enum ChainMode { CHAIN_FWD = 0, CHAIN_SUMMARY = 1 };
 

@@ -183,3 +183,20 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
 
 }  // namespace tc
 }  // namespace kda
+
+namespace kda {
+namespace tc {
+// Hardware base-2 exponential / logarithm (PTX ex2.approx / lg2.approx,
+// flush-to-zero).  Relative error about 2^-22: ample for bf16 operands.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+}  // namespace tc
+}  // namespace kda
