@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                i64, vp], ctypes.c_int),
         "kda_get_device_status": ([vp, vp], ctypes.c_int),
         "kda_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "kda_chunk_fwd_static_scratch": ([P, vp], ctypes.c_int),
         "kda_chunk_fwd_stages": ([P, ctypes.POINTER(ctypes.c_char_p), i32], i32),
         "kda_chunk_fwd_profiled": ([P, vp, ctypes.POINTER(vp), i32], ctypes.c_int),
     }
@@ -202,6 +203,41 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     _check(lib.kda_chunk_fwd(ctypes.byref(a), _stream(stream)), "kda_chunk_fwd")
+    return out, final_state
+
+
+# include/kda.h KDA_STATIC_SCRATCH_BYTES
+KDA_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None,
+                                 dt_bias=None, initial_state=None, cu_seqlens=None,
+                                 l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
+                                 use_exp2=False, output_final_state=True, out=None,
+                                 final_state=None, stream=None):
+    """The forward for callers that cannot allocate device memory: same
+    arguments and results as :func:`kda_chunk_fwd`, but no workspace; the
+    library's fixed scratch array is used instead (problems whose workspace
+    exceeds ``KDA_STATIC_SCRATCH_BYTES`` raise KdaError(KDA_ERR_WORKSPACE)).
+    Output tensors are allocated here only when not supplied.  Calls sharing a
+    GPU must not overlap in time."""
+    torch = _torch()
+    lib = load_library()
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if q.dim() == 3 else q.shape[0]
+    if out is None:
+        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty(N, q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+                                  device=q.device)
+    a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
+                      initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
+                      beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
+                      out=out, final_state=final_state)
+    _check(lib.kda_chunk_fwd_static_scratch(ctypes.byref(a), _stream(stream)),
+           "kda_chunk_fwd_static_scratch")
     return out, final_state
 
 

@@ -126,6 +126,33 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
  * KDA_STATE_V_FIRST), KDA_ERR_ALIGNMENT, KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 
+/* Size of the library's own scratch array used by
+ * kda_chunk_fwd_static_scratch: 32 MiB on every GPU the library runs on. */
+#define KDA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * kda_chunk_fwd for callers that cannot allocate device memory (the pages
+ * have no counterpart of this call).  A plugin whose host owns all device
+ * memory, or a latency-critical path where cudaMalloc is not allowed, passes
+ * its inputs and outputs exactly as for kda_chunk_fwd; args->workspace and
+ * args->workspace_bytes are ignored and the scratch comes from a fixed
+ * KDA_STATIC_SCRATCH_BYTES array inside the library, which no call allocates
+ * or frees (it exists from the time the library is loaded on a GPU until the
+ * process exits).
+ *  - Limit: the problem's kda_chunk_fwd_workspace_size must not exceed
+ *    KDA_STATIC_SCRATCH_BYTES, else KDA_ERR_WORKSPACE and nothing is
+ *    launched (roughly: up to about 360 chunk-heads on the bf16 d=128 path,
+ *    e.g. B=1, T=2048, H=8).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (e.g. on
+ *    two streams) race and must be serialised by the caller.  Leftover
+ *    contents of earlier calls do not affect results.
+ *  - Other errors as kda_chunk_fwd; KDA_ERR_CUDA if the address lookup fails.
+ */
+kda_status kda_chunk_fwd_static_scratch(const kda_fwd_args *args, kda_stream_t stream);
+
 /* Bytes of workspace kda_segment_summary needs. */
 size_t kda_segment_summary_workspace_size(const kda_fwd_args *args, int32_t num_segments);
 
