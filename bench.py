@@ -46,6 +46,28 @@ def intra_alg_bytes_per_token_head(dk, dv):   # inputs the intra-chunk stage mus
     return 2 * dk * 2 + 2 * dv + 4 * dk + 4
 
 
+def dist_env():
+    """(world, rank, local_rank) from the torchrun environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank gets the max (one scalar all-reduce)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, steps: int, ms: float) -> float:
+    """Units of all ranks per second over the slowest rank's time (weak scaling)."""
+    return units_per_rank_step * world * steps / (ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -201,9 +223,7 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank)
 
@@ -276,15 +296,11 @@ def main():
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_per_step = ms / args.steps
     tokens = cfg.B * cfg.T
     token_heads = tokens * H
-    value = tokens * world * args.steps / (ms / 1e3)
+    value = whole_job_rate(tokens, world, args.steps, ms)
     tflops = token_heads * world * args.steps * alg_flops_per_token_head(K, V) / (ms / 1e3) / 1e12
     stage_avg = [sum(es[j].elapsed_time(es[j + 1]) for es in ev_sets) / args.steps
                  for j in range(len(stages))]
@@ -296,9 +312,9 @@ def main():
     dom = max(range(len(stages)), key=lambda i: stage_avg[i])
     dom_name = stages[dom]
     state_bytes = 2 * 4 * K * V * cfg.B * H          # initial + final state
-    if dom_name.startswith("intra"):
+    if dom_name.startswith("intra") or dom_name == "tc_prep":
         dom_bytes = intra_alg_bytes_per_token_head(K, V) * token_heads
-    elif dom_name.startswith("inter"):
+    elif dom_name.startswith("inter") or dom_name == "tc_chain":
         dom_bytes = 2 * V * token_heads + state_bytes  # the output o and the states
     else:
         dom_bytes = alg_bytes_per_token_head(K, V) * token_heads + state_bytes
@@ -344,11 +360,16 @@ def main():
 
 def load_traffic(kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when no capture of the current kernel exists."""
+    None when there is no capture or the kernel source changed since."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(kernel)
+            ent = json.load(f)[kernel]
+        with open(os.path.join(ROOT, ent["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != ent["source_sha256"]:
+                return None
+        return ent["bytes"]
     except Exception:
         return None
 
