@@ -391,8 +391,10 @@ def bench_segment(kda, dev, stream, steps=3, warmup=2):
     S_fin = torch.empty(H, K, V, device=dev)
     flat = lambda x: x.reshape(T, *x.shape[2:])
     q, k, v, g, be = (flat(inp[n]) for n in ("q", "k", "v", "g", "beta"))
-    fa, out, fin, ws = kda.prepare_chunk_fwd(q, k, v, g, be, cu_seqlens=sb, initial_state=S_in, **kw)
+    # the finish reuses the chunks the summary prepared (same workspace)
     sa, _, _, ws_sum = kda.prepare_segment_summary(q, k, v, g, be, sb, M=M, S_tilde=St, **kw)
+    fa, out, fin, ws = kda.prepare_chunk_fwd(q, k, v, g, be, cu_seqlens=sb, initial_state=S_in,
+                                             workspace=ws_sum, extra_flags=kda.KDA_REUSE_PREP, **kw)
     lib = kda.load_library()
     sp = stream.cuda_stream
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]

@@ -24,6 +24,7 @@ KDA_L2NORM_QK = 1 << 0
 KDA_BETA_SIGMOID = 1 << 1
 KDA_GATE_IN_KERNEL = 1 << 2
 KDA_USE_EXP2 = 1 << 3
+KDA_REUSE_PREP = 1 << 4
 KDA_SAFE_GATE = 1 << 8
 KDA_ALLOW_NEG_EIGVAL = 1 << 9
 KDA_STATE_V_FIRST = 1 << 10
@@ -181,9 +182,16 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
                   gate_in_kernel=False, use_exp2=False, output_final_state=True, out=None,
                   final_state=None, h_out=None, v_new_out=None, workspace=None, stream=None,
-                  extra_flags=0):
+                  reuse_prep=False, extra_flags=0):
     """Chunked KDA forward.  Returns ``(out, final_state)`` (final_state is
-    None unless requested).  See ``kda_chunk_fwd`` in include/kda.h."""
+    None unless requested).  ``reuse_prep`` (with ``workspace``) sets
+    KDA_REUSE_PREP: the workspace already holds this problem's intra-chunk
+    results, e.g. from a kda_segment_summary whose seg_bounds are this call's
+    cu_seqlens.  See ``kda_chunk_fwd`` in include/kda.h."""
+    if reuse_prep:
+        if workspace is None:
+            raise ValueError("reuse_prep needs the workspace that holds the prepared chunks")
+        extra_flags |= KDA_REUSE_PREP
     torch = _torch()
     lib = load_library()
     if cu_seqlens is not None:
@@ -300,6 +308,17 @@ def kda_chunk_fwd_profiled(args: kda_fwd_args, events, stream=None):
 def kda_segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_log=None,
                         dt_bias=None, l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
                         use_exp2=False, M=None, S_tilde=None, workspace=None, stream=None):
+    """(see below; pass ``workspace`` to keep the prepared chunks for a
+    following kda_chunk_fwd with ``reuse_prep=True``)"""
+    return _segment_summary(q, k, v, g, beta, seg_bounds, scale=scale, eps=eps, a_log=a_log,
+                            dt_bias=dt_bias, l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid,
+                            gate_in_kernel=gate_in_kernel, use_exp2=use_exp2, M=M,
+                            S_tilde=S_tilde, workspace=workspace, stream=stream)
+
+
+def _segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_log=None,
+                     dt_bias=None, l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
+                     use_exp2=False, M=None, S_tilde=None, workspace=None, stream=None):
     """Segment affine summary.  ``seg_bounds``: int32 device tensor [S+1] of
     token offsets on the flattened token axis.  Returns ``(M, S_tilde)``."""
     torch = _torch()

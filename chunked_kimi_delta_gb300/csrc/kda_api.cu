@@ -18,8 +18,8 @@ namespace {
 inline bool mis16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 constexpr uint32_t kKnownFlags = KDA_L2NORM_QK | KDA_BETA_SIGMOID | KDA_GATE_IN_KERNEL |
-                                 KDA_USE_EXP2 | KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL |
-                                 KDA_STATE_V_FIRST;
+                                 KDA_USE_EXP2 | KDA_REUSE_PREP | KDA_SAFE_GATE |
+                                 KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST;
 constexpr uint32_t kRejectedFlags = KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST;
 
 // Checks shared by the forward and the summary (everything but the outputs).
@@ -162,16 +162,17 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
   tcp::TcMaps maps;
   if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, maps)) return KDA_ERR_CUDA;
 
+  const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);  // device error word
-  if (e == cudaSuccess && si.bounds) {
+  if (e == cudaSuccess && si.bounds && !reuse) {
     e = mark();
     if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
   }
   if (tc) {
     char *pkg = ws + tc_plan(p).off_pkg;
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
-    if (e == cudaSuccess) e = mark();
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !reuse) e = mark();
+    if (e == cudaSuccess && !reuse)
       e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
     if (e == cudaSuccess) e = mark();
     if (e == cudaSuccess) {
@@ -186,8 +187,8 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
       e = tcp::launch_tc_chain(tcp::CHAIN_FWD, ca, si, a->H, st);
     }
   } else {
-    if (e == cudaSuccess) e = mark();
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !reuse) e = mark();
+    if (e == cudaSuccess && !reuse)
       e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);
     if (e == cudaSuccess) e = mark();
     if (e == cudaSuccess) {
@@ -212,12 +213,13 @@ int32_t kda_chunk_fwd_stages(const kda_fwd_args *a, const char **names, int32_t 
   if (check_fwd(a) != KDA_OK) return 0;
   const char *list[3];
   int32_t n = 0;
-  if (a->cu_seqlens) list[n++] = "chunk_map";
+  const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
+  if (a->cu_seqlens && !reuse) list[n++] = "chunk_map";
   if (use_tc(a)) {
-    list[n++] = "tc_prep";
+    if (!reuse) list[n++] = "tc_prep";
     list[n++] = "tc_chain";
   } else {
-    list[n++] = "intra_generic";
+    if (!reuse) list[n++] = "intra_generic";
     list[n++] = "inter_generic";
   }
   for (int32_t i = 0; names && i < n && i < max_names; ++i) names[i] = list[i];

@@ -61,6 +61,14 @@ enum {
   KDA_BETA_SIGMOID = 1u << 1,   /* beta = 1 / (1 + exp(-b)) of the given logits  */
   KDA_GATE_IN_KERNEL = 1u << 2, /* g = -exp(a_log[h]) softplus(x + dt_bias[h,c]) */
   KDA_USE_EXP2 = 1u << 3,       /* work in base 2 internally; same result        */
+  /* kda_chunk_fwd only: the workspace already holds this call's intra-chunk
+   * results (the per-chunk preparation of q, k, v, g, beta: "FwdPrepare" of
+   * "Hyper-Parallel Chunk KDA current implementation design" section 6.3),
+   * left there by the immediately preceding kda_segment_summary on the same
+   * inputs, flags and workspace with seg_bounds equal to this call's
+   * cu_seqlens (or by a kda_chunk_fwd with the same arguments); only the
+   * inter-chunk chain runs.  Caller precondition, not checked. */
+  KDA_REUSE_PREP = 1u << 4,
   /* Named on the pages without a formula (safe_gate/lower_bound,
    * allow_neg_eigval) or a layout this library does not take (V-first
    * state): always rejected with KDA_ERR_UNSUPPORTED. */

@@ -144,3 +144,31 @@ def test_long_segment_workload(cuda_lib):
                        beta=sl(sub["beta"]), cu=[0, L])
     _, f_ref = oracle.chunk_fwd(p, want_out=False)
     check(S_in[1, h], f_ref[0, 0], "bf16", "S_in[1] vs oracle")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_segment_finish_reuses_prepared_chunks(cuda_lib, dtype):
+    """The finish may reuse the summary's prepared chunks (KDA_REUSE_PREP on
+    the summary's workspace); results are identical to recomputing them."""
+    cfg = KdaConfig("reuse", B=1, T=700, H=2, dk=128, dv=128, dtype=dtype, use_exp2=True, seed=13)
+    inp = to_cuda(make(cfg))
+    bounds = (0, 64, 300, 333, 700)
+    sb = torch.tensor(bounds, dtype=torch.int32, device="cuda")
+    kw = fwd_kwargs(cfg, inp)
+    for key in ("initial_state", "cu_seqlens"):
+        kw.pop(key)
+    T = cfg.T
+    flat = lambda x: x.reshape(T, *x.shape[2:])
+    q, k, v, g, b = (flat(inp[n]) for n in ("q", "k", "v", "g", "beta"))
+    a, M, St, ws = cuda_lib.prepare_segment_summary(q, k, v, g, b, sb, **kw)
+    import ctypes
+    lib = cuda_lib.load_library()
+    assert lib.kda_segment_summary(ctypes.byref(a), sb.data_ptr(), len(bounds) - 1, M.data_ptr(),
+                                   St.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    S_in, _ = cuda_lib.kda_state_prefix_scan(M, St, None)
+    S_in = S_in.contiguous()
+    o1, f1 = cuda_lib.kda_chunk_fwd(q, k, v, g, b, cu_seqlens=sb, initial_state=S_in, **kw)
+    o2, f2 = cuda_lib.kda_chunk_fwd(q, k, v, g, b, cu_seqlens=sb, initial_state=S_in,
+                                    workspace=ws, reuse_prep=True, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
