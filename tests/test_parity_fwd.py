@@ -54,10 +54,10 @@ def test_precomputed_gate_and_beta_without_l2norm(cuda_lib, dtype):
     check(fin, f_ref, dtype, "final_state")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_varlen_small(cuda_lib, dtype):
+@pytest.mark.parametrize("dtype,dv", [("f32", 64), ("bf16", 64), ("bf16", 128)])
+def test_varlen_small(cuda_lib, dtype, dv):
     lens = (1, 64, 0, 65, 200, 3)
-    cfg = KdaConfig("varlen_small", dtype=dtype, H=2, dk=128, dv=64, seq_lens=lens,
+    cfg = KdaConfig("varlen_small", dtype=dtype, H=2, dk=128, dv=dv, seq_lens=lens,
                     initial_state=True, seed=9)
     inp = make(cfg)
     out, fin, o_ref, f_ref = _run_both(cuda_lib, cfg, inp)
@@ -75,14 +75,16 @@ def test_empty_batch_passes_initial_state_through(cuda_lib):
     torch.testing.assert_close(fin, inp["initial_state"], rtol=0, atol=0)
 
 
-def test_h_out_and_v_new_out(cuda_lib):
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_h_out_and_v_new_out(cuda_lib, dtype, d):
     """h_out[c] is the state entering chunk c; v_new rows are the corrected
     values beta_r (v_r - (Diag(alpha_r) S_{r-1})^T k_r).  Both are checked
-    against oracle runs over every prefix."""
-    cfg = KdaConfig("save", B=1, T=130, H=2, dk=64, dv=64, dtype="f32", initial_state=True, seed=3)
+    against oracle runs over every prefix (CUDA-core path for fp32 d=64,
+    tensor-core path for bf16 d=128)."""
+    cfg = KdaConfig("save", B=1, T=130, H=2, dk=d, dv=d, dtype=dtype, initial_state=True, seed=3)
     inp_cpu = make(cfg)
     inp = to_cuda(inp_cpu)
-    T, H, K, V = 130, 2, 64, 64
+    T, H, K, V = 130, 2, d, d
     h_out = torch.empty(3, H, K, V, device="cuda")
     vn = torch.empty(1, T, H, V, device="cuda")
     gpu_fwd(cuda_lib, cfg, inp, h_out=h_out, v_new_out=vn)
@@ -99,13 +101,13 @@ def test_h_out_and_v_new_out(cuda_lib):
                                 gate_in_kernel=True, beta_sigmoid=True)
             prefix[t] = oracle.chunk_fwd(pt, S0, want_out=False)[1][0]
     for c in range(3):
-        check(h_out[c], prefix[64 * c], "f32", f"h_out[{c}]")
+        check(h_out[c], prefix[64 * c], dtype, f"h_out[{c}]")
     ref = np.zeros((T, H, V))
     for t in range(T):
         for h in range(H):
             Sd = np.exp(g[t, h])[:, None] * prefix[t][h]
             ref[t, h] = b[t, h] * (p.v[t, h] - Sd.T @ kh[t, h])
-    check(vn[0], ref, "f32", "v_new")
+    check(vn[0], ref, dtype, "v_new")
 
 
 def test_deterministic(cuda_lib):
