@@ -43,25 +43,28 @@ constexpr uint32_t S_OPA = 16384;    // [k E ; q E] K-major, 128 rows (32768)
 constexpr uint32_t S_B1 = 49152;     // 160 rows K-major (2 panels x 20480)
 constexpr uint32_t S_B2A = 90112;    // k^ 2^G, MN-major (16384)
 // after the first MMA the OPA/B1 region is reused:
-constexpr int LFS = 68;              // row stride of L (16-byte aligned rows)
+constexpr int LFS = 68;              // row stride of L and A (16-byte aligned rows)
+constexpr int TTS = 36;              // row stride of the product scratch
 constexpr uint32_t S_LF = 16384;     // fp32 L [64][68]
-constexpr uint32_t S_AF = 33792;     // fp32 A [64][65]
-constexpr uint32_t S_TT = 50432;     // fp32 scratch [32][33]
-constexpr uint32_t S_AINV = 55296;   // bf16 A.diag(beta), K-major 64 rows (8192)
+constexpr uint32_t S_AF = 33792;     // fp32 A [64][68]
+constexpr uint32_t S_TT = 51200;     // fp32 scratch [32][36]
+constexpr uint32_t S_AINV = 56320;   // bf16 A.diag(beta), K-major 64 rows (8192)
 // staging of package parts for bulk stores (regions free at that time):
 constexpr uint32_t S_STG_AQK = 73728;  // Aqk image (8192), written after MMA 1 (B1 dead)
-constexpr uint32_t S_STG_W = 16384;    // w rows of WQ, 2 panels x 8192, after MMA 2
-constexpr uint32_t S_STG_U = 32768;    // U image (32768), after MMA 2
+constexpr uint32_t S_STG_W = 90112;    // w rows of WQ, 2 panels x 8192, after MMA 2 (B2A dead)
+constexpr uint32_t S_STG_U = 49152;    // U image (32768), after MMA 2 (B1 dead)
+// OPA holds nothing between items: phase 1 parks the raw q and k rows there,
+// at the positions phase 2 overwrites with the scaled operands.
 constexpr uint32_t S_MISC = 106496;
 constexpr uint32_t M_RQ = S_MISC;           // fp32 [64] rstd q
 constexpr uint32_t M_RK = S_MISC + 256;     // fp32 [64] rstd k
 constexpr uint32_t M_BETA = S_MISC + 512;   // fp32 [64]
-constexpr uint32_t M_TOT = S_MISC + 768;    // fp32 [4][128] sub-block gate totals
-constexpr uint32_t M_BAR = S_MISC + 2816;   // bar_v, bar_mma
-constexpr uint32_t M_TSLOT = S_MISC + 2832;
-constexpr uint32_t M_ABORT = S_MISC + 2836;
-constexpr uint32_t M_ITEM = S_MISC + 2848;  // 2 x ItemSlot
-constexpr uint32_t SMEM_BYTES = S_MISC + 2912 + 1024;
+constexpr uint32_t M_TOT = S_MISC + 768;    // fp32 [8][128] row-group gate totals
+constexpr uint32_t M_BAR = S_MISC + 4864;   // bar_v, bar_mma
+constexpr uint32_t M_TSLOT = S_MISC + 4880;
+constexpr uint32_t M_ABORT = S_MISC + 4884;
+constexpr uint32_t M_ITEM = S_MISC + 4896;  // 2 x ItemSlot
+constexpr uint32_t SMEM_BYTES = S_MISC + 4960 + 1024;
 
 constexpr uint32_t B1_PANEL = 160 * 128;
 constexpr uint32_t TMEM_COLS = 256;
@@ -103,8 +106,12 @@ __device__ __forceinline__ void put_slot(ItemSlot &sl, const Item &it, bool ok) 
   sl.ok = ok ? 1 : 0;
 }
 
-__device__ __forceinline__ void st_u32(uint8_t *base, uint32_t off, uint32_t v) {
-  *reinterpret_cast<uint32_t *>(base + off) = v;
+__device__ __forceinline__ void st_u64(uint8_t *base, uint32_t off, uint2 v) {
+  *reinterpret_cast<uint2 *>(base + off) = v;
+}
+
+__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
+  return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
 template <typename T>
@@ -152,12 +159,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   tc::tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  // elementwise roles: channel pair p (channels c0, c0 + 1), sub-block R
-  // (rows 16 R .. 16 R + 15)
-  const int p = tid & 63, R = tid >> 6;
-  const int c0 = 2 * p;
-  const uint32_t ch16 = (uint32_t)((c0 & 63) >> 3), cbyte = (uint32_t)(c0 & 7) * 2u;
-  const uint32_t pan = (uint32_t)(c0 >> 6);
+  // elementwise roles: lane = channel quad (channels c0 .. c0 + 3), warp =
+  // row group (rows 8 warp .. 8 warp + 7) inside sub-block R = warp / 2
+  const int c0 = 4 * lane, R = warp >> 1;
+  const uint32_t ch16 = (uint32_t)((lane & 15) >> 1), cbyte = (uint32_t)(lane & 1) * 8u;
+  const uint32_t pan = (uint32_t)(lane >> 4);
 
   const int64_t G = gridDim.x;
   // thread 0 keeps count of the loads and MMAs it started, for the drain
@@ -197,167 +203,182 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       }
     }
 
-    // ---- pass A: row norms of q and k (8 rows per warp), beta; all loads
-    //      are issued before any arithmetic
+    // ---- phase 1: the item's loads (q, k, gate input: 8 rows x 4 channels
+    //      per thread; beta), row norms (warp butterfly over the 16 partial
+    //      sums of its 8 rows), gate in log2 units and the cumulative sums
+    //      of each 8-row group
+    float Gl[8][4];
+    const uint32_t kp128 = pan * 128u * 128u, kp160 = pan * B1_PANEL, kp64 = pan * 64u * 128u;
     {
-      uint2 qa[8], ka[8];
+      uint2 qv[8], kv[8];
+      float4 xs[8];
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
-        const int r = warp * 8 + rr;
-        qa[rr] = make_uint2(0, 0);
-        ka[rr] = make_uint2(0, 0);
+        const int r = 8 * warp + rr;
+        const int64_t off = base_h + r * rowH + c0;
+        qv[rr] = make_uint2(0, 0);
+        kv[rr] = make_uint2(0, 0);
+        xs[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < len) {
-          qa[rr] = ldg_stream(reinterpret_cast<const uint2 *>(qg_in + base_h + r * rowH) + lane);
-          ka[rr] = ldg_stream(reinterpret_cast<const uint2 *>(kg_in + base_h + r * rowH) + lane);
+          qv[rr] = ldg_stream(reinterpret_cast<const uint2 *>(qg_in + off));
+          kv[rr] = ldg_stream(reinterpret_cast<const uint2 *>(kg_in + off));
+          xs[rr] = ldg_stream(reinterpret_cast<const float4 *>(xg_in + off));
         }
       }
-      float sq[8], sk[8];
+      float bload = 0.f;
+      if (tid < 64 && tid < len) bload = beta[(t0 + tid) * H + h];
+      const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
+      float db[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) db[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + j] : 0.f;
+
+      float v[16];
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
-        const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qa[rr]);
-        const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka[rr]);
+        const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[rr]);
+        const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kv[rr]);
         const float2 a0 = __bfloat1622float2(q2[0]), a1 = __bfloat1622float2(q2[1]);
         const float2 b0 = __bfloat1622float2(k2[0]), b1 = __bfloat1622float2(k2[1]);
-        sq[rr] = a0.x * a0.x + a0.y * a0.y + a1.x * a1.x + a1.y * a1.y;
-        sk[rr] = b0.x * b0.x + b0.y * b0.y + b1.x * b1.x + b1.y * b1.y;
+        v[rr] = a0.x * a0.x + a0.y * a0.y + a1.x * a1.x + a1.y * a1.y;
+        v[8 + rr] = b0.x * b0.x + b0.y * b0.y + b1.x * b1.x + b1.y * b1.y;
       }
+      // butterfly: each step halves the values a lane holds; afterwards lane
+      // l holds the warp sum of value ((l>>4)&1)*8 + ((l>>3)&1)*4 + ((l>>2)&1)*2 + ((l>>1)&1)
 #pragma unroll
-      for (int o = 16; o; o >>= 1)
+      for (int st = 0; st < 4; ++st) {
+        const int half = 8 >> st, msk = 16 >> st;
+        const bool up = (lane & msk) != 0;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
-          sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
+        for (int i2 = 0; i2 < half; ++i2) {
+          const float send = up ? v[i2] : v[i2 + half];
+          const float keep = up ? v[i2 + half] : v[i2];
+          v[i2] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
         }
-      if (lane < 8) {
-        const int r = warp * 8 + lane;
-        float vq = sq[0], vk = sk[0];
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      if ((lane & 1) == 0) {
+        const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                        ((lane >> 1) & 1);
+        const int r = 8 * warp + (idx & 7);
+        const float nv = r < len ? (l2n ? rsqrtf(v[0] + gp.eps) : 1.f) : 0.f;
+        (idx < 8 ? rq : rk)[r] = nv;
+      }
+      if (tid < 64) sbeta[tid] = (sig && tid < len) ? 1.f / (1.f + tc::ex2(-bload * kLog2e)) : bload;
 #pragma unroll
-        for (int rr = 1; rr < 8; ++rr)
-          if (lane == rr) { vq = sq[rr]; vk = sk[rr]; }
-        const bool v = r < len;
-        rq[r] = v ? (l2n ? rsqrtf(vq + gp.eps) : 1.f) : 0.f;
-        rk[r] = v ? (l2n ? rsqrtf(vk + gp.eps) : 1.f) : 0.f;
+      for (int rr = 0; rr < 8; ++rr) {
+        const uint32_t rowb = (uint32_t)(8 * warp + rr) * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
+        st_u64(sm + S_OPA, kp128 + rowb, kv[rr]);
+        st_u64(sm + S_OPA, kp128 + 64u * 128u + rowb, qv[rr]);
       }
-      if (tid < 64) {
-        float b = 0.f;
-        if (tid < len) {
-          b = beta[(t0 + tid) * H + h];
-          if (sig) b = 1.f / (1.f + tc::ex2(-b * kLog2e));
-        }
-        sbeta[tid] = b;
-      }
-    }
 
-    // ---- phase 1: gate (log2 units) and the sub-block cumulative sums
-    float Gl[16][2];
-    {
-      const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
-      const float db0 = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0] : 0.f;
-      const float db1 = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + 1] : 0.f;
-      float2 xs[16];
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ii = 0; ii < 16; ++ii) {
-        const int r = 16 * R + ii;
-        xs[ii] = r < len ? ldg_stream(reinterpret_cast<const float2 *>(xg_in + base_h + r * rowH + c0))
-                         : make_float2(0.f, 0.f);
-      }
-      float acc0 = 0.f, acc1 = 0.f;
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = 8 * warp + rr;
+        const float xv[4] = {xs[rr].x, xs[rr].y, xs[rr].z, xs[rr].w};
 #pragma unroll
-      for (int ii = 0; ii < 16; ++ii) {
-        const int r = 16 * R + ii;
-        float g0, g1;
-        if (gate) {
-          // softplus(z) log2 e = max(z, 0) log2 e + log2(1 + 2^{-|z| log2 e})
-          const float z0 = (xs[ii].x + db0) * kLog2e, z1 = (xs[ii].y + db1) * kLog2e;
-          g0 = -A_h * (fmaxf(z0, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z0))));
-          g1 = -A_h * (fmaxf(z1, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z1))));
-        } else {
-          g0 = xs[ii].x * kLog2e;
-          g1 = xs[ii].y * kLog2e;
+        for (int j = 0; j < 4; ++j) {
+          float g;
+          if (gate) {
+            // softplus(z) log2 e = max(z, 0) log2 e + log2(1 + 2^{-|z| log2 e})
+            const float z = (xv[j] + db[j]) * kLog2e;
+            g = -A_h * (fmaxf(z, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z))));
+          } else {
+            g = xv[j] * kLog2e;
+          }
+          if (r >= len) g = 0.f;
+          acc[j] += g;
+          Gl[rr][j] = acc[j];
         }
-        if (r >= len) g0 = g1 = 0.f;
-        acc0 += g0;
-        acc1 += g1;
-        Gl[ii][0] = acc0;
-        Gl[ii][1] = acc1;
       }
-      *reinterpret_cast<float2 *>(tot + R * 128 + c0) = make_float2(acc0, acc1);
+      *reinterpret_cast<float4 *>(tot + warp * 128 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
     // the staging buffers of the previous item must be read out before this
     // item's operand tiles overwrite them
     if (tid == 0) bulk_wait_read();
-    __syncthreads();  // sub-block totals, rstd and beta published
+    __syncthreads();  // group totals, rstd and beta published
 
     // ---- phase 2: operand tiles and the elementwise package parts
     {
-      float bAll[4][2], GC[2];
+      // b_RR = gate sum before sub-block RR, G_C = sum over the chunk
+      float bAll[4][4], GC[4], prev[4];
+      {
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float a = 0.f;
+        for (int gg = 0; gg < 8; ++gg) {
+          const float4 t = *reinterpret_cast<const float4 *>(tot + gg * 128 + c0);
+          const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-        for (int RR = 0; RR < 4; ++RR) {
-          bAll[RR][j] = a;
-          a += tot[RR * 128 + c0 + j];
-        }
-        GC[j] = a;
-      }
-      float bR[2], eb[2], egc[2], cR[4][2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        bR[j] = bAll[0][j];
-#pragma unroll
-        for (int RR = 1; RR < 4; ++RR)
-          if (RR == R) bR[j] = bAll[RR][j];
-        eb[j] = tc::ex2(bR[j]);
-        egc[j] = tc::ex2(GC[j] - bR[j]);
-#pragma unroll
-        for (int RR = 0; RR < 4; ++RR) cR[RR][j] = tc::ex2(fminf(bAll[RR][j] - bR[j], 0.f));
-      }
-      if (R == 0)
-        *reinterpret_cast<float2 *>(pk + PK_GC + c0 * 4) = make_float2(tc::ex2(GC[0]), tc::ex2(GC[1]));
-      const float sc0 = gp.scale * eb[0], sc1 = gp.scale * eb[1];
-      const uint32_t kp128 = pan * 128u * 128u, kp160 = pan * B1_PANEL, kp64 = pan * 64u * 128u;
-      uint32_t qraw8[8], kraw8[8];
-#pragma unroll
-      for (int ii = 0; ii < 16; ++ii) {
-        const int r = 16 * R + ii;
-        if ((ii & 7) == 0) {
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int rj = r + jj;
-            qraw8[jj] = 0;
-            kraw8[jj] = 0;
-            if (rj < len) {
-              qraw8[jj] = ldg_stream(reinterpret_cast<const uint32_t *>(qg_in + base_h + rj * rowH + c0));
-              kraw8[jj] = ldg_stream(reinterpret_cast<const uint32_t *>(kg_in + base_h + rj * rowH + c0));
-            }
+          for (int j = 0; j < 4; ++j) {
+            if ((gg & 1) == 0) bAll[gg >> 1][j] = a[j];
+            if (gg == (warp | 1) - 1) prev[j] = tv[j];
+            a[j] += tv[j];
           }
         }
-        const uint32_t qraw = qraw8[ii & 7], kraw = kraw8[ii & 7];
-        const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw));
-        const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
-        const uint32_t xo = ((ch16 ^ (uint32_t)(ii & 7)) << 4) | cbyte;
-        const float sq = rq[r], sk = rk[r];
-        const float e0 = tc::ex2(Gl[ii][0]), e1 = tc::ex2(Gl[ii][1]);
-        const float f0 = tc::ex2(fminf(-Gl[ii][0], 126.f)), f1 = tc::ex2(fminf(-Gl[ii][1], 126.f));
-        const float kn0 = kf.x * sk, kn1 = kf.y * sk;
-        const float qn0 = qf.x * sq, qn1 = qf.y * sq;
-        const float ke0 = kn0 * e0, ke1 = kn1 * e1;
-        const float kf0 = kn0 * f0, kf1 = kn1 * f1;
-        const float qe0 = qn0 * e0, qe1 = qn1 * e1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) GC[j] = a[j];
+      }
+      // rows of the second group of a sub-block: relative to its start
+      if (warp & 1) {
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) Gl[rr][j] += prev[j];
+      }
+      float bRv[4], egc[4], cR[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float bR = bAll[0][j];
+#pragma unroll
+        for (int RR = 1; RR < 4; ++RR)
+          if (RR == R) bR = bAll[RR][j];
+        bRv[j] = bR;
+        egc[j] = tc::ex2(GC[j] - bR);
+#pragma unroll
+        for (int RR = 1; RR < 4; ++RR) cR[RR][j] = tc::ex2(fminf(bAll[RR][j] - bR, 0.f));
+      }
+      if (warp == 0)
+        *reinterpret_cast<float4 *>(pk + PK_GC + c0 * 4) =
+            make_float4(tc::ex2(GC[0]), tc::ex2(GC[1]), tc::ex2(GC[2]), tc::ex2(GC[3]));
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = 8 * warp + rr;
+        const uint32_t xo = ((ch16 ^ (uint32_t)rr) << 4) | cbyte;
         const uint32_t rowb = (uint32_t)r * 128u + xo;
-        st_u32(sm + S_OPA, kp128 + rowb, pack_bf16(ke0, ke1));
-        st_u32(sm + S_OPA, kp128 + 64u * 128u + rowb, pack_bf16(qe0, qe1));
-        st_u32(sm + S_B1, kp160 + 96u * 128u + rowb, pack_bf16(kf0, kf1));
+        const float sq = rq[r], sk = rk[r];
+        // raw rows parked by this thread in phase 1
+        const uint2 qraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + 64u * 128u + rowb);
+        const uint2 kraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + rowb);
+        const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw);
+        const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kraw);
+        const float2 qa = __bfloat1622float2(q2[0]), qb = __bfloat1622float2(q2[1]);
+        const float2 ka = __bfloat1622float2(k2[0]), kb = __bfloat1622float2(k2[1]);
+        const float qn[4] = {qa.x * sq, qa.y * sq, qb.x * sq, qb.y * sq};
+        const float kn[4] = {ka.x * sk, ka.y * sk, kb.x * sk, kb.y * sk};
+        float ke[4], kf[4], qe[4], kd[4], qg[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float e = tc::ex2(Gl[rr][j]), f = tc::ex2(fminf(-Gl[rr][j], 126.f));
+          const float ea = tc::ex2(Gl[rr][j] + bRv[j]);  // 2^G, G from the chunk start
+          ke[j] = kn[j] * e;
+          kf[j] = kn[j] * f;
+          qe[j] = qn[j] * e;
+          kd[j] = kn[j] * ea;
+          qg[j] = qn[j] * ea * gp.scale;
+        }
+        st_u64(sm + S_OPA, kp128 + rowb, pack4(ke[0], ke[1], ke[2], ke[3]));
+        st_u64(sm + S_OPA, kp128 + 64u * 128u + rowb, pack4(qe[0], qe[1], qe[2], qe[3]));
+        st_u64(sm + S_B1, kp160 + 96u * 128u + rowb, pack4(kf[0], kf[1], kf[2], kf[3]));
 #pragma unroll
         for (int Rp = 1; Rp < 4; ++Rp)
           if (Rp > R)
-            st_u32(sm + S_B1, kp160 + (uint32_t)b1_off(Rp) * 128u + rowb,
-                   pack_bf16(kf0 * cR[Rp][0], kf1 * cR[Rp][1]));
-        st_u32(sm + S_B2A, kp64 + rowb, pack_bf16(ke0 * eb[0], ke1 * eb[1]));
+            st_u64(sm + S_B1, kp160 + (uint32_t)b1_off(Rp) * 128u + rowb,
+                   pack4(kf[0] * cR[Rp][0], kf[1] * cR[Rp][1], kf[2] * cR[Rp][2], kf[3] * cR[Rp][3]));
+        st_u64(sm + S_B2A, kp64 + rowb, pack4(kd[0], kd[1], kd[2], kd[3]));
         // package: qg = scale q^ 2^G (WQ rows 0..63), kg = k^ 2^{G_C - G} (KG)
-        st_u32(pk, PK_WQ + kp128 + rowb, pack_bf16(qe0 * sc0, qe1 * sc1));
-        st_u32(pk, PK_KG + kp64 + rowb, pack_bf16(kf0 * egc[0], kf1 * egc[1]));
+        st_u64(pk, PK_WQ + kp128 + rowb, pack4(qg[0], qg[1], qg[2], qg[3]));
+        st_u64(pk, PK_KG + kp64 + rowb,
+               pack4(kf[0] * egc[0], kf[1] * egc[1], kf[2] * egc[2], kf[3] * egc[3]));
       }
     }
     tc::fence_proxy_async_smem();
@@ -388,8 +409,6 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     // ---- read D1: L (k rows) to shared fp32, Aqk (q rows) to the package;
     //      zero the inverse buffer
     {
-      float *AF = reinterpret_cast<float *>(sm + S_AF);
-      for (int x = tid; x < 64 * 65; x += NT) AF[x] = 0.f;
       const int q4 = warp & 3, cq = warp >> 2;
       const int m = 32 * q4 + lane;          // D1 row = TMEM lane
       const bool krow = m < 64;
@@ -438,9 +457,14 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         if (j0 < 0) continue;
         if (krow) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
+          for (int x = 0; x < 16; x += 4) {
             const int j = j0 + x;
-            if (!diag || j < r) LF[r * LFS + j] = br * d[cix][x];
+            float4 l4;
+            l4.x = (!diag || j < r) ? br * d[cix][x] : 0.f;
+            l4.y = (!diag || j + 1 < r) ? br * d[cix][x + 1] : 0.f;
+            l4.z = (!diag || j + 2 < r) ? br * d[cix][x + 2] : 0.f;
+            l4.w = (!diag || j + 3 < r) ? br * d[cix][x + 3] : 0.f;
+            *reinterpret_cast<float4 *>(LF + r * LFS + j) = l4;
           }
         } else {
           uint32_t pkd[8];
@@ -475,10 +499,12 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       // (1) the four 16 x 16 diagonal blocks X_I = (I + L_II)^-1 by forward
       //     substitution: four lanes per column, lane `part` owns rows
       //     part, part + 4, part + 8, part + 12 and the finished entry of
-      //     each step is broadcast inside the 4-lane group.
+      //     each step is broadcast inside the 4-lane group.  The threads of
+      //     blocks 0 and 2 also clear the block to their right, the zero
+      //     upper corner of each 32 x 32 diagonal half.
       {
         const int col = tid >> 2, part = tid & 3;
-        const int base = 16 * (col >> 4), jj = col & 15;
+        const int blk = col >> 4, base = 16 * blk, jj = col & 15;
         float x[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) x[a] = (part + 4 * a == jj) ? 1.f : 0.f;
@@ -492,61 +518,86 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           }
         }
 #pragma unroll
-        for (int a = 0; a < 4; ++a) AF[(base + part + 4 * a) * 65 + base + jj] = x[a];
-      }
-      __syncthreads();
-      // (2) 32 x 32 diagonal halves: X_10 = -X_1 L_10 X_0, X_32 = -X_3 L_32 X_2
-      //     (two outputs per thread: both halves)
-      {
-        const int ii = tid >> 4, jj = tid & 15;
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const int rI = 32 * pr + 16, cJ = 32 * pr;
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; m += 2) {
-            a0 = fmaf(LF[(rI + ii) * LFS + cJ + m], AF[(cJ + m) * 65 + cJ + jj], a0);
-            a1 = fmaf(LF[(rI + ii) * LFS + cJ + m + 1], AF[(cJ + m + 1) * 65 + cJ + jj], a1);
-          }
-          TT[(16 * pr + ii) * 33 + jj] = a0 + a1;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const int rI = 32 * pr + 16, cJ = 32 * pr;
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; m += 2) {
-            a0 = fmaf(AF[(rI + ii) * 65 + rI + m], TT[(16 * pr + m) * 33 + jj], a0);
-            a1 = fmaf(AF[(rI + ii) * 65 + rI + m + 1], TT[(16 * pr + m + 1) * 33 + jj], a1);
-          }
-          AF[(rI + ii) * 65 + cJ + jj] = -(a0 + a1);
+        for (int a = 0; a < 4; ++a) {
+          AF[(base + part + 4 * a) * LFS + base + jj] = x[a];
+          if ((blk & 1) == 0) AF[(base + part + 4 * a) * LFS + base + 16 + jj] = 0.f;
         }
       }
       __syncthreads();
-      // (3) lower-left 32 x 32 block: A_21 = -A_2 (L_21 A_1)  (4 outputs per thread)
+      // (2) 32 x 32 diagonal halves: X_10 = -X_1 (L_10 X_0), X_32 = -X_3 (L_32 X_2);
+      //     thread = (half, row, column pair)
       {
-        const int ii = tid >> 3, jj = tid & 7;  // rows 0..31, columns jj + 8 c
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int pr = tid >> 7, ii = (tid >> 3) & 15, jc = 2 * (tid & 7);
+        const int rI = 32 * pr + 16, cJ = 32 * pr;
+        float *T2 = TT + pr * 16 * TTS;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          const float l = LF[(32 + ii) * LFS + m];
+        for (int m = 0; m < 16; m += 4) {
+          const float4 l = *reinterpret_cast<const float4 *>(LF + (rI + ii) * LFS + cJ + m);
+          const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) acc[c] = fmaf(l, AF[m * 65 + jj + 8 * c], acc[c]);
+          for (int mm = 0; mm < 4; ++mm) {
+            const float2 x = *reinterpret_cast<const float2 *>(AF + (cJ + m + mm) * LFS + cJ + jc);
+            a0 = fmaf(lv[mm], x.x, a0);
+            a1 = fmaf(lv[mm], x.y, a1);
+          }
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) TT[ii * 33 + jj + 8 * c] = acc[c];
+        *reinterpret_cast<float2 *>(T2 + ii * TTS + jc) = make_float2(a0, a1);
         __syncthreads();
+        a0 = a1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] = 0.f;
+        for (int m = 0; m < 16; m += 4) {
+          const float4 l = *reinterpret_cast<const float4 *>(AF + (rI + ii) * LFS + rI + m);
+          const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          const float xv = AF[(32 + ii) * 65 + 32 + m];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[c] = fmaf(xv, TT[m * 33 + jj + 8 * c], acc[c]);
+          for (int mm = 0; mm < 4; ++mm) {
+            const float2 x = *reinterpret_cast<const float2 *>(T2 + (m + mm) * TTS + jc);
+            a0 = fmaf(lv[mm], x.x, a0);
+            a1 = fmaf(lv[mm], x.y, a1);
+          }
         }
+        *reinterpret_cast<float2 *>(AF + (rI + ii) * LFS + cJ + jc) = make_float2(-a0, -a1);
+      }
+      __syncthreads();
+      // (3) lower-left 32 x 32 block: A_21 = -A_2 (L_21 A_1); thread = 2 x 2
+      //     outputs (rows 2 i2, 2 i2 + 1; columns 2 j2, 2 j2 + 1)
+      {
+        const int i2 = 2 * (tid >> 4), j2 = 2 * (tid & 15);
+        float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) AF[(32 + ii) * 65 + jj + 8 * c] = -acc[c];
+        for (int m = 0; m < 32; m += 4) {
+          const float4 l0 = *reinterpret_cast<const float4 *>(LF + (32 + i2) * LFS + m);
+          const float4 l1 = *reinterpret_cast<const float4 *>(LF + (33 + i2) * LFS + m);
+          const float lv0[4] = {l0.x, l0.y, l0.z, l0.w}, lv1[4] = {l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            const float2 x = *reinterpret_cast<const float2 *>(AF + (m + mm) * LFS + j2);
+            c00 = fmaf(lv0[mm], x.x, c00);
+            c01 = fmaf(lv0[mm], x.y, c01);
+            c10 = fmaf(lv1[mm], x.x, c10);
+            c11 = fmaf(lv1[mm], x.y, c11);
+          }
+        }
+        *reinterpret_cast<float2 *>(TT + i2 * TTS + j2) = make_float2(c00, c01);
+        *reinterpret_cast<float2 *>(TT + (i2 + 1) * TTS + j2) = make_float2(c10, c11);
+        __syncthreads();
+        c00 = c01 = c10 = c11 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 32; m += 4) {
+          const float4 l0 = *reinterpret_cast<const float4 *>(AF + (32 + i2) * LFS + 32 + m);
+          const float4 l1 = *reinterpret_cast<const float4 *>(AF + (33 + i2) * LFS + 32 + m);
+          const float lv0[4] = {l0.x, l0.y, l0.z, l0.w}, lv1[4] = {l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            const float2 x = *reinterpret_cast<const float2 *>(TT + (m + mm) * TTS + j2);
+            c00 = fmaf(lv0[mm], x.x, c00);
+            c01 = fmaf(lv0[mm], x.y, c01);
+            c10 = fmaf(lv1[mm], x.x, c10);
+            c11 = fmaf(lv1[mm], x.y, c11);
+          }
+        }
+        *reinterpret_cast<float2 *>(AF + (32 + i2) * LFS + j2) = make_float2(-c00, -c01);
+        *reinterpret_cast<float2 *>(AF + (33 + i2) * LFS + j2) = make_float2(-c10, -c11);
       }
       __syncthreads();
       // A . diag(beta) -> bf16 K-major tile (two 8-column groups per thread)
@@ -557,8 +608,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
         for (int x = 0; x < 8; x += 2) {
           const int jj = 8 * g + x;
-          const float a0 = (jj <= r) ? AF[r * 65 + jj] * sbeta[jj] : 0.f;
-          const float a1 = (jj + 1 <= r) ? AF[r * 65 + jj + 1] * sbeta[jj + 1] : 0.f;
+          const float a0 = (jj <= r) ? AF[r * LFS + jj] * sbeta[jj] : 0.f;
+          const float a1 = (jj + 1 <= r) ? AF[r * LFS + jj + 1] * sbeta[jj + 1] : 0.f;
           pkd[x / 2] = pack_bf16(a0, a1);
         }
         *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(64, r, 8 * g)) =
@@ -592,6 +643,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     ok = wait_or_flag(bar_mma, mma_phase, err);
     if (ok) { mma_pending = false; mma_phase ^= 1; }
     else *abort_flag = 1;
+    // the Aqk image must be read out before the U staging overwrites it
+    if (tid == 0) bulk_wait_read();
     tc::tc_fence_after();
     __syncthreads();
     if (*abort_flag) break;
