@@ -45,10 +45,13 @@ constexpr uint32_t S_B2A = 90112;    // k^ 2^G, MN-major (16384)
 // after the first MMA the OPA/B1 region is reused:
 constexpr int LFS = 68;              // row stride of L and A (16-byte aligned rows)
 constexpr int TTS = 36;              // row stride of the product scratch
-constexpr uint32_t S_LF = 16384;     // fp32 L [64][68]
-constexpr uint32_t S_AF = 33792;     // fp32 A [64][68]
+constexpr uint32_t S_AF = 16384;     // fp32 A [64][68]
+constexpr uint32_t S_LF = 33792;     // fp32 L [64][68]
 constexpr uint32_t S_TT = 51200;     // fp32 scratch [32][36]
-constexpr uint32_t S_AINV = 56320;   // bf16 A.diag(beta), K-major 64 rows (8192)
+// A' = A.diag(beta) as the block-diagonal operand [A' 0; 0 A'] of the second
+// MMA: K-major, two 64-column panels of 128 rows (32768); written after the
+// inverse, over L and the scratch
+constexpr uint32_t S_AINV = 33792;
 // staging of package parts for bulk stores (regions free at that time):
 constexpr uint32_t S_STG_AQK = 73728;  // Aqk image (8192), written after MMA 1 (B1 dead)
 constexpr uint32_t S_STG_W = 90112;    // w rows of WQ, 2 panels x 8192, after MMA 2 (B2A dead)
@@ -70,6 +73,12 @@ constexpr uint32_t B1_PANEL = 160 * 128;
 constexpr uint32_t TMEM_COLS = 256;
 
 __device__ __forceinline__ int b1_off(int Rp) { return 8 * Rp * (Rp - 1); }  // 0, 16, 48
+
+// Rows of the first MMA's A operand (= TMEM lanes of D1) hold the 16-token
+// blocks in the order 0, 3, 1, 2, so that each 32-lane quarter holds one
+// block with few and one with many D1 column blocks to read.
+__device__ __forceinline__ int lane_block(int Rt) { return (0x1320 >> (4 * Rt)) & 3; }   // 0,2,3,1
+__device__ __forceinline__ int token_block(int Lb) { return (0x2130 >> (4 * Lb)) & 3; }  // 0,3,1,2
 
 struct Item {
   int n, len, h;
@@ -209,6 +218,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     //      of each 8-row group
     float Gl[8][4];
     const uint32_t kp128 = pan * 128u * 128u, kp160 = pan * B1_PANEL, kp64 = pan * 64u * 128u;
+    const int prow0 = 16 * lane_block(R) + 8 * (warp & 1);  // OPA row of this thread's first row
     {
       uint2 qv[8], kv[8];
       float4 xs[8];
@@ -266,9 +276,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       if (tid < 64) sbeta[tid] = (sig && tid < len) ? 1.f / (1.f + tc::ex2(-bload * kLog2e)) : bload;
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
-        const uint32_t rowb = (uint32_t)(8 * warp + rr) * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
-        st_u64(sm + S_OPA, kp128 + rowb, kv[rr]);
-        st_u64(sm + S_OPA, kp128 + 64u * 128u + rowb, qv[rr]);
+        const uint32_t orow = (uint32_t)(prow0 + rr) * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
+        st_u64(sm + S_OPA, kp128 + orow, kv[rr]);
+        st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, qv[rr]);
       }
 
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -345,10 +355,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         const int r = 8 * warp + rr;
         const uint32_t xo = ((ch16 ^ (uint32_t)rr) << 4) | cbyte;
         const uint32_t rowb = (uint32_t)r * 128u + xo;
+        const uint32_t orow = (uint32_t)(prow0 + rr) * 128u + xo;
         const float sq = rq[r], sk = rk[r];
         // raw rows parked by this thread in phase 1
-        const uint2 qraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + 64u * 128u + rowb);
-        const uint2 kraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + rowb);
+        const uint2 qraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + 64u * 128u + orow);
+        const uint2 kraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + orow);
         const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw);
         const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kraw);
         const float2 qa = __bfloat1622float2(q2[0]), qb = __bfloat1622float2(q2[1]);
@@ -366,8 +377,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           kd[j] = kn[j] * ea;
           qg[j] = qn[j] * ea * gp.scale;
         }
-        st_u64(sm + S_OPA, kp128 + rowb, pack4(ke[0], ke[1], ke[2], ke[3]));
-        st_u64(sm + S_OPA, kp128 + 64u * 128u + rowb, pack4(qe[0], qe[1], qe[2], qe[3]));
+        st_u64(sm + S_OPA, kp128 + orow, pack4(ke[0], ke[1], ke[2], ke[3]));
+        st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, pack4(qe[0], qe[1], qe[2], qe[3]));
         st_u64(sm + S_B1, kp160 + 96u * 128u + rowb, pack4(kf[0], kf[1], kf[2], kf[3]));
 #pragma unroll
         for (int Rp = 1; Rp < 4; ++Rp)
@@ -412,8 +423,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       const int q4 = warp & 3, cq = warp >> 2;
       const int m = 32 * q4 + lane;          // D1 row = TMEM lane
       const bool krow = m < 64;
-      const int r = krow ? m : m - 64;
-      const int Rr = r >> 4;
+      const int Rr = token_block((m & 63) >> 4);
+      const int r = 16 * Rr + (m & 15);
       float *LF = reinterpret_cast<float *>(sm + S_LF);
       const float br = sbeta[r];
       uint8_t *saqk = sm + S_STG_AQK;
@@ -425,14 +436,14 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           *reinterpret_cast<uint4 *>(saqk + kmaj_off(64, r, 16 * gi + 8)) = z;
         }
       }
-      // column blocks of D1 this warp reads: rows 0..31 (sub-blocks 0, 1)
-      // need blocks 0, 6, 7; rows 32..63 (sub-blocks 2, 3) need 1..5, 8, 9
+      // column blocks of D1 this warp reads: lanes of token blocks 0 and 3
+      // need blocks 6 and 3, 4, 5, 9; those of blocks 1 and 2 need 0, 7 and
+      // 1, 2, 8
       int chs[4] = {-1, -1, -1, -1};
       if ((q4 & 1) == 0) {
-        if (cq == 0) { chs[0] = 0; chs[1] = 7; } else { chs[0] = 6; }
+        if (cq == 0) { chs[0] = 3; chs[1] = 4; chs[2] = 9; } else { chs[0] = 5; chs[1] = 6; }
       } else {
-        if (cq == 0) { chs[0] = 1; chs[1] = 2; chs[2] = 3; chs[3] = 8; }
-        else { chs[0] = 4; chs[1] = 5; chs[2] = 9; }
+        if (cq == 0) { chs[0] = 0; chs[1] = 1; chs[2] = 7; } else { chs[0] = 2; chs[1] = 8; }
       }
 #pragma unroll
       for (int bt = 0; bt < 2; ++bt) {
@@ -600,7 +611,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         *reinterpret_cast<float2 *>(AF + (33 + i2) * LFS + j2) = make_float2(-c10, -c11);
       }
       __syncthreads();
-      // A . diag(beta) -> bf16 K-major tile (two 8-column groups per thread)
+      // A . diag(beta) -> bf16, into panel 0 rows 0..63 and panel 1 rows
+      // 64..127 of the block-diagonal operand; zeros elsewhere
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int r = (tid >> 3) + 32 * hh, g = tid & 7;
@@ -612,8 +624,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           const float a1 = (jj + 1 <= r) ? AF[r * LFS + jj + 1] * sbeta[jj + 1] : 0.f;
           pkd[x / 2] = pack_bf16(a0, a1);
         }
-        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(64, r, 8 * g)) =
-            make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+        const uint4 av = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]), z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, r, 8 * g)) = av;
+        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, 64 + r, 64 + 8 * g)) = av;
+        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, 64 + r, 8 * g)) = z;
+        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, r, 64 + 8 * g)) = z;
       }
     }
     tc::fence_proxy_async_smem();
@@ -624,18 +639,18 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     __syncthreads();
     if (*abort_flag) break;
 
-    // ---- MMA 2: w = A' (k^ 2^G) -> cols 0..127, u = A' v -> cols 128..255 (M = 64)
+    // ---- MMA 2: [A' 0; 0 A'] x [k^ 2^G; v] -> D2 (128 x 128): w in rows
+    //      0..63, u in rows 64..127
     if (tid == 0) {
       tc::tc_fence_after();
-      const uint32_t idesc = tc::idesc_bf16_f32(64, 128, false, true);
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 128, false, true);
       const uint32_t a0 = tc::smem_u32(sm + S_AINV);
       const uint32_t bw = tc::smem_u32(sm + S_B2A), bu = tc::smem_u32(sm + S_V);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = tc::smem_desc_sw128(a0 + kk * 32, 16, 1024);
-        tc::mma_bf16(tmem, ad, tc::smem_desc_sw128(bw + kk * 2048, 8192, 1024), idesc, kk > 0);
-        tc::mma_bf16(tmem + 128, ad, tc::smem_desc_sw128(bu + kk * 2048, 8192, 1024), idesc, kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        tc::mma_bf16(tmem, tc::smem_desc_sw128(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                     tc::smem_desc_sw128((kk < 4 ? bw : bu) + (kk & 3) * 2048, 8192, 1024), idesc,
+                     kk > 0);
       tc::mma_commit(bar_mma);
       mma_pending = true;
     }
@@ -655,40 +670,36 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       ++v_issued;
     }
 
-    // ---- read D2 (M = 64 layout: row r in lane (r % 16) + 32 (r / 16)):
-    //      w -> package WQ rows 64..127, u -> package U
+    // ---- read D2: w (lanes 0..63) -> package WQ rows 64..127, u (lanes
+    //      64..127) -> package U; warp = (lane quarter, 64-column half)
     {
-      const int q4 = warp & 3;
-      const bool is_u = warp >= 4;
-      const int r = 16 * q4 + lane;  // valid for lane < 16
+      const int q4 = warp & 3, hf = warp >> 2;
+      const bool is_u = q4 >= 2;
+      const int r = 32 * (q4 & 1) + lane;
 #pragma unroll
-      for (int half = 0; half < 4; ++half) {
+      for (int cp = 0; cp < 2; ++cp) {
         float d[2][16];
         __syncwarp();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
-          tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (is_u ? 128 : 0) + 32 * half + 16 * cc,
-                        d[cc]);
+          tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + 64 * hf + 32 * cp + 16 * cc, d[cc]);
         tc::tmem_ld_wait();
-        if (lane < 16) {
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int col = 32 * half + 16 * cc;  // column inside w or u
-            if (!is_u) {
-              uint32_t pkd[8];
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col = 64 * hf + 32 * cp + 16 * cc;  // column inside w or u
+          if (!is_u) {
+            uint32_t pkd[8];
 #pragma unroll
-              for (int x = 0; x < 16; x += 2) pkd[x / 2] = pack_bf16(d[cc][x], d[cc][x + 1]);
-              // rows 64.. of WQ, panel by panel: same swizzle phase (row % 8)
-              *reinterpret_cast<uint4 *>(sm + S_STG_W + kmaj_off(64, r, col)) =
-                  make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-              *reinterpret_cast<uint4 *>(sm + S_STG_W + kmaj_off(64, r, col + 8)) =
-                  make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
-            } else {
+            for (int x = 0; x < 16; x += 2) pkd[x / 2] = pack_bf16(d[cc][x], d[cc][x + 1]);
+            *reinterpret_cast<uint4 *>(sm + S_STG_W + kmaj_off(64, r, col)) =
+                make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+            *reinterpret_cast<uint4 *>(sm + S_STG_W + kmaj_off(64, r, col + 8)) =
+                make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+          } else {
 #pragma unroll
-              for (int x = 0; x < 16; x += 4)
-                *reinterpret_cast<float4 *>(sm + S_STG_U + u_offset(r, col + x)) =
-                    make_float4(d[cc][x], d[cc][x + 1], d[cc][x + 2], d[cc][x + 3]);
-            }
+            for (int x = 0; x < 16; x += 4)
+              *reinterpret_cast<float4 *>(sm + S_STG_U + u_offset(r, col + x)) =
+                  make_float4(d[cc][x], d[cc][x + 1], d[cc][x + 2], d[cc][x + 3]);
           }
         }
       }
