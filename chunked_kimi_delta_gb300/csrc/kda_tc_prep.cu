@@ -48,9 +48,8 @@ constexpr int TTS = 36;              // row stride of the product scratch
 constexpr uint32_t S_AF = 16384;     // fp32 A [64][68]
 constexpr uint32_t S_LF = 33792;     // fp32 L [64][68]
 constexpr uint32_t S_TT = 51200;     // fp32 scratch [32][36]
-// A' = A.diag(beta) as the block-diagonal operand [A' 0; 0 A'] of the second
-// MMA: K-major, two 64-column panels of 128 rows (32768); written after the
-// inverse, over L and the scratch
+// A' = A.diag(beta) stacked twice, [A'; A'] (K-major, 128 rows, 16384): the
+// A operand of both second-stage MMAs; written after the inverse, over L
 constexpr uint32_t S_AINV = 33792;
 // staging of package parts for bulk stores (regions free at that time):
 constexpr uint32_t S_STG_AQK = 73728;  // Aqk image (8192), written after MMA 1 (B1 dead)
@@ -59,7 +58,7 @@ constexpr uint32_t S_STG_U = 49152;    // U image (32768), after MMA 2 (B1 dead)
 // OPA holds nothing between items: phase 1 parks the raw q and k rows there,
 // at the positions phase 2 overwrites with the scaled operands.
 constexpr uint32_t S_MISC = 106496;
-constexpr uint32_t M_RQ = S_MISC;           // fp32 [64] rstd q
+constexpr uint32_t M_RQ = S_MISC;           // fp32 [64] scale x rstd q
 constexpr uint32_t M_RK = S_MISC + 256;     // fp32 [64] rstd k
 constexpr uint32_t M_BETA = S_MISC + 512;   // fp32 [64]
 constexpr uint32_t M_TOT = S_MISC + 768;    // fp32 [8][128] row-group gate totals
@@ -121,6 +120,11 @@ __device__ __forceinline__ void st_u64(uint8_t *base, uint32_t off, uint2 v) {
 
 __device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
   return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
+}
+
+// Barrier over the 128 threads of one half of the CTA (ids 1, 2).
+__device__ __forceinline__ void half_sync(int half) {
+  asm volatile("bar.sync %0, 128;" :: "r"(1 + half) : "memory");
 }
 
 template <typename T>
@@ -238,9 +242,10 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       float bload = 0.f;
       if (tid < 64 && tid < len) bload = beta[(t0 + tid) * H + h];
       const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
-      float db[4];
+      float dbl[4];  // dt_bias in log2 units
 #pragma unroll
-      for (int j = 0; j < 4; ++j) db[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + j] : 0.f;
+      for (int j = 0; j < 4; ++j)
+        dbl[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + j] * kLog2e : 0.f;
 
       float v[16];
 #pragma unroll
@@ -271,7 +276,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
                         ((lane >> 1) & 1);
         const int r = 8 * warp + (idx & 7);
         const float nv = r < len ? (l2n ? rsqrtf(v[0] + gp.eps) : 1.f) : 0.f;
-        (idx < 8 ? rq : rk)[r] = nv;
+        if (idx < 8) rq[r] = nv * gp.scale;  // q rows carry the attention scale
+        else rk[r] = nv;
       }
       if (tid < 64) sbeta[tid] = (sig && tid < len) ? 1.f / (1.f + tc::ex2(-bload * kLog2e)) : bload;
 #pragma unroll
@@ -291,7 +297,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           float g;
           if (gate) {
             // softplus(z) log2 e = max(z, 0) log2 e + log2(1 + 2^{-|z| log2 e})
-            const float z = (xv[j] + db[j]) * kLog2e;
+            const float z = fmaf(xv[j], kLog2e, dbl[j]);
             g = -A_h * (fmaxf(z, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z))));
           } else {
             g = xv[j] * kLog2e;
@@ -335,14 +341,14 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
           for (int j = 0; j < 4; ++j) Gl[rr][j] += prev[j];
       }
-      float bRv[4], egc[4], cR[4][4];
+      float eb[4], egc[4], cR[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float bR = bAll[0][j];
 #pragma unroll
         for (int RR = 1; RR < 4; ++RR)
           if (RR == R) bR = bAll[RR][j];
-        bRv[j] = bR;
+        eb[j] = tc::ex2(bR);
         egc[j] = tc::ex2(GC[j] - bR);
 #pragma unroll
         for (int RR = 1; RR < 4; ++RR) cR[RR][j] = tc::ex2(fminf(bAll[RR][j] - bR, 0.f));
@@ -370,12 +376,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float e = tc::ex2(Gl[rr][j]), f = tc::ex2(fminf(-Gl[rr][j], 126.f));
-          const float ea = tc::ex2(Gl[rr][j] + bRv[j]);  // 2^G, G from the chunk start
           ke[j] = kn[j] * e;
           kf[j] = kn[j] * f;
           qe[j] = qn[j] * e;
-          kd[j] = kn[j] * ea;
-          qg[j] = qn[j] * ea * gp.scale;
+          kd[j] = ke[j] * eb[j];  // k^ 2^G, G from the chunk start
+          qg[j] = qe[j] * eb[j];  // scale q^ 2^G
         }
         st_u64(sm + S_OPA, kp128 + orow, pack4(ke[0], ke[1], ke[2], ke[3]));
         st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, pack4(qe[0], qe[1], qe[2], qe[3]));
@@ -482,8 +487,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
           for (int x = 0; x < 16; x += 2) {
             const int j = j0 + x;
-            const float a0 = (!diag || j <= r) ? gp.scale * d[cix][x] : 0.f;
-            const float a1 = (!diag || j + 1 <= r) ? gp.scale * d[cix][x + 1] : 0.f;
+            const float a0 = (!diag || j <= r) ? d[cix][x] : 0.f;
+            const float a1 = (!diag || j + 1 <= r) ? d[cix][x + 1] : 0.f;
             pkd[x / 2] = pack_bf16(a0, a1);
           }
           *reinterpret_cast<uint4 *>(saqk + kmaj_off(64, r, j0)) =
@@ -534,7 +539,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           if ((blk & 1) == 0) AF[(base + part + 4 * a) * LFS + base + 16 + jj] = 0.f;
         }
       }
-      __syncthreads();
+      // step (2) of a half reads only that half's diagonal blocks
+      half_sync(warp >> 2);
       // (2) 32 x 32 diagonal halves: X_10 = -X_1 (L_10 X_0), X_32 = -X_3 (L_32 X_2);
       //     thread = (half, row, column pair)
       {
@@ -554,7 +560,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           }
         }
         *reinterpret_cast<float2 *>(T2 + ii * TTS + jc) = make_float2(a0, a1);
-        __syncthreads();
+        half_sync(pr);
         a0 = a1 = 0.f;
 #pragma unroll
         for (int m = 0; m < 16; m += 4) {
@@ -611,8 +617,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         *reinterpret_cast<float2 *>(AF + (33 + i2) * LFS + j2) = make_float2(-c10, -c11);
       }
       __syncthreads();
-      // A . diag(beta) -> bf16, into panel 0 rows 0..63 and panel 1 rows
-      // 64..127 of the block-diagonal operand; zeros elsewhere
+      // A . diag(beta) -> bf16, rows r and 64 + r of [A'; A']
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int r = (tid >> 3) + 32 * hh, g = tid & 7;
@@ -624,11 +629,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           const float a1 = (jj + 1 <= r) ? AF[r * LFS + jj + 1] * sbeta[jj + 1] : 0.f;
           pkd[x / 2] = pack_bf16(a0, a1);
         }
-        const uint4 av = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]), z = make_uint4(0, 0, 0, 0);
+        const uint4 av = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
         *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, r, 8 * g)) = av;
-        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, 64 + r, 64 + 8 * g)) = av;
-        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, 64 + r, 8 * g)) = z;
-        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, r, 64 + 8 * g)) = z;
+        *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, 64 + r, 8 * g)) = av;
       }
     }
     tc::fence_proxy_async_smem();
@@ -639,18 +642,19 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     __syncthreads();
     if (*abort_flag) break;
 
-    // ---- MMA 2: [A' 0; 0 A'] x [k^ 2^G; v] -> D2 (128 x 128): w in rows
-    //      0..63, u in rows 64..127
+    // ---- MMA 2: [A'; A'] x k^ 2^G -> D2 columns 0..127 (w in rows 0..63),
+    //      [A'; A'] x v -> columns 128..255 (u in rows 64..127)
     if (tid == 0) {
       tc::tc_fence_after();
       const uint32_t idesc = tc::idesc_bf16_f32(128, 128, false, true);
       const uint32_t a0 = tc::smem_u32(sm + S_AINV);
       const uint32_t bw = tc::smem_u32(sm + S_B2A), bu = tc::smem_u32(sm + S_V);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc::mma_bf16(tmem, tc::smem_desc_sw128(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                     tc::smem_desc_sw128((kk < 4 ? bw : bu) + (kk & 3) * 2048, 8192, 1024), idesc,
-                     kk > 0);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = tc::smem_desc_sw128(a0 + kk * 32, 16, 1024);
+        tc::mma_bf16(tmem, ad, tc::smem_desc_sw128(bw + kk * 2048, 8192, 1024), idesc, kk > 0);
+        tc::mma_bf16(tmem + 128, ad, tc::smem_desc_sw128(bu + kk * 2048, 8192, 1024), idesc, kk > 0);
+      }
       tc::mma_commit(bar_mma);
       mma_pending = true;
     }
@@ -670,8 +674,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       ++v_issued;
     }
 
-    // ---- read D2: w (lanes 0..63) -> package WQ rows 64..127, u (lanes
-    //      64..127) -> package U; warp = (lane quarter, 64-column half)
+    // ---- read D2: w (lanes 0..63 of columns 0..127) -> package WQ rows
+    //      64..127, u (lanes 64..127 of columns 128..255) -> package U;
+    //      warp = (lane quarter, 64-column half)
     {
       const int q4 = warp & 3, hf = warp >> 2;
       const bool is_u = q4 >= 2;
@@ -682,7 +687,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         __syncwarp();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
-          tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + 64 * hf + 32 * cp + 16 * cc, d[cc]);
+          tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (is_u ? 128 : 0) + 64 * hf + 32 * cp + 16 * cc,
+                        d[cc]);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
