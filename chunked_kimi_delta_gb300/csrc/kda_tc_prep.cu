@@ -127,9 +127,34 @@ __device__ __forceinline__ void half_sync(int half) {
   asm volatile("bar.sync %0, 128;" :: "r"(1 + half) : "memory");
 }
 
-template <typename T>
-__device__ __forceinline__ T ldg_stream(const T *p) {
-  return __ldg(p);
+// L2 policy for data touched once - the inputs after their one read, the
+// package (read back only after the whole pass): evicted first, so that it
+// does not push the next items' prefetched inputs out of L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint2 ldg_u2_hint(const void *p, uint64_t pol) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+               : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ float4 ldg_f4_hint(const void *p, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void stg_hint(uint8_t *base, uint32_t off, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;"
+               :: "l"(base + off), "r"(v.x), "r"(v.y), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void bulk_store_hint(void *dst, const void *src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+               :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(tc::smem_u32(src)), "r"(bytes), "l"(pol)
+               : "memory");
 }
 
 __global__ void __launch_bounds__(NT, 2)
@@ -179,6 +204,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   const uint32_t pan = (uint32_t)(lane >> 4);
 
   const int64_t G = gridDim.x;
+  const uint64_t pol_once = policy_evict_first();
   // thread 0 keeps count of the loads and MMAs it started, for the drain
   int64_t v_issued = 0, v_done = 0;
   bool mma_pending = false;
@@ -234,9 +260,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         kv[rr] = make_uint2(0, 0);
         xs[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < len) {
-          qv[rr] = ldg_stream(reinterpret_cast<const uint2 *>(qg_in + off));
-          kv[rr] = ldg_stream(reinterpret_cast<const uint2 *>(kg_in + off));
-          xs[rr] = ldg_stream(reinterpret_cast<const float4 *>(xg_in + off));
+          qv[rr] = ldg_u2_hint(qg_in + off, pol_once);
+          kv[rr] = ldg_u2_hint(kg_in + off, pol_once);
+          xs[rr] = ldg_f4_hint(xg_in + off, pol_once);
         }
       }
       float bload = 0.f;
@@ -392,9 +418,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
                    pack4(kf[0] * cR[Rp][0], kf[1] * cR[Rp][1], kf[2] * cR[Rp][2], kf[3] * cR[Rp][3]));
         st_u64(sm + S_B2A, kp64 + rowb, pack4(kd[0], kd[1], kd[2], kd[3]));
         // package: qg = scale q^ 2^G (WQ rows 0..63), kg = k^ 2^{G_C - G} (KG)
-        st_u64(pk, PK_WQ + kp128 + rowb, pack4(qg[0], qg[1], qg[2], qg[3]));
-        st_u64(pk, PK_KG + kp64 + rowb,
-               pack4(kf[0] * egc[0], kf[1] * egc[1], kf[2] * egc[2], kf[3] * egc[3]));
+        stg_hint(pk, PK_WQ + kp128 + rowb, pack4(qg[0], qg[1], qg[2], qg[3]), pol_once);
+        stg_hint(pk, PK_KG + kp64 + rowb,
+               pack4(kf[0] * egc[0], kf[1] * egc[1], kf[2] * egc[2], kf[3] * egc[3]), pol_once);
       }
     }
     tc::fence_proxy_async_smem();
@@ -503,7 +529,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     tc::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
-      bulk_store(pk + PK_AQK, sm + S_STG_AQK, 8192);
+      bulk_store_hint(pk + PK_AQK, sm + S_STG_AQK, 8192, pol_once);
       bulk_commit();
     }
 
@@ -714,9 +740,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     tc::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
-      bulk_store(pk + PK_WQ + 64 * 128, sm + S_STG_W, 8192);
-      bulk_store(pk + PK_WQ + 16384 + 64 * 128, sm + S_STG_W + 8192, 8192);
-      bulk_store(pk + PK_U, sm + S_STG_U, 32768);
+      bulk_store_hint(pk + PK_WQ + 64 * 128, sm + S_STG_W, 8192, pol_once);
+      bulk_store_hint(pk + PK_WQ + 16384 + 64 * 128, sm + S_STG_W + 8192, 8192, pol_once);
+      bulk_store_hint(pk + PK_U, sm + S_STG_U, 32768, pol_once);
       bulk_commit();
     }
   }
