@@ -24,25 +24,29 @@ namespace tcp {
 constexpr int K = 128, V = 128;
 
 // Package of one (chunk, head), byte offsets.  All tiles are bf16 SW128 except
-// U (fp32, 16-byte chunks of row r permuted by XOR with r % 32) and GC (fp32).
+// U (bf16 rows of 256 bytes, 16-byte chunks of row r permuted by XOR with
+// r % 16) and GC (fp32).
 //   WQ : [qg (rows 0-63); w (rows 64-127)] x 128 channels, K-major, two
 //        64-channel panels of 128 rows           -> A operand of [qg; w] h
+//   U  : u [64 tokens][128] bf16 (the precision of the other WY tiles)
 //   KG : kg = k^ e^{G_C - G} as [token][channel], MN-major, two 64-channel
 //        panels of 64 token rows                  -> A operand of kg^T v_new
 //   AQK: Aqk [64 rows][64 tokens], K-major        -> A operand of Aqk v_new
-//   U  : u [64 tokens][128] fp32
 //   GC : e^{G_C} [128] fp32 (decay of the whole chunk per key channel)
+// WQ and U (read first) and KG, AQK, GC (read last) are contiguous, so that
+// the two halves can be moved separately.
 constexpr uint32_t PK_WQ = 0;
-constexpr uint32_t PK_KG = 32768;
-constexpr uint32_t PK_AQK = 49152;
-constexpr uint32_t PK_U = 57344;
-constexpr uint32_t PK_GC = 90112;
-constexpr uint32_t PK_BYTES = 90624;
+constexpr uint32_t PK_U = 32768;
+constexpr uint32_t PK_KG = 49152;
+constexpr uint32_t PK_AQK = 65536;
+constexpr uint32_t PK_GC = 73728;
+constexpr uint32_t PK_BYTES = 74240;
+constexpr uint32_t PK_FIRST = PK_KG;  // bytes of the first half (WQ, U)
 
 __host__ __device__ __forceinline__ uint32_t u_offset(uint32_t row, uint32_t col) {
-  // fp32 element (row, col) of the U tile
-  const uint32_t chunk = (col >> 2) ^ (row & 31u);
-  return row * 512u + chunk * 16u + (col & 3u) * 4u;
+  // bf16 element (row, col) of the U tile
+  const uint32_t chunk = (col >> 3) ^ (row & 15u);
+  return row * 256u + chunk * 16u + (col & 7u) * 2u;
 }
 
 // K-major SW128 tile with `rows` rows per 64-element K panel: byte offset of

@@ -9,8 +9,16 @@
 //   kg^T v_new       -> U           (tcgen05, M=128, N=128, K=64)
 //   h' = e^{G_C} h + U              (fp32, registers)
 // The fp32 state lives in registers (thread = one key channel x 64 value
-// channels); a bf16 copy in shared memory is the MMA operand.  Packages are
-// double-buffered with bulk copies issued two chunks ahead.
+// channels); a bf16 copy in shared memory is the MMA operand.  Only
+// [qg; w] h -> v_new -> kg^T v_new -> h' is on the recurrence's critical path:
+// warps of lane quarters 2 and 3 compute v_new and signal it through an
+// mbarrier to the thread that issues the MMAs; kg^T v_new commits to its own
+// barrier ahead of Aqk v_new; the output tile P alternates between two TMEM
+// buffers, so the warps of lane quarters 0 and 1 read o of chunk c while the
+// first MMA of chunk c + 1 runs.  Packages are double-buffered in two halves
+// that are refilled as soon as their last reader is done: WQ and U of chunk
+// c + 2 once v_new of chunk c is computed, KG, AQK and GC of chunk c + 1 once
+// the MMAs of chunk c - 1 have finished.
 //
 // Summary mode ("Hyper-Parallel ..." section 5.1, PreProcessFwd; "KDA Context
 // Parallelism (KCP)"): the same chain on the augmented state [S~ | M] with
@@ -26,20 +34,25 @@ namespace {
 
 constexpr int NT = 256;
 constexpr uint32_t S_BUF0 = 0;
-constexpr uint32_t S_BAR = PK_BYTES;         // 3 mbarriers in the gap before buffer 1
-constexpr uint32_t S_BUF1 = 91136;           // 1024-aligned
-constexpr uint32_t S_HB = 182272;            // h bf16, MN-major (K = 128 channels)
-constexpr uint32_t S_VN = 215040;            // v_new bf16, MN-major (K = 64 tokens)
-constexpr uint32_t SMEM_BYTES = 231424 + 1024;
+constexpr uint32_t S_BAR = PK_BYTES;         // mbarriers in the gap before buffer 1
+constexpr uint32_t S_BUF1 = 74752;           // 1024-aligned
+constexpr uint32_t S_HB = 149504;            // h bf16, MN-major (K = 128 channels)
+constexpr uint32_t S_VN = 182272;            // v_new bf16, MN-major (K = 64 tokens)
+constexpr uint32_t SMEM_BYTES = 198656 + 1024;
 constexpr uint32_t BUF_STRIDE = S_BUF1 - S_BUF0;
+constexpr uint32_t TMEM_COLS = 512;          // P (two buffers) and U
 
 template <int MODE>
 __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s, int H) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(sm + S_BAR);  // [2]
-  uint64_t *bar_mma = full + 2;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(full + 3);
+  uint64_t *fullA = reinterpret_cast<uint64_t *>(sm + S_BAR);  // [2] WQ, U of a buffer
+  uint64_t *fullB = fullA + 2;   // [2] KG, AQK, GC of a buffer
+  uint64_t *bar_ma = fullA + 4;  // [qg; w] h
+  uint64_t *bar_mc = fullA + 5;  // kg^T v_new
+  uint64_t *bar_mb = fullA + 6;  // Aqk v_new
+  uint64_t *vn_ready = fullA + 7;  // v_new of the chunk is in shared memory (4 warp arrivals)
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(fullA + 8);
   volatile uint32_t *abort_flag = tslot + 1;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -54,13 +67,18 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   const int64_t unit = (int64_t)n * H + h;
 
   if (warp == 0) {
-    tc::tmem_alloc(tslot, 256);
+    tc::tmem_alloc(tslot, TMEM_COLS);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(full, 1);
-    tc::mbar_init(full + 1, 1);
-    tc::mbar_init(bar_mma, 1);
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(fullA + x, 1);
+      tc::mbar_init(fullB + x, 1);
+    }
+    tc::mbar_init(bar_ma, 1);
+    tc::mbar_init(bar_mc, 1);
+    tc::mbar_init(bar_mb, 1);
+    tc::mbar_init(vn_ready, 4);
     tc::mbar_fence_init();
     *abort_flag = 0;
   }
@@ -97,39 +115,83 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tP = tmem, tU = tmem + 128;
+  const uint32_t tU = tmem + 256;  // P buffers at columns 0 and 128
 
-  // thread 0 keeps count of the copies and MMAs it started, for the drain
-  int64_t loads_issued = 0, loads_done = 0;
-  bool mma_pending = false;
-  if (tid == 0) {
+  // thread LEAD (lane 0 of the first v_new warp) starts the package copies
+  // and the MMAs and keeps count of them, for the drain.  Buffer b holds
+  // chunks b, b + 2, ...; its first half (WQ, U) is free once v_new of its
+  // chunk is done, its second half (KG, AQK, GC) once the chunk's last MMA is.
+  constexpr int LEAD = 64;
+  int64_t a_issued = 0, a_done = 0, b_issued = 0, b_done = 0;
+  auto load_a = [&](int64_t cc) {
+    const int bb = (int)(cc & 1);
+    tc::mbar_arrive_expect_tx(fullA + bb, PK_FIRST);
+    bulk_load(sm + S_BUF0 + bb * BUF_STRIDE, a.pkg + (size_t)((c0 + cc) * H + h) * PK_BYTES, PK_FIRST,
+              fullA + bb);
+    ++a_issued;
+  };
+  auto load_b = [&](int64_t cc) {
+    const int bb = (int)(cc & 1);
+    tc::mbar_arrive_expect_tx(fullB + bb, PK_BYTES - PK_FIRST);
+    bulk_load(sm + S_BUF0 + bb * BUF_STRIDE + PK_FIRST,
+              a.pkg + (size_t)((c0 + cc) * H + h) * PK_BYTES + PK_FIRST, PK_BYTES - PK_FIRST, fullB + bb);
+    ++b_issued;
+  };
+  bool ma_pending = false, mc_pending = false, mb_issued = false;
+  uint32_t ma_par = 0, mc_par = 0, mb_par = 0;  // parity of the last completion
+  if (tid == LEAD) {
     for (int64_t c = 0; c < 2 && c < nch; ++c) {
-      ++loads_issued;
-      tc::mbar_arrive_expect_tx(full + c, PK_BYTES);
-      bulk_load(sm + S_BUF0 + c * BUF_STRIDE, a.pkg + (size_t)((c0 + c) * H + h) * PK_BYTES, PK_BYTES,
-                full + c);
+      load_a(c);
+      load_b(c);
     }
   }
 
-  uint32_t mph = 0;
+  // o of a finished chunk: P rows 0..63 of its buffer, by the warps of lane
+  // quarters 0 and 1 once Aqk v_new has landed (Mb completion number cp)
+  auto read_o = [&](int64_t cp, int lenp) {
+    // tcgen05.ld needs the whole warp: act on a warp-uniform verdict
+    const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar_mb, (uint32_t)(cp & 1), a.err));
+    if (!ok) { *abort_flag = 1; return; }
+    tc::tc_fence_after();
+    const uint32_t tPp = tmem + 128u * (uint32_t)(cp & 1);
+    const int r = 32 * q4 + lane;
+    const int64_t tcp = t0 + cp * BT;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float d[16];
+      __syncwarp();
+      tc::tmem_ld16(tPp + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
+      tc::tmem_ld_wait();
+      if (r < lenp) {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                               ((tcp + r) * H + h) * V + 64 * hf + 16 * cc);
+        dst[0] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                            pack_bf16(d[6], d[7]));
+        dst[1] = make_uint4(pack_bf16(d[8], d[9]), pack_bf16(d[10], d[11]), pack_bf16(d[12], d[13]),
+                            pack_bf16(d[14], d[15]));
+      }
+    }
+  };
+
   for (int64_t c = 0; c < nch; ++c) {
     const int b = (int)(c & 1);
     uint8_t *buf = sm + S_BUF0 + b * BUF_STRIDE;
     const int64_t tc0 = t0 + c * BT;
     const int len = (int)((t1 - tc0) < BT ? (t1 - tc0) : BT);
-    bool ok = wait_or_flag(full + b, (uint32_t)((c >> 1) & 1), a.err);
+    const uint32_t tP = tmem + 128u * (uint32_t)b;
+    bool ok = wait_or_flag(fullA + b, (uint32_t)((c >> 1) & 1), a.err);
     if (!ok) *abort_flag = 1;
-    else loads_done = c + 1;
+    else if (tid == LEAD) a_done = c + 1;
     if (MODE == CHAIN_FWD && a.h_out) {
       float4 *dst = reinterpret_cast<float4 *>(a.h_out + (((c0 + c) * H + h) * K + kr) * V + 64 * hf);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
     }
-    __syncthreads();
+    __syncthreads();  // h (bf16) of this chunk and the package are in place
     if (*abort_flag) break;
 
-    // ---- [qg; w] h -> P
-    if (tid == 0) {
+    // ---- [qg; w] h -> P (this chunk's buffer)
+    if (tid == LEAD) {
       tc::tc_fence_after();
       const uint32_t idesc = tc::idesc_bf16_f32(128, 128, false, true);
       const uint32_t a0 = tc::smem_u32(buf + PK_WQ), b0 = tc::smem_u32(sm + S_HB);
@@ -137,19 +199,29 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
       for (int kk = 0; kk < 8; ++kk)
         tc::mma_bf16(tP, tc::smem_desc_sw128(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                      tc::smem_desc_sw128(b0 + kk * 2048, 16384, 1024), idesc, kk > 0);
-      tc::mma_commit(bar_mma);
-      mma_pending = true;
+      tc::mma_commit(bar_ma);
+      ma_pending = true;
+      ma_par = (uint32_t)(c & 1);
     }
-    __syncwarp();
-    ok = wait_or_flag(bar_mma, mph, a.err);
-    if (ok) { mma_pending = false; mph ^= 1; }
-    else *abort_flag = 1;
-    tc::tc_fence_after();
-    __syncthreads();
-    if (*abort_flag) break;
+    // warps of lane quarters 0 and 1: o of the previous chunk, off the
+    // recurrence's critical path
+    if (MODE == CHAIN_FWD && q4 < 2 && c > 0) read_o(c - 1, BT);
 
-    // ---- v_new = u - w h  (P rows 64..127 live in TMEM lanes 64..127)
+    // ---- v_new = u - w h  (P rows 64..127 live in TMEM lanes 64..127), by
+    //      the warps of lane quarters 2 and 3
     if (q4 >= 2) {
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, wait_or_flag(bar_ma, (uint32_t)(c & 1), a.err));
+      if (tid == LEAD && ok) {
+        ma_pending = false;
+        // every MMA of chunk c - 1 has finished: the second half of its
+        // buffer takes chunk c + 1
+        if (c > 0 && c + 1 < nch && !*abort_flag) load_b(c + 1);
+      }
+      if (!ok) *abort_flag = 1;
+      tc::tc_fence_after();
+    }
+    if (ok && q4 >= 2) {
       const int r = 32 * (q4 - 2) + lane;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -159,15 +231,19 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
         tc::tmem_ld_wait();
         const int col = 64 * hf + 16 * cc;
         float vn[16];
+        if (MODE == CHAIN_SUMMARY && part == 1) {
 #pragma unroll
-        for (int x = 0; x < 16; x += 4) {
-          float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!(MODE == CHAIN_SUMMARY && part == 1))
-            u4 = *reinterpret_cast<const float4 *>(buf + PK_U + u_offset(r, col + x));
-          vn[x] = u4.x - d[x];
-          vn[x + 1] = u4.y - d[x + 1];
-          vn[x + 2] = u4.z - d[x + 2];
-          vn[x + 3] = u4.w - d[x + 3];
+          for (int x = 0; x < 16; ++x) vn[x] = -d[x];
+        } else {
+          const uint4 ua = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, col));
+          const uint4 ub = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, col + 8));
+          const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const float2 u2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[x]));
+            vn[2 * x] = u2.x - d[2 * x];
+            vn[2 * x + 1] = u2.y - d[2 * x + 1];
+          }
         }
         *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col)) =
             make_uint4(pack_bf16(vn[0], vn[1]), pack_bf16(vn[2], vn[3]), pack_bf16(vn[4], vn[5]),
@@ -182,16 +258,40 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
         }
       }
     }
-    tc::tc_fence_before();
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (*abort_flag) break;
+    if (q4 >= 2) {
+      // publish v_new (generic writes, read by the tensor cores) and the end
+      // of this warp's TMEM reads of P
+      tc::tc_fence_before();
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(vn_ready);
+    }
 
-    // ---- P[0:64] += Aqk v_new (rows 64..127 of the A operand are unused),
-    //      kg^T v_new -> U
-    if (tid == 0) {
+    // ---- kg^T v_new -> U (critical path, own barrier), then
+    //      P[0:64] += Aqk v_new (rows 64..127 of the A operand are unused)
+    bool go = false;
+    if (tid == LEAD) {
+      go = !*abort_flag && wait_or_flag(vn_ready, (uint32_t)(c & 1), a.err);
+      if (go) {
+        // WQ and U of this chunk are consumed: the first half takes chunk c + 2
+        if (c + 2 < nch) load_a(c + 2);
+        go = wait_or_flag(fullB + b, (uint32_t)((c >> 1) & 1), a.err);
+        if (go) b_done = c + 1;
+      }
+      if (!go) *abort_flag = 1;
+    }
+    if (go) {
       tc::tc_fence_after();
       const uint32_t vn0 = tc::smem_u32(sm + S_VN);
+      const uint32_t idc = tc::idesc_bf16_f32(128, 128, true, true);
+      const uint32_t g0 = tc::smem_u32(buf + PK_KG);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16(tU, tc::smem_desc_sw128(g0 + kk * 2048, 8192, 1024),
+                     tc::smem_desc_sw128(vn0 + kk * 2048, 8192, 1024), idc, kk > 0);
+      tc::mma_commit(bar_mc);
+      mc_pending = true;
+      mc_par = (uint32_t)(c & 1);
       if (MODE == CHAIN_FWD) {
         const uint32_t idb = tc::idesc_bf16_f32(128, 128, false, true);
         const uint32_t q0 = tc::smem_u32(buf + PK_AQK);
@@ -199,26 +299,20 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_bf16(tP, tc::smem_desc_sw128(q0 + kk * 32, 16, 1024),
                        tc::smem_desc_sw128(vn0 + kk * 2048, 8192, 1024), idb, true);
+        tc::mma_commit(bar_mb);
+        mb_issued = true;
+        mb_par = (uint32_t)(c & 1);
       }
-      const uint32_t idc = tc::idesc_bf16_f32(128, 128, true, true);
-      const uint32_t g0 = tc::smem_u32(buf + PK_KG);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc::mma_bf16(tU, tc::smem_desc_sw128(g0 + kk * 2048, 8192, 1024),
-                     tc::smem_desc_sw128(vn0 + kk * 2048, 8192, 1024), idc, kk > 0);
-      tc::mma_commit(bar_mma);
-      mma_pending = true;
     }
     __syncwarp();
-    ok = wait_or_flag(bar_mma, mph, a.err);
-    if (ok) { mma_pending = false; mph ^= 1; }
-    else *abort_flag = 1;
-    tc::tc_fence_after();
-    __syncthreads();
-    if (*abort_flag) break;
-
-    // ---- h' = e^{G_C} h + kg^T v_new
-    {
+    ok = __all_sync(0xffffffffu, wait_or_flag(bar_mc, (uint32_t)(c & 1), a.err));
+    if (tid == LEAD && ok) mc_pending = false;
+    if (!ok) {
+      *abort_flag = 1;
+    } else {
+      tc::tc_fence_after();
+      wait_or_flag(fullB + b, (uint32_t)((c >> 1) & 1), a.err);  // complete: acquires GC
+      // ---- h' = e^{G_C} h + kg^T v_new
       const float gcv = reinterpret_cast<const float *>(buf + PK_GC)[kr];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -230,35 +324,13 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
       }
       store_hb();
     }
-    // ---- o = qg h + Aqk v_new (P rows 0..63)
-    if (MODE == CHAIN_FWD && q4 < 2) {
-      const int r = 32 * q4 + lane;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float d[16];
-        __syncwarp();
-        tc::tmem_ld16(tP + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
-        tc::tmem_ld_wait();
-        if (r < len) {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
-                                                 ((tc0 + r) * H + h) * V + 64 * hf + 16 * cc);
-          dst[0] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
-                              pack_bf16(d[6], d[7]));
-          dst[1] = make_uint4(pack_bf16(d[8], d[9]), pack_bf16(d[10], d[11]),
-                              pack_bf16(d[12], d[13]), pack_bf16(d[14], d[15]));
-        }
-      }
-    }
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (*abort_flag) break;
-    if (tid == 0 && c + 2 < nch) {
-      ++loads_issued;
-      tc::mbar_arrive_expect_tx(full + b, PK_BYTES);
-      bulk_load(buf, a.pkg + (size_t)((c0 + c + 2) * H + h) * PK_BYTES, PK_BYTES, full + b);
-    }
   }
+  // o of the last chunk
+  __syncthreads();
+  if (MODE == CHAIN_FWD && nch > 0 && !*abort_flag && q4 < 2) read_o(nch - 1, (int)(t1 - (t0 + (nch - 1) * BT)));
+  __syncthreads();
 
   if (*abort_flag == 0) {
     if (MODE == CHAIN_FWD) {
@@ -273,15 +345,18 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
     }
-  } else if (tid == 0) {
-    // a wait gave up: let the copies and the MMA this CTA started finish
-    // (each wait bounded) before its shared and tensor memory are released
-    if (mma_pending) drain_wait(bar_mma, mph);
-    for (int64_t c = loads_done; c < loads_issued; ++c) drain_wait(full + (c & 1), (uint32_t)((c >> 1) & 1));
+  } else if (tid == LEAD) {
+    // a wait gave up: let the MMAs and copies this CTA started finish (each
+    // wait bounded) before its tensor and shared memory are released
+    if (ma_pending) drain_wait(bar_ma, ma_par);
+    if (mc_pending) drain_wait(bar_mc, mc_par);
+    if (mb_issued) drain_wait(bar_mb, mb_par);
+    for (int64_t c = a_done; c < a_issued; ++c) drain_wait(fullA + (c & 1), (uint32_t)((c >> 1) & 1));
+    for (int64_t c = b_done; c < b_issued; ++c) drain_wait(fullB + (c & 1), (uint32_t)((c >> 1) & 1));
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
 }  // namespace

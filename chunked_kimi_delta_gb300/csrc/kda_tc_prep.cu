@@ -54,7 +54,7 @@ constexpr uint32_t S_AINV = 33792;
 // staging of package parts for bulk stores (regions free at that time):
 constexpr uint32_t S_STG_AQK = 73728;  // Aqk image (8192), written after MMA 1 (B1 dead)
 constexpr uint32_t S_STG_W = 90112;    // w rows of WQ, 2 panels x 8192, after MMA 2 (B2A dead)
-constexpr uint32_t S_STG_U = 49152;    // U image (32768), after MMA 2 (B1 dead)
+constexpr uint32_t S_STG_U = 49152;    // U image (16384), after MMA 2 (B1 dead)
 // OPA holds nothing between items: phase 1 parks the raw q and k rows there,
 // at the positions phase 2 overwrites with the scaled operands.
 constexpr uint32_t S_MISC = 106496;
@@ -728,10 +728,13 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
             *reinterpret_cast<uint4 *>(sm + S_STG_W + kmaj_off(64, r, col + 8)) =
                 make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
           } else {
+            uint32_t pku[8];
 #pragma unroll
-            for (int x = 0; x < 16; x += 4)
-              *reinterpret_cast<float4 *>(sm + S_STG_U + u_offset(r, col + x)) =
-                  make_float4(d[cc][x], d[cc][x + 1], d[cc][x + 2], d[cc][x + 3]);
+            for (int x = 0; x < 16; x += 2) pku[x / 2] = pack_bf16(d[cc][x], d[cc][x + 1]);
+            *reinterpret_cast<uint4 *>(sm + S_STG_U + u_offset(r, col)) =
+                make_uint4(pku[0], pku[1], pku[2], pku[3]);
+            *reinterpret_cast<uint4 *>(sm + S_STG_U + u_offset(r, col + 8)) =
+                make_uint4(pku[4], pku[5], pku[6], pku[7]);
           }
         }
       }
@@ -742,7 +745,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     if (tid == 0) {
       bulk_store_hint(pk + PK_WQ + 64 * 128, sm + S_STG_W, 8192, pol_once);
       bulk_store_hint(pk + PK_WQ + 16384 + 64 * 128, sm + S_STG_W + 8192, 8192, pol_once);
-      bulk_store_hint(pk + PK_U, sm + S_STG_U, 32768, pol_once);
+      bulk_store_hint(pk + PK_U, sm + S_STG_U, 16384, pol_once);
       bulk_commit();
     }
   }
