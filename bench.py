@@ -434,27 +434,29 @@ def bench_segment(kda, dev, stream, steps=3, warmup=2):
 
 
 def bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world, steps=3):
-    """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of q, k, v, gate, beta, then the step, then D2H of o."""
+    """Same step through the public API with the step's inputs and output in
+    page-locked host memory: kda_chunk_fwd_host streams q, k, v, gate, beta
+    to the GPU and o back, overlapping the copies with the kernels."""
     import torch
     names = ["q", "k", "v", "g", "beta"]
     host = {n: torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True) for n in names}
     for n in names:
         host[n].copy_(inp[n])
-    o_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dev_in = {n: inp[n] for n in names}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
+    K = cfg.dk
+    ha, o_host, hfin, hws = kda.prepare_chunk_fwd_host(
+        host["q"], host["k"], host["v"], host["g"], host["beta"], device=inp["q"].device,
+        final_state=fin, scale=float(K ** -0.5), a_log=inp["a_log"], dt_bias=inp["dt_bias"],
+        initial_state=S0, l2norm_qk=True, beta_sigmoid=True, gate_in_kernel=True, use_exp2=True)
     d2h = o_host.numel() * o_host.element_size()
+    sp = stream.cuda_stream
 
     def step():
-        for n in names:
-            dev_in[n].copy_(host[n], non_blocking=True)
         kda.kda_state_gather(pool, idx, packed=S0, stream=stream)
-        st = lib.kda_chunk_fwd(ctypes.byref(fa), stream.cuda_stream)
+        st = lib.kda_chunk_fwd_host(ctypes.byref(ha), sp)
         if st:
-            raise kda.KdaError(st, "kda_chunk_fwd")
+            raise kda.KdaError(st, "kda_chunk_fwd_host")
         kda.kda_state_scatter(pool, idx, fin, stream=stream)
-        o_host.copy_(out, non_blocking=True)
 
     step()
     torch.cuda.synchronize()
@@ -467,7 +469,8 @@ def bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world, st
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
     return {"value": cfg.B * cfg.T * world / (ms / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "api": "kda_chunk_fwd_host (host q/k/v/gate/beta/o, page-locked)"}
 
 
 if __name__ == "__main__":

@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kda_get_device_status": ([vp, vp], ctypes.c_int),
         "kda_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "kda_chunk_fwd_static_scratch": ([P, vp], ctypes.c_int),
+        "kda_chunk_fwd_host_workspace_size": ([P], ctypes.c_size_t),
+        "kda_chunk_fwd_host": ([P, vp], ctypes.c_int),
         "kda_chunk_fwd_stages": ([P, ctypes.POINTER(ctypes.c_char_p), i32], i32),
         "kda_chunk_fwd_profiled": ([P, vp, ctypes.POINTER(vp), i32], ctypes.c_int),
     }
@@ -216,6 +218,46 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
 
 # include/kda.h KDA_STATIC_SCRATCH_BYTES
 KDA_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+# include/kda.h KDA_HOST_BLOCK_TOKENS
+KDA_HOST_BLOCK_TOKENS = 1024
+
+
+def prepare_chunk_fwd_host(q, k, v, g, beta, *, device=None, output_final_state=True,
+                           workspace=None, **kw):
+    """Builds the ``kda_fwd_args`` of a host-IO forward once: q, k, v, g, beta
+    and the returned ``out`` are host (CPU) tensors, ``out`` page-locked;
+    final_state and the workspace live on ``device`` (default: the current
+    CUDA device).  Returns (args, out, final_state, ws)."""
+    torch = _torch()
+    lib = load_library()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    for t in (q, k, v, g, beta):
+        if t.is_cuda:
+            raise ValueError("kda_chunk_fwd_host takes q, k, v, g, beta in host memory")
+    out = kw.pop("out", None)
+    if out is None:
+        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, pin_memory=True)
+    fin = kw.pop("final_state", None)
+    if output_final_state and fin is None:
+        fin = torch.empty(q.shape[0], q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+                          device=device)
+    a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
+    ws = _workspace(lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(a)), device, workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    return a, out, fin, ws
+
+
+def kda_chunk_fwd_host(q, k, v, g, beta, *, stream=None, **kw):
+    """Forward on host-resident q, k, v, g, beta [B, T, H, D] (page-locked for
+    overlap): the library streams them through the GPU in blocks of
+    KDA_HOST_BLOCK_TOKENS tokens and writes o back to a host tensor.
+    Returns ``(out, final_state)`` (out on the host, final_state on the GPU);
+    both are complete when ``stream`` (default: current) passes the call.
+    See ``kda_chunk_fwd_host`` in include/kda.h."""
+    lib = load_library()
+    a, out, fin, ws = prepare_chunk_fwd_host(q, k, v, g, beta, **kw)
+    _check(lib.kda_chunk_fwd_host(ctypes.byref(a), _stream(stream)), "kda_chunk_fwd_host")
+    return out, fin
 
 
 def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None,

@@ -7,6 +7,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "kda_profile.h"
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
@@ -133,9 +135,11 @@ size_t kda_segment_summary_workspace_size(const kda_fwd_args *a, int32_t num_seg
 }
 
 // Launch sequence of the forward.  When events are given, events[i] is
-// recorded before stage i and events[count] after the last stage.
+// recorded before stage i and events[count] after the last stage.  The device
+// error word is cleared first unless keep_err (the blocks of a host-IO call
+// share one word, cleared once).
 static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
-                          int32_t nev) {
+                          int32_t nev, bool keep_err = false) {
   kda_status s = check_fwd(a);
   if (s != KDA_OK) return s;
   const FwdPlan p = fwd_plan(a);
@@ -163,7 +167,7 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
   if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, maps)) return KDA_ERR_CUDA;
 
   const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
-  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);  // device error word
+  cudaError_t e = keep_err ? cudaSuccess : cudaMemsetAsync(ws, 0, 4, st);  // device error word
   if (e == cudaSuccess && si.bounds && !reuse) {
     e = mark();
     if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
@@ -235,6 +239,171 @@ kda_status kda_chunk_fwd_profiled(const kda_fwd_args *a, kda_stream_t stream,
     if (!events[i]) return KDA_ERR_INVALID_ARG;
   return run_fwd(a, reinterpret_cast<cudaStream_t>(stream),
                  reinterpret_cast<cudaEvent_t const *>(events), num_events);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Host-IO forward: the batch in blocks of KDA_HOST_BLOCK_TOKENS tokens of
+// every sequence, with the copies on two streams of the library's own.
+struct HostPlan {
+  int64_t Tb;                        // tokens per block (last block: fewer)
+  int64_t nblk;
+  size_t off_sub, sub_bytes;         // workspace of one block's forward
+  size_t off_in[2], in_bytes;        // staged q, k, v, g, beta of a block
+  size_t off_out[2], out_bytes;      // staged o of a block
+  size_t off_state, state_bytes;     // carried state when final_state is NULL
+  size_t total;
+  size_t esz;                        // bytes per q/k/v/o element
+};
+
+kda_status check_host(const kda_fwd_args *a) {
+  kda_status s = check_fwd(a);
+  if (s != KDA_OK) return s;
+  if (a->cu_seqlens || a->h_out || a->v_new_out || (a->flags & KDA_REUSE_PREP))
+    return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+// Sub-problem of block t: the same arguments on [B, Tb_t] staged tokens.
+kda_fwd_args block_args(const kda_fwd_args *a, int64_t Tb_t) {
+  kda_fwd_args b = *a;
+  b.T = (int32_t)Tb_t;
+  return b;
+}
+
+HostPlan host_plan(const kda_fwd_args *a) {
+  HostPlan h{};
+  h.esz = a->qkv_dtype == KDA_BF16 ? 2 : 4;
+  h.Tb = a->T < KDA_HOST_BLOCK_TOKENS ? a->T : KDA_HOST_BLOCK_TOKENS;
+  h.nblk = h.Tb > 0 ? (a->T + h.Tb - 1) / h.Tb : 0;
+  const kda_fwd_args b = block_args(a, h.Tb);
+  size_t o = 0;
+  h.off_sub = o;
+  h.sub_bytes = plan_bytes(&b, fwd_plan(&b));
+  o = align256(o + h.sub_bytes);
+  const size_t tok = (size_t)a->B * h.Tb * a->H;  // token-heads of a block
+  h.in_bytes = tok * ((size_t)(2 * a->dk + a->dv) * h.esz + (size_t)a->dk * 4 + 4);
+  h.out_bytes = tok * a->dv * h.esz;
+  for (int j = 0; j < 2; ++j) { h.off_in[j] = o; o = align256(o + h.in_bytes); }
+  for (int j = 0; j < 2; ++j) { h.off_out[j] = o; o = align256(o + h.out_bytes); }
+  h.state_bytes = a->final_state ? 0 : (size_t)a->B * a->H * a->dk * a->dv * 4;
+  h.off_state = o;
+  o = align256(o + h.state_bytes);
+  h.total = o;
+  return h;
+}
+
+struct HostStreams {
+  cudaStream_t in = nullptr, out = nullptr;
+};
+
+// The library's two copy streams on the current device, created once.
+kda_status host_streams(HostStreams *hs) {
+  static std::mutex mu;
+  static HostStreams cache[64];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  HostStreams &c = cache[dev];
+  if (!c.in) {
+    if (cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaStreamDestroy(c.in);
+      c.in = nullptr;
+      return KDA_ERR_CUDA;
+    }
+  }
+  *hs = c;
+  return KDA_OK;
+}
+
+// Copy rows [t0, t0 + n) of every sequence of a [B, T, H, width] host tensor
+// into a contiguous [B, n, H, width] device block.
+cudaError_t copy_in(void *dst, const void *src, int64_t B, int64_t T, int64_t t0, int64_t n,
+                    size_t row_bytes, cudaStream_t s) {
+  return cudaMemcpy2DAsync(dst, n * row_bytes, static_cast<const char *>(src) + t0 * row_bytes,
+                           T * row_bytes, n * row_bytes, B, cudaMemcpyHostToDevice, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_chunk_fwd_host_workspace_size(const kda_fwd_args *a) {
+  if (check_host(a) != KDA_OK) return 0;
+  return host_plan(a).total;
+}
+
+kda_status kda_chunk_fwd_host(const kda_fwd_args *a, kda_stream_t stream) {
+  kda_status s = check_host(a);
+  if (s != KDA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((int64_t)a->B * a->T == 0) return run_fwd(a, st, nullptr, 0);  // no tokens: no copies
+  const HostPlan hp = host_plan(a);
+  if (!a->workspace || a->workspace_bytes < hp.total) return KDA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+  HostStreams hs;
+  if ((s = host_streams(&hs)) != KDA_OK) return s;
+  char *ws = static_cast<char *>(a->workspace);
+  float *carry = a->final_state ? a->final_state : reinterpret_cast<float *>(ws + hp.off_state);
+
+  cudaEvent_t ev[7] = {};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 7 && e == cudaSuccess; ++i)
+    e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+  cudaEvent_t ev_start = ev[6], *ev_in = ev, *ev_comp = ev + 2, *ev_out = ev + 4;
+  // the workspace and the device buffers are free once earlier work on `stream` is done
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + hp.off_sub, 0, 4, st);  // shared error word
+  if (e == cudaSuccess) e = cudaEventRecord(ev_start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.in, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.out, ev_start, 0);
+
+  const int64_t B = a->B, T = a->T, H = a->H;
+  const size_t rq = (size_t)H * a->dk * hp.esz, rv = (size_t)H * a->dv * hp.esz;
+  const size_t rg = (size_t)H * a->dk * 4, rb = (size_t)H * 4;
+  for (int64_t t = 0; t < hp.nblk && e == cudaSuccess; ++t) {
+    const int j = (int)(t & 1);
+    const int64_t t0 = t * hp.Tb, n = (T - t0) < hp.Tb ? (T - t0) : hp.Tb;
+    char *in = ws + hp.off_in[j];
+    const size_t nb = (size_t)B * n;  // staged rows
+    void *dq = in, *dk = in + nb * rq, *dv = in + 2 * nb * rq, *dg = in + 2 * nb * rq + nb * rv;
+    void *db = static_cast<char *>(dg) + nb * rg;
+    // inputs of block t (after block t - 2 has finished reading this buffer)
+    if (t >= 2) e = cudaStreamWaitEvent(hs.in, ev_comp[j], 0);
+    if (e == cudaSuccess) e = copy_in(dq, a->q, B, T, t0, n, rq, hs.in);
+    if (e == cudaSuccess) e = copy_in(dk, a->k, B, T, t0, n, rq, hs.in);
+    if (e == cudaSuccess) e = copy_in(dv, a->v, B, T, t0, n, rv, hs.in);
+    if (e == cudaSuccess) e = copy_in(dg, a->g, B, T, t0, n, rg, hs.in);
+    if (e == cudaSuccess) e = copy_in(db, a->beta, B, T, t0, n, rb, hs.in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in[j], hs.in);
+    // the forward of block t (after block t - 2's o has left this buffer)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in[j], 0);
+    if (e == cudaSuccess && t >= 2) e = cudaStreamWaitEvent(st, ev_out[j], 0);
+    if (e != cudaSuccess) break;
+    kda_fwd_args b = block_args(a, n);
+    b.q = dq; b.k = dk; b.v = dv; b.g = static_cast<float *>(dg); b.beta = static_cast<float *>(db);
+    b.out = ws + hp.off_out[j];
+    b.initial_state = t == 0 ? a->initial_state : carry;
+    b.final_state = carry;
+    b.workspace = ws + hp.off_sub;
+    b.workspace_bytes = hp.sub_bytes;
+    if ((s = run_fwd(&b, st, nullptr, 0, true)) != KDA_OK) break;
+    e = cudaEventRecord(ev_comp[j], st);
+    // o of block t back to the host
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.out, ev_comp[j], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(static_cast<char *>(a->out) + t0 * rv, T * rv, ws + hp.off_out[j], n * rv,
+                            n * rv, B, cudaMemcpyDeviceToHost, hs.out);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out[j], hs.out);
+  }
+  // `stream` passes the call once the last copy out is done
+  if (e == cudaSuccess && s == KDA_OK) e = cudaStreamWaitEvent(st, ev_out[(hp.nblk - 1) & 1], 0);
+  for (int i = 0; i < 7; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  if (s != KDA_OK) return s;
+  return cuda_status(e);
 }
 
 kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,

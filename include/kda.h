@@ -149,8 +149,8 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  * process exits).
  *  - Limit: the problem's kda_chunk_fwd_workspace_size must not exceed
  *    KDA_STATIC_SCRATCH_BYTES, else KDA_ERR_WORKSPACE and nothing is
- *    launched (roughly: up to about 360 chunk-heads on the bf16 d=128 path,
- *    e.g. B=1, T=2048, H=8).
+ *    launched (roughly: up to about 450 chunk-heads on the bf16 d=128 path,
+ *    e.g. B=1, T=2048, H=14).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
@@ -160,6 +160,39 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  *  - Other errors as kda_chunk_fwd; KDA_ERR_CUDA if the address lookup fails.
  */
 kda_status kda_chunk_fwd_static_scratch(const kda_fwd_args *args, kda_stream_t stream);
+
+/* Tokens per block of kda_chunk_fwd_host. */
+#define KDA_HOST_BLOCK_TOKENS 1024
+
+/* Bytes of device workspace kda_chunk_fwd_host needs (0 when the arguments
+ * are invalid for it). */
+size_t kda_chunk_fwd_host_workspace_size(const kda_fwd_args *args);
+
+/*
+ * kda_chunk_fwd with q, k, v, g, beta and out in HOST memory (the pages have
+ * no counterpart of this call: they assume device-resident inputs).  The
+ * forward streams the batch through the device workspace in blocks of
+ * KDA_HOST_BLOCK_TOKENS tokens of every sequence: the host-to-device copies
+ * of block t+1 and the device-to-host copy of o of block t-1 run on two
+ * internal streams while block t computes on `stream`; the state moves from
+ * block to block on the device.  Blocks end on chunk boundaries and the fp32
+ * state is handed over as is, so the results are bit-identical to
+ * kda_chunk_fwd's on the same inputs.
+ *  - Host buffers: same layouts as kda_chunk_fwd (BSND only); page-locked
+ *    memory lets the copies overlap the kernels (pageable memory works but
+ *    the copies then serialise with the host).  The host buffers must stay
+ *    valid until `stream` has passed the call.
+ *  - Device: initial_state, final_state (device pointers or NULL), a_log,
+ *    dt_bias and the workspace (kda_chunk_fwd_host_workspace_size bytes,
+ *    256-byte aligned).
+ *  - Stream order: nothing starts before earlier work on `stream`; when
+ *    `stream` passes the call, out (host) and final_state are complete.  The
+ *    internal streams are created on the first call per device and shared by
+ *    all calls on it.
+ *  - Errors as kda_chunk_fwd, plus KDA_ERR_UNSUPPORTED for cu_seqlens,
+ *    h_out, v_new_out or KDA_REUSE_PREP.
+ */
+kda_status kda_chunk_fwd_host(const kda_fwd_args *args, kda_stream_t stream);
 
 /* Bytes of workspace kda_segment_summary needs. */
 size_t kda_segment_summary_workspace_size(const kda_fwd_args *args, int32_t num_segments);

@@ -127,3 +127,22 @@ def _load_fresh(path):
         return kda.load_library(path)
     finally:
         kda._lib = saved
+
+
+def test_host_io_checks(lib):
+    """kda_chunk_fwd_host: block workspace independent of T beyond one block,
+    and the unsupported options rejected before anything is launched."""
+    f = lambda a: lib.kda_chunk_fwd_host(ctypes.byref(a), None)
+    ws = lambda a: lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(a))
+    one = ws(_args(T=kda.KDA_HOST_BLOCK_TOKENS))
+    assert one > 0 and ws(_args(T=8 * kda.KDA_HOST_BLOCK_TOKENS)) == one
+    assert 0 < ws(_args(T=64)) < one
+    assert ws(_args(T=100, final_state=1 << 26)) < ws(_args(T=100))  # no carried-state buffer
+    assert ws(_args(cu_seqlens=1 << 24, num_seqs=2, B=1)) == 0
+    assert f(_args(cu_seqlens=1 << 24, num_seqs=2, B=1)) == 2
+    assert f(_args(h_out=1 << 24)) == 2
+    assert f(_args(v_new_out=1 << 24)) == 2
+    assert f(_args(flags=kda.KDA_REUSE_PREP)) == 2
+    assert f(_args(q=None)) == 1
+    assert f(_args()) == 4                                       # no workspace
+    assert lib.kda_chunk_fwd_host(None, None) == 1
