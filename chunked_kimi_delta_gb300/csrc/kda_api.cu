@@ -188,7 +188,7 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
       ca.h_out = a->h_out;
       ca.v_new_out = a->v_new_out;
       ca.err = err;
-      e = tcp::launch_tc_chain(tcp::CHAIN_FWD, ca, si, a->H, st);
+      e = tcp::launch_tc_chain(ca, si, a->H, st);
     }
   } else {
     if (e == cudaSuccess && !reuse) e = mark();
@@ -435,14 +435,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess)
       e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
-    if (e == cudaSuccess) {
-      tcp::ChainArgs ca{};
-      ca.pkg = pkg;
-      ca.S_tilde = S_tilde;
-      ca.M = M;
-      ca.err = err;
-      e = tcp::launch_tc_chain(tcp::CHAIN_SUMMARY, ca, si, a->H, st);
-    }
+    if (e == cudaSuccess) e = tcp::launch_tc_summary(pkg, S_tilde, M, si, a->H, err, st);
   } else {
     if (e == cudaSuccess)
       e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);

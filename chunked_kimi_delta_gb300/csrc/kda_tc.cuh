@@ -1,16 +1,18 @@
 // kda_tc.cuh - shared definitions of the tensor-core (tcgen05) forward path
 // for bf16 inputs with d_k = d_v = 128.
 //
-// The path has two kernels:
-//   prep  (kda_tc_prep.cu): per (chunk, head) - gate, cumulative decay, L2
-//         norms, the decay-weighted A_kk / A_qk products, the triangular
-//         inverse and the WY products w = A (k.beta.e^G), u = A (v.beta);
-//   chain (kda_tc_chain.cu): per (sequence, head) - the sequential state
-//         recurrence v_new = u - w h, o = qg h + Aqk v_new,
-//         h' = e^{G_C} h + kg^T v_new.
-// prep hands each chunk to chain as a "package": a byte image of the shared
-// memory tiles chain feeds to the tensor cores, so chain moves it with one
-// bulk copy and no re-layout.
+// The path has three kernels:
+//   prep    (kda_tc_prep.cu): per (chunk, head) - gate, cumulative decay, L2
+//           norms, the decay-weighted A_kk / A_qk products, the triangular
+//           inverse and the WY products w = A (k.beta.e^G), u = A (v.beta);
+//   chain   (kda_tc_chain.cu): per (sequence, head) - the sequential state
+//           recurrence v_new = u - w h, o = qg h + Aqk v_new,
+//           h' = e^{G_C} h + kg^T v_new;
+//   summary (kda_tc_summary.cu): per (segment, head) - the same recurrence
+//           on the augmented state [S~ | M] for the segment summary.
+// prep hands each chunk to the others as a "package": a byte image of the
+// shared memory tiles they feed to the tensor cores, so it moves with bulk
+// copies and no re-layout.
 #pragma once
 
 #include <cuda.h>
@@ -158,8 +160,6 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
                            const float *beta, const GateParams &gp, const SeqInfo &s,
                            int64_t nchunks, int H, char *pkg, uint32_t *err, cudaStream_t st);
 
-enum ChainMode { CHAIN_FWD = 0, CHAIN_SUMMARY = 1 };
-
 struct ChainArgs {
   const char *pkg;
   void *out;                    // bf16 [T_tot, H, V]
@@ -167,12 +167,15 @@ struct ChainArgs {
   float *final_state;           // [N, H, K, V] or null
   float *h_out;                 // [nchunks, H, K, V] or null
   float *v_new_out;             // [T_tot, H, V] or null
-  float *S_tilde, *M;           // summary outputs
   uint32_t *err;
 };
 
-cudaError_t launch_tc_chain(ChainMode mode, const ChainArgs &a, const SeqInfo &s, int H,
-                            cudaStream_t st);
+cudaError_t launch_tc_chain(const ChainArgs &a, const SeqInfo &s, int H, cudaStream_t st);
+
+// Segment summary (kda_tc_summary.cu): M and S~ of every (segment, head)
+// from the packages of its chunks.
+cudaError_t launch_tc_summary(const char *pkg, float *S_tilde, float *M, const SeqInfo &s, int H,
+                              uint32_t *err, cudaStream_t st);
 
 }  // namespace tcp
 }  // namespace kda

@@ -20,10 +20,6 @@
 // c + 2 once v_new of chunk c is computed, KG, AQK and GC of chunk c + 1 once
 // the MMAs of chunk c - 1 have finished.
 //
-// Summary mode ("Hyper-Parallel ..." section 5.1, PreProcessFwd; "KDA Context
-// Parallelism (KCP)"): the same chain on the augmented state [S~ | M] with
-// X_0 = [0 | I] and values [u | 0]; blockIdx.y = 0 carries the S~ columns,
-// blockIdx.y = 1 the M columns; nothing else is written.
 #include <cuda_bf16.h>
 
 #include "kda_tc.cuh"
@@ -42,7 +38,6 @@ constexpr uint32_t SMEM_BYTES = 198656 + 1024;
 constexpr uint32_t BUF_STRIDE = S_BUF1 - S_BUF0;
 constexpr uint32_t TMEM_COLS = 512;          // P (two buffers) and U
 
-template <int MODE>
 __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s, int H) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -59,7 +54,6 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   const int q4 = warp & 3, hf = warp >> 2;
   const int kr = 32 * q4 + lane;  // key channel (state row) owned by this thread
   const int n = blockIdx.x / H, h = blockIdx.x % H;
-  const int part = blockIdx.y;
   int64_t t0, t1;
   seq_range(s, n, t0, t1);
   const int64_t c0 = seq_first_chunk(s, n);
@@ -85,21 +79,16 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 
   // initial state -> registers and the bf16 operand
   float hr[64];
-  if (MODE == CHAIN_FWD) {
-    if (a.initial_state) {
-      const float4 *src = reinterpret_cast<const float4 *>(a.initial_state + (unit * K + kr) * V + 64 * hf);
+  if (a.initial_state) {
+    const float4 *src = reinterpret_cast<const float4 *>(a.initial_state + (unit * K + kr) * V + 64 * hf);
 #pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const float4 v = src[x];
-        hr[4 * x] = v.x; hr[4 * x + 1] = v.y; hr[4 * x + 2] = v.z; hr[4 * x + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int x = 0; x < 64; ++x) hr[x] = 0.f;
+    for (int x = 0; x < 16; ++x) {
+      const float4 v = src[x];
+      hr[4 * x] = v.x; hr[4 * x + 1] = v.y; hr[4 * x + 2] = v.z; hr[4 * x + 3] = v.w;
     }
   } else {
 #pragma unroll
-    for (int x = 0; x < 64; ++x) hr[x] = (part == 1 && kr == 64 * hf + x) ? 1.f : 0.f;
+    for (int x = 0; x < 64; ++x) hr[x] = 0.f;
   }
   auto store_hb = [&]() {
 #pragma unroll
@@ -182,7 +171,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     bool ok = wait_or_flag(fullA + b, (uint32_t)((c >> 1) & 1), a.err);
     if (!ok) *abort_flag = 1;
     else if (tid == LEAD) a_done = c + 1;
-    if (MODE == CHAIN_FWD && a.h_out) {
+    if (a.h_out) {
       float4 *dst = reinterpret_cast<float4 *>(a.h_out + (((c0 + c) * H + h) * K + kr) * V + 64 * hf);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
@@ -205,7 +194,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     }
     // warps of lane quarters 0 and 1: o of the previous chunk, off the
     // recurrence's critical path
-    if (MODE == CHAIN_FWD && q4 < 2 && c > 0) read_o(c - 1, BT);
+    if (q4 < 2 && c > 0) read_o(c - 1, BT);
 
     // ---- v_new = u - w h  (P rows 64..127 live in TMEM lanes 64..127), by
     //      the warps of lane quarters 2 and 3
@@ -231,10 +220,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
         tc::tmem_ld_wait();
         const int col = 64 * hf + 16 * cc;
         float vn[16];
-        if (MODE == CHAIN_SUMMARY && part == 1) {
-#pragma unroll
-          for (int x = 0; x < 16; ++x) vn[x] = -d[x];
-        } else {
+        {
           const uint4 ua = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, col));
           const uint4 ub = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, col + 8));
           const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
@@ -251,7 +237,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
         *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col + 8)) =
             make_uint4(pack_bf16(vn[8], vn[9]), pack_bf16(vn[10], vn[11]), pack_bf16(vn[12], vn[13]),
                        pack_bf16(vn[14], vn[15]));
-        if (MODE == CHAIN_FWD && a.v_new_out && r < len) {
+        if (a.v_new_out && r < len) {
           float4 *dst = reinterpret_cast<float4 *>(a.v_new_out + ((tc0 + r) * H + h) * V + col);
 #pragma unroll
           for (int x = 0; x < 4; ++x) dst[x] = make_float4(vn[4 * x], vn[4 * x + 1], vn[4 * x + 2], vn[4 * x + 3]);
@@ -292,7 +278,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
       tc::mma_commit(bar_mc);
       mc_pending = true;
       mc_par = (uint32_t)(c & 1);
-      if (MODE == CHAIN_FWD) {
+      {
         const uint32_t idb = tc::idesc_bf16_f32(128, 128, false, true);
         const uint32_t q0 = tc::smem_u32(buf + PK_AQK);
 #pragma unroll
@@ -329,19 +315,12 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   }
   // o of the last chunk
   __syncthreads();
-  if (MODE == CHAIN_FWD && nch > 0 && !*abort_flag && q4 < 2) read_o(nch - 1, (int)(t1 - (t0 + (nch - 1) * BT)));
+  if (nch > 0 && !*abort_flag && q4 < 2) read_o(nch - 1, (int)(t1 - (t0 + (nch - 1) * BT)));
   __syncthreads();
 
   if (*abort_flag == 0) {
-    if (MODE == CHAIN_FWD) {
-      if (a.final_state) {
-        float4 *dst = reinterpret_cast<float4 *>(a.final_state + (unit * K + kr) * V + 64 * hf);
-#pragma unroll
-        for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
-      }
-    } else {
-      float *base = part == 0 ? a.S_tilde + (unit * K + kr) * V : a.M + (unit * K + kr) * K;
-      float4 *dst = reinterpret_cast<float4 *>(base + 64 * hf);
+    if (a.final_state) {
+      float4 *dst = reinterpret_cast<float4 *>(a.final_state + (unit * K + kr) * V + 64 * hf);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
     }
@@ -361,21 +340,13 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 
 }  // namespace
 
-cudaError_t launch_tc_chain(ChainMode mode, const ChainArgs &a, const SeqInfo &s, int H,
-                            cudaStream_t st) {
-  const dim3 grid((unsigned)((int64_t)s.N * H), mode == CHAIN_SUMMARY ? 2 : 1);
-  if (grid.x == 0) return cudaSuccess;
-  if (mode == CHAIN_FWD) {
-    cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel<CHAIN_FWD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    tc_chain_kernel<CHAIN_FWD><<<grid, NT, SMEM_BYTES, st>>>(a, s, H);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel<CHAIN_SUMMARY>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    tc_chain_kernel<CHAIN_SUMMARY><<<grid, NT, SMEM_BYTES, st>>>(a, s, H);
-  }
+cudaError_t launch_tc_chain(const ChainArgs &a, const SeqInfo &s, int H, cudaStream_t st) {
+  const int64_t units = (int64_t)s.N * H;
+  if (units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  tc_chain_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(a, s, H);
   return cudaGetLastError();
 }
 
