@@ -346,11 +346,18 @@ def main():
         result["e2e"] = bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world)
     if rank == 0 and not args.no_cpu_baseline:
         inp_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-        secs, th, threads = cpu_oracle_sample(cfg, inp_cpu, [(0, h) for h in range(H)], 8192)
+        # whole sequences of the batch (all heads, all tokens), cycling through
+        # the batch rows until about 10 s of CPU work (at most 16 sequences)
+        secs, th, nseq, threads = 0.0, 0, 0, 1
+        while secs < 10.0 and nseq < 16:
+            b = nseq % cfg.B
+            s_, n_, threads = cpu_oracle_sample(cfg, inp_cpu, [(b, h) for h in range(H)], cfg.T)
+            secs, th, nseq = secs + s_, th + n_, nseq + 1
         result["cpu_baseline"] = {
             "value": th / secs / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"fp64 oracle on batch row 0, all {H} heads x 8192 tokens "
-                      f"({th} token-heads, {secs:.1f} s); tokens/s = token-heads/s / H"}
+            "sample": f"fp64 oracle on {nseq} whole sequences of the batch (rows 0..{cfg.B - 1} in "
+                      f"turn), all {H} heads x {cfg.T} tokens each ({th} token-heads, {secs:.1f} s); "
+                      f"tokens/s = token-heads/s / H"}
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
