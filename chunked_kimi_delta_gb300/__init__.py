@@ -55,6 +55,21 @@ class kda_fwd_args(ctypes.Structure):
     ]
 
 
+class kda_decode_args(ctypes.Structure):
+    """Mirror of ``kda_decode_args`` in include/kda.h."""
+    _fields_ = [
+        ("N", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("qkv_dtype", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("scale", ctypes.c_float), ("eps", ctypes.c_float),
+        ("flags", ctypes.c_uint32), ("out", ctypes.c_void_p), ("cache", ctypes.c_void_p),
+        ("cache_dtype", ctypes.c_int), ("num_rows", ctypes.c_int64),
+        ("row_stride_elems", ctypes.c_int64), ("idx", ctypes.c_void_p), ("idx_dtype", ctypes.c_int),
+        ("init_flags", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -83,6 +98,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kda_chunk_fwd_static_scratch": ([P, vp], ctypes.c_int),
         "kda_chunk_fwd_host_workspace_size": ([P], ctypes.c_size_t),
         "kda_chunk_fwd_host": ([P, vp], ctypes.c_int),
+        "kda_recurrent_step": ([ctypes.POINTER(kda_decode_args), vp], ctypes.c_int),
         "kda_chunk_fwd_stages": ([P, ctypes.POINTER(ctypes.c_char_p), i32], i32),
         "kda_chunk_fwd_profiled": ([P, vp, ctypes.POINTER(vp), i32], ctypes.c_int),
     }
@@ -448,6 +464,40 @@ def kda_state_scatter(cache, idx, packed, *, stream=None):
                                  _ptr(idx), _idx_code(idx), _ptr(packed), _dtype_code(packed),
                                  idx.numel(), _stream(stream)), "kda_state_scatter")
     return cache
+
+
+def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=None, eps=1e-6,
+                       a_log=None, dt_bias=None, l2norm_qk=True, beta_sigmoid=False,
+                       gate_in_kernel=False, out=None, stream=None):
+    """Recurrent decode step on pool states, in place: q, k, g [N, T, H, dk],
+    v [N, T, H, dv], beta [N, T, H]; ``cache`` [rows, H, dk, dv] (any row
+    stride); ``idx`` [N] rows of the pool.  Returns out [N, T, H, dv].  See
+    ``kda_recurrent_step`` in include/kda.h."""
+    torch = _torch()
+    lib = load_library()
+    if q.dim() != 4:
+        raise ValueError("q/k/v are [N, T, H, D]")
+    _contig(q, k, v, g, beta, idx, init_flags, a_log, dt_bias)
+    if init_flags is not None and init_flags.dtype != torch.bool:
+        raise TypeError("init_flags must be bool")
+    if out is None:
+        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+    _contig(out)
+    n_rows, stride, _ = _rows(cache)
+    a = kda_decode_args()
+    a.N, a.T, a.H, a.dk, a.dv = q.shape[0], q.shape[1], q.shape[2], q.shape[3], v.shape[3]
+    a.qkv_dtype = _dtype_code(q)
+    a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
+    a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
+    a.scale = float(q.shape[-1] ** -0.5 if scale is None else scale)
+    a.eps = float(eps)
+    a.flags = ((KDA_L2NORM_QK if l2norm_qk else 0) | (KDA_BETA_SIGMOID if beta_sigmoid else 0)
+               | (KDA_GATE_IN_KERNEL if gate_in_kernel else 0))
+    a.out = _ptr(out)
+    a.cache, a.cache_dtype, a.num_rows, a.row_stride_elems = _ptr(cache), _dtype_code(cache), n_rows, stride
+    a.idx, a.idx_dtype, a.init_flags = _ptr(idx), _idx_code(idx), _ptr(init_flags)
+    _check(lib.kda_recurrent_step(ctypes.byref(a), _stream(stream)), "kda_recurrent_step")
+    return out
 
 
 def kda_get_device_status(workspace, stream=None) -> int:

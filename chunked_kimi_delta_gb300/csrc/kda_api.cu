@@ -498,6 +498,32 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
                                           n_sel, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
+  if (!a || a->N < 0 || a->T < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
+  if (a->flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
+  if (a->flags & (kRejectedFlags | KDA_REUSE_PREP)) return KDA_ERR_UNSUPPORTED;
+  if ((a->dk != 64 && a->dk != 128) || (a->dv != 64 && a->dv != 128)) return KDA_ERR_UNSUPPORTED;
+  if (a->qkv_dtype != KDA_F32 && a->qkv_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (a->cache_dtype != KDA_F32 && a->cache_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (a->idx_dtype != KDA_I32 && a->idx_dtype != KDA_I64) return KDA_ERR_INVALID_ARG;
+  if (a->num_rows < 1 || a->row_stride_elems < (int64_t)a->H * a->dk * a->dv) return KDA_ERR_INVALID_ARG;
+  if ((a->flags & KDA_GATE_IN_KERNEL) && !a->a_log) return KDA_ERR_INVALID_ARG;
+  if (a->N == 0) return KDA_OK;
+  if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out || !a->cache || !a->idx)
+    return KDA_ERR_INVALID_ARG;
+  if ((int64_t)a->N * a->T * a->H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+  GateParams gp;
+  gp.a_log = a->a_log;
+  gp.dt_bias = a->dt_bias;
+  gp.scale = a->scale;
+  gp.eps = a->eps;
+  gp.flags = a->flags;
+  return cuda_status(launch_decode(a->qkv_dtype, a->cache_dtype, a->idx_dtype, a->dk, a->dv, a->N,
+                                   a->T, a->H, a->q, a->k, a->v, a->g, a->beta, gp, a->out, a->cache,
+                                   a->num_rows, a->row_stride_elems, a->idx, a->init_flags,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_get_device_status(void *workspace, kda_stream_t stream) {
   if (!workspace) return KDA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -138,6 +138,13 @@ struct GateParams {
 
 cudaError_t launch_chunk_map(const SeqInfo &s, int32_t *chunk_off, cudaStream_t st);
 
+// Recurrent decode step on pool rows (kda_decode.cu).
+cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_dtype idx_dtype,
+                          int dk, int dv, int N, int T, int H, const void *q, const void *k,
+                          const void *v, const float *g, const float *beta, const GateParams &gp,
+                          void *out, void *cache, int64_t num_rows, int64_t row_stride,
+                          const void *idx, const bool *init_flags, cudaStream_t st);
+
 // Generic (CUDA-core, fp32 arithmetic) intra-chunk stage: writes w, u, qg, kg,
 // Aqk, gC of the plan.
 cudaError_t launch_generic_intra(kda_dtype dt, const void *q, const void *k, const void *v,

@@ -274,6 +274,54 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
                              kda_index_dtype idx_dtype, const void *packed,
                              kda_dtype packed_dtype, int64_t n_sel, kda_stream_t stream);
 
+/*
+ * Recurrent decode step on states kept in a cache pool: the token-by-token
+ * form of the recurrence ("KDA Chunk Backward - TPU/Pallas Kernel Design"
+ * section 1) for the decode path named in the vllm-ascend KDA prefill state
+ * copy article ("背景": decode goes through the recurrent kernel, prefill
+ * through the chunked one), with the state read from and written back to the
+ * pool in place.  For each sequence i in [0, N) and head h:
+ *   S = cache_row[idx[i]][h]   if 0 <= idx[i] < num_rows and (init_flags is
+ *                              NULL or init_flags[i]),   0 otherwise
+ *   for t in [0, T):  S = Diag(alpha_t) S;  delta = v_t - S^T k^_t;
+ *                     S = S + beta_t k^_t delta^T;  out_t = scale S^T q^_t
+ *   cache_row[idx[i]][h] = S   if 0 <= idx[i] < num_rows (converted to the
+ *                              cache dtype; bf16 rounds to nearest even)
+ * alpha, k^, q^ and beta as in kda_chunk_fwd (flags KDA_L2NORM_QK,
+ * KDA_BETA_SIGMOID, KDA_GATE_IN_KERNEL; the gate is a natural-log decay,
+ * KDA_USE_EXP2 is accepted and changes nothing).  All arithmetic fp32.
+ * Layouts: q, k [N, T, H, dk], v and out [N, T, H, dv] of qkv_dtype; g
+ * [N, T, H, dk] and beta [N, T, H] fp32; the pool holds num_rows rows,
+ * row_stride_elems apart, whose first H*dk*dv elements are the states
+ * [H, dk, dv] (K-first, as final_state), the rest of a row untouched;
+ * idx [N] int32/int64; init_flags [N] bool or NULL.  Valid rows must be
+ * unique (caller precondition, not checked).  N == 0 launches nothing.
+ * Errors: KDA_ERR_INVALID_ARG (null pointers with N > 0, N < 0, T < 1,
+ * H < 1, num_rows < 1, row_stride_elems < H*dk*dv, unknown flags, a_log
+ * missing with KDA_GATE_IN_KERNEL), KDA_ERR_UNSUPPORTED (dk or dv not 64 /
+ * 128, KDA_REUSE_PREP / KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL /
+ * KDA_STATE_V_FIRST), KDA_ERR_CUDA.
+ */
+typedef struct {
+  int32_t N, T, H, dk, dv;
+  kda_dtype qkv_dtype;
+  const void *q, *k, *v;
+  const float *g;
+  const float *a_log, *dt_bias;
+  const float *beta;
+  float scale, eps;
+  uint32_t flags;
+  void *out;
+  void *cache;
+  kda_dtype cache_dtype;
+  int64_t num_rows, row_stride_elems;
+  const void *idx;
+  kda_index_dtype idx_dtype;
+  const bool *init_flags;
+} kda_decode_args;
+
+kda_status kda_recurrent_step(const kda_decode_args *args, kda_stream_t stream);
+
 /* Reads and clears the device error word kept at the start of a forward or
  * summary workspace: synchronises the stream, returns KDA_OK or
  * KDA_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up.  Every

@@ -146,3 +146,31 @@ def test_host_io_checks(lib):
     assert f(_args(q=None)) == 1
     assert f(_args()) == 4                                       # no workspace
     assert lib.kda_chunk_fwd_host(None, None) == 1
+
+
+def test_decode_checks(lib):
+    def args(**kw):
+        a = kda.kda_decode_args()
+        a.N, a.T, a.H, a.dk, a.dv = 4, 1, 2, 128, 128
+        a.qkv_dtype, a.cache_dtype, a.idx_dtype = kda.KDA_BF16, kda.KDA_F32, kda.KDA_I32
+        base = 1 << 20
+        a.q, a.k, a.v, a.g, a.beta, a.out, a.cache, a.idx = (base * (i + 1) for i in range(8))
+        a.num_rows, a.row_stride_elems = 8, 2 * 128 * 128
+        a.scale, a.eps = 0.088, 1e-6
+        for key, val in kw.items():
+            setattr(a, key, val)
+        return a
+    f = lambda a: lib.kda_recurrent_step(ctypes.byref(a), None)
+    assert f(args(T=0)) == 1
+    assert f(args(N=-1)) == 1
+    assert f(args(q=None)) == 1
+    assert f(args(idx=None)) == 1
+    assert f(args(row_stride_elems=100)) == 1
+    assert f(args(num_rows=0)) == 1
+    assert f(args(dk=96)) == 2
+    assert f(args(flags=kda.KDA_REUSE_PREP)) == 2
+    assert f(args(flags=kda.KDA_SAFE_GATE)) == 2
+    assert f(args(flags=kda.KDA_GATE_IN_KERNEL)) == 1   # a_log missing
+    assert f(args(flags=1 << 20)) == 1
+    assert f(args(N=0, q=None, idx=None)) == 0           # nothing to do
+    assert lib.kda_recurrent_step(None, None) == 1
