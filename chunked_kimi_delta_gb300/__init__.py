@@ -471,7 +471,9 @@ def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=N
                        gate_in_kernel=False, out=None, stream=None):
     """Recurrent decode step on pool states, in place: q, k, g [N, T, H, dk],
     v [N, T, H, dv], beta [N, T, H]; ``cache`` [rows, H, dk, dv] (any row
-    stride); ``idx`` [N] rows of the pool.  Returns out [N, T, H, dv].  See
+    stride); ``idx`` [N] rows of the pool.  Returns out [N, T, H, dv].
+    ``workspace``: a device tensor of >= 256 bytes (error word; selects the
+    streaming kernel), "auto" (a fresh one) or None (direct kernel).  See
     ``kda_recurrent_step`` in include/kda.h."""
     torch = _torch()
     lib = load_library()

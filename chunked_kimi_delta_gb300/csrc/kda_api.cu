@@ -512,6 +512,7 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out || !a->cache || !a->idx)
     return KDA_ERR_INVALID_ARG;
   if ((int64_t)a->N * a->T * a->H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   GateParams gp;
   gp.a_log = a->a_log;
   gp.dt_bias = a->dt_bias;
@@ -520,8 +521,7 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   gp.flags = a->flags;
   return cuda_status(launch_decode(a->qkv_dtype, a->cache_dtype, a->idx_dtype, a->dk, a->dv, a->N,
                                    a->T, a->H, a->q, a->k, a->v, a->g, a->beta, gp, a->out, a->cache,
-                                   a->num_rows, a->row_stride_elems, a->idx, a->init_flags,
-                                   reinterpret_cast<cudaStream_t>(stream)));
+                                   a->num_rows, a->row_stride_elems, a->idx, a->init_flags, st));
 }
 
 kda_status kda_get_device_status(void *workspace, kda_stream_t stream) {

@@ -296,6 +296,8 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
  * [H, dk, dv] (K-first, as final_state), the rest of a row untouched;
  * idx [N] int32/int64; init_flags [N] bool or NULL.  Valid rows must be
  * unique (caller precondition, not checked).  N == 0 launches nothing.
+ * Pools whose base and row stride are 16-byte aligned move states with
+ * vector accesses, others element by element (same results).
  * Errors: KDA_ERR_INVALID_ARG (null pointers with N > 0, N < 0, T < 1,
  * H < 1, num_rows < 1, row_stride_elems < H*dk*dv, unknown flags, a_log
  * missing with KDA_GATE_IN_KERNEL), KDA_ERR_UNSUPPORTED (dk or dv not 64 /

@@ -24,12 +24,15 @@ def _pool(rows, H, dk, dv, dtype, gap, seed):
                                               ("bf16", torch.bfloat16)])
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
 @pytest.mark.parametrize("T", [1, 5])
-def test_decode_against_oracle(cuda_lib, dtype, pool_dtype, dk, dv, T):
+@pytest.mark.parametrize("layout", ["aligned", "unaligned"])
+def test_decode_against_oracle(cuda_lib, dtype, pool_dtype, dk, dv, T, layout):
     N, H, rows = 6, 3, 9
     cfg = KdaConfig("decode", B=N, T=T, H=H, dk=dk, dv=dv, dtype=dtype, beta_sigmoid=True,
                     gate_in_kernel=True, seed=dk + dv + T)
     inp = make(cfg)
-    base, pool = _pool(rows, H, dk, dv, pool_dtype, gap=40, seed=T)
+    # gap 40 keeps the rows 16-byte aligned (vector accesses); gap 3 does not
+    # (element-wise accesses)
+    base, pool = _pool(rows, H, dk, dv, pool_dtype, gap=40 if layout == "aligned" else 3, seed=T)
     before = base.clone()
     idx = torch.tensor([4, -1, 0, 9, 7, 2], dtype=torch.int32)     # -1 and 9 (= rows) invalid
     flags = torch.tensor([True, True, False, True, True, True])       # row 0: start from zero
@@ -104,3 +107,23 @@ def test_decode_matches_chunked_forward(cuda_lib):
     check(out.reshape(o_ref.shape), o_ref, "bf16", "decode o")
     check(pool, f_ref, "bf16", "decode state")
     check(o_c.reshape(o_ref.shape), o_ref, "bf16", "chunked o")
+
+
+def test_decode_layouts_agree_bit_for_bit(cuda_lib):
+    """Vector and element-wise state accesses compute the same thing:
+    identical outputs and states on a 64-sequence, 32-head pool step."""
+    N, H, dk, dv, rows = 64, 32, 128, 128, 512
+    cfg = KdaConfig("decode_forms", B=N, T=1, H=H, dk=dk, dv=dv, dtype="bf16", beta_sigmoid=True,
+                    gate_in_kernel=True, seed=12)
+    inp = make(cfg, device="cuda")
+    _, pool = _pool(rows, H, dk, dv, torch.float32, gap=0, seed=2)
+    base2 = torch.zeros(rows, H * dk * dv + 3, device="cuda")
+    pool2 = base2[:, :H * dk * dv].view(rows, H, dk, dv)
+    pool2.copy_(pool)
+    idx = torch.randperm(rows, generator=torch.Generator().manual_seed(0))[:N].to(torch.int32).cuda()
+    kw = dict(scale=scale_of(cfg), a_log=inp["a_log"], dt_bias=inp["dt_bias"], beta_sigmoid=True,
+              gate_in_kernel=True)
+    o1 = cuda_lib.kda_recurrent_step(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], pool, idx, **kw)
+    o2 = cuda_lib.kda_recurrent_step(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], pool2, idx, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(pool, pool2)
