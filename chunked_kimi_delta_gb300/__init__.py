@@ -52,6 +52,7 @@ class kda_fwd_args(ctypes.Structure):
         ("out", ctypes.c_void_p), ("final_state", ctypes.c_void_p),
         ("h_out", ctypes.c_void_p), ("v_new_out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("Hk", ctypes.c_int32),
     ]
 
 
@@ -66,7 +67,7 @@ class kda_decode_args(ctypes.Structure):
         ("flags", ctypes.c_uint32), ("out", ctypes.c_void_p), ("cache", ctypes.c_void_p),
         ("cache_dtype", ctypes.c_int), ("num_rows", ctypes.c_int64),
         ("row_stride_elems", ctypes.c_int64), ("idx", ctypes.c_void_p), ("idx_dtype", ctypes.c_int),
-        ("init_flags", ctypes.c_void_p),
+        ("init_flags", ctypes.c_void_p), ("Hk", ctypes.c_int32),
     ]
 
 
@@ -152,12 +153,29 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _check_shapes(q, k, v, g, beta, out):
+    """q, k [.., Hk, dk]; v, out [.., H, dv]; g [.., H, dk]; beta [.., H]
+    with the same leading dims, Hk dividing H (the kernels trust these)."""
+    lead, H = tuple(v.shape[:-2]), v.shape[-2]
+    if k.shape != q.shape or tuple(q.shape[:-2]) != lead:
+        raise ValueError("q and k must be [.., Hk, dk] with v's leading dims")
+    if q.shape[-2] < 1 or H % q.shape[-2] != 0:
+        raise ValueError("the key heads of q/k must divide the value heads of v")
+    if tuple(g.shape) != lead + (H, q.shape[-1]):
+        raise ValueError("g must be [.., H, dk]")
+    if tuple(beta.shape) != lead + (H,):
+        raise ValueError("beta must be [.., H]")
+    if out is not None and out.shape != v.shape:
+        raise ValueError("out must have v's shape")
+
+
 def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias=None,
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
                   gate_in_kernel=False, use_exp2=False, extra_flags=0, out=None,
                   final_state=None, h_out=None, v_new_out=None) -> kda_fwd_args:
     """Fills a ``kda_fwd_args`` from tensors (BSND [B,T,H,D], or TND [T,H,D]
-    with ``cu_seqlens``)."""
+    with ``cu_seqlens``).  q and k may carry fewer heads than v (grouped key
+    heads, Hk dividing H): value head h reads key head h // (H // Hk)."""
     _contig(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state,
             h_out, v_new_out)
     a = kda_fwd_args()
@@ -172,7 +190,8 @@ def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
             raise ValueError("with cu_seqlens, q/k/v are [T_total, H, D]")
         a.num_seqs = cu_seqlens.numel() - 1
         a.cu_seqlens = _ptr(cu_seqlens)
-    a.H, a.dk, a.dv, a.chunk = q.shape[-2], q.shape[-1], v.shape[-1], CHUNK
+    _check_shapes(q, k, v, g, beta, out)
+    a.H, a.Hk, a.dk, a.dv, a.chunk = v.shape[-2], q.shape[-2], q.shape[-1], v.shape[-1], CHUNK
     a.qkv_dtype = _dtype_code(q)
     a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
     a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
@@ -217,9 +236,9 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
     else:
         N = 1 if q.dim() == 3 else q.shape[0]
     if out is None:
-        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     if output_final_state and final_state is None:
-        final_state = torch.empty(N, q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+        final_state = torch.empty(N, v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
                                   device=q.device)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
@@ -252,10 +271,10 @@ def prepare_chunk_fwd_host(q, k, v, g, beta, *, device=None, output_final_state=
             raise ValueError("kda_chunk_fwd_host takes q, k, v, g, beta in host memory")
     out = kw.pop("out", None)
     if out is None:
-        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, pin_memory=True)
+        out = torch.empty(v.shape, dtype=q.dtype, pin_memory=True)
     fin = kw.pop("final_state", None)
     if output_final_state and fin is None:
-        fin = torch.empty(q.shape[0], q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+        fin = torch.empty(q.shape[0], v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
                           device=device)
     a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
     ws = _workspace(lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(a)), device, workspace)
@@ -294,9 +313,9 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_lo
     else:
         N = 1 if q.dim() == 3 else q.shape[0]
     if out is None:
-        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     if output_final_state and final_state is None:
-        final_state = torch.empty(N, q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+        final_state = torch.empty(N, v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
                                   device=q.device)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
@@ -317,10 +336,10 @@ def prepare_chunk_fwd(q, k, v, g, beta, *, output_final_state=True, workspace=No
     N = (cu.numel() - 1) if cu is not None else (1 if q.dim() == 3 else q.shape[0])
     out = kw.pop("out", None)
     if out is None:
-        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     fin = kw.pop("final_state", None)
     if output_final_state and fin is None:
-        fin = torch.empty(N, q.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+        fin = torch.empty(N, v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
                           device=q.device)
     a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
@@ -335,7 +354,7 @@ def prepare_segment_summary(q, k, v, g, beta, seg_bounds, *, M=None, S_tilde=Non
     torch = _torch()
     lib = load_library()
     S = seg_bounds.numel() - 1
-    H, K, V = q.shape[-2], q.shape[-1], v.shape[-1]
+    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
     if M is None:
         M = torch.empty(S, H, K, K, dtype=torch.float32, device=q.device)
     if S_tilde is None:
@@ -382,7 +401,7 @@ def _segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_lo
     torch = _torch()
     lib = load_library()
     S = seg_bounds.numel() - 1
-    H, K, V = q.shape[-2], q.shape[-1], v.shape[-1]
+    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
     if M is None:
         M = torch.empty(S, H, K, K, dtype=torch.float32, device=q.device)
     if S_tilde is None:
@@ -469,12 +488,11 @@ def kda_state_scatter(cache, idx, packed, *, stream=None):
 def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=None, eps=1e-6,
                        a_log=None, dt_bias=None, l2norm_qk=True, beta_sigmoid=False,
                        gate_in_kernel=False, out=None, stream=None):
-    """Recurrent decode step on pool states, in place: q, k, g [N, T, H, dk],
-    v [N, T, H, dv], beta [N, T, H]; ``cache`` [rows, H, dk, dv] (any row
-    stride); ``idx`` [N] rows of the pool.  Returns out [N, T, H, dv].
-    ``workspace``: a device tensor of >= 256 bytes (error word; selects the
-    streaming kernel), "auto" (a fresh one) or None (direct kernel).  See
-    ``kda_recurrent_step`` in include/kda.h."""
+    """Recurrent decode step on pool states, in place: q, k [N, T, Hk, dk]
+    (Hk dividing H), g [N, T, H, dk], v [N, T, H, dv], beta [N, T, H];
+    ``cache`` [rows, H, dk, dv] (any row stride); ``idx`` [N] rows of the
+    pool.  Returns out [N, T, H, dv].  See ``kda_recurrent_step`` in
+    include/kda.h."""
     torch = _torch()
     lib = load_library()
     if q.dim() != 4:
@@ -483,11 +501,13 @@ def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=N
     if init_flags is not None and init_flags.dtype != torch.bool:
         raise TypeError("init_flags must be bool")
     if out is None:
-        out = torch.empty(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     _contig(out)
     n_rows, stride, _ = _rows(cache)
     a = kda_decode_args()
-    a.N, a.T, a.H, a.dk, a.dv = q.shape[0], q.shape[1], q.shape[2], q.shape[3], v.shape[3]
+    _check_shapes(q, k, v, g, beta, out)
+    a.N, a.T, a.H, a.Hk = q.shape[0], q.shape[1], v.shape[2], q.shape[2]
+    a.dk, a.dv = q.shape[3], v.shape[3]
     a.qkv_dtype = _dtype_code(q)
     a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
     a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)

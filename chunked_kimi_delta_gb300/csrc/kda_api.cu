@@ -28,6 +28,7 @@ constexpr uint32_t kRejectedFlags = KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL | KDA_S
 kda_status check_common(const kda_fwd_args *a) {
   if (!a) return KDA_ERR_INVALID_ARG;
   if (a->B < 1 || a->T < 0 || a->H < 1) return KDA_ERR_INVALID_ARG;
+  if (a->Hk < 0 || (a->Hk > 0 && a->H % a->Hk != 0)) return KDA_ERR_INVALID_ARG;
   if (a->flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
   if (a->qkv_dtype != KDA_F32 && a->qkv_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   const bool any_tokens = (int64_t)a->B * a->T > 0;
@@ -54,16 +55,23 @@ kda_status check_fwd(const kda_fwd_args *a) {
   return KDA_OK;
 }
 
+// Heads of q and k (grouped key heads when fewer than H).
+inline int key_heads(const kda_fwd_args *a) { return a->Hk > 0 ? a->Hk : a->H; }
+
 FwdPlan fwd_plan(const kda_fwd_args *a) {
   const bool ragged = a->cu_seqlens != nullptr;
   const int64_t T_tot = (int64_t)a->B * a->T;
   const int32_t N = ragged ? a->num_seqs : a->B;
-  return make_plan(T_tot, N, ragged, a->T, a->H, a->dk, a->dv);
+  FwdPlan p = make_plan(T_tot, N, ragged, a->T, a->H, a->dk, a->dv);
+  p.Hk = key_heads(a);
+  return p;
 }
 
 FwdPlan summary_plan(const kda_fwd_args *a, int32_t num_segments) {
   const int64_t T_tot = (int64_t)a->B * a->T;
-  return make_plan(T_tot, num_segments, true, a->T, a->H, a->dk, a->dv);
+  FwdPlan p = make_plan(T_tot, num_segments, true, a->T, a->H, a->dk, a->dv);
+  p.Hk = key_heads(a);
+  return p;
 }
 
 // The tensor-core path takes bf16 inputs with d_k = d_v = 128; every other
@@ -164,7 +172,8 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
   const size_t off_co = tc ? tc_plan(p).off_chunk_off : p.off_chunk_off;
   si.chunk_off = reinterpret_cast<int32_t *>(ws + off_co);
   tcp::TcMaps maps;
-  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, maps)) return KDA_ERR_CUDA;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps))
+    return KDA_ERR_CUDA;
 
   const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
   cudaError_t e = keep_err ? cudaSuccess : cudaMemsetAsync(ws, 0, 4, st);  // device error word
@@ -177,7 +186,8 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess && !reuse) e = mark();
     if (e == cudaSuccess && !reuse)
-      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H,
+                              p.Hk, pkg, err, st);
     if (e == cudaSuccess) e = mark();
     if (e == cudaSuccess) {
       tcp::ChainArgs ca{};
@@ -284,7 +294,8 @@ HostPlan host_plan(const kda_fwd_args *a) {
   h.sub_bytes = plan_bytes(&b, fwd_plan(&b));
   o = align256(o + h.sub_bytes);
   const size_t tok = (size_t)a->B * h.Tb * a->H;  // token-heads of a block
-  h.in_bytes = tok * ((size_t)(2 * a->dk + a->dv) * h.esz + (size_t)a->dk * 4 + 4);
+  const size_t tok_k = (size_t)a->B * h.Tb * key_heads(a);
+  h.in_bytes = tok_k * 2 * a->dk * h.esz + tok * ((size_t)a->dv * h.esz + (size_t)a->dk * 4 + 4);
   h.out_bytes = tok * a->dv * h.esz;
   for (int j = 0; j < 2; ++j) { h.off_in[j] = o; o = align256(o + h.in_bytes); }
   for (int j = 0; j < 2; ++j) { h.off_out[j] = o; o = align256(o + h.out_bytes); }
@@ -361,7 +372,7 @@ kda_status kda_chunk_fwd_host(const kda_fwd_args *a, kda_stream_t stream) {
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.out, ev_start, 0);
 
   const int64_t B = a->B, T = a->T, H = a->H;
-  const size_t rq = (size_t)H * a->dk * hp.esz, rv = (size_t)H * a->dv * hp.esz;
+  const size_t rq = (size_t)key_heads(a) * a->dk * hp.esz, rv = (size_t)H * a->dv * hp.esz;
   const size_t rg = (size_t)H * a->dk * 4, rb = (size_t)H * 4;
   for (int64_t t = 0; t < hp.nblk && e == cudaSuccess; ++t) {
     const int j = (int)(t & 1);
@@ -426,7 +437,8 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
   const bool tc = use_tc(a);
   si.chunk_off = reinterpret_cast<int32_t *>(ws + (tc ? tc_plan(p).off_chunk_off : p.off_chunk_off));
   tcp::TcMaps maps;
-  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, maps)) return KDA_ERR_CUDA;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps))
+    return KDA_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
   if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
@@ -434,7 +446,8 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     char *pkg = ws + tc_plan(p).off_pkg;
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess)
-      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H,
+                              p.Hk, pkg, err, st);
     if (e == cudaSuccess) e = tcp::launch_tc_summary(pkg, S_tilde, M, si, a->H, err, st);
   } else {
     if (e == cudaSuccess)
@@ -500,6 +513,7 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
 
 kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   if (!a || a->N < 0 || a->T < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
+  if (a->Hk < 0 || (a->Hk > 0 && a->H % a->Hk != 0)) return KDA_ERR_INVALID_ARG;
   if (a->flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
   if (a->flags & (kRejectedFlags | KDA_REUSE_PREP)) return KDA_ERR_UNSUPPORTED;
   if ((a->dk != 64 && a->dk != 128) || (a->dv != 64 && a->dv != 128)) return KDA_ERR_UNSUPPORTED;
@@ -520,7 +534,8 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   gp.eps = a->eps;
   gp.flags = a->flags;
   return cuda_status(launch_decode(a->qkv_dtype, a->cache_dtype, a->idx_dtype, a->dk, a->dv, a->N,
-                                   a->T, a->H, a->q, a->k, a->v, a->g, a->beta, gp, a->out, a->cache,
+                                   a->T, a->H, a->Hk > 0 ? a->Hk : a->H, a->q, a->k, a->v, a->g,
+                                   a->beta, gp, a->out, a->cache,
                                    a->num_rows, a->row_stride_elems, a->idx, a->init_flags, st));
 }
 

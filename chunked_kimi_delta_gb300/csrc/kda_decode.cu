@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta, GateParams gp,
               Tin *__restrict__ out, Tc *cache, int64_t num_rows, int64_t row_stride,
-              const Tidx *__restrict__ idx, const bool *__restrict__ init_flags, int T, int H) {
+              const Tidx *__restrict__ idx, const bool *__restrict__ init_flags, int T, int H,
+              int Hk) {
   constexpr int NQ = VS / 4;                // column quads of the slice
   constexpr int RG = kDecThreads / NQ;      // row groups
   constexpr int R = K / RG;                 // rows per thread
@@ -125,11 +126,12 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
   };
 
   for (int t = 0; t < T; ++t) {
-    const int64_t tok = ((int64_t)n * T + t) * H + h;  // token-head index
+    const int64_t tok = ((int64_t)n * T + t) * H + h;              // token-head index
+    const int64_t tokk = ((int64_t)n * T + t) * Hk + h / (H / Hk);  // and of q, k
     // ---- stage the token: gate, raw q / k (norms below), this slice of v, beta
     float kq2 = 0.f;  // k^2 (threads < K) or q^2 (threads K .. 2K-1)
     if (tid < K) {
-      const float kc = ldf(k + tok * K + tid);
+      const float kc = ldf(k + tokk * K + tid);
       s_k[tid] = kc;
       kq2 = kc * kc;
       float gv = g[tok * K + tid];
@@ -139,7 +141,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
       }
       s_a[tid] = expf(gv);
     } else if (tid < 2 * K) {
-      const float qc = ldf(q + tok * K + (tid - K));
+      const float qc = ldf(q + tokk * K + (tid - K));
       s_q[tid - K] = qc;
       kq2 = qc * qc;
     }
@@ -222,14 +224,15 @@ template <typename Tin, typename Tc, typename Tidx>
 cudaError_t dispatch_kv(int dk, int dv, bool aligned, int64_t units, cudaStream_t st, const void *q,
                         const void *k, const void *v, const float *g, const float *beta,
                         const GateParams &gp, void *out, void *cache, int64_t num_rows,
-                        int64_t row_stride, const void *idx, const bool *init_flags, int T, int H) {
+                        int64_t row_stride, const void *idx, const bool *init_flags, int T, int H,
+                        int Hk) {
   const Tin *qq = static_cast<const Tin *>(q), *kk = static_cast<const Tin *>(k),
             *vv = static_cast<const Tin *>(v);
 #define KDA_DEC(KK, VV, VEC)                                                                      \
   decode_kernel<Tin, Tc, Tidx, KK, VV, VV, VEC>                                                   \
       <<<(unsigned)units, kDecThreads, 0, st>>>(                                                  \
           qq, kk, vv, g, beta, gp, static_cast<Tin *>(out), static_cast<Tc *>(cache), num_rows,     \
-          row_stride, static_cast<const Tidx *>(idx), init_flags, T, H)
+          row_stride, static_cast<const Tidx *>(idx), init_flags, T, H, Hk)
 #define KDA_DEC2(KK, VV)              \
   if (aligned) KDA_DEC(KK, VV, true); \
   else KDA_DEC(KK, VV, false)
@@ -245,7 +248,7 @@ cudaError_t dispatch_kv(int dk, int dv, bool aligned, int64_t units, cudaStream_
 }  // namespace
 
 cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_dtype idx_dtype,
-                          int dk, int dv, int N, int T, int H, const void *q, const void *k,
+                          int dk, int dv, int N, int T, int H, int Hk, const void *q, const void *k,
                           const void *v, const float *g, const float *beta, const GateParams &gp,
                           void *out, void *cache, int64_t num_rows, int64_t row_stride,
                           const void *idx, const bool *init_flags, cudaStream_t st) {
@@ -258,7 +261,7 @@ cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_
   const bool aligned = (reinterpret_cast<uintptr_t>(cache) & 15u) == 0 && ((size_t)row_stride * esz) % 16 == 0;
 #define KDA_DEC_IDX(TI, TC, TX)                                                                     \
   return dispatch_kv<TI, TC, TX>(dk, dv, aligned, units, st, q, k, v, g, beta, gp, out, cache,       \
-                                 num_rows, row_stride, idx, init_flags, T, H)
+                                 num_rows, row_stride, idx, init_flags, T, H, Hk)
   const bool ibf = qkv_dtype == KDA_BF16, cbf = cache_dtype == KDA_BF16, i64 = idx_dtype == KDA_I64;
   if (ibf && cbf && i64) KDA_DEC_IDX(__nv_bfloat16, __nv_bfloat16, int64_t);
   if (ibf && cbf) KDA_DEC_IDX(__nv_bfloat16, __nv_bfloat16, int32_t);

@@ -67,7 +67,7 @@ template <typename Tin, int K, int V>
 __global__ void __launch_bounds__(256)
 generic_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                      const Tin *__restrict__ v, const float *__restrict__ g,
-                     const float *__restrict__ beta, GateParams gp, SeqInfo s, int H,
+                     const float *__restrict__ beta, GateParams gp, SeqInfo s, int H, int Hk,
                      float *__restrict__ w_out, float *__restrict__ u_out,
                      float *__restrict__ qg_out, float *__restrict__ kg_out,
                      float *__restrict__ aqk_out, float *__restrict__ gc_out) {
@@ -97,8 +97,9 @@ generic_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float qv = 0.f, kv = 0.f, gv = 0.f;
     if (r < len) {
       const int64_t off = ((t0 + r) * H + h) * (int64_t)K + cc;
-      qv = to_f32(q[off]);
-      kv = to_f32(k[off]);
+      const int64_t offk = ((t0 + r) * Hk + h / (H / Hk)) * (int64_t)K + cc;  // grouped key heads
+      qv = to_f32(q[offk]);
+      kv = to_f32(k[offk]);
       gv = g[off];
       if (gate) {
         const float z = gv + (gp.dt_bias ? gp.dt_bias[h * K + cc] : 0.f);
@@ -349,7 +350,7 @@ cudaError_t intra_dispatch(const void *q, const void *k, const void *v, const fl
   dim3 grid((unsigned)p.nchunks, p.H);
   kern<<<grid, 256, smem, st>>>(
       static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v), g,
-      beta, gp, s, p.H, reinterpret_cast<float *>(ws + p.off_w),
+      beta, gp, s, p.H, p.Hk, reinterpret_cast<float *>(ws + p.off_w),
       reinterpret_cast<float *>(ws + p.off_u), reinterpret_cast<float *>(ws + p.off_qg),
       reinterpret_cast<float *>(ws + p.off_kg), reinterpret_cast<float *>(ws + p.off_aqk),
       reinterpret_cast<float *>(ws + p.off_gc));

@@ -84,6 +84,7 @@ inline int64_t chunks_upper_bound(int64_t T_tot, int32_t N, bool ragged, int32_t
 struct FwdPlan {
   int64_t T_tot, nchunks;
   int32_t N, H, K, V;
+  int32_t Hk;  // heads of q and k; value head h reads key head h / (H / Hk)
   size_t off_chunk_off, off_w, off_u, off_qg, off_kg, off_aqk, off_gc, total;
 };
 
@@ -94,6 +95,7 @@ inline FwdPlan make_plan(int64_t T_tot, int32_t N, bool ragged, int32_t T, int H
   p.T_tot = T_tot;
   p.N = N;
   p.H = H;
+  p.Hk = H;
   p.K = K;
   p.V = V;
   p.nchunks = chunks_upper_bound(T_tot, N, ragged, T);
@@ -140,7 +142,7 @@ cudaError_t launch_chunk_map(const SeqInfo &s, int32_t *chunk_off, cudaStream_t 
 
 // Recurrent decode step on pool rows (kda_decode.cu).
 cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_dtype idx_dtype,
-                          int dk, int dv, int N, int T, int H, const void *q, const void *k,
+                          int dk, int dv, int N, int T, int H, int Hk, const void *q, const void *k,
                           const void *v, const float *g, const float *beta, const GateParams &gp,
                           void *out, void *cache, int64_t num_rows, int64_t row_stride,
                           const void *idx, const bool *init_flags, cudaStream_t st);

@@ -154,11 +154,12 @@ struct TcMaps {
 // Encodes the four input tensor maps; false when the driver entry point is
 // unavailable or a map is rejected.
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
-                     int H, TcMaps &maps);
+                     int H, int Hk, TcMaps &maps);
 
 cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
                            const float *beta, const GateParams &gp, const SeqInfo &s,
-                           int64_t nchunks, int H, char *pkg, uint32_t *err, cudaStream_t st);
+                           int64_t nchunks, int H, int Hk, char *pkg, uint32_t *err,
+                           cudaStream_t st);
 
 struct ChainArgs {
   const char *pkg;

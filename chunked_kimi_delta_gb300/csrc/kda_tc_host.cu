@@ -41,11 +41,11 @@ bool encode3(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void 
 }  // namespace
 
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
-                     int H, TcMaps &maps) {
+                     int H, int Hk, TcMaps &maps) {
   if (T_tot <= 0) return false;
-  return encode3(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, K, H, T_tot, 128,
+  return encode3(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, K, Hk, T_tot, 128,
                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode3(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, K, H, T_tot, 128,
+         encode3(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, K, Hk, T_tot, 128,
                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
          encode3(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, V, H, T_tot, 64,
                  CU_TENSOR_MAP_SWIZZLE_128B) &&

@@ -135,6 +135,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ uint2 ldg_u2_hint(const void *p, uint64_t pol) {
   uint2 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(NT, 2)
 tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restrict__ qg_in,
                const __nv_bfloat16 *__restrict__ kg_in, const float *__restrict__ xg_in,
                const float *__restrict__ beta, GateParams gp, SeqInfo s, int64_t nitems, int H,
-               char *__restrict__ pkg, uint32_t *err) {
+               int Hk, char *__restrict__ pkg, uint32_t *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *rq = reinterpret_cast<float *>(sm + M_RQ);
@@ -179,7 +184,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   const bool l2n = (gp.flags & KDA_L2NORM_QK) != 0;
   const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
   constexpr float kLog2e = 1.4426950408889634f;
-  const int64_t rowH = (int64_t)H * 128;  // elements between consecutive tokens
+  const int64_t rowH = (int64_t)H * 128;    // elements between tokens of the gate input
+  const int64_t rowHk = (int64_t)Hk * 128;  // and of q, k (grouped key heads)
+  const int grp = H / Hk;                   // value heads per key head
 
   if (warp == 0) {
     tc::tmem_alloc(tslot, TMEM_COLS);
@@ -205,6 +212,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 
   const int64_t G = gridDim.x;
   const uint64_t pol_once = policy_evict_first();
+  // q, k rows shared by a group of value heads are read once per head
+  const uint64_t pol_qk = grp > 1 ? policy_evict_normal() : pol_once;
   // thread 0 keeps count of the loads and MMAs it started, for the drain
   int64_t v_issued = 0, v_done = 0;
   bool mma_pending = false;
@@ -227,7 +236,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     const int len = it.len, h = it.h;
     const int64_t t0 = it.t0;
     uint8_t *pk = reinterpret_cast<uint8_t *>(pkg + (size_t)(it.gc * H + h) * PK_BYTES);
-    const int64_t base_h = t0 * rowH + (int64_t)h * 128;  // element offset of (t0, h, 0)
+    const int64_t base_h = t0 * rowH + (int64_t)h * 128;           // (t0, h, 0) of the gate input
+    const int64_t base_k = t0 * rowHk + (int64_t)(h / grp) * 128;  // (t0, h / grp, 0) of q, k
     Item nx;
     bool okn = false;
     if (tid == 0) {
@@ -236,8 +246,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       okn = wn < nitems && nx.ok;
       put_slot(slots[(i + 1) & 1], nx, okn);
       if (okn) {
-        tma_prefetch_l2_3d(&maps.q, 0, nx.h, (int32_t)nx.t0);
-        tma_prefetch_l2_3d(&maps.k, 0, nx.h, (int32_t)nx.t0);
+        tma_prefetch_l2_3d(&maps.q, 0, nx.h / grp, (int32_t)nx.t0);
+        tma_prefetch_l2_3d(&maps.k, 0, nx.h / grp, (int32_t)nx.t0);
         tma_prefetch_l2_3d(&maps.x, 0, nx.h, (int32_t)nx.t0);
       }
     }
@@ -255,13 +265,13 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = 8 * warp + rr;
-        const int64_t off = base_h + r * rowH + c0;
+        const int64_t off = base_h + r * rowH + c0, offk = base_k + r * rowHk + c0;
         qv[rr] = make_uint2(0, 0);
         kv[rr] = make_uint2(0, 0);
         xs[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < len) {
-          qv[rr] = ldg_u2_hint(qg_in + off, pol_once);
-          kv[rr] = ldg_u2_hint(kg_in + off, pol_once);
+          qv[rr] = ldg_u2_hint(qg_in + offk, pol_qk);
+          kv[rr] = ldg_u2_hint(kg_in + offk, pol_qk);
           xs[rr] = ldg_f4_hint(xg_in + off, pol_once);
         }
       }
@@ -770,7 +780,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 
 cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
                            const float *beta, const GateParams &gp, const SeqInfo &s,
-                           int64_t nchunks, int H, char *pkg, uint32_t *err, cudaStream_t st) {
+                           int64_t nchunks, int H, int Hk, char *pkg, uint32_t *err,
+                           cudaStream_t st) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -787,7 +798,7 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
   const int grid = (int)(nitems < slots ? nitems : slots);
   tc_prep_kernel<<<grid, NT, SMEM_BYTES, st>>>(maps, static_cast<const __nv_bfloat16 *>(q),
                                               static_cast<const __nv_bfloat16 *>(k), x, beta, gp, s,
-                                              nitems, H, pkg, err);
+                                              nitems, H, Hk, pkg, err);
   return cudaGetLastError();
 }
 

@@ -85,6 +85,10 @@ enum {
  * Layout: tokens are BSND [B, T, H, D] when cu_seqlens is NULL, or TND
  * [T_total, H, D] packed sequences when cu_seqlens is given (then B must be
  * 1 and T = T_total).  q and k have d_k channels, v and out d_v channels.
+ * Grouped key heads (same design, section 4.2: q/k may have fewer heads
+ * than v): q and k carry Hk heads, v, g, beta, out and every state carry the
+ * H value heads; value head h reads key head h / (H / Hk).  Hk = 0 means
+ * Hk = H (every field named H below is the value-head count).
  * Every sequence starts from its own initial state (section 6.5 of the same
  * design); chunks restart at every sequence start, the last one may be
  * partial.
@@ -116,6 +120,8 @@ typedef struct {
   float *v_new_out;         /* [.., H, dv] fp32 corrected values u - w h, or NULL */
   void *workspace;          /* device scratch, >= kda_chunk_fwd_workspace_size   */
   size_t workspace_bytes;   /* and 256-byte aligned                              */
+  int32_t Hk;               /* key heads of q and k: 0 (= H) or a divisor of H;  */
+                            /* q, k are [.., Hk, dk]; otherwise INVALID_ARG      */
 } kda_fwd_args;
 
 /* Bytes of workspace kda_chunk_fwd needs for these arguments (0 when the
@@ -128,8 +134,8 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
  * With no tokens (B*T == 0, or only empty sequences) the final state is the
  * initial state; q/k/v/g/beta/out may then be NULL.
  * Errors: KDA_ERR_INVALID_ARG (null q/k/v/g/beta/out with tokens, B or H < 1,
- * T < 0, a_log
- * missing with KDA_GATE_IN_KERNEL, cu_seqlens with B != 1), KDA_ERR_UNSUPPORTED
+ * T < 0, Hk < 0 or not dividing H, a_log missing with KDA_GATE_IN_KERNEL,
+ * cu_seqlens with B != 1), KDA_ERR_UNSUPPORTED
  * (dk or dv not 64/128, chunk != 64, KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL /
  * KDA_STATE_V_FIRST), KDA_ERR_ALIGNMENT, KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
@@ -290,7 +296,7 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
  * alpha, k^, q^ and beta as in kda_chunk_fwd (flags KDA_L2NORM_QK,
  * KDA_BETA_SIGMOID, KDA_GATE_IN_KERNEL; the gate is a natural-log decay,
  * KDA_USE_EXP2 is accepted and changes nothing).  All arithmetic fp32.
- * Layouts: q, k [N, T, H, dk], v and out [N, T, H, dv] of qkv_dtype; g
+ * Layouts: q, k [N, T, Hk, dk], v and out [N, T, H, dv] of qkv_dtype; g
  * [N, T, H, dk] and beta [N, T, H] fp32; the pool holds num_rows rows,
  * row_stride_elems apart, whose first H*dk*dv elements are the states
  * [H, dk, dv] (K-first, as final_state), the rest of a row untouched;
@@ -299,7 +305,8 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
  * Pools whose base and row stride are 16-byte aligned move states with
  * vector accesses, others element by element (same results).
  * Errors: KDA_ERR_INVALID_ARG (null pointers with N > 0, N < 0, T < 1,
- * H < 1, num_rows < 1, row_stride_elems < H*dk*dv, unknown flags, a_log
+ * H < 1, Hk < 0 or not dividing H, num_rows < 1, row_stride_elems <
+ * H*dk*dv, unknown flags, a_log
  * missing with KDA_GATE_IN_KERNEL), KDA_ERR_UNSUPPORTED (dk or dv not 64 /
  * 128, KDA_REUSE_PREP / KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL /
  * KDA_STATE_V_FIRST), KDA_ERR_CUDA.
@@ -320,6 +327,8 @@ typedef struct {
   const void *idx;
   kda_index_dtype idx_dtype;
   const bool *init_flags;
+  int32_t Hk;               /* key heads of q and k ([N, T, Hk, dk]): 0 (= H) or */
+                            /* a divisor of H, value head h reads key head h/(H/Hk) */
 } kda_decode_args;
 
 kda_status kda_recurrent_step(const kda_decode_args *args, kda_stream_t stream);

@@ -70,6 +70,9 @@ def test_fwd_argument_checks(lib):
     assert f(_args(flags=kda.KDA_GATE_IN_KERNEL)) == 1          # a_log missing
     assert f(_args(q=(1 << 20) + 8)) == 3                        # misaligned
     assert f(_args(cu_seqlens=1 << 24, num_seqs=3)) == 1         # cu_seqlens needs B = 1
+    assert f(_args(Hk=3)) == 1                                   # key heads must divide H
+    assert f(_args(Hk=-1)) == 1
+    assert f(_args(Hk=2)) == 4                                   # grouped keys: valid
     assert f(_args()) == 4                                       # no workspace
     a = _args()
     need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(a))
@@ -79,6 +82,14 @@ def test_fwd_argument_checks(lib):
     a.workspace, a.workspace_bytes = (1 << 30) + 16, need
     assert f(a) == 3                                             # workspace not 256-aligned
     assert lib.kda_chunk_fwd(None, None) == 1
+
+
+def test_grouped_key_heads_shrink_host_staging(lib):
+    """Hk = 0 reads as Hk = H; fewer key heads stage fewer q/k bytes."""
+    size = lambda **kw: lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(_args(**kw)))
+    assert size(Hk=0) == size(Hk=4) > size(Hk=1) > 0
+    dev = lambda **kw: lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args(**kw)))
+    assert dev(Hk=1) == dev(Hk=0) > 0                            # the packages are per value head
 
 
 def test_workspace_grows_with_tokens(lib):
@@ -173,4 +184,33 @@ def test_decode_checks(lib):
     assert f(args(flags=kda.KDA_GATE_IN_KERNEL)) == 1   # a_log missing
     assert f(args(flags=1 << 20)) == 1
     assert f(args(N=0, q=None, idx=None)) == 0           # nothing to do
+    assert f(args(Hk=3, N=0)) == 1                       # key heads must divide H
+    assert f(args(Hk=-2, N=0)) == 1
+    assert f(args(Hk=1, N=0)) == 0
     assert lib.kda_recurrent_step(None, None) == 1
+
+
+def test_binding_shapes_for_grouped_key_heads():
+    """make_fwd_args reads H from v and Hk from q/k, and rejects shapes the
+    kernels would read past (host logic only, no launch)."""
+    import torch
+    B, T, H, Hk, dk, dv = 2, 5, 6, 2, 64, 64
+    q = torch.zeros(B, T, Hk, dk)
+    v = torch.zeros(B, T, H, dv)
+    g = torch.zeros(B, T, H, dk)
+    beta = torch.zeros(B, T, H)
+    a = kda.make_fwd_args(q, q, v, g, beta)
+    assert (a.H, a.Hk, a.dk, a.dv) == (H, Hk, dk, dv)
+    bad = [
+        dict(q=torch.zeros(B, T, 4, dk), k=torch.zeros(B, T, 4, dk)),   # 4 does not divide 6
+        dict(k=torch.zeros(B, T, H, dk)),                               # q, k differ
+        dict(g=torch.zeros(B, T, Hk, dk)),                              # gate per value head
+        dict(beta=torch.zeros(B, T, Hk)),
+        dict(out=torch.zeros(B, T, Hk, dv)),                            # out is v-shaped
+    ]
+    for kw in bad:
+        args = dict(q=q, k=q, v=v, g=g, beta=beta)
+        out = kw.pop("out", None)
+        args.update(kw)
+        with pytest.raises(ValueError):
+            kda.make_fwd_args(args["q"], args["k"], args["v"], args["g"], args["beta"], out=out)
