@@ -162,6 +162,10 @@ __device__ __forceinline__ void bulk_store_hint(void *dst, const void *src, uint
                : "memory");
 }
 
+// GROUPED: q, k have Hk < H heads (value head h reads key head h / (H / Hk));
+// the ungrouped instantiation shares the gate input's addressing, which keeps
+// its per-row address arithmetic out of the issue-bound load phase.
+template <bool GROUPED>
 __global__ void __launch_bounds__(NT, 2)
 tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restrict__ qg_in,
                const __nv_bfloat16 *__restrict__ kg_in, const float *__restrict__ xg_in,
@@ -185,8 +189,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
   constexpr float kLog2e = 1.4426950408889634f;
   const int64_t rowH = (int64_t)H * 128;    // elements between tokens of the gate input
-  const int64_t rowHk = (int64_t)Hk * 128;  // and of q, k (grouped key heads)
-  const int grp = H / Hk;                   // value heads per key head
+  const int64_t rowHk = GROUPED ? (int64_t)Hk * 128 : rowH;  // and of q, k
+  const int grp = GROUPED ? H / Hk : 1;                       // value heads per key head
 
   if (warp == 0) {
     tc::tmem_alloc(tslot, TMEM_COLS);
@@ -213,7 +217,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   const int64_t G = gridDim.x;
   const uint64_t pol_once = policy_evict_first();
   // q, k rows shared by a group of value heads are read once per head
-  const uint64_t pol_qk = grp > 1 ? policy_evict_normal() : pol_once;
+  const uint64_t pol_qk = GROUPED ? policy_evict_normal() : pol_once;
   // thread 0 keeps count of the loads and MMAs it started, for the drain
   int64_t v_issued = 0, v_done = 0;
   bool mma_pending = false;
@@ -237,7 +241,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     const int64_t t0 = it.t0;
     uint8_t *pk = reinterpret_cast<uint8_t *>(pkg + (size_t)(it.gc * H + h) * PK_BYTES);
     const int64_t base_h = t0 * rowH + (int64_t)h * 128;           // (t0, h, 0) of the gate input
-    const int64_t base_k = t0 * rowHk + (int64_t)(h / grp) * 128;  // (t0, h / grp, 0) of q, k
+    const int64_t base_k = t0 * rowHk + (int64_t)(GROUPED ? h / grp : h) * 128;  // (t0, h / grp, 0) of q, k
     Item nx;
     bool okn = false;
     if (tid == 0) {
@@ -265,7 +269,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = 8 * warp + rr;
-        const int64_t off = base_h + r * rowH + c0, offk = base_k + r * rowHk + c0;
+        const int64_t off = base_h + r * rowH + c0;
+        const int64_t offk = GROUPED ? base_k + r * rowHk + c0 : off;
         qv[rr] = make_uint2(0, 0);
         kv[rr] = make_uint2(0, 0);
         xs[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -789,16 +794,17 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = Hk != H ? tc_prep_kernel<true> : tc_prep_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int64_t nitems = nchunks * H;
   if (nitems == 0) return cudaSuccess;
   const int64_t slots = 2 * (int64_t)sms;
   const int grid = (int)(nitems < slots ? nitems : slots);
-  tc_prep_kernel<<<grid, NT, SMEM_BYTES, st>>>(maps, static_cast<const __nv_bfloat16 *>(q),
-                                              static_cast<const __nv_bfloat16 *>(k), x, beta, gp, s,
-                                              nitems, H, Hk, pkg, err);
+  kern<<<grid, NT, SMEM_BYTES, st>>>(maps, static_cast<const __nv_bfloat16 *>(q),
+                                     static_cast<const __nv_bfloat16 *>(k), x, beta, gp, s, nitems,
+                                     H, Hk, pkg, err);
   return cudaGetLastError();
 }
 
