@@ -1,5 +1,5 @@
-"""fp64 CPU oracle for the chunked KDA forward, segment summary, prefix scan
-and state-pool gather/scatter.
+"""fp64 CPU oracle for the chunked KDA forward, its backward, segment summary,
+prefix scan and state-pool gather/scatter.
 
 TEST INFRASTRUCTURE ONLY.  The product (the CUDA library under
 ``chunked_kimi_delta_gb300`` and its binding) never imports, links or calls
@@ -8,6 +8,8 @@ baseline leg of ``bench.py`` do.  The oracle shares no code with the CUDA path.
 
 * ``chunk_fwd``, ``preprocess``, ``segment_summary``, ``state_prefix_scan``:
   the token-by-token recurrence in C (``kda_oracle.c``), fp64.
+* ``chunk_bwd``: gradients of the same recurrence by reverse-mode
+  differentiation, token by token, in C, fp64.
 * ``chunked.py``: an independent fp64 chunked form of the same forward (the
   WY representation), used only to pin the recurrence.
 * ``state_copy.py``: gather/scatter as plain indexed copies.
@@ -72,8 +74,9 @@ def _lib():
         lib.kdaref_segment_summary.argtypes = [P, vp, i64, vp, vp, i32]
         lib.kdaref_state_prefix_scan.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, vp, vp]
         lib.kdaref_max_threads.argtypes = [i32]
+        lib.kdaref_chunk_bwd.argtypes = [P] + [vp] * 11 + [i32]
         for f in ("kdaref_chunk_fwd", "kdaref_preprocess", "kdaref_segment_summary",
-                  "kdaref_state_prefix_scan", "kdaref_max_threads"):
+                  "kdaref_state_prefix_scan", "kdaref_max_threads", "kdaref_chunk_bwd"):
             getattr(lib, f).restype = ctypes.c_int
         _lib_handle = lib
     return _lib_handle
@@ -203,3 +206,35 @@ def state_prefix_scan(M, S_tilde, S0=None):
     if one:
         return S_in[0], fin[0]
     return S_in, fin
+
+
+def chunk_bwd(prob: Problem, initial_state=None, d_out=None, d_final=None, *, nthreads=0):
+    """Gradients of L = sum(d_out * out) + sum(d_final * final_state) with
+    respect to the inputs as given (raw q, k; beta logits with
+    ``beta_sigmoid``; raw gate input x with ``gate_in_kernel``).  Returns a
+    dict: dq, dk, dg [T,H,dk]; dv [T,H,dv]; dbeta [T,H]; da_log [H] and
+    ddt_bias [H,dk] (zeros without ``gate_in_kernel``); d_initial
+    [N,H,dk,dv]."""
+    N, H, K, V, T = prob.num_seqs, prob.H, prob.dk, prob.dv, prob.T
+    S0 = _f64(initial_state)
+    if S0 is not None:
+        S0 = S0.reshape(N, H, K, V)
+    do = _f64(d_out)
+    if do is not None:
+        do = do.reshape(T, H, V)
+    dfin = _f64(d_final)
+    if dfin is not None:
+        dfin = dfin.reshape(N, H, K, V)
+    r = dict(dq=np.zeros((T, H, K)), dk=np.zeros((T, H, K)), dv=np.zeros((T, H, V)),
+             dg=np.zeros((T, H, K)), dbeta=np.zeros((T, H)), d_initial=np.zeros((N, H, K, V)))
+    dal = np.zeros((N, H))
+    ddt = np.zeros((N, H, K))
+    p = prob._c()
+    rc = _lib().kdaref_chunk_bwd(ctypes.byref(p), _ptr(S0), _ptr(do), _ptr(dfin), _ptr(r["dq"]),
+                                 _ptr(r["dk"]), _ptr(r["dv"]), _ptr(r["dg"]), _ptr(r["dbeta"]),
+                                 _ptr(dal), _ptr(ddt), _ptr(r["d_initial"]), nthreads)
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    r["da_log"] = dal.sum(axis=0)
+    r["ddt_bias"] = ddt.sum(axis=0)
+    return r

@@ -313,3 +313,212 @@ int kdaref_state_prefix_scan(const double *M, const double *S_tilde, const doubl
   free(T);
   return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward pass: gradients of  L = sum(d_out . out) + sum(d_final . final)
+ * with respect to every input of kdaref_chunk_fwd, by reverse-mode
+ * differentiation of the token recurrence above ([TPU] sections 1 and 2 list
+ * the same gradients: dq, dk, dv, dbeta, dg, dA_log, ddt_bias and the
+ * initial-state gradient dh0; [HP] section 5.2 npu_chunk_kda_bwd_finalize
+ * returns the same seven plus dh0 from bwd_dhu).
+ *
+ * Per token, with S' = Diag(alpha) S_{t-1}, delta = v - S'^T k^,
+ * S_t = S' + beta k^ delta^T and o_t = scale S_t^T q^, going backwards with
+ * dS = dL/dS_t (d_final at the last token of a sequence):
+ *   dS    += scale q^ do^T          dq^  = scale S_t do
+ *   ddelta = beta dS^T k^           dbeta = k^T dS delta     dk^ = beta dS delta
+ *   dv     = ddelta                 dS'  = dS - k^ ddelta^T  dk^ -= S' ddelta
+ *   dg_c   = alpha_c sum_j dS'_cj S_{t-1,cj}                 dS_{t-1} = Diag(alpha) dS'
+ * then through the preprocessing:
+ *   L2 norm (x^ = x r, r = (sum x^2 + eps)^-1/2):  dx = r dx^ - r^3 (x . dx^) x
+ *   sigmoid:  db = dbeta beta (1 - beta)
+ *   gate g = -exp(a_log) softplus(z), z = x + dt_bias:
+ *             dz = -exp(a_log) sigmoid(z) dg;  dx = dz;  ddt_bias += dz;  da_log += g dg
+ * The states S_{t-1} of a sequence are recomputed forward from checkpoints
+ * kept every KDAREF_CKPT tokens.
+ * ------------------------------------------------------------------------ */
+#define KDAREF_CKPT 64
+
+/* Raw-input gradients of one token from the gradients of its preprocessed
+ * values (dqh, dkh over K channels, dbeta, dgn = gradient of the natural-log
+ * decay).  dq, dk, dg are rows of [T, H, dk]; *db the token's beta gradient;
+ * dalog / ddtb accumulate this head's parameter gradients. */
+static void preprocess_bwd(const kdaref_problem *p, int64_t t, int h, const double *dqh,
+                           const double *dkh, double dbeta, const double *dgn, double *dq,
+                           double *dk, double *db, double *dg, double *dalog, double *ddtb) {
+  const int K = p->dk;
+  const int64_t row = t * p->H + h;
+  const double *q = p->q + row * K;
+  const double *k = p->k + row * K;
+  if (p->flags & KDAREF_L2NORM_QK) {
+    double sq = 0.0, sk = 0.0, pq = 0.0, pk = 0.0;
+    for (int c = 0; c < K; ++c) {
+      sq += q[c] * q[c];
+      sk += k[c] * k[c];
+      pq += q[c] * dqh[c];
+      pk += k[c] * dkh[c];
+    }
+    const double rq = 1.0 / sqrt(sq + p->eps), rk = 1.0 / sqrt(sk + p->eps);
+    for (int c = 0; c < K; ++c) {
+      dq[c] = rq * dqh[c] - rq * rq * rq * pq * q[c];
+      dk[c] = rk * dkh[c] - rk * rk * rk * pk * k[c];
+    }
+  } else {
+    for (int c = 0; c < K; ++c) { dq[c] = dqh[c]; dk[c] = dkh[c]; }
+  }
+  double b = p->beta[row];
+  if (p->flags & KDAREF_BETA_SIGMOID) {
+    const double s = 1.0 / (1.0 + exp(-b));
+    *db = dbeta * s * (1.0 - s);
+  } else {
+    *db = dbeta;
+  }
+  const double *x = p->g + row * K;
+  if (p->flags & KDAREF_GATE_IN_KERNEL) {
+    const double A = exp(p->a_log[h]);
+    for (int c = 0; c < K; ++c) {
+      const double z = x[c] + (p->dt_bias ? p->dt_bias[(int64_t)h * K + c] : 0.0);
+      const double sig = 1.0 / (1.0 + exp(-z));
+      const double dz = -A * sig * dgn[c];
+      dg[c] = dz;
+      ddtb[c] += dz;
+      *dalog += -A * softplus(z) * dgn[c];
+    }
+  } else {
+    for (int c = 0; c < K; ++c) dg[c] = dgn[c];
+  }
+}
+
+/* Gradients.  d_out [T_total, H, dv] (NULL = zeros); d_final [N, H, dk, dv]
+ * (NULL = zeros); outputs dq, dk, dg [T_total, H, dk], dv [T_total, H, dv],
+ * dbeta [T_total, H] (with respect to the inputs as given: logits, raw gate
+ * input), da_log_part [N, H] and ddt_bias_part [N, H, dk] (per-sequence
+ * parts of the parameter gradients, to be summed over N), d_initial
+ * [N, H, dk, dv] (may be NULL). */
+int kdaref_chunk_bwd(const kdaref_problem *p, const double *initial_state,
+                     const double *d_out, const double *d_final, double *dq, double *dk,
+                     double *dv, double *dg, double *dbeta, double *da_log_part,
+                     double *ddt_bias_part, double *d_initial, int nthreads) {
+  const int K = p->dk, V = p->dv, H = p->H;
+  const int64_t units = p->num_seqs * H;
+  const int64_t SS = (int64_t)K * V;
+  int err = 0;
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    scratch_t w;
+    int64_t maxlen = 0;
+    for (int64_t n = 0; n < p->num_seqs; ++n) {
+      const int64_t len = p->cu_seqlens[n + 1] - p->cu_seqlens[n];
+      if (len > maxlen) maxlen = len;
+    }
+    const int64_t nck = maxlen / KDAREF_CKPT + 1;
+    double *ck = (double *)malloc(sizeof(double) * SS * nck);              /* checkpoints */
+    double *blk = (double *)malloc(sizeof(double) * SS * (KDAREF_CKPT + 1)); /* a block's states */
+    double *dS = (double *)malloc(sizeof(double) * SS);
+    double *dSd = (double *)malloc(sizeof(double) * SS);
+    double *Sd = (double *)malloc(sizeof(double) * SS);
+    double *vec = (double *)malloc(sizeof(double) * (5 * K + 2 * V));
+    if (!scratch_alloc(&w, K, V) || !ck || !blk || !dS || !dSd || !Sd || !vec) {
+#pragma omp atomic write
+      err = 1;
+    } else {
+      double *dqh = vec, *dkh = vec + K, *dgn = vec + 2 * K, *alpha = vec + 3 * K;
+      double *ddelta = vec + 5 * K, *delta = vec + 5 * K + V;
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t u = 0; u < units; ++u) {
+        const int64_t n = u / H;
+        const int h = (int)(u % H);
+        const int64_t a = p->cu_seqlens[n], b = p->cu_seqlens[n + 1];
+        double *dalog = da_log_part + u, *ddtb = ddt_bias_part + u * K;
+        *dalog = 0.0;
+        memset(ddtb, 0, sizeof(double) * K);
+        /* forward: checkpoint the state entering every KDAREF_CKPT-th token */
+        double *S = blk;
+        if (initial_state) memcpy(S, initial_state + u * SS, sizeof(double) * SS);
+        else memset(S, 0, sizeof(double) * SS);
+        for (int64_t t = a; t < b; ++t) {
+          if ((t - a) % KDAREF_CKPT == 0)
+            memcpy(ck + ((t - a) / KDAREF_CKPT) * SS, S, sizeof(double) * SS);
+          run_range(p, t, t + 1, h, S, NULL, &w);
+        }
+        /* backward, block by block from the end */
+        if (d_final) memcpy(dS, d_final + u * SS, sizeof(double) * SS);
+        else memset(dS, 0, sizeof(double) * SS);
+        for (int64_t c0 = b > a ? (b - 1 - a) / KDAREF_CKPT * KDAREF_CKPT : 0; b > a && c0 >= 0;
+             c0 -= KDAREF_CKPT) {
+          const int64_t t0 = a + c0, t1 = (t0 + KDAREF_CKPT < b) ? t0 + KDAREF_CKPT : b;
+          /* blk[i] = state entering token t0 + i, i = 0 .. t1 - t0 */
+          memcpy(blk, ck + (c0 / KDAREF_CKPT) * SS, sizeof(double) * SS);
+          for (int64_t t = t0; t < t1; ++t) {
+            memcpy(blk + (t - t0 + 1) * SS, blk + (t - t0) * SS, sizeof(double) * SS);
+            run_range(p, t, t + 1, h, blk + (t - t0 + 1) * SS, NULL, &w);
+          }
+          for (int64_t t = t1 - 1; t >= t0; --t) {
+            const double *Sp = blk + (t - t0) * SS;   /* S_{t-1} */
+            const double *St = blk + (t - t0 + 1) * SS; /* S_t */
+            double beta;
+            preprocess_token(p, t, h, w.qh, w.kh, &beta, w.g);
+            const double *v = p->v + (t * H + h) * V;
+            const double *dov = d_out ? d_out + (t * H + h) * V : NULL;
+            for (int c = 0; c < K; ++c) alpha[c] = exp(w.g[c]);
+            for (int c = 0; c < K; ++c)
+              for (int j = 0; j < V; ++j) Sd[(int64_t)c * V + j] = alpha[c] * Sp[(int64_t)c * V + j];
+            for (int j = 0; j < V; ++j) {
+              double s = 0.0;
+              for (int c = 0; c < K; ++c) s += Sd[(int64_t)c * V + j] * w.kh[c];
+              delta[j] = v[j] - s;
+            }
+            /* o_t = scale S_t^T q^ */
+            for (int c = 0; c < K; ++c) {
+              double s = 0.0;
+              if (dov)
+                for (int j = 0; j < V; ++j) s += St[(int64_t)c * V + j] * dov[j];
+              dqh[c] = p->scale * s;
+              if (dov)
+                for (int j = 0; j < V; ++j) dS[(int64_t)c * V + j] += p->scale * w.qh[c] * dov[j];
+            }
+            /* S_t = S' + beta k^ delta^T */
+            double dbt = 0.0;
+            for (int j = 0; j < V; ++j) {
+              double s = 0.0;
+              for (int c = 0; c < K; ++c) s += dS[(int64_t)c * V + j] * w.kh[c];
+              ddelta[j] = beta * s;
+              dbt += s * delta[j];
+            }
+            for (int c = 0; c < K; ++c) {
+              double s = 0.0;
+              for (int j = 0; j < V; ++j) s += dS[(int64_t)c * V + j] * delta[j];
+              dkh[c] = beta * s;
+            }
+            /* delta = v - S'^T k^ */
+            double *dvr = dv + (t * H + h) * V;
+            for (int j = 0; j < V; ++j) dvr[j] = ddelta[j];
+            for (int c = 0; c < K; ++c) {
+              double s = 0.0;
+              for (int j = 0; j < V; ++j) {
+                dSd[(int64_t)c * V + j] = dS[(int64_t)c * V + j] - w.kh[c] * ddelta[j];
+                s += Sd[(int64_t)c * V + j] * ddelta[j];
+              }
+              dkh[c] -= s;
+            }
+            /* S' = Diag(alpha) S_{t-1} */
+            for (int c = 0; c < K; ++c) {
+              double s = 0.0;
+              for (int j = 0; j < V; ++j) s += dSd[(int64_t)c * V + j] * Sp[(int64_t)c * V + j];
+              dgn[c] = alpha[c] * s;
+              for (int j = 0; j < V; ++j) dS[(int64_t)c * V + j] = alpha[c] * dSd[(int64_t)c * V + j];
+            }
+            const int64_t row = t * H + h;
+            preprocess_bwd(p, t, h, dqh, dkh, dbt, dgn, dq + row * K, dk + row * K, dbeta + row,
+                           dg + row * K, dalog, ddtb);
+          }
+        }
+        if (d_initial) memcpy(d_initial + u * SS, dS, sizeof(double) * SS);
+      }
+    }
+    scratch_free(&w);
+    free(ck); free(blk); free(dS); free(dSd); free(Sd); free(vec);
+  }
+  return err;
+}

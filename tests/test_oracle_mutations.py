@@ -29,6 +29,44 @@ MUTATIONS = [
 ]
 
 
+# Mistakes in the backward, rejected by the finite-difference pins.
+BWD_MUTATIONS = [
+    ("backward: decay of the carried gradient dropped",
+     "dS[(int64_t)c * V + j] = alpha[c] * dSd[(int64_t)c * V + j];",
+     "dS[(int64_t)c * V + j] = dSd[(int64_t)c * V + j];"),
+    ("backward: prediction term of dS' dropped",
+     "dSd[(int64_t)c * V + j] = dS[(int64_t)c * V + j] - w.kh[c] * ddelta[j];",
+     "dSd[(int64_t)c * V + j] = dS[(int64_t)c * V + j];"),
+    ("backward: beta missing from dk", "dkh[c] = beta * s;", "dkh[c] = s;"),
+    ("backward: L2-norm projection dropped",
+     "dq[c] = rq * dqh[c] - rq * rq * rq * pq * q[c];", "dq[c] = rq * dqh[c];"),
+    ("backward: sigmoid derivative wrong", "*db = dbeta * s * (1.0 - s);", "*db = dbeta * s;"),
+    ("backward: a_log gradient sign", "*dalog += -A * softplus(z) * dgn[c];",
+     "*dalog += A * softplus(z) * dgn[c];"),
+    ("backward: output gradient reads S_{t-1}",
+     "if (dov)\n                for (int j = 0; j < V; ++j) s += St[(int64_t)c * V + j] * dov[j];",
+     "if (dov)\n                for (int j = 0; j < V; ++j) s += Sp[(int64_t)c * V + j] * dov[j];"),
+]
+
+
+def _mutate_and_run(tmp_path, orig, planted, pins):
+    src = open(os.path.join(ROOT, "oracle", "kda_oracle.c")).read()
+    assert orig in src, "mutation site no longer exists"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
+                    ignore=shutil.ignore_patterns("__pycache__", "test_oracle_mutations.py"))
+    (tmp_path / "oracle" / "kda_oracle.c").write_text(src.replace(orig, planted, 1))
+    return subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                           pins], cwd=tmp_path, capture_output=True, text=True)
+
+
+@pytest.mark.parametrize("what,orig,planted", BWD_MUTATIONS, ids=[m[0] for m in BWD_MUTATIONS])
+def test_backward_pins_reject_planted_mistake(tmp_path, what, orig, planted):
+    r = _mutate_and_run(tmp_path, orig, planted, "tests/test_oracle_bwd_pins.py")
+    assert r.returncode != 0, f"pins accepted an oracle with '{what}':\n{r.stdout[-2000:]}"
+
+
 @pytest.mark.parametrize("what,orig,planted", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_pins_reject_planted_mistake(tmp_path, what, orig, planted):
     src = open(os.path.join(ROOT, "oracle", "kda_oracle.c")).read()
