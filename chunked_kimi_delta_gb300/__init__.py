@@ -71,6 +71,19 @@ class kda_decode_args(ctypes.Structure):
     ]
 
 
+class kda_bwd_args(ctypes.Structure):
+    """Mirror of ``kda_bwd_args`` in include/kda.h."""
+    _fields_ = [
+        ("fwd", kda_fwd_args),
+        ("d_out", ctypes.c_void_p), ("d_final_state", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p),
+        ("da_log", ctypes.c_void_p), ("ddt_bias", ctypes.c_void_p),
+        ("d_initial_state", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 _lib = None
 
 
@@ -102,6 +115,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kda_recurrent_step": ([ctypes.POINTER(kda_decode_args), vp], ctypes.c_int),
         "kda_chunk_fwd_stages": ([P, ctypes.POINTER(ctypes.c_char_p), i32], i32),
         "kda_chunk_fwd_profiled": ([P, vp, ctypes.POINTER(vp), i32], ctypes.c_int),
+        "kda_chunk_bwd_workspace_size": ([ctypes.POINTER(kda_bwd_args)], ctypes.c_size_t),
+        "kda_chunk_bwd": ([ctypes.POINTER(kda_bwd_args), vp], ctypes.c_int),
     }
     for name, (argt, rest) in sigs.items():
         f = getattr(lib, name)
@@ -520,6 +535,66 @@ def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=N
     a.idx, a.idx_dtype, a.init_flags = _ptr(idx), _idx_code(idx), _ptr(init_flags)
     _check(lib.kda_recurrent_step(ctypes.byref(a), _stream(stream)), "kda_recurrent_step")
     return out
+
+
+def prepare_chunk_bwd(q, k, v, g, beta, d_out, *, d_final_state=None, initial_state=None,
+                      want_d_initial_state=None, workspace=None, **kw):
+    """Builds the ``kda_bwd_args`` of a backward once (gradient tensors and
+    workspace allocated).  ``kw`` are the forward's keyword arguments
+    (scale, eps, a_log, dt_bias, cu_seqlens, l2norm_qk, beta_sigmoid,
+    gate_in_kernel, use_exp2).  Returns (args, grads, ws) with grads a dict
+    of dq, dk, dv, dg, dbeta, da_log, ddt_bias, d_initial_state."""
+    torch = _torch()
+    lib = load_library()
+    cu = kw.get("cu_seqlens")
+    N = (cu.numel() - 1) if cu is not None else (1 if q.dim() == 3 else q.shape[0])
+    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    dev = q.device
+    if d_out is not None:
+        if d_out.shape != v.shape or d_out.dtype != q.dtype:
+            raise ValueError("d_out must have v's shape and q's dtype")
+        _contig(d_out)
+    if d_final_state is not None:
+        if tuple(d_final_state.shape) != (N, H, K, V) or d_final_state.dtype != torch.float32:
+            raise ValueError("d_final_state must be fp32 [N, H, dk, dv]")
+        _contig(d_final_state)
+    if want_d_initial_state is None:
+        want_d_initial_state = initial_state is not None
+    gate = kw.get("gate_in_kernel", False)
+    grads = dict(
+        dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+        dg=torch.empty(g.shape, dtype=torch.float32, device=dev),
+        dbeta=torch.empty(beta.shape, dtype=torch.float32, device=dev),
+        da_log=torch.empty(H, dtype=torch.float32, device=dev) if gate else None,
+        ddt_bias=torch.empty(H, K, dtype=torch.float32, device=dev) if gate else None,
+        d_initial_state=(torch.empty(N, H, K, V, dtype=torch.float32, device=dev)
+                         if want_d_initial_state else None),
+    )
+    b = kda_bwd_args()
+    b.fwd = make_fwd_args(q, k, v, g, beta, initial_state=initial_state, **kw)
+    b.d_out, b.d_final_state = _ptr(d_out), _ptr(d_final_state)
+    b.dq, b.dk, b.dv = _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"])
+    b.dg, b.dbeta = _ptr(grads["dg"]), _ptr(grads["dbeta"])
+    b.da_log, b.ddt_bias = _ptr(grads["da_log"]), _ptr(grads["ddt_bias"])
+    b.d_initial_state = _ptr(grads["d_initial_state"])
+    ws = _workspace(lib.kda_chunk_bwd_workspace_size(ctypes.byref(b)), dev, workspace)
+    b.workspace, b.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    return b, grads, ws
+
+
+def kda_chunk_bwd(q, k, v, g, beta, d_out, *, stream=None, **kw):
+    """Chunked KDA backward: gradients of <d_out, o> + <d_final_state,
+    final_state> with respect to the forward's inputs as given (raw q, k;
+    beta logits with ``beta_sigmoid``; raw gate input with
+    ``gate_in_kernel``).  Takes the forward's tensors and keyword arguments
+    plus ``d_final_state`` and ``want_d_initial_state``.  Returns a dict of
+    dq, dk, dv (q's dtype), dg, dbeta, da_log, ddt_bias (None without
+    ``gate_in_kernel``) and d_initial_state (fp32).  See ``kda_chunk_bwd`` in
+    include/kda.h."""
+    lib = load_library()
+    b, grads, ws = prepare_chunk_bwd(q, k, v, g, beta, d_out, **kw)
+    _check(lib.kda_chunk_bwd(ctypes.byref(b), _stream(stream)), "kda_chunk_bwd")
+    return grads
 
 
 def kda_get_device_status(workspace, stream=None) -> int:

@@ -539,6 +539,130 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
                                    a->num_rows, a->row_stride_elems, a->idx, a->init_flags, st));
 }
 
+}  // extern "C"
+
+namespace {
+
+kda_status check_bwd(const kda_bwd_args *b) {
+  if (!b) return KDA_ERR_INVALID_ARG;
+  const kda_fwd_args *a = &b->fwd;
+  kda_status s = check_common(a);
+  if (s != KDA_OK) return s;
+  if (a->cu_seqlens && (a->B != 1 || a->num_seqs < 1)) return KDA_ERR_INVALID_ARG;
+  if (a->flags & KDA_REUSE_PREP) return KDA_ERR_UNSUPPORTED;
+  if ((int64_t)a->B * a->T > 0 && (!b->dq || !b->dk || !b->dv || !b->dg || !b->dbeta))
+    return KDA_ERR_INVALID_ARG;
+  if (mis16(a->initial_state) || mis16(a->cu_seqlens) || mis16(b->d_out) || mis16(b->d_final_state) ||
+      mis16(b->dq) || mis16(b->dk) || mis16(b->dv) || mis16(b->dg) || mis16(b->dbeta) ||
+      mis16(b->da_log) || mis16(b->ddt_bias) || mis16(b->d_initial_state))
+    return KDA_ERR_ALIGNMENT;
+  return KDA_OK;
+}
+
+// Backward workspace: the generic forward plan (recomputed intermediates),
+// then the states, state gradients and per-token scratch of the backward.
+struct BwdPlan {
+  FwdPlan f;
+  size_t off_h, off_vn, off_dhn, off_dvn, off_dqg, off_dw, off_dkg, off_dgc, off_palog, off_pdtb;
+  size_t off_dqv, off_dkv, total;
+};
+
+BwdPlan bwd_plan(const kda_bwd_args *b) {
+  BwdPlan p{};
+  p.f = fwd_plan(&b->fwd);
+  const size_t th = (size_t)p.f.T_tot * p.f.H, ch = (size_t)p.f.nchunks * p.f.H;
+  const size_t K = p.f.K, V = p.f.V;
+  size_t o = p.f.total;
+  p.off_h = o;     o = align256(o + 4 * ch * K * V);
+  p.off_vn = o;    o = align256(o + 4 * th * V);
+  p.off_dhn = o;   o = align256(o + 4 * ch * K * V);
+  p.off_dvn = o;   o = align256(o + 4 * th * V);
+  p.off_dqg = o;   o = align256(o + 4 * th * K);
+  p.off_dw = o;    o = align256(o + 4 * th * K);
+  p.off_dkg = o;   o = align256(o + 4 * th * K);
+  p.off_dgc = o;   o = align256(o + 4 * ch * K);
+  p.off_palog = o; o = align256(o + 4 * ch);
+  p.off_pdtb = o;  o = align256(o + 4 * ch * K);
+  p.off_dqv = p.off_dkv = 0;
+  if (p.f.Hk != p.f.H) {
+    p.off_dqv = o; o = align256(o + 4 * th * K);
+    p.off_dkv = o; o = align256(o + 4 * th * K);
+  }
+  p.total = o;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *b) {
+  if (check_bwd(b) != KDA_OK) return 0;
+  return bwd_plan(b).total;
+}
+
+kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
+  kda_status s = check_bwd(b);
+  if (s != KDA_OK) return s;
+  const kda_fwd_args *a = &b->fwd;
+  const BwdPlan p = bwd_plan(b);
+  if (!b->workspace || b->workspace_bytes < p.total) return KDA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(b->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(b->workspace);
+  auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+
+  SeqInfo si{};
+  si.bounds = a->cu_seqlens;
+  si.chunk_off = reinterpret_cast<int32_t *>(ws + p.f.off_chunk_off);
+  si.T_tot = p.f.T_tot;
+  si.T = a->T;
+  si.N = p.f.N;
+  const GateParams gp = gate_params(a);
+
+  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
+  if (e == cudaSuccess && si.bounds) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
+  // recompute: the per-chunk intermediates, the state entering every chunk, v_new
+  if (e == cudaSuccess && p.f.T_tot > 0)
+    e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gp, si, p.f, ws, st);
+  if (e == cudaSuccess && p.f.T_tot > 0) {
+    InterOut io{};
+    io.h_out = f32(p.off_h);
+    io.v_new_out = f32(p.off_vn);
+    io.initial_state = a->initial_state;
+    e = launch_generic_inter(a->qkv_dtype, false, io, si, p.f, ws, st);
+  }
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + p.off_palog, 0, p.off_pdtb - p.off_palog, st);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(ws + p.off_pdtb, 0, 4 * (size_t)p.f.nchunks * p.f.H * p.f.K, st);
+  if (e == cudaSuccess) {
+    BwdLaunch l{};
+    l.s = si;
+    l.H = p.f.H;
+    l.Hk = p.f.Hk;
+    l.nchunks = p.f.T_tot > 0 ? p.f.nchunks : 0;
+    l.q = a->q; l.k = a->k; l.v = a->v; l.g = a->g; l.beta = a->beta;
+    l.gp = gp;
+    l.d_out = b->d_out;
+    l.d_final = b->d_final_state;
+    l.w = f32(p.f.off_w); l.qg = f32(p.f.off_qg); l.kg = f32(p.f.off_kg);
+    l.aqk = f32(p.f.off_aqk); l.gc = f32(p.f.off_gc);
+    l.h = f32(p.off_h); l.vn = f32(p.off_vn);
+    l.dhn = f32(p.off_dhn); l.dvn = f32(p.off_dvn); l.dqg = f32(p.off_dqg); l.dw = f32(p.off_dw);
+    l.dkg = f32(p.off_dkg); l.dgc = f32(p.off_dgc);
+    l.part_alog = f32(p.off_palog); l.part_dtb = f32(p.off_pdtb);
+    l.dqv = p.off_dqv ? f32(p.off_dqv) : nullptr;
+    l.dkv = p.off_dkv ? f32(p.off_dkv) : nullptr;
+    l.dq = b->dq; l.dk = b->dk; l.dv = b->dv;
+    l.dg = b->dg; l.dbeta = b->dbeta; l.d_initial = b->d_initial_state;
+    e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st);
+  }
+  if (e == cudaSuccess)
+    e = launch_bwd_param_reduce(p.f.nchunks, p.f.H, p.f.K, f32(p.off_palog), f32(p.off_pdtb), b->da_log,
+                                b->ddt_bias, st);
+  return cuda_status(e);
+}
+
 kda_status kda_get_device_status(void *workspace, kda_stream_t stream) {
   if (!workspace) return KDA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -312,7 +312,7 @@ generic_inter_kernel(bool summary, SeqInfo s, int H, int V, const float *__restr
         for (int cc = 0; cc < K; ++cc) acc = fmaf(sQg[r * K + cc], sH[cc * VT + j], acc);
         for (int s2 = 0; s2 <= r; ++s2) acc = fmaf(sA[r * BT + s2], sVn[s2 * VT + j], acc);
         const int64_t off = ((t + r) * H + h) * (int64_t)V + col;
-        static_cast<Tout *>(io.out)[off] = from_f32<Tout>(acc);
+        if (io.out) static_cast<Tout *>(io.out)[off] = from_f32<Tout>(acc);
         if (io.v_new_out) io.v_new_out[off] = sVn[r * VT + j];
       }
       __syncthreads();

@@ -164,6 +164,28 @@ struct InterOut {
 cudaError_t launch_generic_inter(kda_dtype dt, bool summary, const InterOut &io, const SeqInfo &s,
                                  const FwdPlan &p, const char *ws, cudaStream_t st);
 
+// Backward on CUDA cores (kda_bwd.cu): pointers of one call.  w, qg, kg, aqk,
+// gc, h and vn are the forward's recomputed intermediates; dhn, dvn, dqg,
+// dw, dkg, dgc, part_* and (grouped key heads) dqv, dkv are scratch.
+struct BwdLaunch {
+  SeqInfo s;
+  int H, Hk;
+  int64_t nchunks;
+  const void *q, *k, *v;
+  const float *g, *beta;
+  GateParams gp;
+  const void *d_out;
+  const float *d_final;
+  const float *w, *qg, *kg, *aqk, *gc, *h, *vn;
+  float *dhn, *dvn, *dqg, *dw, *dkg, *dgc, *part_alog, *part_dtb, *dqv, *dkv;
+  void *dq, *dk, *dv;
+  float *dg, *dbeta, *d_initial;
+};
+cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
+cudaError_t launch_bwd_param_reduce(int64_t nchunks, int H, int K, const float *part_alog,
+                                    const float *part_dtb, float *da_log, float *ddt_bias,
+                                    cudaStream_t st);
+
 cudaError_t launch_prefix_scan(const float *M, const float *S_tilde, const float *S0, int C,
                                int S, int H, int K, int V, float *S_in, float *S_final,
                                cudaStream_t st);

@@ -160,3 +160,17 @@ def oracle_kwargs(cfg: KdaConfig) -> dict:
     """The method flags of ``cfg`` as keyword booleans (no arithmetic)."""
     return dict(l2norm=cfg.l2norm, beta_sigmoid=cfg.beta_sigmoid,
                 gate_in_kernel=cfg.gate_in_kernel, use_exp2=cfg.use_exp2)
+
+
+def make_cotangents(cfg: KdaConfig, inputs: dict, device="cpu", seed: Optional[int] = None) -> dict:
+    """Seeded cotangents of a backward: d_out ~ N(0,1) with v's shape in
+    cfg.dtype, d_final_state ~ N(0, 0.1) fp32 [N, H, dk, dv]."""
+    seed = (cfg.seed if seed is None else seed) + 7919
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    v = inputs["v"]
+    N = (inputs["cu_seqlens"].numel() - 1) if inputs.get("cu_seqlens") is not None else cfg.B
+    d_out = torch.randn(*v.shape, generator=gen, device=device, dtype=torch.float32)
+    d_fin = torch.randn(N, cfg.H, cfg.dk, cfg.dv, generator=gen, device=device,
+                        dtype=torch.float32) * 0.1
+    return dict(d_out=d_out.to(torch_dtype(cfg.dtype)), d_final_state=d_fin)

@@ -333,6 +333,53 @@ typedef struct {
 
 kda_status kda_recurrent_step(const kda_decode_args *args, kda_stream_t stream);
 
+/*
+ * Arguments of the chunked backward ("KDA Chunk Backward - TPU/Pallas Kernel
+ * Design", sections 1-2: the six stages recompute, dAv, reverse state
+ * gradient, WY backward, intra-chunk backward, reverse cumsum, then gate and
+ * L2-norm backward; "Hyper-Parallel Chunk KDA current implementation
+ * design" section 5.2: the gradients bwd_finalize returns plus dh0).
+ *
+ * The gradients are those of L = <d_out, out> + <d_final_state, final_state>
+ * of the forward described by `fwd`, with respect to its inputs as given:
+ * q, k (raw, before the L2 norm), v, the gate input g (raw x with
+ * KDA_GATE_IN_KERNEL, else the natural-log decay), beta (logits with
+ * KDA_BETA_SIGMOID), a_log, dt_bias and initial_state.  With grouped key
+ * heads the q/k gradients are summed over the value heads sharing a key head
+ * (same design, section 4.2).  fwd.out, final_state, h_out, v_new_out and
+ * fwd.workspace are ignored; every other field of fwd means what it means
+ * for kda_chunk_fwd (KDA_REUSE_PREP is rejected).
+ */
+typedef struct {
+  kda_fwd_args fwd;
+  const void *d_out;           /* [.., H, dv] qkv_dtype, or NULL (= zeros)     */
+  const float *d_final_state;  /* [N, H, dk, dv] fp32, or NULL (= zeros)       */
+  void *dq, *dk;               /* [.., Hk, dk] qkv_dtype, written              */
+  void *dv;                    /* [.., H, dv] qkv_dtype, written               */
+  float *dg;                   /* [.., H, dk] fp32, written                    */
+  float *dbeta;                /* [.., H] fp32, written                        */
+  float *da_log;               /* [H] fp32 or NULL; zeros without              */
+                               /* KDA_GATE_IN_KERNEL                           */
+  float *ddt_bias;             /* [H, dk] fp32 or NULL; likewise               */
+  float *d_initial_state;      /* [N, H, dk, dv] fp32 or NULL (not written)    */
+  void *workspace;             /* device scratch, >= kda_chunk_bwd_workspace_size */
+  size_t workspace_bytes;      /* and 256-byte aligned                         */
+} kda_bwd_args;
+
+/* Workspace bytes kda_chunk_bwd needs for these arguments; 0 when they fail
+ * the argument checks.  It holds the recomputed forward intermediates, the
+ * state entering and the state gradient leaving every chunk (fp32,
+ * dk*dv*4 bytes per chunk and head each), and per-token fp32 scratch. */
+size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *args);
+
+/* The chunked KDA backward (fp32 arithmetic on CUDA cores for every dtype and
+ * head size).  Deterministic: no atomics; every sum runs in a fixed order.
+ * Errors: those of kda_chunk_fwd for `fwd` (except that out may be NULL),
+ * KDA_ERR_INVALID_ARG (null dq/dk/dv/dg/dbeta with tokens),
+ * KDA_ERR_UNSUPPORTED (KDA_REUSE_PREP), KDA_ERR_ALIGNMENT,
+ * KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
+kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream);
+
 /* Reads and clears the device error word kept at the start of a forward or
  * summary workspace: synchronises the stream, returns KDA_OK or
  * KDA_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up.  Every

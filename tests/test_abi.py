@@ -214,3 +214,30 @@ def test_binding_shapes_for_grouped_key_heads():
         args.update(kw)
         with pytest.raises(ValueError):
             kda.make_fwd_args(args["q"], args["k"], args["v"], args["g"], args["beta"], out=out)
+
+
+def test_bwd_argument_checks(lib):
+    def bargs(**kw):
+        b = kda.kda_bwd_args()
+        b.fwd = _args()
+        base = 1 << 24
+        b.dq, b.dk, b.dv, b.dg, b.dbeta = (base * (i + 1) for i in range(5))
+        for key, val in kw.items():
+            setattr(b, key, val)
+        return b
+    f = lambda b: lib.kda_chunk_bwd(ctypes.byref(b), None)
+    size = lambda b: lib.kda_chunk_bwd_workspace_size(ctypes.byref(b))
+    assert f(bargs()) == 4                                   # no workspace
+    assert size(bargs()) > lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args()))
+    assert f(bargs(dq=None)) == 1
+    assert f(bargs(dbeta=None)) == 1
+    assert f(bargs(dv=(1 << 24) + 4)) == 3
+    assert f(bargs(fwd=_args(flags=kda.KDA_REUSE_PREP))) == 2
+    assert f(bargs(fwd=_args(dk=96))) == 2
+    assert f(bargs(fwd=_args(Hk=3))) == 1
+    assert size(bargs(fwd=_args(Hk=2))) > size(bargs())     # per-value-head dq/dk scratch
+    assert size(bargs(dq=None)) == 0
+    b = bargs()
+    b.workspace, b.workspace_bytes = (1 << 30) + 16, size(b)
+    assert f(b) == 3
+    assert lib.kda_chunk_bwd(None, None) == 1
