@@ -221,6 +221,7 @@ def main():
     ap.add_argument("--no-segment", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -345,6 +346,8 @@ def main():
         result["segment_mode"] = bench_segment(kda, dev, stream)
     if rank == 0 and not args.no_decode:
         result["decode"] = bench_decode(kda, dev, stream, hbm_peak)
+    if rank == 0 and not args.no_bwd:
+        result["bwd"] = bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak)
     if not args.no_e2e:
         result["e2e"] = bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world)
     if rank == 0 and not args.no_cpu_baseline:
@@ -426,6 +429,55 @@ def bench_decode(kda, dev, stream, hbm_peak, steps=50, warmup=5):
             "l2_policy": "256 MiB buffer written between steps (flush)",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "alg_bytes_per_launch": state_bytes + io_bytes}}
+
+
+def bwd_alg_bytes_per_token_head(dk, dv):
+    """Reads q, k, v, d_out (bf16), gate, beta (fp32); writes dq, dk, dv (bf16),
+    dg, dbeta (fp32)."""
+    return (2 * dk * 2 + dv * 2 + dv * 2 + 4 * dk + 4) + (2 * dk * 2 + dv * 2 + 4 * dk + 4)
+
+
+def bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak, steps=5, warmup=3):
+    """Backward of the same workload (B=4, T=8192, H=32, d=128, bf16): all
+    gradients (q, k, v, gate input, beta logits, a_log, dt_bias, initial
+    state) of <d_out, o> + <d_final, final_state>."""
+    import torch
+    from chunked_kimi_delta_gb300.inputs import make_cotangents
+    cot = make_cotangents(cfg, inp, device=dev)
+    K, V, H = cfg.dk, cfg.dv, cfg.H
+    b, grads, ws = kda.prepare_chunk_bwd(
+        inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cot["d_out"],
+        d_final_state=cot["d_final_state"], initial_state=S0, scale=float(K ** -0.5),
+        a_log=inp["a_log"], dt_bias=inp["dt_bias"], l2norm_qk=True, beta_sigmoid=True,
+        gate_in_kernel=True, use_exp2=True)
+    sp = stream.cuda_stream
+
+    def one():
+        st = lib.kda_chunk_bwd(ctypes.byref(b), sp)
+        if st:
+            raise kda.KdaError(st, "kda_chunk_bwd")
+
+    for _ in range(warmup):
+        one()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, e in evs:
+        a.record(stream)
+        one()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(e) for a, e in evs)
+    th = cfg.B * cfg.T * H
+    nbytes = bwd_alg_bytes_per_token_head(K, V) * th + 3 * 4 * K * V * cfg.B * H
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"{cfg.name} backward: B={cfg.B} T={cfg.T} H={H} d={K}, bf16 q/k/v/d_out and "
+                        f"dq/dk/dv, fp32 gate/beta gradients, dA_log, ddt_bias, initial-state gradient",
+            "tokens_per_s": cfg.B * cfg.T / (ms / 1e3), "ms_per_step": ms, "steps": steps,
+            "launches_per_step": 6,
+            "l2_policy": "inputs (1.6 GB) larger than L2 (129 MB); no flush",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "alg_bytes_per_launch": nbytes,
+                         "scope": "whole backward call"}}
 
 
 def bench_segment(kda, dev, stream, steps=3, warmup=2):
