@@ -10,6 +10,9 @@ baseline leg of ``bench.py`` do.  The oracle shares no code with the CUDA path.
   the token-by-token recurrence in C (``kda_oracle.c``), fp64.
 * ``chunk_bwd``: gradients of the same recurrence by reverse-mode
   differentiation, token by token, in C, fp64.
+* ``segment_bwd_summary``, ``state_grad_scan``: the backward twins of the
+  segment summary and the prefix scan (the local state gradient of each
+  segment, composed in reverse time order with the transposed transitions).
 * ``chunked.py``: an independent fp64 chunked form of the same forward (the
   WY representation), used only to pin the recurrence.
 * ``state_copy.py``: gather/scatter as plain indexed copies.
@@ -128,6 +131,17 @@ class Problem:
         self.flags = ((_L2NORM_QK if l2norm else 0) | (_BETA_SIGMOID if beta_sigmoid else 0)
                       | (_GATE_IN_KERNEL if gate_in_kernel else 0) | (_USE_EXP2 if use_exp2 else 0))
 
+    def with_bounds(self, cu_seqlens):
+        """The same inputs with other range bounds on the token axis (each
+        range an independent sequence)."""
+        import copy
+        p = copy.copy(self)
+        cs = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+        if cs[0] != 0 or cs[-1] != self.T or np.any(np.diff(cs) < 0):
+            raise ValueError("bounds must run from 0 to T_total, non-decreasing")
+        p.cu = cs
+        return p
+
     @property
     def num_seqs(self):
         return len(self.cu) - 1
@@ -238,3 +252,43 @@ def chunk_bwd(prob: Problem, initial_state=None, d_out=None, d_final=None, *, nt
     r["da_log"] = dal.sum(axis=0)
     r["ddt_bias"] = ddt.sum(axis=0)
     return r
+
+
+def segment_bwd_summary(prob: Problem, seg_bounds, d_out=None, nthreads=0):
+    """E[s, h]: the gradient of <d_out, o> restricted to segment s with
+    respect to the state entering the segment ("Hyper-Parallel Chunk KDA
+    current implementation design" section 5.2, bwd pre-process: the local
+    backward summary; "KDA Chunk Backward - TPU/Pallas Kernel Design" section
+    2.4, dS_ext).  The outputs of a segment are affine in its entering state,
+    so E does not depend on that state: it is the initial-state gradient of
+    the segment run alone, with no final-state cotangent.  [S, H, dk, dv]."""
+    r = chunk_bwd(prob.with_bounds(seg_bounds), None, d_out, None, nthreads=nthreads)
+    return r["d_initial"]
+
+
+def state_grad_scan(M, E, dS_final=None):
+    """Reverse-order scan of the state gradient across segments (same
+    sections: summaries are exchanged in reverse time order).  For each chain
+    c and head h, with g = dS_final[c, h] (zeros when None):
+        for j = S-1 .. 0:  dS_out[c, j, h] = g;  g = M[c, j, h]^T g + E[c, j, h]
+        dS_initial[c, h] = g
+    M: [C, S, H, dk, dk] (or [S, H, dk, dk]); E: the same with dv.  Returns
+    (dS_out, dS_initial); dS_out[c, j] is the gradient of the state leaving
+    segment j."""
+    M = _f64(M)
+    E = _f64(E)
+    one = M.ndim == 4
+    if one:
+        M, E = M[None], E[None]
+    C, S, H, K, _ = M.shape
+    V = E.shape[-1]
+    g = np.zeros((C, H, K, V)) if dS_final is None else _f64(dS_final).reshape(C, H, K, V).copy()
+    dS_out = np.zeros((C, S, H, K, V))
+    for c in range(C):
+        for h in range(H):
+            for j in range(S - 1, -1, -1):
+                dS_out[c, j, h] = g[c, h]
+                g[c, h] = M[c, j, h].T @ g[c, h] + E[c, j, h]
+    if one:
+        return dS_out[0], g[0]
+    return dS_out, g

@@ -170,3 +170,68 @@ def test_beta_zero_closed_form():
         want += scale * np.outer(np.exp(G[t]) * qh[t], do[t, 0])
     np.testing.assert_allclose(r["d_initial"][0, 0], want, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(r["dv"], 0.0)
+
+
+# ------------------------------------------- backward summary and reverse scan
+
+def _segment_problem(T, H, K, V, seed_flags):
+    cu = [0, T]
+    x = _inputs(T, H, K, V, n_seqs_cu=cu, **seed_flags)
+    return x, cu
+
+
+@pytest.mark.parametrize("bounds", [(0, 5, 13, 20), (0, 1, 20), (0, 20)])
+def test_segment_mode_backward_reproduces_unsplit_backward(bounds):
+    """Forward summary -> scan -> backward summary -> reverse scan -> per-segment
+    backward equals the backward of the whole sequence (fp64), for splits at
+    any token.  A transposed or left-applied M, a forward-ordered scan or a
+    wrong local term fails this."""
+    flags = dict(gate_in_kernel=True, beta_sigmoid=True, l2norm=True)
+    T, H, K, V = 20, 2, 4, 3
+    x, cu = _segment_problem(T, H, K, V, flags)
+    S0 = x["S0"]
+    do = RNG.standard_normal((T, H, V))
+    dfin = RNG.standard_normal((1, H, K, V))
+    p = _prob(x, cu, flags)
+    whole = oracle.chunk_bwd(p, S0, do, dfin)
+    M, St = oracle.segment_summary(p, bounds)
+    S_in, _ = oracle.state_prefix_scan(M, St, S0[0])
+    E = oracle.segment_bwd_summary(p, bounds, do)
+    dS_out, dS0 = oracle.state_grad_scan(M, E, dfin[0])
+    seg = oracle.chunk_bwd(p.with_bounds(bounds), S_in, do, dS_out)
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "da_log", "ddt_bias"):
+        np.testing.assert_allclose(seg[name], whole[name], rtol=1e-10, atol=1e-12, err_msg=name)
+    np.testing.assert_allclose(dS0, whole["d_initial"][0], rtol=1e-10, atol=1e-12)
+    # the first segment's entering-state gradient is the whole initial-state gradient
+    np.testing.assert_allclose(seg["d_initial"][0], whole["d_initial"][0], rtol=1e-10, atol=1e-12)
+
+
+def test_backward_summary_is_the_affine_map_of_the_transition():
+    """For one segment: d_initial(d_final) = M^T d_final + E, with M the
+    forward transition of the segment (the gradient map is its adjoint)."""
+    flags = dict(gate_in_kernel=False, beta_sigmoid=True, l2norm=True)
+    T, H, K, V = 9, 1, 5, 3
+    x, cu = _segment_problem(T, H, K, V, flags)
+    do = RNG.standard_normal((T, H, V))
+    p = _prob(x, cu, flags)
+    M, _ = oracle.segment_summary(p, [0, T])
+    E = oracle.segment_bwd_summary(p, [0, T], do)
+    for _ in range(3):
+        dfin = RNG.standard_normal((1, H, K, V))
+        r = oracle.chunk_bwd(p, x["S0"], do, dfin)
+        want = M[0, 0].T @ dfin[0, 0] + E[0, 0]
+        np.testing.assert_allclose(r["d_initial"][0, 0], want, rtol=1e-11, atol=1e-12)
+
+
+def test_state_grad_scan_small_closed_form():
+    """Two segments, scalar-sized states: dS_out[1] = g, dS_out[0] = M1^T g + E1,
+    dS0 = M0^T (M1^T g + E1) + E0."""
+    rng = np.random.default_rng(3)
+    M = rng.standard_normal((2, 1, 2, 2))
+    E = rng.standard_normal((2, 1, 2, 3))
+    g = rng.standard_normal((1, 2, 3))
+    dS_out, dS0 = oracle.state_grad_scan(M, E, g)
+    np.testing.assert_allclose(dS_out[1, 0], g[0])
+    mid = M[1, 0].T @ g[0] + E[1, 0]
+    np.testing.assert_allclose(dS_out[0, 0], mid)
+    np.testing.assert_allclose(dS0[0], M[0, 0].T @ mid + E[0, 0])
