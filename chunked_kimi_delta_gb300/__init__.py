@@ -117,6 +117,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kda_chunk_fwd_profiled": ([P, vp, ctypes.POINTER(vp), i32], ctypes.c_int),
         "kda_chunk_bwd_workspace_size": ([ctypes.POINTER(kda_bwd_args)], ctypes.c_size_t),
         "kda_chunk_bwd": ([ctypes.POINTER(kda_bwd_args), vp], ctypes.c_int),
+        "kda_segment_bwd_summary_workspace_size": ([P, i32], ctypes.c_size_t),
+        "kda_segment_bwd_summary": ([P, vp, vp, i32, vp, vp], ctypes.c_int),
+        "kda_state_grad_scan": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp], ctypes.c_int),
     }
     for name, (argt, rest) in sigs.items():
         f = getattr(lib, name)
@@ -595,6 +598,53 @@ def kda_chunk_bwd(q, k, v, g, beta, d_out, *, stream=None, **kw):
     b, grads, ws = prepare_chunk_bwd(q, k, v, g, beta, d_out, **kw)
     _check(lib.kda_chunk_bwd(ctypes.byref(b), _stream(stream)), "kda_chunk_bwd")
     return grads
+
+
+def kda_segment_bwd_summary(q, k, v, g, beta, d_out, seg_bounds, *, E=None, workspace=None,
+                            stream=None, **kw):
+    """Backward segment summary: E [S, H, dk, dv], the gradient of
+    <d_out, o> over each segment with respect to the state entering it.
+    ``seg_bounds``: int32 device tensor [S+1] of token offsets on the
+    flattened token axis; ``kw``: the forward's keyword arguments.  See
+    ``kda_segment_bwd_summary`` in include/kda.h."""
+    torch = _torch()
+    lib = load_library()
+    S = seg_bounds.numel() - 1
+    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    if E is None:
+        E = torch.empty(S, H, K, V, dtype=torch.float32, device=q.device)
+    if d_out is not None and (d_out.shape != v.shape or d_out.dtype != q.dtype):
+        raise ValueError("d_out must have v's shape and q's dtype")
+    _contig(seg_bounds, E, d_out)
+    kw.pop("initial_state", None)
+    kw.pop("cu_seqlens", None)
+    a = make_fwd_args(q, k, v, g, beta, **kw)
+    ws = _workspace(lib.kda_segment_bwd_summary_workspace_size(ctypes.byref(a), S), q.device,
+                    workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib.kda_segment_bwd_summary(ctypes.byref(a), _ptr(d_out), seg_bounds.data_ptr(), S,
+                                       E.data_ptr(), _stream(stream)), "kda_segment_bwd_summary")
+    return E
+
+
+def kda_state_grad_scan(M, E, dS_final=None, *, dS_out=None, dS_initial=None, stream=None):
+    """Reverse-order state-gradient scan.  M [C,S,H,K,K] or [S,H,K,K]; E
+    likewise with V; dS_final [C,H,K,V] / [H,K,V] or None.  Returns
+    ``(dS_out, dS_initial)``."""
+    torch = _torch()
+    lib = load_library()
+    one = M.dim() == 4
+    C = 1 if one else M.shape[0]
+    S, H, K = M.shape[-4], M.shape[-3], M.shape[-1]
+    V = E.shape[-1]
+    if dS_out is None:
+        dS_out = torch.empty(E.shape, dtype=torch.float32, device=M.device)
+    if dS_initial is None:
+        dS_initial = torch.empty(*(() if one else (C,)), H, K, V, dtype=torch.float32, device=M.device)
+    _contig(M, E, dS_final, dS_out, dS_initial)
+    _check(lib.kda_state_grad_scan(_ptr(M), _ptr(E), _ptr(dS_final), C, S, H, K, V, _ptr(dS_out),
+                                   _ptr(dS_initial), _stream(stream)), "kda_state_grad_scan")
+    return dS_out, dS_initial
 
 
 def kda_get_device_status(workspace, stream=None) -> int:

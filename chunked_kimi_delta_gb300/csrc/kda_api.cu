@@ -663,6 +663,63 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   return cuda_status(e);
 }
 
+size_t kda_segment_bwd_summary_workspace_size(const kda_fwd_args *a, int32_t num_segments) {
+  if (check_common(a) != KDA_OK || num_segments < 1) return 0;
+  return summary_plan(a, num_segments).total;  // the generic per-chunk intermediates
+}
+
+kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
+                                   const int32_t *seg_bounds, int32_t num_segments, float *E,
+                                   kda_stream_t stream) {
+  kda_status s = check_common(a);
+  if (s != KDA_OK) return s;
+  if (a->flags & KDA_REUSE_PREP) return KDA_ERR_UNSUPPORTED;
+  if (num_segments < 1 || !seg_bounds || !E) return KDA_ERR_INVALID_ARG;
+  if (mis16(seg_bounds) || mis16(E) || mis16(d_out)) return KDA_ERR_ALIGNMENT;
+  const FwdPlan p = summary_plan(a, num_segments);
+  if (!a->workspace || a->workspace_bytes < p.total) return KDA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(a->workspace);
+  auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+  SeqInfo si{};
+  si.bounds = seg_bounds;
+  si.chunk_off = reinterpret_cast<int32_t *>(ws + p.off_chunk_off);
+  si.T_tot = p.T_tot;
+  si.T = a->T;
+  si.N = num_segments;
+  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
+  if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
+  if (e == cudaSuccess && p.T_tot > 0)
+    e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws,
+                             st);
+  if (e == cudaSuccess) {
+    BwdLaunch l{};
+    l.s = si;
+    l.H = p.H;
+    l.Hk = p.Hk;
+    l.d_out = d_out;
+    l.w = f32(p.off_w); l.qg = f32(p.off_qg); l.kg = f32(p.off_kg);
+    l.aqk = f32(p.off_aqk); l.gc = f32(p.off_gc);
+    l.d_initial = E;  // d_final = 0, dhn / dvn not kept
+    e = launch_bwd_dh(a->qkv_dtype, a->dk, a->dv, l, st);
+  }
+  return cuda_status(e);
+}
+
+kda_status kda_state_grad_scan(const float *M, const float *E, const float *dS_final,
+                               int32_t num_chains, int32_t num_segments, int32_t H, int32_t dk,
+                               int32_t dv, float *dS_out, float *dS_initial, kda_stream_t stream) {
+  if (!M || !E || !dS_out) return KDA_ERR_INVALID_ARG;
+  if (num_chains < 1 || num_segments < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+  if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return KDA_ERR_UNSUPPORTED;
+  if ((int64_t)num_chains * H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+  if (mis16(M) || mis16(E) || mis16(dS_final) || mis16(dS_out) || mis16(dS_initial))
+    return KDA_ERR_ALIGNMENT;
+  return cuda_status(launch_prefix_scan(M, E, dS_final, num_chains, num_segments, H, dk, dv, dS_out,
+                                        dS_initial, reinterpret_cast<cudaStream_t>(stream), true));
+}
+
 kda_status kda_get_device_status(void *workspace, kda_stream_t stream) {
   if (!workspace) return KDA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

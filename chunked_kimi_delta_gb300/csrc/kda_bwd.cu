@@ -85,7 +85,8 @@ bwd_dh_kernel(SeqInfo s, int H, int V, const float *__restrict__ w, const float 
       sA[i] = r < len ? aqk[((t + r) * H + h) * BT + (i % BT)] : 0.f;
     }
     for (int cc = tid; cc < K; cc += 256) sGc[cc] = gc[(ci * H + h) * K + cc];
-    for (int cc = rb; cc < K; cc += 8) dhn[((ci * H + h) * K + cc) * V + col] = sD[cc * VT + j];
+    if (dhn)
+      for (int cc = rb; cc < K; cc += 8) dhn[((ci * H + h) * K + cc) * V + col] = sD[cc * VT + j];
     __syncthreads();
 
     // dv_new = Aqk^T dO + kg dh'
@@ -94,7 +95,7 @@ bwd_dh_kernel(SeqInfo s, int H, int V, const float *__restrict__ w, const float 
       if (r < len) {
         for (int s2 = r; s2 < len; ++s2) acc = fmaf(sA[s2 * BT + r], sO[s2 * VT + j], acc);
         for (int cc = 0; cc < K; ++cc) acc = fmaf(sKg[r * K + cc], sD[cc * VT + j], acc);
-        dvn[((t + r) * H + h) * (int64_t)V + col] = acc;
+        if (dvn) dvn[((t + r) * H + h) * (int64_t)V + col] = acc;
       }
       sDv[r * VT + j] = acc;
     }
@@ -632,24 +633,28 @@ __global__ void bwd_group_sum_kernel(int64_t rows, int H, int Hk, int K, const f
   dk[i] = from_f32<Tin>(b);
 }
 
+template <typename Tin, int K>
+cudaError_t dh_dispatch(const BwdLaunch &b, int V, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (K * VT + 3 * BT * K + 2 * BT * VT + BT * BT + K);
+  auto kern = bwd_dh_kernel<Tin, K>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((int64_t)b.s.N * b.H), V / VT);
+  if (grid.x == 0) return cudaSuccess;
+  kern<<<grid, 256, smem, st>>>(b.s, b.H, V, b.w, b.qg, b.kg, b.aqk, b.gc,
+                                static_cast<const Tin *>(b.d_out), b.d_final, b.dhn, b.dvn,
+                                b.d_initial);
+  return cudaGetLastError();
+}
+
 template <typename Tin, int K, int V>
 cudaError_t bwd_dispatch(const BwdLaunch &b, cudaStream_t st) {
   const SeqInfo &s = b.s;
   const int H = b.H, Hk = b.Hk;
   const Tin *dO = static_cast<const Tin *>(b.d_out);
   // B1: reverse chain of the state gradient
-  {
-    const size_t smem = sizeof(float) * (K * VT + 3 * BT * K + 2 * BT * VT + BT * BT + K);
-    auto kern = bwd_dh_kernel<Tin, K>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((int64_t)s.N * H), V / VT);
-    if (grid.x) {
-      kern<<<grid, 256, smem, st>>>(s, H, V, b.w, b.qg, b.kg, b.aqk, b.gc, dO, b.d_final, b.dhn, b.dvn,
-                                    b.d_initial);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-  }
+  cudaError_t e0 = dh_dispatch<Tin, K>(b, V, st);
+  if (e0 != cudaSuccess) return e0;
   if (b.nchunks == 0) return cudaSuccess;
   // B2: state-contraction terms
   {
@@ -708,6 +713,17 @@ cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, c
     KDA_BWD(__nv_bfloat16, 128, 64) KDA_BWD(__nv_bfloat16, 128, 128)
   }
 #undef KDA_BWD
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st) {
+  if (dt == KDA_F32) {
+    if (K == 64) return dh_dispatch<float, 64>(b, V, st);
+    if (K == 128) return dh_dispatch<float, 128>(b, V, st);
+  } else {
+    if (K == 64) return dh_dispatch<__nv_bfloat16, 64>(b, V, st);
+    if (K == 128) return dh_dispatch<__nv_bfloat16, 128>(b, V, st);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -182,13 +182,17 @@ struct BwdLaunch {
   float *dg, *dbeta, *d_initial;
 };
 cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
+// The reverse state-gradient chain alone (dhn / dvn may be null: not written).
+cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
 cudaError_t launch_bwd_param_reduce(int64_t nchunks, int H, int K, const float *part_alog,
                                     const float *part_dtb, float *da_log, float *ddt_bias,
                                     cudaStream_t st);
 
+// reverse = false: S_in[j] = S; S = M_j S + S~_j over j = 0 .. S-1.
+// reverse = true:  S_in[j] = S; S = M_j^T S + S~_j over j = S-1 .. 0.
 cudaError_t launch_prefix_scan(const float *M, const float *S_tilde, const float *S0, int C,
                                int S, int H, int K, int V, float *S_in, float *S_final,
-                               cudaStream_t st);
+                               cudaStream_t st, bool reverse = false);
 
 cudaError_t launch_state_gather(const void *cache, kda_dtype dt, int64_t num_rows,
                                 int64_t row_stride, int64_t payload, const void *idx,

@@ -11,6 +11,11 @@
 // sequential; each step is a K x K by K x 32 product on CUDA cores in fp32,
 // with M_j staged in shared memory and the running state held in registers
 // (each warp owns K/8 rows of the tile, one column per lane).
+//
+// The reverse form is the backward twin ("Hyper-Parallel Chunk KDA current
+// implementation design" section 5.2; "KDA Chunk Backward - TPU/Pallas Kernel
+// Design" section 2.4): the state gradient runs from the last segment to the
+// first through the transposed transitions, g <- M_j^T g + E_j.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -21,7 +26,7 @@ template <int K>
 __global__ void __launch_bounds__(256)
 prefix_scan_kernel(const float *__restrict__ M, const float *__restrict__ St,
                    const float *__restrict__ S0, int S, int H, int V, float *__restrict__ S_in,
-                   float *__restrict__ S_final) {
+                   float *__restrict__ S_final, bool reverse) {
   constexpr int R = K / 8;  // rows of the tile per warp
   extern __shared__ float smem[];
   float *sM = smem;                // [K][K+1]
@@ -37,7 +42,8 @@ prefix_scan_kernel(const float *__restrict__ M, const float *__restrict__ St,
     const int r = rb + 8 * i;
     reg[i] = S0 ? S0[(st0 * K + r) * V + col] : 0.f;
   }
-  for (int seg = 0; seg < S; ++seg) {
+  for (int step = 0; step < S; ++step) {
+    const int seg = reverse ? S - 1 - step : step;
     const int64_t u = ((int64_t)ch * S + seg) * H + h;
     __syncthreads();  // previous step done with sM / sS
 #pragma unroll
@@ -47,7 +53,10 @@ prefix_scan_kernel(const float *__restrict__ M, const float *__restrict__ St,
       S_in[(u * K + r) * V + col] = reg[i];
     }
     const float *Mu = M + u * K * K;
-    for (int x = tid; x < K * K; x += 256) sM[(x / K) * (K + 1) + (x % K)] = Mu[x];
+    if (reverse)  // sM = M^T
+      for (int x = tid; x < K * K; x += 256) sM[(x % K) * (K + 1) + (x / K)] = Mu[x];
+    else
+      for (int x = tid; x < K * K; x += 256) sM[(x / K) * (K + 1) + (x % K)] = Mu[x];
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -68,22 +77,23 @@ prefix_scan_kernel(const float *__restrict__ M, const float *__restrict__ St,
 
 template <int K>
 cudaError_t scan_dispatch(const float *M, const float *St, const float *S0, int C, int S, int H,
-                          int V, float *S_in, float *S_final, cudaStream_t st) {
+                          int V, float *S_in, float *S_final, cudaStream_t st, bool reverse) {
   const size_t smem = sizeof(float) * (K * (K + 1) + K * 32);
   auto kern = prefix_scan_kernel<K>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((int64_t)C * H), V / 32);
-  kern<<<grid, 256, smem, st>>>(M, St, S0, S, H, V, S_in, S_final);
+  kern<<<grid, 256, smem, st>>>(M, St, S0, S, H, V, S_in, S_final, reverse);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefix_scan(const float *M, const float *S_tilde, const float *S0, int C, int S,
-                               int H, int K, int V, float *S_in, float *S_final, cudaStream_t st) {
-  if (K == 64) return scan_dispatch<64>(M, S_tilde, S0, C, S, H, V, S_in, S_final, st);
-  if (K == 128) return scan_dispatch<128>(M, S_tilde, S0, C, S, H, V, S_in, S_final, st);
+                               int H, int K, int V, float *S_in, float *S_final, cudaStream_t st,
+                               bool reverse) {
+  if (K == 64) return scan_dispatch<64>(M, S_tilde, S0, C, S, H, V, S_in, S_final, st, reverse);
+  if (K == 128) return scan_dispatch<128>(M, S_tilde, S0, C, S, H, V, S_in, S_final, st, reverse);
   return cudaErrorInvalidValue;
 }
 

@@ -380,6 +380,42 @@ size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *args);
  * KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
 kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream);
 
+/*
+ * Backward segment summary, the backward twin of kda_segment_summary
+ * ("Hyper-Parallel Chunk KDA current implementation design" section 5.2,
+ * npu_chunk_kda_pre_process_bwd: the local backward affine summary; "KDA
+ * Chunk Backward - TPU/Pallas Kernel Design" section 2.4, dS_ext).  For
+ * segment s = tokens [seg_bounds[s], seg_bounds[s+1]) and head h:
+ *   E[s,h] = gradient of <d_out, o> over the segment's tokens with respect
+ *            to the state entering the segment          [S, H, dk, dv] fp32
+ * The segment's outputs are affine in that state, so E does not depend on
+ * it; with the forward transition M of kda_segment_summary, the gradient of
+ * the state entering the segment is M^T dS_out + E (the backward summary is
+ * [E | M^T]; M is not recomputed here).  Uses q, k, v, g, a_log, dt_bias,
+ * beta, flags, sizes, Hk and workspace of args (workspace of
+ * kda_segment_bwd_summary_workspace_size); d_out [.., H, dv] qkv_dtype or
+ * NULL (E = 0).  CUDA cores, fp32.  Errors as kda_segment_summary, plus
+ * KDA_ERR_UNSUPPORTED for KDA_REUSE_PREP. */
+size_t kda_segment_bwd_summary_workspace_size(const kda_fwd_args *args, int32_t num_segments);
+kda_status kda_segment_bwd_summary(const kda_fwd_args *args, const void *d_out,
+                                   const int32_t *seg_bounds, int32_t num_segments, float *E,
+                                   kda_stream_t stream);
+
+/*
+ * Reverse-order scan of the state gradient across segments (same sections:
+ * the summaries are exchanged in reverse time order).  For every chain c and
+ * head h, with g = dS_final[c,h] (zeros when NULL):
+ *   for j = num_segments-1 .. 0:  dS_out[c,j,h] = g;  g = M[c,j,h]^T g + E[c,j,h]
+ *   dS_initial[c,h] = g   (when not NULL)
+ * dS_out[c,j] is the gradient of the state leaving segment j: the d_final
+ * of that segment's kda_chunk_bwd.  M: [C, S, H, dk, dk]; E, dS_out:
+ * [C, S, H, dk, dv]; dS_final, dS_initial: [C, H, dk, dv]; fp32, computed in
+ * fp32 on CUDA cores.  dS_out must not alias the inputs.  Errors as
+ * kda_state_prefix_scan. */
+kda_status kda_state_grad_scan(const float *M, const float *E, const float *dS_final,
+                               int32_t num_chains, int32_t num_segments, int32_t H, int32_t dk,
+                               int32_t dv, float *dS_out, float *dS_initial, kda_stream_t stream);
+
 /* Reads and clears the device error word kept at the start of a forward or
  * summary workspace: synchronises the stream, returns KDA_OK or
  * KDA_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up.  Every

@@ -241,3 +241,20 @@ def test_bwd_argument_checks(lib):
     b.workspace, b.workspace_bytes = (1 << 30) + 16, size(b)
     assert f(b) == 3
     assert lib.kda_chunk_bwd(None, None) == 1
+
+
+def test_backward_summary_and_grad_scan_checks(lib):
+    a = _args()
+    f = lambda *x: lib.kda_segment_bwd_summary(ctypes.byref(a), *x)
+    assert f(None, 1 << 20, 0, 1 << 22, None) == 1                  # no segments
+    assert f(None, None, 2, 1 << 22, None) == 1                     # no bounds
+    assert f(None, 1 << 20, 2, None, None) == 1                     # no E
+    assert f((1 << 24) + 2, 1 << 20, 2, 1 << 22, None) == 3        # d_out misaligned
+    assert f(None, 1 << 20, 2, 1 << 22, None) == 4                  # no workspace
+    assert lib.kda_segment_bwd_summary_workspace_size(ctypes.byref(a), 2) > 0
+    assert lib.kda_segment_bwd_summary_workspace_size(ctypes.byref(a), 0) == 0
+    g = lambda *x: lib.kda_state_grad_scan(*x)
+    assert g(None, 1 << 20, None, 1, 2, 2, 64, 64, 1 << 21, None, None) == 1
+    assert g(1 << 20, 1 << 21, None, 1, 0, 2, 64, 64, 1 << 22, None, None) == 1
+    assert g(1 << 20, 1 << 21, None, 1, 2, 2, 96, 64, 1 << 22, None, None) == 2
+    assert g(1 << 20, 1 << 21, (1 << 23) + 4, 1, 2, 2, 64, 64, 1 << 22, None, None) == 3
