@@ -348,6 +348,8 @@ def main():
         result["decode"] = bench_decode(kda, dev, stream, hbm_peak)
     if rank == 0 and not args.no_bwd:
         result["bwd"] = bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak)
+    if rank == 0 and not args.no_bwd and not args.no_segment:
+        result["segment_mode_bwd"] = bench_segment_bwd(kda, dev, stream)
     if not args.no_e2e:
         result["e2e"] = bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world)
     if rank == 0 and not args.no_cpu_baseline:
@@ -478,6 +480,73 @@ def bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak, steps=5, warmup=3):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "alg_bytes_per_launch": nbytes,
                          "scope": "whole backward call"}}
+
+
+def bench_segment_bwd(kda, dev, stream, steps=1, warmup=1):
+    """Segment-mode backward on the long-sequence workload (T = 2^20, H = 8,
+    16 segments): forward summary -> scan -> backward summary -> reverse
+    scan -> per-segment backward, all gradients."""
+    import torch
+    from chunked_kimi_delta_gb300.inputs import CONFIGS, make_cotangents, make_inputs
+    cfg = CONFIGS["long_segment_bf16"]
+    inp = make_inputs(cfg, device=dev)
+    cot = make_cotangents(cfg, inp, device=dev)
+    T, H, K, V = cfg.T, cfg.H, cfg.dk, cfg.dv
+    S = cfg.num_segments
+    sb = inp["seg_bounds"]
+    kw = dict(scale=float(K ** -0.5), a_log=inp["a_log"], dt_bias=inp["dt_bias"], l2norm_qk=True,
+              beta_sigmoid=True, gate_in_kernel=True, use_exp2=True)
+    flat = lambda x: x.reshape(T, *x.shape[2:])
+    q, k, v, g, be = (flat(inp[n]) for n in ("q", "k", "v", "g", "beta"))
+    dO = flat(cot["d_out"])
+    M = torch.empty(S, H, K, K, device=dev)
+    St = torch.empty(S, H, K, V, device=dev)
+    S_in = torch.empty(S, H, K, V, device=dev)
+    E = torch.empty(S, H, K, V, device=dev)
+    dS_out = torch.empty(S, H, K, V, device=dev)
+    dS0 = torch.empty(H, K, V, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    bargs = {}
+
+    def one(rec):
+        if rec:
+            ev[0].record(stream)
+        kda.kda_segment_summary(q, k, v, g, be, sb, M=M, S_tilde=St, stream=stream, **kw)
+        kda.kda_state_prefix_scan(M, St, None, S_in=S_in, stream=stream)
+        if rec:
+            ev[1].record(stream)
+        kda.kda_segment_bwd_summary(q, k, v, g, be, dO, sb, E=E, stream=stream, **kw)
+        if rec:
+            ev[2].record(stream)
+        kda.kda_state_grad_scan(M, E, cot["d_final_state"][0], dS_out=dS_out, dS_initial=dS0,
+                                stream=stream)
+        if rec:
+            ev[3].record(stream)
+        if "b" not in bargs:
+            bargs["b"] = kda.prepare_chunk_bwd(q, k, v, g, be, dO, d_final_state=dS_out,
+                                               initial_state=S_in, cu_seqlens=sb, **kw)
+        st = kda.load_library().kda_chunk_bwd(ctypes.byref(bargs["b"][0]), stream.cuda_stream)
+        if st:
+            raise kda.KdaError(st, "segment backward finish")
+        if rec:
+            ev[4].record(stream)
+
+    for _ in range(warmup):
+        one(False)
+    torch.cuda.synchronize()
+    parts = [0.0] * 4
+    for _ in range(steps):
+        one(True)
+        ev[4].synchronize()
+        for i in range(4):
+            parts[i] += ev[i].elapsed_time(ev[i + 1])
+    parts = [x / steps for x in parts]
+    total = sum(parts)
+    return {"workload": f"long_segment_bf16 backward: B=1 T={T} H={H} d={K} bf16, {S} segments, "
+                        f"all gradients",
+            "tokens_per_s": T / (total / 1e3), "ms_per_pass": total,
+            "fwd_summary_scan_ms": parts[0], "bwd_summary_ms": parts[1], "grad_scan_ms": parts[2],
+            "finish_ms": parts[3]}
 
 
 def bench_segment(kda, dev, stream, steps=3, warmup=2):

@@ -187,10 +187,16 @@ def _check_shapes(q, k, v, g, beta, out):
         raise ValueError("out must have v's shape")
 
 
+def _state_shape(N, q, v, v_first=False):
+    """Shape of N recurrent states: [N, H, dk, dv], or [N, H, dv, dk] V-first."""
+    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    return (N, H, V, K) if v_first else (N, H, K, V)
+
+
 def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias=None,
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
-                  gate_in_kernel=False, use_exp2=False, extra_flags=0, out=None,
-                  final_state=None, h_out=None, v_new_out=None) -> kda_fwd_args:
+                  gate_in_kernel=False, use_exp2=False, state_v_first=False, extra_flags=0,
+                  out=None, final_state=None, h_out=None, v_new_out=None) -> kda_fwd_args:
     """Fills a ``kda_fwd_args`` from tensors (BSND [B,T,H,D], or TND [T,H,D]
     with ``cu_seqlens``).  q and k may carry fewer heads than v (grouped key
     heads, Hk dividing H): value head h reads key head h // (H // Hk)."""
@@ -218,7 +224,7 @@ def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
     a.initial_state = _ptr(initial_state)
     a.flags = ((KDA_L2NORM_QK if l2norm_qk else 0) | (KDA_BETA_SIGMOID if beta_sigmoid else 0)
                | (KDA_GATE_IN_KERNEL if gate_in_kernel else 0) | (KDA_USE_EXP2 if use_exp2 else 0)
-               | extra_flags)
+               | (KDA_STATE_V_FIRST if state_v_first else 0) | extra_flags)
     a.out, a.final_state = _ptr(out), _ptr(final_state)
     a.h_out, a.v_new_out = _ptr(h_out), _ptr(v_new_out)
     return a
@@ -237,7 +243,7 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
                   gate_in_kernel=False, use_exp2=False, output_final_state=True, out=None,
                   final_state=None, h_out=None, v_new_out=None, workspace=None, stream=None,
-                  reuse_prep=False, extra_flags=0):
+                  reuse_prep=False, state_v_first=False, extra_flags=0):
     """Chunked KDA forward.  Returns ``(out, final_state)`` (final_state is
     None unless requested).  ``reuse_prep`` (with ``workspace``) sets
     KDA_REUSE_PREP: the workspace already holds this problem's intra-chunk
@@ -256,12 +262,12 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
     if out is None:
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     if output_final_state and final_state is None:
-        final_state = torch.empty(N, v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+        final_state = torch.empty(_state_shape(N, q, v, state_v_first), dtype=torch.float32,
                                   device=q.device)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
                       beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
-                      extra_flags=extra_flags, out=out, final_state=final_state, h_out=h_out,
+                      state_v_first=state_v_first, extra_flags=extra_flags, out=out, final_state=final_state, h_out=h_out,
                       v_new_out=v_new_out)
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
@@ -292,8 +298,8 @@ def prepare_chunk_fwd_host(q, k, v, g, beta, *, device=None, output_final_state=
         out = torch.empty(v.shape, dtype=q.dtype, pin_memory=True)
     fin = kw.pop("final_state", None)
     if output_final_state and fin is None:
-        fin = torch.empty(q.shape[0], v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
-                          device=device)
+        fin = torch.empty(_state_shape(q.shape[0], q, v, kw.get("state_v_first", False)),
+                          dtype=torch.float32, device=device)
     a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
     ws = _workspace(lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(a)), device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
@@ -317,7 +323,7 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_lo
                                  dt_bias=None, initial_state=None, cu_seqlens=None,
                                  l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
                                  use_exp2=False, output_final_state=True, out=None,
-                                 final_state=None, stream=None):
+                                 final_state=None, state_v_first=False, stream=None):
     """The forward for callers that cannot allocate device memory: same
     arguments and results as :func:`kda_chunk_fwd`, but no workspace; the
     library's fixed scratch array is used instead (problems whose workspace
@@ -333,12 +339,12 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_lo
     if out is None:
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     if output_final_state and final_state is None:
-        final_state = torch.empty(N, v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
+        final_state = torch.empty(_state_shape(N, q, v, state_v_first), dtype=torch.float32,
                                   device=q.device)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
                       beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
-                      out=out, final_state=final_state)
+                      state_v_first=state_v_first, out=out, final_state=final_state)
     _check(lib.kda_chunk_fwd_static_scratch(ctypes.byref(a), _stream(stream)),
            "kda_chunk_fwd_static_scratch")
     return out, final_state
@@ -357,8 +363,8 @@ def prepare_chunk_fwd(q, k, v, g, beta, *, output_final_state=True, workspace=No
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     fin = kw.pop("final_state", None)
     if output_final_state and fin is None:
-        fin = torch.empty(N, v.shape[-2], q.shape[-1], v.shape[-1], dtype=torch.float32,
-                          device=q.device)
+        fin = torch.empty(_state_shape(N, q, v, kw.get("state_v_first", False)),
+                          dtype=torch.float32, device=q.device)
     a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
@@ -505,11 +511,11 @@ def kda_state_scatter(cache, idx, packed, *, stream=None):
 
 def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=None, eps=1e-6,
                        a_log=None, dt_bias=None, l2norm_qk=True, beta_sigmoid=False,
-                       gate_in_kernel=False, out=None, stream=None):
+                       gate_in_kernel=False, state_v_first=False, out=None, stream=None):
     """Recurrent decode step on pool states, in place: q, k [N, T, Hk, dk]
     (Hk dividing H), g [N, T, H, dk], v [N, T, H, dv], beta [N, T, H];
-    ``cache`` [rows, H, dk, dv] (any row stride); ``idx`` [N] rows of the
-    pool.  Returns out [N, T, H, dv].  See ``kda_recurrent_step`` in
+    ``cache`` [rows, H, dk, dv] ([rows, H, dv, dk] with ``state_v_first``;
+    any row stride); ``idx`` [N] rows of the pool.  Returns out [N, T, H, dv].  See ``kda_recurrent_step`` in
     include/kda.h."""
     torch = _torch()
     lib = load_library()
@@ -532,7 +538,8 @@ def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=N
     a.scale = float(q.shape[-1] ** -0.5 if scale is None else scale)
     a.eps = float(eps)
     a.flags = ((KDA_L2NORM_QK if l2norm_qk else 0) | (KDA_BETA_SIGMOID if beta_sigmoid else 0)
-               | (KDA_GATE_IN_KERNEL if gate_in_kernel else 0))
+               | (KDA_GATE_IN_KERNEL if gate_in_kernel else 0)
+               | (KDA_STATE_V_FIRST if state_v_first else 0))
     a.out = _ptr(out)
     a.cache, a.cache_dtype, a.num_rows, a.row_stride_elems = _ptr(cache), _dtype_code(cache), n_rows, stride
     a.idx, a.idx_dtype, a.init_flags = _ptr(idx), _idx_code(idx), _ptr(init_flags)
@@ -558,8 +565,9 @@ def prepare_chunk_bwd(q, k, v, g, beta, d_out, *, d_final_state=None, initial_st
             raise ValueError("d_out must have v's shape and q's dtype")
         _contig(d_out)
     if d_final_state is not None:
-        if tuple(d_final_state.shape) != (N, H, K, V) or d_final_state.dtype != torch.float32:
-            raise ValueError("d_final_state must be fp32 [N, H, dk, dv]")
+        if (tuple(d_final_state.shape) != _state_shape(N, q, v, kw.get("state_v_first", False))
+                or d_final_state.dtype != torch.float32):
+            raise ValueError("d_final_state must be fp32 [N, H, dk, dv] ([N, H, dv, dk] V-first)")
         _contig(d_final_state)
     if want_d_initial_state is None:
         want_d_initial_state = initial_state is not None
@@ -570,7 +578,8 @@ def prepare_chunk_bwd(q, k, v, g, beta, d_out, *, d_final_state=None, initial_st
         dbeta=torch.empty(beta.shape, dtype=torch.float32, device=dev),
         da_log=torch.empty(H, dtype=torch.float32, device=dev) if gate else None,
         ddt_bias=torch.empty(H, K, dtype=torch.float32, device=dev) if gate else None,
-        d_initial_state=(torch.empty(N, H, K, V, dtype=torch.float32, device=dev)
+        d_initial_state=(torch.empty(_state_shape(N, q, v, kw.get("state_v_first", False)),
+                                     dtype=torch.float32, device=dev)
                          if want_d_initial_state else None),
     )
     b = kda_bwd_args()

@@ -22,7 +22,9 @@ inline bool mis16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) &
 constexpr uint32_t kKnownFlags = KDA_L2NORM_QK | KDA_BETA_SIGMOID | KDA_GATE_IN_KERNEL |
                                  KDA_USE_EXP2 | KDA_REUSE_PREP | KDA_SAFE_GATE |
                                  KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST;
-constexpr uint32_t kRejectedFlags = KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST;
+constexpr uint32_t kRejectedFlags = KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL;
+
+inline bool v_first(const kda_fwd_args *a) { return (a->flags & KDA_STATE_V_FIRST) != 0; }
 
 // Checks shared by the forward and the summary (everything but the outputs).
 kda_status check_common(const kda_fwd_args *a) {
@@ -93,8 +95,26 @@ TcPlan tc_plan(const FwdPlan &p) {
   return t;
 }
 
+// K-first copies of the caller's V-first states (initial, final, h_out),
+// after the forward's own workspace.
+struct VfPlan {
+  size_t off_init, off_fin, off_hout, total;
+};
+VfPlan vf_plan(const kda_fwd_args *a, const FwdPlan &p, size_t base) {
+  VfPlan v{};
+  size_t o = base;
+  if (v_first(a)) {
+    const size_t SS = (size_t)p.N * p.H * p.K * p.V * 4;
+    if (a->initial_state) { v.off_init = o; o = align256(o + SS); }
+    if (a->final_state) { v.off_fin = o; o = align256(o + SS); }
+    if (a->h_out) { v.off_hout = o; o = align256(o + (size_t)p.nchunks * p.H * p.K * p.V * 4); }
+  }
+  v.total = o;
+  return v;
+}
+
 size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p) {
-  return use_tc(a) ? tc_plan(p).total : p.total;
+  return vf_plan(a, p, use_tc(a) ? tc_plan(p).total : p.total).total;
 }
 
 kda_status check_workspace(const kda_fwd_args *a, const FwdPlan &p) {
@@ -146,10 +166,50 @@ size_t kda_segment_summary_workspace_size(const kda_fwd_args *a, int32_t num_seg
 // recorded before stage i and events[count] after the last stage.  The device
 // error word is cleared first unless keep_err (the blocks of a host-IO call
 // share one word, cleared once).
+static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
+                                 int32_t nev, bool keep_err);
+
+// V-first states: converted to K-first copies in the workspace around the
+// K-first forward ("Hyper-Parallel Chunk KDA current implementation design",
+// section 4.1, state_v_first).
 static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
                           int32_t nev, bool keep_err = false) {
   kda_status s = check_fwd(a);
   if (s != KDA_OK) return s;
+  if (!v_first(a)) return run_fwd_kfirst(a, st, ev, nev, keep_err);
+  const FwdPlan p = fwd_plan(a);
+  if ((s = check_workspace(a, p)) != KDA_OK) return s;
+  char *ws = static_cast<char *>(a->workspace);
+  const VfPlan v = vf_plan(a, p, use_tc(a) ? tc_plan(p).total : p.total);
+  kda_fwd_args b = *a;
+  b.flags &= ~(uint32_t)KDA_STATE_V_FIRST;
+  b.workspace_bytes = v.off_init ? v.off_init : (v.off_fin ? v.off_fin : (v.off_hout ? v.off_hout : v.total));
+  cudaError_t e = cudaSuccess;
+  if (a->initial_state) {
+    b.initial_state = reinterpret_cast<float *>(ws + v.off_init);
+    e = launch_transpose_states(a->initial_state, const_cast<float *>(b.initial_state),
+                                (int64_t)p.N * p.H, p.V, p.K, nullptr, 0, st);
+  }
+  if (a->final_state) b.final_state = reinterpret_cast<float *>(ws + v.off_fin);
+  if (a->h_out) b.h_out = reinterpret_cast<float *>(ws + v.off_hout);
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  if ((s = run_fwd_kfirst(&b, st, ev, nev, keep_err)) != KDA_OK) return s;
+  if (a->final_state)
+    e = launch_transpose_states(b.final_state, a->final_state, (int64_t)p.N * p.H, p.K, p.V, nullptr,
+                                0, st);
+  if (e == cudaSuccess && a->h_out) {
+    // only the chunks that exist: their count is on the device for packed sequences
+    const int32_t *count = a->cu_seqlens ? reinterpret_cast<const int32_t *>(ws + (use_tc(a)
+                               ? tc_plan(p).off_chunk_off : p.off_chunk_off)) + p.N
+                                         : nullptr;
+    e = launch_transpose_states(b.h_out, a->h_out, p.nchunks * p.H, p.K, p.V, count, p.H, st);
+  }
+  return cuda_status(e);
+}
+
+static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
+                                 int32_t nev, bool keep_err) {
+  kda_status s;
   const FwdPlan p = fwd_plan(a);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
   char *ws = static_cast<char *>(a->workspace);
@@ -288,7 +348,11 @@ HostPlan host_plan(const kda_fwd_args *a) {
   h.esz = a->qkv_dtype == KDA_BF16 ? 2 : 4;
   h.Tb = a->T < KDA_HOST_BLOCK_TOKENS ? a->T : KDA_HOST_BLOCK_TOKENS;
   h.nblk = h.Tb > 0 ? (a->T + h.Tb - 1) / h.Tb : 0;
-  const kda_fwd_args b = block_args(a, h.Tb);
+  kda_fwd_args b = block_args(a, h.Tb);
+  if (v_first(a)) {  // every block converts its entering and leaving state (size only)
+    static const float placeholder[4] = {0.f, 0.f, 0.f, 0.f};
+    b.initial_state = b.final_state = const_cast<float *>(placeholder);
+  }
   size_t o = 0;
   h.off_sub = o;
   h.sub_bytes = plan_bytes(&b, fwd_plan(&b));
@@ -422,6 +486,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
                                kda_stream_t stream) {
   kda_status s = check_common(a);
   if (s != KDA_OK) return s;
+  if (v_first(a)) return KDA_ERR_UNSUPPORTED;  // summaries are K-first
   if (num_segments < 1 || !seg_bounds || !M || !S_tilde) return KDA_ERR_INVALID_ARG;
   if (mis16(seg_bounds) || mis16(M) || mis16(S_tilde)) return KDA_ERR_ALIGNMENT;
   const FwdPlan p = summary_plan(a, num_segments);
@@ -515,7 +580,7 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   if (!a || a->N < 0 || a->T < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
   if (a->Hk < 0 || (a->Hk > 0 && a->H % a->Hk != 0)) return KDA_ERR_INVALID_ARG;
   if (a->flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
-  if (a->flags & (kRejectedFlags | KDA_REUSE_PREP)) return KDA_ERR_UNSUPPORTED;
+  if (a->flags & (kRejectedFlags | KDA_REUSE_PREP)) return KDA_ERR_UNSUPPORTED;  // V-first is taken
   if ((a->dk != 64 && a->dk != 128) || (a->dv != 64 && a->dv != 128)) return KDA_ERR_UNSUPPORTED;
   if (a->qkv_dtype != KDA_F32 && a->qkv_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (a->cache_dtype != KDA_F32 && a->cache_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
@@ -536,7 +601,8 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   return cuda_status(launch_decode(a->qkv_dtype, a->cache_dtype, a->idx_dtype, a->dk, a->dv, a->N,
                                    a->T, a->H, a->Hk > 0 ? a->Hk : a->H, a->q, a->k, a->v, a->g,
                                    a->beta, gp, a->out, a->cache,
-                                   a->num_rows, a->row_stride_elems, a->idx, a->init_flags, st));
+                                   a->num_rows, a->row_stride_elems, a->idx, a->init_flags,
+                                   (a->flags & KDA_STATE_V_FIRST) != 0, st));
 }
 
 }  // extern "C"
@@ -564,7 +630,9 @@ kda_status check_bwd(const kda_bwd_args *b) {
 struct BwdPlan {
   FwdPlan f;
   size_t off_h, off_vn, off_dhn, off_dvn, off_dqg, off_dw, off_dkg, off_dgc, off_palog, off_pdtb;
-  size_t off_dqv, off_dkv, total;
+  size_t off_dqv, off_dkv;
+  size_t off_vf_init, off_vf_dfin, off_vf_dinit;  // K-first copies of V-first states
+  size_t total;
 };
 
 BwdPlan bwd_plan(const kda_bwd_args *b) {
@@ -587,6 +655,13 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
   if (p.f.Hk != p.f.H) {
     p.off_dqv = o; o = align256(o + 4 * th * K);
     p.off_dkv = o; o = align256(o + 4 * th * K);
+  }
+  p.off_vf_init = p.off_vf_dfin = p.off_vf_dinit = 0;
+  if (v_first(&b->fwd)) {
+    const size_t SS = 4 * (size_t)p.f.N * p.f.H * K * V;
+    if (b->fwd.initial_state) { p.off_vf_init = o; o = align256(o + SS); }
+    if (b->d_final_state) { p.off_vf_dfin = o; o = align256(o + SS); }
+    if (b->d_initial_state) { p.off_vf_dinit = o; o = align256(o + SS); }
   }
   p.total = o;
   return p;
@@ -620,7 +695,24 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   si.N = p.f.N;
   const GateParams gp = gate_params(a);
 
-  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
+  // V-first states: K-first copies in the workspace
+  const float *init = a->initial_state, *dfin = b->d_final_state;
+  float *dinit = b->d_initial_state;
+  const int64_t nstates = (int64_t)p.f.N * p.f.H;
+  cudaError_t e = cudaSuccess;
+  if (v_first(a)) {
+    if (init) {
+      e = launch_transpose_states(init, f32(p.off_vf_init), nstates, p.f.V, p.f.K, nullptr, 0, st);
+      init = f32(p.off_vf_init);
+    }
+    if (e == cudaSuccess && dfin) {
+      e = launch_transpose_states(dfin, f32(p.off_vf_dfin), nstates, p.f.V, p.f.K, nullptr, 0, st);
+      dfin = f32(p.off_vf_dfin);
+    }
+    if (dinit) dinit = f32(p.off_vf_dinit);
+  }
+
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, st);
   if (e == cudaSuccess && si.bounds) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
   // recompute: the per-chunk intermediates, the state entering every chunk, v_new
   if (e == cudaSuccess && p.f.T_tot > 0)
@@ -629,7 +721,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
     InterOut io{};
     io.h_out = f32(p.off_h);
     io.v_new_out = f32(p.off_vn);
-    io.initial_state = a->initial_state;
+    io.initial_state = init;
     e = launch_generic_inter(a->qkv_dtype, false, io, si, p.f, ws, st);
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(ws + p.off_palog, 0, p.off_pdtb - p.off_palog, st);
@@ -644,7 +736,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
     l.q = a->q; l.k = a->k; l.v = a->v; l.g = a->g; l.beta = a->beta;
     l.gp = gp;
     l.d_out = b->d_out;
-    l.d_final = b->d_final_state;
+    l.d_final = dfin;
     l.w = f32(p.f.off_w); l.qg = f32(p.f.off_qg); l.kg = f32(p.f.off_kg);
     l.aqk = f32(p.f.off_aqk); l.gc = f32(p.f.off_gc);
     l.h = f32(p.off_h); l.vn = f32(p.off_vn);
@@ -654,12 +746,14 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
     l.dqv = p.off_dqv ? f32(p.off_dqv) : nullptr;
     l.dkv = p.off_dkv ? f32(p.off_dkv) : nullptr;
     l.dq = b->dq; l.dk = b->dk; l.dv = b->dv;
-    l.dg = b->dg; l.dbeta = b->dbeta; l.d_initial = b->d_initial_state;
+    l.dg = b->dg; l.dbeta = b->dbeta; l.d_initial = dinit;
     e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st);
   }
   if (e == cudaSuccess)
     e = launch_bwd_param_reduce(p.f.nchunks, p.f.H, p.f.K, f32(p.off_palog), f32(p.off_pdtb), b->da_log,
                                 b->ddt_bias, st);
+  if (e == cudaSuccess && v_first(a) && dinit)
+    e = launch_transpose_states(dinit, b->d_initial_state, nstates, p.f.K, p.f.V, nullptr, 0, st);
   return cuda_status(e);
 }
 
@@ -673,7 +767,7 @@ kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
                                    kda_stream_t stream) {
   kda_status s = check_common(a);
   if (s != KDA_OK) return s;
-  if (a->flags & KDA_REUSE_PREP) return KDA_ERR_UNSUPPORTED;
+  if (a->flags & (KDA_REUSE_PREP | KDA_STATE_V_FIRST)) return KDA_ERR_UNSUPPORTED;
   if (num_segments < 1 || !seg_bounds || !E) return KDA_ERR_INVALID_ARG;
   if (mis16(seg_bounds) || mis16(E) || mis16(d_out)) return KDA_ERR_ALIGNMENT;
   const FwdPlan p = summary_plan(a, num_segments);

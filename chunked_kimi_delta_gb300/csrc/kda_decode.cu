@@ -80,7 +80,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
               const float *__restrict__ g, const float *__restrict__ beta, GateParams gp,
               Tin *__restrict__ out, Tc *cache, int64_t num_rows, int64_t row_stride,
               const Tidx *__restrict__ idx, const bool *__restrict__ init_flags, int T, int H,
-              int Hk) {
+              int Hk, bool vfirst) {
   constexpr int NQ = VS / 4;                // column quads of the slice
   constexpr int RG = kDecThreads / NQ;      // row groups
   constexpr int R = K / RG;                 // rows per thread
@@ -101,12 +101,20 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
   const bool load = valid && (!init_flags || init_flags[n]);
   Tc *state = cache + (valid ? row * row_stride : 0) + (int64_t)h * K * V;
   Tc *mine = state + (int64_t)(R * rg) * V + c0 + 4 * cq;  // this thread's first element
+  // V-first pool states ([V, K] per head): element (row, column) at column * K + row
+  Tc *mine_vf = state + (int64_t)(c0 + 4 * cq) * K + R * rg;
 
   float s[R][4];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    if (load) ld4_any(mine + (int64_t)r * V, s[r], VEC);
-    else s[r][0] = s[r][1] = s[r][2] = s[r][3] = 0.f;
+    if (!load) {
+      s[r][0] = s[r][1] = s[r][2] = s[r][3] = 0.f;
+    } else if (vfirst) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[r][j] = to_f32<Tc>(mine_vf[(int64_t)j * K + r]);
+    } else {
+      ld4_any(mine + (int64_t)r * V, s[r], VEC);
+    }
   }
 
   const bool gate = (gp.flags & KDA_GATE_IN_KERNEL) != 0;
@@ -212,7 +220,14 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
 
   if (valid) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) st4_any(mine + (int64_t)r * V, s[r], VEC);
+    for (int r = 0; r < R; ++r) {
+      if (vfirst) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mine_vf[(int64_t)j * K + r] = from_f32<Tc>(s[r][j]);
+      } else {
+        st4_any(mine + (int64_t)r * V, s[r], VEC);
+      }
+    }
   }
 }
 
@@ -225,14 +240,14 @@ cudaError_t dispatch_kv(int dk, int dv, bool aligned, int64_t units, cudaStream_
                         const void *k, const void *v, const float *g, const float *beta,
                         const GateParams &gp, void *out, void *cache, int64_t num_rows,
                         int64_t row_stride, const void *idx, const bool *init_flags, int T, int H,
-                        int Hk) {
+                        int Hk, bool vfirst) {
   const Tin *qq = static_cast<const Tin *>(q), *kk = static_cast<const Tin *>(k),
             *vv = static_cast<const Tin *>(v);
 #define KDA_DEC(KK, VV, VEC)                                                                      \
   decode_kernel<Tin, Tc, Tidx, KK, VV, VV, VEC>                                                   \
       <<<(unsigned)units, kDecThreads, 0, st>>>(                                                  \
           qq, kk, vv, g, beta, gp, static_cast<Tin *>(out), static_cast<Tc *>(cache), num_rows,     \
-          row_stride, static_cast<const Tidx *>(idx), init_flags, T, H, Hk)
+          row_stride, static_cast<const Tidx *>(idx), init_flags, T, H, Hk, vfirst)
 #define KDA_DEC2(KK, VV)              \
   if (aligned) KDA_DEC(KK, VV, true); \
   else KDA_DEC(KK, VV, false)
@@ -251,17 +266,18 @@ cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_
                           int dk, int dv, int N, int T, int H, int Hk, const void *q, const void *k,
                           const void *v, const float *g, const float *beta, const GateParams &gp,
                           void *out, void *cache, int64_t num_rows, int64_t row_stride,
-                          const void *idx, const bool *init_flags, cudaStream_t st) {
+                          const void *idx, const bool *init_flags, bool vfirst, cudaStream_t st) {
   const int64_t units = (int64_t)N * H;
   if (units == 0) return cudaSuccess;
   // vector accesses need 16-byte aligned states: the pool base and the row
   // stride (a state's offset inside a row, h*dk*dv elements, and each
   // thread's column quad are multiples of 16 bytes)
   const size_t esz = cache_dtype == KDA_BF16 ? 2 : 4;
-  const bool aligned = (reinterpret_cast<uintptr_t>(cache) & 15u) == 0 && ((size_t)row_stride * esz) % 16 == 0;
+  const bool aligned = !vfirst && (reinterpret_cast<uintptr_t>(cache) & 15u) == 0 &&
+                       ((size_t)row_stride * esz) % 16 == 0;
 #define KDA_DEC_IDX(TI, TC, TX)                                                                     \
   return dispatch_kv<TI, TC, TX>(dk, dv, aligned, units, st, q, k, v, g, beta, gp, out, cache,       \
-                                 num_rows, row_stride, idx, init_flags, T, H, Hk)
+                                 num_rows, row_stride, idx, init_flags, T, H, Hk, vfirst)
   const bool ibf = qkv_dtype == KDA_BF16, cbf = cache_dtype == KDA_BF16, i64 = idx_dtype == KDA_I64;
   if (ibf && cbf && i64) KDA_DEC_IDX(__nv_bfloat16, __nv_bfloat16, int64_t);
   if (ibf && cbf) KDA_DEC_IDX(__nv_bfloat16, __nv_bfloat16, int32_t);

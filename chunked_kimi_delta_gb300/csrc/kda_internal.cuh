@@ -140,12 +140,17 @@ struct GateParams {
 
 cudaError_t launch_chunk_map(const SeqInfo &s, int32_t *chunk_off, cudaStream_t st);
 
+// n fp32 matrices R x C -> C x R (kda_layout.cu); with count_ptr only the
+// first (*count_ptr) * per_count matrices.
+cudaError_t launch_transpose_states(const float *src, float *dst, int64_t n, int R, int C,
+                                    const int32_t *count_ptr, int per_count, cudaStream_t st);
+
 // Recurrent decode step on pool rows (kda_decode.cu).
 cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_dtype idx_dtype,
                           int dk, int dv, int N, int T, int H, int Hk, const void *q, const void *k,
                           const void *v, const float *g, const float *beta, const GateParams &gp,
                           void *out, void *cache, int64_t num_rows, int64_t row_stride,
-                          const void *idx, const bool *init_flags, cudaStream_t st);
+                          const void *idx, const bool *init_flags, bool vfirst, cudaStream_t st);
 
 // Generic (CUDA-core, fp32 arithmetic) intra-chunk stage: writes w, u, qg, kg,
 // Aqk, gC of the plan.

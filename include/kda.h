@@ -70,10 +70,17 @@ enum {
    * inter-chunk chain runs.  Caller precondition, not checked. */
   KDA_REUSE_PREP = 1u << 4,
   /* Named on the pages without a formula (safe_gate/lower_bound,
-   * allow_neg_eigval) or a layout this library does not take (V-first
-   * state): always rejected with KDA_ERR_UNSUPPORTED. */
+   * allow_neg_eigval): always rejected with KDA_ERR_UNSUPPORTED. */
   KDA_SAFE_GATE = 1u << 8,
   KDA_ALLOW_NEG_EIGVAL = 1u << 9,
+  /* state_v_first (same design, section 4.1): every recurrent state the call
+   * takes or returns - initial_state, final_state, h_out of the forward;
+   * initial_state, d_final_state, d_initial_state of the backward; the pool
+   * states of kda_recurrent_step - has its last two dimensions as [dv, dk]
+   * instead of [dk, dv].  The library computes K-first and converts at the
+   * boundary (through workspace copies, included in the workspace sizes).
+   * kda_segment_summary and kda_segment_bwd_summary return K-first summaries
+   * and reject the flag with KDA_ERR_UNSUPPORTED. */
   KDA_STATE_V_FIRST = 1u << 10
 };
 
@@ -107,7 +114,8 @@ typedef struct {
   const float *beta;        /* [.., H] fp32: logits with KDA_BETA_SIGMOID        */
   float scale;              /* output scale, usually dk^-1/2                     */
   float eps;                /* L2-norm epsilon, usually 1e-6                     */
-  const float *initial_state; /* [N, H, dk, dv] fp32 or NULL (= zeros)           */
+  const float *initial_state; /* [N, H, dk, dv] fp32 or NULL (= zeros); [N, H,    */
+                              /* dv, dk] with KDA_STATE_V_FIRST (so every state) */
   const int32_t *cu_seqlens;  /* device [num_seqs+1] token offsets or NULL;      */
                               /* caller precondition: 0 = cu[0] <= .. <= cu[N] = T */
   int32_t num_seqs;         /* N when cu_seqlens is given; ignored otherwise     */
@@ -136,8 +144,8 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
  * Errors: KDA_ERR_INVALID_ARG (null q/k/v/g/beta/out with tokens, B or H < 1,
  * T < 0, Hk < 0 or not dividing H, a_log missing with KDA_GATE_IN_KERNEL,
  * cu_seqlens with B != 1), KDA_ERR_UNSUPPORTED
- * (dk or dv not 64/128, chunk != 64, KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL /
- * KDA_STATE_V_FIRST), KDA_ERR_ALIGNMENT, KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
+ * (dk or dv not 64/128, chunk != 64, KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL),
+ * KDA_ERR_ALIGNMENT, KDA_ERR_WORKSPACE, KDA_ERR_CUDA. */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 
 /* Size of the library's own scratch array used by
@@ -308,8 +316,9 @@ kda_status kda_state_scatter(void *cache, kda_dtype cache_dtype, int64_t num_row
  * H < 1, Hk < 0 or not dividing H, num_rows < 1, row_stride_elems <
  * H*dk*dv, unknown flags, a_log
  * missing with KDA_GATE_IN_KERNEL), KDA_ERR_UNSUPPORTED (dk or dv not 64 /
- * 128, KDA_REUSE_PREP / KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL /
- * KDA_STATE_V_FIRST), KDA_ERR_CUDA.
+ * 128, KDA_REUSE_PREP / KDA_SAFE_GATE / KDA_ALLOW_NEG_EIGVAL), KDA_ERR_CUDA.
+ * With KDA_STATE_V_FIRST the pool states are [H, dv, dk] (element-wise
+ * accesses).
  */
 typedef struct {
   int32_t N, T, H, dk, dv;

@@ -65,7 +65,7 @@ def test_fwd_argument_checks(lib):
     assert f(_args(chunk=32)) == 2
     assert f(_args(flags=kda.KDA_SAFE_GATE)) == 2
     assert f(_args(flags=kda.KDA_ALLOW_NEG_EIGVAL)) == 2
-    assert f(_args(flags=kda.KDA_STATE_V_FIRST)) == 2
+    assert f(_args(flags=kda.KDA_STATE_V_FIRST)) == 4           # V-first: taken (no workspace)
     assert f(_args(flags=1 << 20)) == 1
     assert f(_args(flags=kda.KDA_GATE_IN_KERNEL)) == 1          # a_log missing
     assert f(_args(q=(1 << 20) + 8)) == 3                        # misaligned
@@ -258,3 +258,16 @@ def test_backward_summary_and_grad_scan_checks(lib):
     assert g(1 << 20, 1 << 21, None, 1, 0, 2, 64, 64, 1 << 22, None, None) == 1
     assert g(1 << 20, 1 << 21, None, 1, 2, 2, 96, 64, 1 << 22, None, None) == 2
     assert g(1 << 20, 1 << 21, (1 << 23) + 4, 1, 2, 2, 64, 64, 1 << 22, None, None) == 3
+
+
+def test_v_first_workspace_and_rejections(lib):
+    """V-first states need K-first copies in the workspace; the summaries are
+    K-first only."""
+    size = lambda **kw: lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args(**kw)))
+    vf = kda.KDA_STATE_V_FIRST
+    assert size(flags=vf) == size()                               # no states: nothing to convert
+    assert size(flags=vf, initial_state=1 << 20, final_state=1 << 21) > size(
+        initial_state=1 << 20, final_state=1 << 21)
+    a = _args(flags=vf)
+    assert lib.kda_segment_summary(ctypes.byref(a), 1 << 20, 2, 1 << 21, 1 << 22, None) == 2
+    assert lib.kda_segment_bwd_summary(ctypes.byref(a), None, 1 << 20, 2, 1 << 22, None) == 2
