@@ -635,12 +635,14 @@ struct BwdPlan {
   size_t total;
 };
 
+// The recompute runs on the tensor-core forward (packages) where the forward
+// does, else on the generic one (fp32 per-token intermediates).
 BwdPlan bwd_plan(const kda_bwd_args *b) {
   BwdPlan p{};
   p.f = fwd_plan(&b->fwd);
   const size_t th = (size_t)p.f.T_tot * p.f.H, ch = (size_t)p.f.nchunks * p.f.H;
   const size_t K = p.f.K, V = p.f.V;
-  size_t o = p.f.total;
+  size_t o = use_tc(&b->fwd) ? tc_plan(p.f).total : p.f.total;
   p.off_h = o;     o = align256(o + 4 * ch * K * V);
   p.off_vn = o;    o = align256(o + 4 * th * V);
   p.off_dhn = o;   o = align256(o + 4 * ch * K * V);
@@ -687,13 +689,19 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   char *ws = static_cast<char *>(b->workspace);
   auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
 
+  const bool tc = use_tc(a);
   SeqInfo si{};
   si.bounds = a->cu_seqlens;
-  si.chunk_off = reinterpret_cast<int32_t *>(ws + p.f.off_chunk_off);
+  si.chunk_off = reinterpret_cast<int32_t *>(ws + (tc ? tc_plan(p.f).off_chunk_off : p.f.off_chunk_off));
   si.T_tot = p.f.T_tot;
   si.T = a->T;
   si.N = p.f.N;
   const GateParams gp = gate_params(a);
+  uint32_t *err = reinterpret_cast<uint32_t *>(ws);
+  char *pkg = ws + tc_plan(p.f).off_pkg;
+  tcp::TcMaps maps;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.f.T_tot, a->H, p.f.Hk, maps))
+    return KDA_ERR_CUDA;
 
   // V-first states: K-first copies in the workspace
   const float *init = a->initial_state, *dfin = b->d_final_state;
@@ -715,14 +723,29 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, st);
   if (e == cudaSuccess && si.bounds) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
   // recompute: the per-chunk intermediates, the state entering every chunk, v_new
-  if (e == cudaSuccess && p.f.T_tot > 0)
-    e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gp, si, p.f, ws, st);
-  if (e == cudaSuccess && p.f.T_tot > 0) {
-    InterOut io{};
-    io.h_out = f32(p.off_h);
-    io.v_new_out = f32(p.off_vn);
-    io.initial_state = init;
-    e = launch_generic_inter(a->qkv_dtype, false, io, si, p.f, ws, st);
+  if (tc) {
+    if (e == cudaSuccess)
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gp, si, p.f.nchunks, a->H, p.f.Hk, pkg,
+                              err, st);
+    if (e == cudaSuccess) {
+      tcp::ChainArgs ca{};
+      ca.pkg = pkg;
+      ca.initial_state = init;
+      ca.h_out = f32(p.off_h);
+      ca.v_new_out = f32(p.off_vn);
+      ca.err = err;
+      e = tcp::launch_tc_chain(ca, si, a->H, st);
+    }
+  } else {
+    if (e == cudaSuccess && p.f.T_tot > 0)
+      e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gp, si, p.f, ws, st);
+    if (e == cudaSuccess && p.f.T_tot > 0) {
+      InterOut io{};
+      io.h_out = f32(p.off_h);
+      io.v_new_out = f32(p.off_vn);
+      io.initial_state = init;
+      e = launch_generic_inter(a->qkv_dtype, false, io, si, p.f, ws, st);
+    }
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(ws + p.off_palog, 0, p.off_pdtb - p.off_palog, st);
   if (e == cudaSuccess)
@@ -737,8 +760,10 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
     l.gp = gp;
     l.d_out = b->d_out;
     l.d_final = dfin;
-    l.w = f32(p.f.off_w); l.qg = f32(p.f.off_qg); l.kg = f32(p.f.off_kg);
-    l.aqk = f32(p.f.off_aqk); l.gc = f32(p.f.off_gc);
+    if (!tc) {  // the generic intermediates (the tensor-core path keeps packages instead)
+      l.w = f32(p.f.off_w); l.qg = f32(p.f.off_qg); l.kg = f32(p.f.off_kg);
+      l.aqk = f32(p.f.off_aqk); l.gc = f32(p.f.off_gc);
+    }
     l.h = f32(p.off_h); l.vn = f32(p.off_vn);
     l.dhn = f32(p.off_dhn); l.dvn = f32(p.off_dvn); l.dqg = f32(p.off_dqg); l.dw = f32(p.off_dw);
     l.dkg = f32(p.off_dkg); l.dgc = f32(p.off_dgc);
@@ -747,7 +772,18 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
     l.dkv = p.off_dkv ? f32(p.off_dkv) : nullptr;
     l.dq = b->dq; l.dk = b->dk; l.dv = b->dv;
     l.dg = b->dg; l.dbeta = b->dbeta; l.d_initial = dinit;
-    e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st);
+    if (tc) {  // reverse chain on the tensor cores from the packages
+      tcp::BwdChainArgs ba{};
+      ba.pkg = pkg;
+      ba.d_out = b->d_out;
+      ba.d_final = dfin;
+      ba.dhn = l.dhn;
+      ba.dvn = l.dvn;
+      ba.d_initial = dinit;
+      ba.err = err;
+      e = tcp::launch_tc_bwd_dh(ba, si, a->H, p.f.T_tot, st);
+    }
+    if (e == cudaSuccess) e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st, !tc);
   }
   if (e == cudaSuccess)
     e = launch_bwd_param_reduce(p.f.nchunks, p.f.H, p.f.K, f32(p.off_palog), f32(p.off_pdtb), b->da_log,

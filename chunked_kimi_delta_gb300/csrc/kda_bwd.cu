@@ -648,13 +648,15 @@ cudaError_t dh_dispatch(const BwdLaunch &b, int V, cudaStream_t st) {
 }
 
 template <typename Tin, int K, int V>
-cudaError_t bwd_dispatch(const BwdLaunch &b, cudaStream_t st) {
+cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, cudaStream_t st) {
   const SeqInfo &s = b.s;
   const int H = b.H, Hk = b.Hk;
   const Tin *dO = static_cast<const Tin *>(b.d_out);
-  // B1: reverse chain of the state gradient
-  cudaError_t e0 = dh_dispatch<Tin, K>(b, V, st);
-  if (e0 != cudaSuccess) return e0;
+  // B1: reverse chain of the state gradient (unless the caller ran it)
+  if (with_dh) {
+    cudaError_t e0 = dh_dispatch<Tin, K>(b, V, st);
+    if (e0 != cudaSuccess) return e0;
+  }
   if (b.nchunks == 0) return cudaSuccess;
   // B2: state-contraction terms
   {
@@ -703,9 +705,10 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st) {
+cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st,
+                               bool with_dh) {
 #define KDA_BWD(T_, K_, V_) \
-  if (K == K_ && V == V_) return bwd_dispatch<T_, K_, V_>(b, st);
+  if (K == K_ && V == V_) return bwd_dispatch<T_, K_, V_>(b, with_dh, st);
   if (dt == KDA_F32) {
     KDA_BWD(float, 64, 64) KDA_BWD(float, 64, 128) KDA_BWD(float, 128, 64) KDA_BWD(float, 128, 128)
   } else {

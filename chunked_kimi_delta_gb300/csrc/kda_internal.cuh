@@ -186,7 +186,9 @@ struct BwdLaunch {
   void *dq, *dk, *dv;
   float *dg, *dbeta, *d_initial;
 };
-cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
+// with_dh = false: dhn, dvn and d_initial come from the tensor-core reverse chain.
+cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st,
+                               bool with_dh = true);
 // The reverse state-gradient chain alone (dhn / dvn may be null: not written).
 cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
 cudaError_t launch_bwd_param_reduce(int64_t nchunks, int H, int K, const float *part_alog,

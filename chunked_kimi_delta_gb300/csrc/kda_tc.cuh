@@ -163,7 +163,7 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
 
 struct ChainArgs {
   const char *pkg;
-  void *out;                    // bf16 [T_tot, H, V]
+  void *out;                    // bf16 [T_tot, H, V] or null (not written)
   const float *initial_state;   // [N, H, K, V] or null
   float *final_state;           // [N, H, K, V] or null
   float *h_out;                 // [nchunks, H, K, V] or null
@@ -172,6 +172,23 @@ struct ChainArgs {
 };
 
 cudaError_t launch_tc_chain(const ChainArgs &a, const SeqInfo &s, int H, cudaStream_t st);
+
+// Reverse chain of the state gradient (kda_tc_bwd.cu), from the packages of
+// the forward: dh' of every chunk, dv_new and the initial-state gradient.
+struct BwdChainArgs {
+  const char *pkg;
+  const void *d_out;            // bf16 [T_tot, H, V] or null (zeros)
+  const float *d_final;         // [N, H, K, V] or null (zeros)
+  float *dhn;                   // [nchunks, H, K, V]: gradient of the state leaving each chunk, or null
+  float *dvn;                   // [T_tot, H, V] fp32 or null
+  float *d_initial;             // [N, H, K, V] or null
+  uint32_t *err;
+};
+cudaError_t launch_tc_bwd_dh(const BwdChainArgs &a, const SeqInfo &s, int H, int64_t T_tot,
+                             cudaStream_t st);
+
+// TMA map of a bf16 [T_tot, H, 128] tensor in the forward's v-tile layout.
+bool make_value_map(const void *x, int64_t T_tot, int H, CUtensorMap &map);
 
 // Segment summary (kda_tc_summary.cu): M and S~ of every (segment, head)
 // from the packages of its chunks.

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
       __syncwarp();
       tc::tmem_ld16(tPp + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
       tc::tmem_ld_wait();
-      if (r < lenp) {
+      if (a.out && r < lenp) {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
                                                ((tcp + r) * H + h) * V + 64 * hf + 16 * cc);
         dst[0] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),

@@ -53,5 +53,11 @@ bool make_input_maps(const void *q, const void *k, const void *v, const float *x
                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool make_value_map(const void *x, int64_t T_tot, int H, CUtensorMap &map) {
+  if (T_tot <= 0) return false;
+  return encode3(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, V, H, T_tot, 64,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace tcp
 }  // namespace kda
