@@ -28,6 +28,7 @@ KDA_REUSE_PREP = 1 << 4
 KDA_SAFE_GATE = 1 << 8
 KDA_ALLOW_NEG_EIGVAL = 1 << 9
 KDA_STATE_V_FIRST = 1 << 10
+KDA_LAYOUT_HEAD_MAJOR = 1 << 11
 CHUNK = 64
 
 
@@ -171,51 +172,71 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
-def _check_shapes(q, k, v, g, beta, out):
-    """q, k [.., Hk, dk]; v, out [.., H, dv]; g [.., H, dk]; beta [.., H]
-    with the same leading dims, Hk dividing H (the kernels trust these)."""
-    lead, H = tuple(v.shape[:-2]), v.shape[-2]
-    if k.shape != q.shape or tuple(q.shape[:-2]) != lead:
-        raise ValueError("q and k must be [.., Hk, dk] with v's leading dims")
-    if q.shape[-2] < 1 or H % q.shape[-2] != 0:
+def _heads(x, head_major=False):
+    """Head count of a [.., heads, D] (token-major) or [.., heads, T, D]
+    (head-major) tensor."""
+    return x.shape[-3] if head_major else x.shape[-2]
+
+
+def _check_shapes(q, k, v, g, beta, out, head_major=False):
+    """Token-major: q, k [.., Hk, dk]; v, out [.., H, dv]; g [.., H, dk];
+    beta [.., H].  Head-major: q, k [.., Hk, T, dk]; v, out [.., H, T, dv];
+    g [.., H, T, dk]; beta [.., H, T].  Same leading dims, Hk dividing H
+    (the kernels trust these)."""
+    if head_major:
+        lead, H, T = tuple(v.shape[:-3]), v.shape[-3], v.shape[-2]
+        qlead, Hk = tuple(q.shape[:-3]) + (q.shape[-2],), q.shape[-3]
+        lead_t = lead + (T,)
+        g_shape, b_shape = lead + (H, T, q.shape[-1]), lead + (H, T)
+    else:
+        lead, H = tuple(v.shape[:-2]), v.shape[-2]
+        qlead, Hk, lead_t = tuple(q.shape[:-2]), q.shape[-2], lead
+        g_shape, b_shape = lead + (H, q.shape[-1]), lead + (H,)
+    if k.shape != q.shape or qlead != lead_t:
+        raise ValueError("q and k must have v's leading dims and token count")
+    if Hk < 1 or H % Hk != 0:
         raise ValueError("the key heads of q/k must divide the value heads of v")
-    if tuple(g.shape) != lead + (H, q.shape[-1]):
-        raise ValueError("g must be [.., H, dk]")
-    if tuple(beta.shape) != lead + (H,):
-        raise ValueError("beta must be [.., H]")
+    if tuple(g.shape) != g_shape:
+        raise ValueError("g must have v's layout with dk channels")
+    if tuple(beta.shape) != b_shape:
+        raise ValueError("beta must be v's layout without the channel axis")
     if out is not None and out.shape != v.shape:
         raise ValueError("out must have v's shape")
 
 
-def _state_shape(N, q, v, v_first=False):
+def _state_shape(N, q, v, v_first=False, head_major=False):
     """Shape of N recurrent states: [N, H, dk, dv], or [N, H, dv, dk] V-first."""
-    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    H, K, V = _heads(v, head_major), q.shape[-1], v.shape[-1]
     return (N, H, V, K) if v_first else (N, H, K, V)
 
 
 def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias=None,
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
-                  gate_in_kernel=False, use_exp2=False, state_v_first=False, extra_flags=0,
-                  out=None, final_state=None, h_out=None, v_new_out=None) -> kda_fwd_args:
+                  gate_in_kernel=False, use_exp2=False, state_v_first=False, head_major=False,
+                  extra_flags=0, out=None, final_state=None, h_out=None,
+                  v_new_out=None) -> kda_fwd_args:
     """Fills a ``kda_fwd_args`` from tensors (BSND [B,T,H,D], or TND [T,H,D]
     with ``cu_seqlens``).  q and k may carry fewer heads than v (grouped key
     heads, Hk dividing H): value head h reads key head h // (H // Hk)."""
     _contig(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state,
             h_out, v_new_out)
     a = kda_fwd_args()
-    if q.dim() == 3:    # TND: one token axis
-        a.B, a.T = 1, q.shape[0]
-    elif q.dim() == 4:  # BSND
-        a.B, a.T = q.shape[0], q.shape[1]
+    tax = 1 if head_major else 0  # token axis of a 3-D tensor
+    if q.dim() == 3:    # TND [T, H, D] / NTD [H, T, D]: one token axis
+        a.B, a.T = 1, q.shape[tax]
+    elif q.dim() == 4:  # BSND [B, T, H, D] / BNSD [B, H, T, D]
+        a.B, a.T = q.shape[0], q.shape[1 + tax]
     else:
-        raise ValueError("q/k/v are [B, T, H, D] or [T_total, H, D]")
+        raise ValueError("q/k/v are [B, T, H, D] or [T_total, H, D] (head-major: [B, H, T, D], "
+                         "[H, T_total, D])")
     if cu_seqlens is not None:
         if q.dim() != 3:
-            raise ValueError("with cu_seqlens, q/k/v are [T_total, H, D]")
+            raise ValueError("with cu_seqlens, q/k/v have one token axis")
         a.num_seqs = cu_seqlens.numel() - 1
         a.cu_seqlens = _ptr(cu_seqlens)
-    _check_shapes(q, k, v, g, beta, out)
-    a.H, a.Hk, a.dk, a.dv, a.chunk = v.shape[-2], q.shape[-2], q.shape[-1], v.shape[-1], CHUNK
+    _check_shapes(q, k, v, g, beta, out, head_major)
+    a.H, a.Hk = _heads(v, head_major), _heads(q, head_major)
+    a.dk, a.dv, a.chunk = q.shape[-1], v.shape[-1], CHUNK
     a.qkv_dtype = _dtype_code(q)
     a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
     a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
@@ -224,7 +245,8 @@ def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
     a.initial_state = _ptr(initial_state)
     a.flags = ((KDA_L2NORM_QK if l2norm_qk else 0) | (KDA_BETA_SIGMOID if beta_sigmoid else 0)
                | (KDA_GATE_IN_KERNEL if gate_in_kernel else 0) | (KDA_USE_EXP2 if use_exp2 else 0)
-               | (KDA_STATE_V_FIRST if state_v_first else 0) | extra_flags)
+               | (KDA_STATE_V_FIRST if state_v_first else 0)
+               | (KDA_LAYOUT_HEAD_MAJOR if head_major else 0) | extra_flags)
     a.out, a.final_state = _ptr(out), _ptr(final_state)
     a.h_out, a.v_new_out = _ptr(h_out), _ptr(v_new_out)
     return a
@@ -243,7 +265,7 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
                   gate_in_kernel=False, use_exp2=False, output_final_state=True, out=None,
                   final_state=None, h_out=None, v_new_out=None, workspace=None, stream=None,
-                  reuse_prep=False, state_v_first=False, extra_flags=0):
+                  reuse_prep=False, state_v_first=False, head_major=False, extra_flags=0):
     """Chunked KDA forward.  Returns ``(out, final_state)`` (final_state is
     None unless requested).  ``reuse_prep`` (with ``workspace``) sets
     KDA_REUSE_PREP: the workspace already holds this problem's intra-chunk
@@ -262,12 +284,12 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
     if out is None:
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     if output_final_state and final_state is None:
-        final_state = torch.empty(_state_shape(N, q, v, state_v_first), dtype=torch.float32,
-                                  device=q.device)
+        final_state = torch.empty(_state_shape(N, q, v, state_v_first, head_major),
+                                  dtype=torch.float32, device=q.device)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
                       beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
-                      state_v_first=state_v_first, extra_flags=extra_flags, out=out, final_state=final_state, h_out=h_out,
+                      state_v_first=state_v_first, head_major=head_major, extra_flags=extra_flags, out=out, final_state=final_state, h_out=h_out,
                       v_new_out=v_new_out)
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
@@ -363,7 +385,8 @@ def prepare_chunk_fwd(q, k, v, g, beta, *, output_final_state=True, workspace=No
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     fin = kw.pop("final_state", None)
     if output_final_state and fin is None:
-        fin = torch.empty(_state_shape(N, q, v, kw.get("state_v_first", False)),
+        fin = torch.empty(_state_shape(N, q, v, kw.get("state_v_first", False),
+                                       kw.get("head_major", False)),
                           dtype=torch.float32, device=q.device)
     a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
@@ -378,7 +401,7 @@ def prepare_segment_summary(q, k, v, g, beta, seg_bounds, *, M=None, S_tilde=Non
     torch = _torch()
     lib = load_library()
     S = seg_bounds.numel() - 1
-    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    H, K, V = _heads(v, kw.get("head_major", False)), q.shape[-1], v.shape[-1]
     if M is None:
         M = torch.empty(S, H, K, K, dtype=torch.float32, device=q.device)
     if S_tilde is None:
@@ -408,24 +431,27 @@ def kda_chunk_fwd_profiled(args: kda_fwd_args, events, stream=None):
 
 def kda_segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_log=None,
                         dt_bias=None, l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
-                        use_exp2=False, M=None, S_tilde=None, workspace=None, stream=None):
+                        use_exp2=False, head_major=False, M=None, S_tilde=None, workspace=None,
+                        stream=None):
     """(see below; pass ``workspace`` to keep the prepared chunks for a
     following kda_chunk_fwd with ``reuse_prep=True``)"""
     return _segment_summary(q, k, v, g, beta, seg_bounds, scale=scale, eps=eps, a_log=a_log,
                             dt_bias=dt_bias, l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid,
-                            gate_in_kernel=gate_in_kernel, use_exp2=use_exp2, M=M,
-                            S_tilde=S_tilde, workspace=workspace, stream=stream)
+                            gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
+                            head_major=head_major, M=M, S_tilde=S_tilde, workspace=workspace,
+                            stream=stream)
 
 
 def _segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_log=None,
                      dt_bias=None, l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
-                     use_exp2=False, M=None, S_tilde=None, workspace=None, stream=None):
+                     use_exp2=False, head_major=False, M=None, S_tilde=None, workspace=None,
+                     stream=None):
     """Segment affine summary.  ``seg_bounds``: int32 device tensor [S+1] of
     token offsets on the flattened token axis.  Returns ``(M, S_tilde)``."""
     torch = _torch()
     lib = load_library()
     S = seg_bounds.numel() - 1
-    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    H, K, V = _heads(v, head_major), q.shape[-1], v.shape[-1]
     if M is None:
         M = torch.empty(S, H, K, K, dtype=torch.float32, device=q.device)
     if S_tilde is None:
@@ -433,7 +459,7 @@ def _segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_lo
     _contig(seg_bounds, M, S_tilde)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid,
-                      gate_in_kernel=gate_in_kernel, use_exp2=use_exp2)
+                      gate_in_kernel=gate_in_kernel, use_exp2=use_exp2, head_major=head_major)
     ws = _workspace(lib.kda_segment_summary_workspace_size(ctypes.byref(a), S), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     _check(lib.kda_segment_summary(ctypes.byref(a), seg_bounds.data_ptr(), S, M.data_ptr(),
@@ -558,14 +584,15 @@ def prepare_chunk_bwd(q, k, v, g, beta, d_out, *, d_final_state=None, initial_st
     lib = load_library()
     cu = kw.get("cu_seqlens")
     N = (cu.numel() - 1) if cu is not None else (1 if q.dim() == 3 else q.shape[0])
-    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    hm = kw.get("head_major", False)
+    H, K, V = _heads(v, hm), q.shape[-1], v.shape[-1]
     dev = q.device
     if d_out is not None:
         if d_out.shape != v.shape or d_out.dtype != q.dtype:
             raise ValueError("d_out must have v's shape and q's dtype")
         _contig(d_out)
     if d_final_state is not None:
-        if (tuple(d_final_state.shape) != _state_shape(N, q, v, kw.get("state_v_first", False))
+        if (tuple(d_final_state.shape) != _state_shape(N, q, v, kw.get("state_v_first", False), hm)
                 or d_final_state.dtype != torch.float32):
             raise ValueError("d_final_state must be fp32 [N, H, dk, dv] ([N, H, dv, dk] V-first)")
         _contig(d_final_state)
@@ -578,7 +605,7 @@ def prepare_chunk_bwd(q, k, v, g, beta, d_out, *, d_final_state=None, initial_st
         dbeta=torch.empty(beta.shape, dtype=torch.float32, device=dev),
         da_log=torch.empty(H, dtype=torch.float32, device=dev) if gate else None,
         ddt_bias=torch.empty(H, K, dtype=torch.float32, device=dev) if gate else None,
-        d_initial_state=(torch.empty(_state_shape(N, q, v, kw.get("state_v_first", False)),
+        d_initial_state=(torch.empty(_state_shape(N, q, v, kw.get("state_v_first", False), hm),
                                      dtype=torch.float32, device=dev)
                          if want_d_initial_state else None),
     )
@@ -619,7 +646,7 @@ def kda_segment_bwd_summary(q, k, v, g, beta, d_out, seg_bounds, *, E=None, work
     torch = _torch()
     lib = load_library()
     S = seg_bounds.numel() - 1
-    H, K, V = v.shape[-2], q.shape[-1], v.shape[-1]
+    H, K, V = _heads(v, kw.get("head_major", False)), q.shape[-1], v.shape[-1]
     if E is None:
         E = torch.empty(S, H, K, V, dtype=torch.float32, device=q.device)
     if d_out is not None and (d_out.shape != v.shape or d_out.dtype != q.dtype):

@@ -21,10 +21,12 @@ inline bool mis16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) &
 
 constexpr uint32_t kKnownFlags = KDA_L2NORM_QK | KDA_BETA_SIGMOID | KDA_GATE_IN_KERNEL |
                                  KDA_USE_EXP2 | KDA_REUSE_PREP | KDA_SAFE_GATE |
-                                 KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST;
+                                 KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST |
+                                 KDA_LAYOUT_HEAD_MAJOR;
 constexpr uint32_t kRejectedFlags = KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL;
 
 inline bool v_first(const kda_fwd_args *a) { return (a->flags & KDA_STATE_V_FIRST) != 0; }
+inline bool head_major(const kda_fwd_args *a) { return (a->flags & KDA_LAYOUT_HEAD_MAJOR) != 0; }
 
 // Checks shared by the forward and the summary (everything but the outputs).
 kda_status check_common(const kda_fwd_args *a) {
@@ -113,8 +115,58 @@ VfPlan vf_plan(const kda_fwd_args *a, const FwdPlan &p, size_t base) {
   return v;
 }
 
+// Token-major copies of a head-major call's per-token tensors, after the
+// rest of the workspace.  The inputs always; out / v_new_out / d_out when
+// the call has them (with_out: out is written by the call).
+struct HmPlan {
+  size_t off_q, off_k, off_v, off_g, off_b, off_o, off_vn, total;
+};
+HmPlan hm_plan(const kda_fwd_args *a, bool with_out, size_t base) {
+  HmPlan m{};
+  const size_t tok = (size_t)a->B * a->T, esz = a->qkv_dtype == KDA_BF16 ? 2 : 4;
+  const size_t Hk = a->Hk > 0 ? a->Hk : a->H;
+  size_t o = base;
+  m.off_q = o; o = align256(o + tok * Hk * a->dk * esz);
+  m.off_k = o; o = align256(o + tok * Hk * a->dk * esz);
+  m.off_v = o; o = align256(o + tok * a->H * a->dv * esz);
+  m.off_g = o; o = align256(o + tok * a->H * a->dk * 4);
+  m.off_b = o; o = align256(o + tok * a->H * 4);
+  m.off_o = m.off_vn = 0;
+  if (with_out) { m.off_o = o; o = align256(o + tok * a->H * a->dv * esz); }
+  if (with_out && a->v_new_out) { m.off_vn = o; o = align256(o + tok * a->H * a->dv * 4); }
+  m.total = o;
+  return m;
+}
+
+// (batch, tokens per batch row) of the swap between the layouts.
+inline void hm_dims(const kda_fwd_args *a, int64_t &B, int64_t &T) {
+  B = a->cu_seqlens ? 1 : a->B;
+  T = a->cu_seqlens ? (int64_t)a->B * a->T : a->T;
+}
+
+// Head-major inputs -> token-major copies in the workspace ws; b points at them.
+cudaError_t hm_inputs_in(const kda_fwd_args *a, char *ws, const HmPlan &m, kda_fwd_args *b,
+                         cudaStream_t st) {
+  int64_t B, T;
+  hm_dims(a, B, T);
+  const int esz = a->qkv_dtype == KDA_BF16 ? 2 : 4, Hk = a->Hk > 0 ? a->Hk : a->H;
+  b->flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
+  b->q = ws + m.off_q;
+  b->k = ws + m.off_k;
+  b->v = ws + m.off_v;
+  b->g = reinterpret_cast<float *>(ws + m.off_g);
+  b->beta = reinterpret_cast<float *>(ws + m.off_b);
+  cudaError_t e = launch_swap_token_head(a->q, ws + m.off_q, B, Hk, T, a->dk * esz, true, st);
+  if (e == cudaSuccess) e = launch_swap_token_head(a->k, ws + m.off_k, B, Hk, T, a->dk * esz, true, st);
+  if (e == cudaSuccess) e = launch_swap_token_head(a->v, ws + m.off_v, B, a->H, T, a->dv * esz, true, st);
+  if (e == cudaSuccess) e = launch_swap_token_head(a->g, ws + m.off_g, B, a->H, T, a->dk * 4, true, st);
+  if (e == cudaSuccess) e = launch_swap_token_head(a->beta, ws + m.off_b, B, a->H, T, 4, true, st);
+  return e;
+}
+
 size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p) {
-  return vf_plan(a, p, use_tc(a) ? tc_plan(p).total : p.total).total;
+  const size_t base = vf_plan(a, p, use_tc(a) ? tc_plan(p).total : p.total).total;
+  return head_major(a) ? hm_plan(a, true, base).total : base;
 }
 
 kda_status check_workspace(const kda_fwd_args *a, const FwdPlan &p) {
@@ -176,6 +228,29 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
                           int32_t nev, bool keep_err = false) {
   kda_status s = check_fwd(a);
   if (s != KDA_OK) return s;
+  if (head_major(a) && (int64_t)a->B * a->T > 0) {
+    // head-major tensors: token-major copies around the token-major forward
+    const FwdPlan p = fwd_plan(a);
+    if ((s = check_workspace(a, p)) != KDA_OK) return s;
+    kda_fwd_args b = *a;
+    b.flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
+    const size_t base = plan_bytes(&b, p);
+    const HmPlan m = hm_plan(a, true, base);
+    char *ws = static_cast<char *>(a->workspace);
+    cudaError_t e = hm_inputs_in(a, ws, m, &b, st);
+    b.out = ws + m.off_o;
+    b.v_new_out = a->v_new_out ? reinterpret_cast<float *>(ws + m.off_vn) : nullptr;
+    b.workspace_bytes = base;
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if ((s = run_fwd(&b, st, ev, nev, keep_err)) != KDA_OK) return s;
+    int64_t B, T;
+    hm_dims(a, B, T);
+    const int esz = a->qkv_dtype == KDA_BF16 ? 2 : 4;
+    e = launch_swap_token_head(b.out, a->out, B, a->H, T, a->dv * esz, false, st);
+    if (e == cudaSuccess && a->v_new_out)
+      e = launch_swap_token_head(b.v_new_out, a->v_new_out, B, a->H, T, a->dv * 4, false, st);
+    return cuda_status(e);
+  }
   if (!v_first(a)) return run_fwd_kfirst(a, st, ev, nev, keep_err);
   const FwdPlan p = fwd_plan(a);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
@@ -331,7 +406,7 @@ struct HostPlan {
 kda_status check_host(const kda_fwd_args *a) {
   kda_status s = check_fwd(a);
   if (s != KDA_OK) return s;
-  if (a->cu_seqlens || a->h_out || a->v_new_out || (a->flags & KDA_REUSE_PREP))
+  if (a->cu_seqlens || a->h_out || a->v_new_out || (a->flags & (KDA_REUSE_PREP | KDA_LAYOUT_HEAD_MAJOR)))
     return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
@@ -489,6 +564,18 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
   if (v_first(a)) return KDA_ERR_UNSUPPORTED;  // summaries are K-first
   if (num_segments < 1 || !seg_bounds || !M || !S_tilde) return KDA_ERR_INVALID_ARG;
   if (mis16(seg_bounds) || mis16(M) || mis16(S_tilde)) return KDA_ERR_ALIGNMENT;
+  if (head_major(a) && (int64_t)a->B * a->T > 0) {  // token-major copies of the inputs
+    kda_fwd_args b = *a;
+    b.flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
+    const size_t base = plan_bytes(&b, summary_plan(&b, num_segments));
+    const HmPlan m = hm_plan(a, false, base);
+    if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    if (hm_inputs_in(a, static_cast<char *>(a->workspace), m, &b, st0) != cudaSuccess) return KDA_ERR_CUDA;
+    b.workspace_bytes = base;
+    return kda_segment_summary(&b, seg_bounds, num_segments, M, S_tilde, stream);
+  }
   const FwdPlan p = summary_plan(a, num_segments);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -580,7 +667,8 @@ kda_status kda_recurrent_step(const kda_decode_args *a, kda_stream_t stream) {
   if (!a || a->N < 0 || a->T < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
   if (a->Hk < 0 || (a->Hk > 0 && a->H % a->Hk != 0)) return KDA_ERR_INVALID_ARG;
   if (a->flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
-  if (a->flags & (kRejectedFlags | KDA_REUSE_PREP)) return KDA_ERR_UNSUPPORTED;  // V-first is taken
+  if (a->flags & (kRejectedFlags | KDA_REUSE_PREP | KDA_LAYOUT_HEAD_MAJOR))
+    return KDA_ERR_UNSUPPORTED;  // V-first is taken
   if ((a->dk != 64 && a->dk != 128) || (a->dv != 64 && a->dv != 128)) return KDA_ERR_UNSUPPORTED;
   if (a->qkv_dtype != KDA_F32 && a->qkv_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (a->cache_dtype != KDA_F32 && a->cache_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
@@ -673,15 +761,69 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
 
 extern "C" {
 
+// Head-major backward: token-major copies of the inputs and d_out (the
+// forward's out region), then of the gradients dq, dk, dv, dg, dbeta.
+struct HmBwd {
+  HmPlan in;
+  size_t off_dq, off_dk, off_dv, off_dg, off_db, total;
+};
+HmBwd hm_bwd_plan(const kda_bwd_args *b, size_t base) {
+  HmBwd h{};
+  const kda_fwd_args *a = &b->fwd;
+  h.in = hm_plan(a, true, base);
+  const size_t tok = (size_t)a->B * a->T, esz = a->qkv_dtype == KDA_BF16 ? 2 : 4;
+  const size_t Hk = a->Hk > 0 ? a->Hk : a->H;
+  size_t o = h.in.total;
+  h.off_dq = o; o = align256(o + tok * Hk * a->dk * esz);
+  h.off_dk = o; o = align256(o + tok * Hk * a->dk * esz);
+  h.off_dv = o; o = align256(o + tok * a->H * a->dv * esz);
+  h.off_dg = o; o = align256(o + tok * a->H * a->dk * 4);
+  h.off_db = o; o = align256(o + tok * a->H * 4);
+  h.total = o;
+  return h;
+}
+
 size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *b) {
   if (check_bwd(b) != KDA_OK) return 0;
-  return bwd_plan(b).total;
+  const size_t base = bwd_plan(b).total;
+  return head_major(&b->fwd) ? hm_bwd_plan(b, base).total : base;
 }
 
 kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   kda_status s = check_bwd(b);
   if (s != KDA_OK) return s;
   const kda_fwd_args *a = &b->fwd;
+  if (head_major(a) && (int64_t)a->B * a->T > 0) {
+    const size_t base = bwd_plan(b).total;
+    const HmBwd m = hm_bwd_plan(b, base);
+    if (!b->workspace || b->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(b->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(b->workspace);
+    int64_t B, T;
+    hm_dims(a, B, T);
+    const int esz = a->qkv_dtype == KDA_BF16 ? 2 : 4, Hk = a->Hk > 0 ? a->Hk : a->H;
+    kda_bwd_args c = *b;
+    cudaError_t e = hm_inputs_in(a, ws, m.in, &c.fwd, st0);
+    if (e == cudaSuccess && b->d_out) {
+      e = launch_swap_token_head(b->d_out, ws + m.in.off_o, B, a->H, T, a->dv * esz, true, st0);
+      c.d_out = ws + m.in.off_o;
+    }
+    c.dq = ws + m.off_dq;
+    c.dk = ws + m.off_dk;
+    c.dv = ws + m.off_dv;
+    c.dg = reinterpret_cast<float *>(ws + m.off_dg);
+    c.dbeta = reinterpret_cast<float *>(ws + m.off_db);
+    c.workspace_bytes = base;
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if ((s = kda_chunk_bwd(&c, stream)) != KDA_OK) return s;
+    e = launch_swap_token_head(c.dq, b->dq, B, Hk, T, a->dk * esz, false, st0);
+    if (e == cudaSuccess) e = launch_swap_token_head(c.dk, b->dk, B, Hk, T, a->dk * esz, false, st0);
+    if (e == cudaSuccess) e = launch_swap_token_head(c.dv, b->dv, B, a->H, T, a->dv * esz, false, st0);
+    if (e == cudaSuccess) e = launch_swap_token_head(c.dg, b->dg, B, a->H, T, a->dk * 4, false, st0);
+    if (e == cudaSuccess) e = launch_swap_token_head(c.dbeta, b->dbeta, B, a->H, T, 4, false, st0);
+    return cuda_status(e);
+  }
   const BwdPlan p = bwd_plan(b);
   if (!b->workspace || b->workspace_bytes < p.total) return KDA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(b->workspace) & 255u) return KDA_ERR_ALIGNMENT;
@@ -795,7 +937,9 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
 
 size_t kda_segment_bwd_summary_workspace_size(const kda_fwd_args *a, int32_t num_segments) {
   if (check_common(a) != KDA_OK || num_segments < 1) return 0;
-  return summary_plan(a, num_segments).total;  // the generic per-chunk intermediates
+  const FwdPlan p = summary_plan(a, num_segments);  // packages or generic intermediates
+  const size_t base = use_tc(a) ? tc_plan(p).total : p.total;
+  return head_major(a) ? hm_plan(a, true, base).total : base;  // + token-major inputs and d_out
 }
 
 kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
@@ -806,20 +950,62 @@ kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
   if (a->flags & (KDA_REUSE_PREP | KDA_STATE_V_FIRST)) return KDA_ERR_UNSUPPORTED;
   if (num_segments < 1 || !seg_bounds || !E) return KDA_ERR_INVALID_ARG;
   if (mis16(seg_bounds) || mis16(E) || mis16(d_out)) return KDA_ERR_ALIGNMENT;
+  if (head_major(a) && (int64_t)a->B * a->T > 0) {  // token-major copies of the inputs, d_out
+    kda_fwd_args b = *a;
+    b.flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
+    const FwdPlan pb = summary_plan(&b, num_segments);
+    const size_t base = use_tc(&b) ? tc_plan(pb).total : pb.total;
+    const HmPlan m = hm_plan(a, true, base);
+    if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(a->workspace);
+    cudaError_t e = hm_inputs_in(a, ws, m, &b, st0);
+    const void *dO = nullptr;
+    if (e == cudaSuccess && d_out) {
+      int64_t B, T;
+      hm_dims(a, B, T);
+      e = launch_swap_token_head(d_out, ws + m.off_o, B, a->H, T,
+                                 a->dv * (a->qkv_dtype == KDA_BF16 ? 2 : 4), true, st0);
+      dO = ws + m.off_o;
+    }
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    b.workspace_bytes = base;
+    return kda_segment_bwd_summary(&b, dO, seg_bounds, num_segments, E, stream);
+  }
   const FwdPlan p = summary_plan(a, num_segments);
-  if (!a->workspace || a->workspace_bytes < p.total) return KDA_ERR_WORKSPACE;
+  const bool tc = use_tc(a);
+  if (!a->workspace || a->workspace_bytes < (tc ? tc_plan(p).total : p.total)) return KDA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(a->workspace);
   auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
   SeqInfo si{};
   si.bounds = seg_bounds;
-  si.chunk_off = reinterpret_cast<int32_t *>(ws + p.off_chunk_off);
+  si.chunk_off = reinterpret_cast<int32_t *>(ws + (tc ? tc_plan(p).off_chunk_off : p.off_chunk_off));
   si.T_tot = p.T_tot;
   si.T = a->T;
   si.N = num_segments;
+  tcp::TcMaps maps;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps)) return KDA_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
   if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
+  if (tc) {  // the packages, then the reverse chain on the tensor cores
+    char *pkg = ws + tc_plan(p).off_pkg;
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws);
+    if (e == cudaSuccess)
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, p.Hk,
+                              pkg, err, st);
+    if (e == cudaSuccess) {
+      tcp::BwdChainArgs ba{};
+      ba.pkg = pkg;
+      ba.d_out = d_out;
+      ba.d_initial = E;  // d_final = 0, dhn / dvn not kept
+      ba.err = err;
+      e = tcp::launch_tc_bwd_dh(ba, si, a->H, p.T_tot, st);
+    }
+    return cuda_status(e);
+  }
   if (e == cudaSuccess && p.T_tot > 0)
     e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws,
                              st);

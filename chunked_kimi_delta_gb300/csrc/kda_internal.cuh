@@ -144,6 +144,9 @@ cudaError_t launch_chunk_map(const SeqInfo &s, int32_t *chunk_off, cudaStream_t 
 // first (*count_ptr) * per_count matrices.
 cudaError_t launch_transpose_states(const float *src, float *dst, int64_t n, int R, int C,
                                     const int32_t *count_ptr, int per_count, cudaStream_t st);
+// [B, H, T, row] <-> [B, T, H, row] (row_bytes a multiple of 4).
+cudaError_t launch_swap_token_head(const void *src, void *dst, int64_t B, int H, int64_t T,
+                                   int row_bytes, bool to_token_major, cudaStream_t st);
 
 // Recurrent decode step on pool rows (kda_decode.cu).
 cudaError_t launch_decode(kda_dtype qkv_dtype, kda_dtype cache_dtype, kda_index_dtype idx_dtype,

@@ -5,6 +5,12 @@
 // their last two dimensions as [V, K]; the library works K-first ([K, V])
 // internally and converts at the boundary.  A state is a dense fp32 matrix,
 // states follow one another.
+//
+// Section 4.2 of the same design lists the token layouts BSND [B, T, H, D],
+// TND [T, H, D] and the head-major BNSD [B, H, T, D], NTD [H, T, D].  The
+// kernels work token-major; head-major tensors are converted at the
+// boundary by swapping the token and head axes, row by row (a row is the D
+// elements of one (token, head)).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -36,7 +42,54 @@ transpose_kernel(const float *__restrict__ src, float *__restrict__ dst, int R, 
   }
 }
 
+// One unit = U bytes (16 when a row's bytes are a multiple of 16, else the
+// element size); thread = unit of the destination.
+template <typename Unit>
+__global__ void __launch_bounds__(256)
+swap_token_head_kernel(const Unit *__restrict__ src, Unit *__restrict__ dst, int64_t B, int H,
+                       int64_t T, int units_per_row, bool to_token_major, int64_t total) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int u = (int)(i % units_per_row);
+  const int64_t row = i / units_per_row;  // destination row
+  int64_t b, t;
+  int h;
+  if (to_token_major) {  // destination [B][T][H]
+    h = (int)(row % H);
+    const int64_t bt = row / H;
+    t = bt % T;
+    b = bt / T;
+    dst[i] = src[(((b * H + h) * T) + t) * units_per_row + u];
+  } else {  // destination [B][H][T]
+    t = row % T;
+    const int64_t bh = row / T;
+    h = (int)(bh % H);
+    b = bh / H;
+    dst[i] = src[(((b * T + t) * H) + h) * units_per_row + u];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_token_head(const void *src, void *dst, int64_t B, int H, int64_t T,
+                                   int row_bytes, bool to_token_major, cudaStream_t st) {
+  const int64_t rows = B * H * T;
+  if (rows == 0) return cudaSuccess;
+  if (row_bytes % 16 == 0) {
+    const int upr = row_bytes / 16;
+    const int64_t total = rows * upr;
+    swap_token_head_kernel<uint4><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
+        static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), B, H, T, upr, to_token_major, total);
+  } else {
+    if (row_bytes % 4 != 0) return cudaErrorInvalidValue;
+    const int upr = row_bytes / 4;
+    const int64_t total = rows * upr;
+    swap_token_head_kernel<uint32_t><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
+        static_cast<const uint32_t *>(src), static_cast<uint32_t *>(dst), B, H, T, upr, to_token_major,
+        total);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose_states(const float *src, float *dst, int64_t n, int R, int C,
                                     const int32_t *count_ptr, int per_count, cudaStream_t st) {

@@ -81,7 +81,16 @@ enum {
    * boundary (through workspace copies, included in the workspace sizes).
    * kda_segment_summary and kda_segment_bwd_summary return K-first summaries
    * and reject the flag with KDA_ERR_UNSUPPORTED. */
-  KDA_STATE_V_FIRST = 1u << 10
+  KDA_STATE_V_FIRST = 1u << 10,
+  /* Head-major token layouts (same design, section 4.2): BNSD [B, H, T, D]
+   * instead of BSND [B, T, H, D] without cu_seqlens, NTD [H, T_total, D]
+   * instead of TND [T_total, H, D] with it.  Applies to q, k (Hk heads), v,
+   * g, beta ([B, H, T] / [H, T_total]), out and v_new_out of the forward and
+   * summaries, and to d_out, dq, dk, dv, dg, dbeta of the backward.  The
+   * kernels work token-major; the library converts at the boundary through
+   * workspace copies (included in the workspace sizes).  Rejected with
+   * KDA_ERR_UNSUPPORTED by kda_chunk_fwd_host and kda_recurrent_step. */
+  KDA_LAYOUT_HEAD_MAJOR = 1u << 11
 };
 
 /*

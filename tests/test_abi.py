@@ -271,3 +271,34 @@ def test_v_first_workspace_and_rejections(lib):
     a = _args(flags=vf)
     assert lib.kda_segment_summary(ctypes.byref(a), 1 << 20, 2, 1 << 21, 1 << 22, None) == 2
     assert lib.kda_segment_bwd_summary(ctypes.byref(a), None, 1 << 20, 2, 1 << 22, None) == 2
+
+
+def test_head_major_layout_checks(lib):
+    hmf = kda.KDA_LAYOUT_HEAD_MAJOR
+    size = lambda **kw: lib.kda_chunk_fwd_workspace_size(ctypes.byref(_args(**kw)))
+    assert size(flags=hmf) > size()                      # token-major copies of every tensor
+    assert lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(_args(flags=hmf))) == 0
+    assert lib.kda_chunk_fwd_host(ctypes.byref(_args(flags=hmf)), None) == 2
+    d = kda.kda_decode_args()
+    d.N, d.T, d.H, d.dk, d.dv = 0, 1, 2, 128, 128
+    d.qkv_dtype, d.cache_dtype, d.idx_dtype = kda.KDA_BF16, kda.KDA_F32, kda.KDA_I32
+    d.num_rows, d.row_stride_elems, d.flags = 8, 2 * 128 * 128, hmf
+    assert lib.kda_recurrent_step(ctypes.byref(d), None) == 2
+
+
+def test_binding_head_major_shapes():
+    """make_fwd_args reads B, T, H, Hk from head-major shapes."""
+    import torch
+    B, T, H, Hk, dk, dv = 2, 7, 4, 2, 64, 128
+    q = torch.zeros(B, Hk, T, dk)
+    v = torch.zeros(B, H, T, dv)
+    g = torch.zeros(B, H, T, dk)
+    beta = torch.zeros(B, H, T)
+    a = kda.make_fwd_args(q, q, v, g, beta, head_major=True)
+    assert (a.B, a.T, a.H, a.Hk, a.dk, a.dv) == (B, T, H, Hk, dk, dv)
+    assert a.flags & kda.KDA_LAYOUT_HEAD_MAJOR
+    with pytest.raises(ValueError):
+        kda.make_fwd_args(q, q, v, g, beta)                 # read token-major: shapes disagree
+    cu = torch.tensor([0, 3, 7], dtype=torch.int32)
+    a = kda.make_fwd_args(q[0], q[0], v[0], g[0], beta[0], head_major=True, cu_seqlens=cu)
+    assert (a.B, a.T, a.num_seqs) == (1, T, 2)
