@@ -718,7 +718,9 @@ kda_status check_bwd(const kda_bwd_args *b) {
 struct BwdPlan {
   FwdPlan f;
   size_t off_h, off_vn, off_dhn, off_dvn, off_dqg, off_dw, off_dkg, off_dgc, off_palog, off_pdtb;
+  size_t off_himg, off_vnimg, off_dhimg, off_dvimg;  // bf16 tile images (tensor-core path)
   size_t off_dqv, off_dkv;
+  size_t off_ainv;                                // A of every chunk (tensor-core recompute)
   size_t off_vf_init, off_vf_dfin, off_vf_dinit;  // K-first copies of V-first states
   size_t total;
 };
@@ -730,10 +732,19 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
   p.f = fwd_plan(&b->fwd);
   const size_t th = (size_t)p.f.T_tot * p.f.H, ch = (size_t)p.f.nchunks * p.f.H;
   const size_t K = p.f.K, V = p.f.V;
-  size_t o = use_tc(&b->fwd) ? tc_plan(p.f).total : p.f.total;
-  p.off_h = o;     o = align256(o + 4 * ch * K * V);
+  const bool tc = use_tc(&b->fwd);
+  size_t o = tc ? tc_plan(p.f).total : p.f.total;
+  p.off_h = p.off_dhn = p.off_himg = p.off_vnimg = p.off_dhimg = p.off_dvimg = 0;
+  if (tc) {  // states and state gradients travel as bf16 operand-tile images
+    p.off_himg = o;  o = align256(o + ch * 32768);
+    p.off_vnimg = o; o = align256(o + ch * 16384);
+    p.off_dhimg = o; o = align256(o + ch * 32768);
+    p.off_dvimg = o; o = align256(o + ch * 16384);
+  } else {
+    p.off_h = o;     o = align256(o + 4 * ch * K * V);
+    p.off_dhn = o;   o = align256(o + 4 * ch * K * V);
+  }
   p.off_vn = o;    o = align256(o + 4 * th * V);
-  p.off_dhn = o;   o = align256(o + 4 * ch * K * V);
   p.off_dvn = o;   o = align256(o + 4 * th * V);
   p.off_dqg = o;   o = align256(o + 4 * th * K);
   p.off_dw = o;    o = align256(o + 4 * th * K);
@@ -746,6 +757,8 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
     p.off_dqv = o; o = align256(o + 4 * th * K);
     p.off_dkv = o; o = align256(o + 4 * th * K);
   }
+  p.off_ainv = 0;
+  if (use_tc(&b->fwd)) { p.off_ainv = o; o = align256(o + 4 * ch * BT * BT); }
   p.off_vf_init = p.off_vf_dfin = p.off_vf_dinit = 0;
   if (v_first(&b->fwd)) {
     const size_t SS = 4 * (size_t)p.f.N * p.f.H * K * V;
@@ -868,13 +881,14 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   if (tc) {
     if (e == cudaSuccess)
       e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gp, si, p.f.nchunks, a->H, p.f.Hk, pkg,
-                              err, st);
+                              err, st, f32(p.off_ainv));
     if (e == cudaSuccess) {
       tcp::ChainArgs ca{};
       ca.pkg = pkg;
       ca.initial_state = init;
-      ca.h_out = f32(p.off_h);
       ca.v_new_out = f32(p.off_vn);
+      ca.h_img = reinterpret_cast<uint8_t *>(ws + p.off_himg);
+      ca.vn_img = reinterpret_cast<uint8_t *>(ws + p.off_vnimg);
       ca.err = err;
       e = tcp::launch_tc_chain(ca, si, a->H, st);
     }
@@ -906,26 +920,41 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
       l.w = f32(p.f.off_w); l.qg = f32(p.f.off_qg); l.kg = f32(p.f.off_kg);
       l.aqk = f32(p.f.off_aqk); l.gc = f32(p.f.off_gc);
     }
-    l.h = f32(p.off_h); l.vn = f32(p.off_vn);
-    l.dhn = f32(p.off_dhn); l.dvn = f32(p.off_dvn); l.dqg = f32(p.off_dqg); l.dw = f32(p.off_dw);
+    l.h = tc ? nullptr : f32(p.off_h);
+    l.vn = f32(p.off_vn);
+    l.dhn = tc ? nullptr : f32(p.off_dhn);
+    l.dvn = f32(p.off_dvn); l.dqg = f32(p.off_dqg); l.dw = f32(p.off_dw);
     l.dkg = f32(p.off_dkg); l.dgc = f32(p.off_dgc);
     l.part_alog = f32(p.off_palog); l.part_dtb = f32(p.off_pdtb);
     l.dqv = p.off_dqv ? f32(p.off_dqv) : nullptr;
     l.dkv = p.off_dkv ? f32(p.off_dkv) : nullptr;
     l.dq = b->dq; l.dk = b->dk; l.dv = b->dv;
     l.dg = b->dg; l.dbeta = b->dbeta; l.d_initial = dinit;
+    l.a_in = tc ? f32(p.off_ainv) : nullptr;
     if (tc) {  // reverse chain on the tensor cores from the packages
       tcp::BwdChainArgs ba{};
       ba.pkg = pkg;
       ba.d_out = b->d_out;
       ba.d_final = dfin;
-      ba.dhn = l.dhn;
       ba.dvn = l.dvn;
       ba.d_initial = dinit;
+      ba.dh_img = reinterpret_cast<uint8_t *>(ws + p.off_dhimg);
+      ba.dv_img = reinterpret_cast<uint8_t *>(ws + p.off_dvimg);
       ba.err = err;
       e = tcp::launch_tc_bwd_dh(ba, si, a->H, p.f.T_tot, st);
+      if (e == cudaSuccess) {  // the state-contraction terms on the tensor cores
+        tcp::BwdStateArgs sa{};
+        sa.h_img = reinterpret_cast<const uint8_t *>(ws + p.off_himg);
+        sa.vn_img = reinterpret_cast<const uint8_t *>(ws + p.off_vnimg);
+        sa.dh_img = ba.dh_img;
+        sa.dv_img = ba.dv_img;
+        sa.d_out = b->d_out;
+        sa.dqg = l.dqg; sa.dw = l.dw; sa.dkg = l.dkg; sa.dgc = l.dgc;
+        sa.err = err;
+        e = tcp::launch_tc_bwd_state(sa, si, p.f.nchunks, a->H, st);
+      }
     }
-    if (e == cudaSuccess) e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st, !tc);
+    if (e == cudaSuccess) e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st, !tc, !tc);
   }
   if (e == cudaSuccess)
     e = launch_bwd_param_reduce(p.f.nchunks, p.f.H, p.f.K, f32(p.off_palog), f32(p.off_pdtb), b->da_log,

@@ -218,7 +218,8 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
                  const float *__restrict__ dkg, const float *__restrict__ dgc,
                  Tdq *__restrict__ dq_out, Tdq *__restrict__ dk_out, Tin *__restrict__ dv_out,
                  float *__restrict__ dg_out, float *__restrict__ dbeta_out,
-                 float *__restrict__ part_alog, float *__restrict__ part_dtb) {
+                 float *__restrict__ part_alog, float *__restrict__ part_dtb,
+                 const float *__restrict__ a_in) {
   using L = IntraSmem<K, V>;
   constexpr int KP = L::KP, XP = L::XP;
   constexpr int NP = 256 / K, NR = BT / NP;  // channel mapping: rows part + NP m
@@ -302,7 +303,13 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
   }
   __syncthreads();
 
-  // 3. L (strictly lower, beta-weighted) into sP, then A = (I + L)^-1 into sA
+  // 3. A = (I + L)^-1 into sA: from the forward's intra-chunk stage when it
+  //    kept it, else L (strictly lower, beta-weighted) into sP and forward
+  //    substitution
+  if (a_in) {
+    const float *src = a_in + (c * H + h) * (BT * BT);
+    for (int i = tid; i < BT * BT; i += 256) sA[(i >> 6) * 65 + (i & 63)] = src[i];
+  } else {
   for (int p = tid; p < BT * BT; p += 256) {
     const int r = p / BT, j = p % BT;
     float acc = 0.f;
@@ -324,6 +331,7 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
       if (part == 0) sA[i * 65 + col] = (i == col) ? 1.f : (i > col ? -acc : 0.f);
       __syncwarp();
     }
+  }
   }
   __syncthreads();
 
@@ -648,7 +656,7 @@ cudaError_t dh_dispatch(const BwdLaunch &b, int V, cudaStream_t st) {
 }
 
 template <typename Tin, int K, int V>
-cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, cudaStream_t st) {
+cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, bool with_state, cudaStream_t st) {
   const SeqInfo &s = b.s;
   const int H = b.H, Hk = b.Hk;
   const Tin *dO = static_cast<const Tin *>(b.d_out);
@@ -658,8 +666,8 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, cudaStream_t st) {
     if (e0 != cudaSuccess) return e0;
   }
   if (b.nchunks == 0) return cudaSuccess;
-  // B2: state-contraction terms
-  {
+  // B2: state-contraction terms (unless the caller ran them)
+  if (with_state) {
     const size_t smem = sizeof(float) * (2 * VT * (K + 1) + 3 * BT * VT);
     auto kern = bwd_state_kernel<Tin, K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -681,7 +689,7 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, cudaStream_t st) {
       kern<<<grid, 256, smem, st>>>(
           static_cast<const Tin *>(b.q), static_cast<const Tin *>(b.k), static_cast<const Tin *>(b.v),
           b.g, b.beta, b.gp, s, H, Hk, dO, b.dvn, b.vn, b.dqg, b.dw, b.dkg, b.dgc, b.dqv, b.dkv,
-          static_cast<Tin *>(b.dv), b.dg, b.dbeta, b.part_alog, b.part_dtb);
+          static_cast<Tin *>(b.dv), b.dg, b.dbeta, b.part_alog, b.part_dtb, b.a_in);
     } else {
       auto kern = bwd_intra_kernel<Tin, Tin, K, V>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -690,7 +698,7 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, cudaStream_t st) {
           static_cast<const Tin *>(b.q), static_cast<const Tin *>(b.k), static_cast<const Tin *>(b.v),
           b.g, b.beta, b.gp, s, H, Hk, dO, b.dvn, b.vn, b.dqg, b.dw, b.dkg, b.dgc,
           static_cast<Tin *>(b.dq), static_cast<Tin *>(b.dk), static_cast<Tin *>(b.dv), b.dg, b.dbeta,
-          b.part_alog, b.part_dtb);
+          b.part_alog, b.part_dtb, b.a_in);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (grouped) {
@@ -706,9 +714,9 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st,
-                               bool with_dh) {
+                               bool with_dh, bool with_state) {
 #define KDA_BWD(T_, K_, V_) \
-  if (K == K_ && V == V_) return bwd_dispatch<T_, K_, V_>(b, with_dh, st);
+  if (K == K_ && V == V_) return bwd_dispatch<T_, K_, V_>(b, with_dh, with_state, st);
   if (dt == KDA_F32) {
     KDA_BWD(float, 64, 64) KDA_BWD(float, 64, 128) KDA_BWD(float, 128, 64) KDA_BWD(float, 128, 128)
   } else {

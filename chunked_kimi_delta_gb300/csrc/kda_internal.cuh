@@ -188,10 +188,12 @@ struct BwdLaunch {
   float *dhn, *dvn, *dqg, *dw, *dkg, *dgc, *part_alog, *part_dtb, *dqv, *dkv;
   void *dq, *dk, *dv;
   float *dg, *dbeta, *d_initial;
+  const float *a_in;  // [nchunks, H, 64, 64] A = (I + L)^-1 from the forward, or null (recomputed)
 };
-// with_dh = false: dhn, dvn and d_initial come from the tensor-core reverse chain.
+// with_dh = false: dvn and d_initial come from the tensor-core reverse chain;
+// with_state = false: dqg, dw, dkg, dgc from the tensor-core state kernel.
 cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st,
-                               bool with_dh = true);
+                               bool with_dh = true, bool with_state = true);
 // The reverse state-gradient chain alone (dhn / dvn may be null: not written).
 cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
 cudaError_t launch_bwd_param_reduce(int64_t nchunks, int H, int K, const float *part_alog,

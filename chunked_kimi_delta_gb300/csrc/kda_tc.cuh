@@ -159,7 +159,9 @@ bool make_input_maps(const void *q, const void *k, const void *v, const float *x
 cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
                            const float *beta, const GateParams &gp, const SeqInfo &s,
                            int64_t nchunks, int H, int Hk, char *pkg, uint32_t *err,
-                           cudaStream_t st);
+                           cudaStream_t st, float *a_out = nullptr);
+// a_out: when given, [nchunks, H, 64, 64] fp32 receives A = (I + L)^-1 of
+// every item (the backward's intra-chunk stage reuses it).
 
 struct ChainArgs {
   const char *pkg;
@@ -168,6 +170,10 @@ struct ChainArgs {
   float *final_state;           // [N, H, K, V] or null
   float *h_out;                 // [nchunks, H, K, V] or null
   float *v_new_out;             // [T_tot, H, V] or null
+  // bf16 byte images of the chain's operand tiles, per (chunk, head), for
+  // the backward (or null): h entering the chunk (32 KB, MN-major K = 128
+  // channels), v_new (16 KB, MN-major K = 64 tokens)
+  uint8_t *h_img, *vn_img;
   uint32_t *err;
 };
 
@@ -182,8 +188,25 @@ struct BwdChainArgs {
   float *dhn;                   // [nchunks, H, K, V]: gradient of the state leaving each chunk, or null
   float *dvn;                   // [T_tot, H, V] fp32 or null
   float *d_initial;             // [N, H, K, V] or null
+  // bf16 byte images per (chunk, head), or null: dh' (the gradient of the
+  // state leaving the chunk, 32 KB, layout of the forward's h tile) and
+  // -dv_new (16 KB, layout of the forward's v_new tile)
+  uint8_t *dh_img, *dv_img;
   uint32_t *err;
 };
+
+// State-contraction terms of the backward per (chunk, head), on the tensor
+// cores, from the chains' tile images: d(qg) = dO h^T, dw = -dv_new h^T,
+// dkg = v_new dh'^T (fp32 [T_tot, H, K]) and d(e^{G_C}) = sum_v dh' . h (fp32
+// [nchunks, H, K]).
+struct BwdStateArgs {
+  const uint8_t *h_img, *vn_img, *dh_img, *dv_img;
+  const void *d_out;            // bf16 [T_tot, H, V] or null (zeros)
+  float *dqg, *dw, *dkg, *dgc;
+  uint32_t *err;
+};
+cudaError_t launch_tc_bwd_state(const BwdStateArgs &a, const SeqInfo &s, int64_t nchunks, int H,
+                                cudaStream_t st);
 cudaError_t launch_tc_bwd_dh(const BwdChainArgs &a, const SeqInfo &s, int H, int64_t T_tot,
                              cudaStream_t st);
 

@@ -93,15 +93,20 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
 #pragma unroll
     for (int x = 0; x < 64; ++x) dh[x] = 0.f;
   }
-  auto store_hb = [&]() {
+  // dh' (bf16) -> the MMA operand tile; with dh_img also its byte image for
+  // chunk ci (the gradient of the state leaving it)
+  auto store_hb = [&](int64_t ci) {
+    uint8_t *img = (a.dh_img && ci >= 0) ? a.dh_img + (size_t)((c0 + ci) * H + h) * 32768 : nullptr;
 #pragma unroll
     for (int x = 0; x < 64; x += 8) {
       const uint4 v = make_uint4(pack_bf16(dh[x], dh[x + 1]), pack_bf16(dh[x + 2], dh[x + 3]),
                                  pack_bf16(dh[x + 4], dh[x + 5]), pack_bf16(dh[x + 6], dh[x + 7]));
-      *reinterpret_cast<uint4 *>(sm + S_HB + mnmaj_off(128, kr, 64 * hf + x)) = v;
+      const uint32_t off = mnmaj_off(128, kr, 64 * hf + x);
+      *reinterpret_cast<uint4 *>(sm + S_HB + off) = v;
+      if (img) *reinterpret_cast<uint4 *>(img + off) = v;
     }
   };
-  store_hb();
+  store_hb(nch - 1);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -142,6 +147,9 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
     bool ok = wait_or_flag(full + b, (uint32_t)((i >> 1) & 1), a.err);
     if (!ok) *abort_flag = 1;
     else if (tid == 0) done = i + 1;
+    // e^{G_C} of this chunk, read now: the buffer is refilled as soon as the
+    // chunk's last MMA has finished
+    const float gcv = ok ? reinterpret_cast<const float *>(buf + B_GC)[kr] : 0.f;
     if (a.dhn) {  // gradient of the state leaving chunk c
       float4 *dst = reinterpret_cast<float4 *>(a.dhn + (((c0 + c) * H + h) * K + kr) * V + 64 * hf);
 #pragma unroll
@@ -202,12 +210,17 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
 #pragma unroll
             for (int x = 0; x < 4; ++x) dst[x] = make_float4(d[4 * x], d[4 * x + 1], d[4 * x + 2], d[4 * x + 3]);
           }
-          *reinterpret_cast<uint4 *>(sm + S_DV + mnmaj_off(64, r, col)) =
-              make_uint4(pack_bf16(-d[0], -d[1]), pack_bf16(-d[2], -d[3]), pack_bf16(-d[4], -d[5]),
-                         pack_bf16(-d[6], -d[7]));
-          *reinterpret_cast<uint4 *>(sm + S_DV + mnmaj_off(64, r, col + 8)) =
-              make_uint4(pack_bf16(-d[8], -d[9]), pack_bf16(-d[10], -d[11]), pack_bf16(-d[12], -d[13]),
-                         pack_bf16(-d[14], -d[15]));
+          const uint4 v0 = make_uint4(pack_bf16(-d[0], -d[1]), pack_bf16(-d[2], -d[3]),
+                                      pack_bf16(-d[4], -d[5]), pack_bf16(-d[6], -d[7]));
+          const uint4 v1 = make_uint4(pack_bf16(-d[8], -d[9]), pack_bf16(-d[10], -d[11]),
+                                      pack_bf16(-d[12], -d[13]), pack_bf16(-d[14], -d[15]));
+          *reinterpret_cast<uint4 *>(sm + S_DV + mnmaj_off(64, r, col)) = v0;
+          *reinterpret_cast<uint4 *>(sm + S_DV + mnmaj_off(64, r, col + 8)) = v1;
+          if (a.dv_img) {
+            uint8_t *img = a.dv_img + (size_t)((c0 + c) * H + h) * 16384;
+            *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col)) = v0;
+            *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col + 8)) = v1;
+          }
         }
       }
     }
@@ -255,7 +268,6 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
       }
       tc::tc_fence_after();
       // ---- dh = e^{G_C} . dh' + D2
-      const float gcv = reinterpret_cast<const float *>(buf + B_GC)[kr];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float d[16];
@@ -264,7 +276,7 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
 #pragma unroll
         for (int x = 0; x < 16; ++x) dh[16 * cc + x] = fmaf(gcv, dh[16 * cc + x], d[x]);
       }
-      store_hb();
+      store_hb(c - 1);
     }
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();
@@ -289,7 +301,175 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// State-contraction terms per (chunk, head) ([TPU] section 2.3, the parts of
+// the WY backward that involve the states): with h the state entering the
+// chunk and dh' the gradient of the state leaving it,
+//   d(qg) = dO h^T,   dw = -dv_new h^T,   dkg = v_new dh'^T   (tcgen05, M=64,
+//   N=128, K=128 value channels), d(e^{G_C}) = sum_v dh' . h  (fp32).
+// The operands are the chains' bf16 tile images: the MN-major h / dh' tiles
+// (K = channels) serve as K-major B operands of h^T / dh'^T, the MN-major
+// v_new / -dv_new tiles (K = tokens) and the TMA dO tile as K-major A.
+// ---------------------------------------------------------------------------
+constexpr uint32_t T_H = 0, T_DH = 32768, T_DV = 65536, T_VN = 81920, T_DO = 98304;
+constexpr uint32_t T_BAR = 114688;
+constexpr uint32_t T_SMEM = T_BAR + 64 + 1024;
+constexpr uint32_t T_TMEM = 256;
+
+__global__ void __launch_bounds__(NT, 1)
+tc_bwd_state_kernel(const __grid_constant__ CUtensorMap map_do, BwdStateArgs a, SeqInfo s, int H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + T_BAR);
+  uint64_t *bar1 = full + 1, *bar2 = full + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(full + 3);
+  volatile uint32_t *abort_flag = tslot + 1;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y;
+  int n, len;
+  int64_t t0;
+  if (!chunk_lookup(s, c, n, t0, len)) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q4 = warp & 3, hf = warp >> 2;
+  const bool has_do = a.d_out != nullptr;
+  const size_t item = (size_t)(c * H + h);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, T_TMEM);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(full, 1);
+    tc::mbar_init(bar1, 1);
+    tc::mbar_init(bar2, 1);
+    tc::mbar_fence_init();
+    *abort_flag = 0;
+    tc::mbar_arrive_expect_tx(full, has_do ? 114688u : 98304u);
+    bulk_load(sm + T_H, a.h_img + item * 32768, 32768, full);
+    bulk_load(sm + T_DH, a.dh_img + item * 32768, 32768, full);
+    bulk_load(sm + T_DV, a.dv_img + item * 16384, 16384, full);
+    bulk_load(sm + T_VN, a.vn_img + item * 16384, 16384, full);
+    if (has_do) {
+      tma_load_3d(sm + T_DO, &map_do, full, 0, h, (int32_t)t0);
+      tma_load_3d(sm + T_DO + 8192, &map_do, full, 64, h, (int32_t)t0);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  bool ok = wait_or_flag(full, 0, a.err);
+  if (!ok) *abort_flag = 1;
+  __syncthreads();
+  bool issued1 = false, issued2 = false;
+  if (!*abort_flag && tid == 0) {
+    tc::tc_fence_after();
+    const uint32_t id = tc::idesc_bf16_f32(64, 128, false, false);
+    const uint32_t hb = tc::smem_u32(sm + T_H), db = tc::smem_u32(sm + T_DH);
+    const uint32_t ob = tc::smem_u32(sm + T_DO), vb = tc::smem_u32(sm + T_VN);
+    if (has_do)  // d(qg) = dO h^T -> columns 0..127
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc::mma_bf16(tmem, tc::smem_desc_sw128(ob + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                     tc::smem_desc_sw128(hb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), id, kk > 0);
+    // dkg = v_new dh'^T -> columns 128..255
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      tc::mma_bf16(tmem + 128, tc::smem_desc_sw128(vb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                   tc::smem_desc_sw128(db + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), id, kk > 0);
+    tc::mma_commit(bar1);
+    issued1 = true;
+  }
+  // d(e^{G_C}) = sum_v dh' . h per key channel, while the MMAs run
+  if (!*abort_flag && tid < K) {
+    float acc = 0.f;
+#pragma unroll 4
+    for (int v8 = 0; v8 < V; v8 += 8) {
+      const uint4 x = *reinterpret_cast<const uint4 *>(sm + T_H + mnmaj_off(128, tid, v8));
+      const uint4 y = *reinterpret_cast<const uint4 *>(sm + T_DH + mnmaj_off(128, tid, v8));
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xs[e]));
+        const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ys[e]));
+        acc = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, acc));
+      }
+    }
+    a.dgc[item * K + tid] = acc;
+  }
+  // readout of a 64 x 128 product (M = 64 layout: row r in TMEM lane
+  // (r % 16) + 32 (r / 16)) into fp32 [T_tot, H, K] rows below len
+  auto readout = [&](uint32_t tcol, float *dst, bool zero) {
+    const int r = 16 * q4 + lane;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float d[16];
+      __syncwarp();
+      tc::tmem_ld16(tcol + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
+      tc::tmem_ld_wait();
+      if (lane < 16 && r < len) {
+        float4 *o = reinterpret_cast<float4 *>(dst + ((t0 + r) * H + h) * (int64_t)K + 64 * hf + 16 * cc);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          o[x] = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                      : make_float4(d[4 * x], d[4 * x + 1], d[4 * x + 2], d[4 * x + 3]);
+      }
+    }
+  };
+  __syncwarp();
+  ok = !*abort_flag && __all_sync(0xffffffffu, wait_or_flag(bar1, 0, a.err));
+  if (!ok) *abort_flag = 1;
+  else {
+    tc::tc_fence_after();
+    readout(tmem, a.dqg, !has_do);
+    readout(tmem + 128, a.dkg, false);
+  }
+  tc::tc_fence_before();
+  __syncthreads();  // columns 0..127 are free again
+  if (!*abort_flag && tid == 0) {
+    tc::tc_fence_after();
+    // dw = (-dv_new) h^T -> columns 0..127
+    const uint32_t id = tc::idesc_bf16_f32(64, 128, false, false);
+    const uint32_t hb = tc::smem_u32(sm + T_H), vb = tc::smem_u32(sm + T_DV);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      tc::mma_bf16(tmem, tc::smem_desc_sw128(vb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                   tc::smem_desc_sw128(hb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), id, kk > 0);
+    tc::mma_commit(bar2);
+    issued2 = true;
+  }
+  __syncwarp();
+  ok = !*abort_flag && __all_sync(0xffffffffu, wait_or_flag(bar2, 0, a.err));
+  if (!ok) *abort_flag = 1;
+  else {
+    tc::tc_fence_after();
+    readout(tmem, a.dw, false);
+  }
+  if (*abort_flag && tid == 0) {  // bounded drain of what this CTA started
+    drain_wait(full, 0);
+    if (issued1) drain_wait(bar1, 0);
+    if (issued2) drain_wait(bar2, 0);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, T_TMEM);
+}
+
 }  // namespace
+
+cudaError_t launch_tc_bwd_state(const BwdStateArgs &a, const SeqInfo &s, int64_t nchunks, int H,
+                                cudaStream_t st) {
+  if (nchunks == 0 || H == 0) return cudaSuccess;
+  CUtensorMap map_do;
+  memset(&map_do, 0, sizeof(map_do));  // not read without d_out
+  if (a.d_out && (s.T_tot <= 0 || !make_value_map(a.d_out, s.T_tot, H, map_do))) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)T_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)nchunks, (unsigned)H);
+  tc_bwd_state_kernel<<<grid, NT, T_SMEM, st>>>(map_do, a, s, H);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tc_bwd_dh(const BwdChainArgs &a, const SeqInfo &s, int H, int64_t T_tot,
                              cudaStream_t st) {

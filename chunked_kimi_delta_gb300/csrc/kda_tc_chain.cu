@@ -90,15 +90,20 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 #pragma unroll
     for (int x = 0; x < 64; ++x) hr[x] = 0.f;
   }
-  auto store_hb = [&]() {
+  // h (bf16) -> the MMA operand tile; with h_img also the tile's byte image
+  // for chunk ci (the state entering it), for the backward
+  auto store_hb = [&](int64_t ci) {
+    uint8_t *img = (a.h_img && ci < nch) ? a.h_img + (size_t)((c0 + ci) * H + h) * 32768 : nullptr;
 #pragma unroll
     for (int x = 0; x < 64; x += 8) {
       const uint4 v = make_uint4(pack_bf16(hr[x], hr[x + 1]), pack_bf16(hr[x + 2], hr[x + 3]),
                                  pack_bf16(hr[x + 4], hr[x + 5]), pack_bf16(hr[x + 6], hr[x + 7]));
-      *reinterpret_cast<uint4 *>(sm + S_HB + mnmaj_off(128, kr, 64 * hf + x)) = v;
+      const uint32_t off = mnmaj_off(128, kr, 64 * hf + x);
+      *reinterpret_cast<uint4 *>(sm + S_HB + off) = v;
+      if (img) *reinterpret_cast<uint4 *>(img + off) = v;
     }
   };
-  store_hb();
+  store_hb(0);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -231,12 +236,17 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
             vn[2 * x + 1] = u2.y - d[2 * x + 1];
           }
         }
-        *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col)) =
-            make_uint4(pack_bf16(vn[0], vn[1]), pack_bf16(vn[2], vn[3]), pack_bf16(vn[4], vn[5]),
-                       pack_bf16(vn[6], vn[7]));
-        *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col + 8)) =
-            make_uint4(pack_bf16(vn[8], vn[9]), pack_bf16(vn[10], vn[11]), pack_bf16(vn[12], vn[13]),
-                       pack_bf16(vn[14], vn[15]));
+        const uint4 v0 = make_uint4(pack_bf16(vn[0], vn[1]), pack_bf16(vn[2], vn[3]),
+                                    pack_bf16(vn[4], vn[5]), pack_bf16(vn[6], vn[7]));
+        const uint4 v1 = make_uint4(pack_bf16(vn[8], vn[9]), pack_bf16(vn[10], vn[11]),
+                                    pack_bf16(vn[12], vn[13]), pack_bf16(vn[14], vn[15]));
+        *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col)) = v0;
+        *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col + 8)) = v1;
+        if (a.vn_img) {  // the tile's byte image, for the backward
+          uint8_t *img = a.vn_img + (size_t)((c0 + c) * H + h) * 16384;
+          *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col)) = v0;
+          *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col + 8)) = v1;
+        }
         if (a.v_new_out && r < len) {
           float4 *dst = reinterpret_cast<float4 *>(a.v_new_out + ((tc0 + r) * H + h) * V + col);
 #pragma unroll
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 #pragma unroll
         for (int x = 0; x < 16; ++x) hr[16 * cc + x] = fmaf(gcv, hr[16 * cc + x], d[x]);
       }
-      store_hb();
+      store_hb(c + 1);
     }
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();

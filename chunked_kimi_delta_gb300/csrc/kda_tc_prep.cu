@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(NT, 2)
 tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restrict__ qg_in,
                const __nv_bfloat16 *__restrict__ kg_in, const float *__restrict__ xg_in,
                const float *__restrict__ beta, GateParams gp, SeqInfo s, int64_t nitems, int H,
-               int Hk, char *__restrict__ pkg, uint32_t *err) {
+               int Hk, char *__restrict__ pkg, float *__restrict__ a_out, uint32_t *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *rq = reinterpret_cast<float *>(sm + M_RQ);
@@ -658,6 +658,17 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         *reinterpret_cast<float2 *>(AF + (33 + i2) * LFS + j2) = make_float2(-c10, -c11);
       }
       __syncthreads();
+      if (a_out) {  // A = (I + L)^-1 of the item in fp32, for a backward (rows past the end: 0)
+        float4 *dst = reinterpret_cast<float4 *>(a_out + (size_t)(it.gc * H + h) * (BT * BT));
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int e = 4 * (tid + 256 * x), r = e >> 6, j = e & 63;
+          float v4[4];
+#pragma unroll
+          for (int y = 0; y < 4; ++y) v4[y] = (r < len && j + y <= r) ? AF[r * LFS + j + y] : 0.f;
+          dst[tid + 256 * x] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+        }
+      }
       // A . diag(beta) -> bf16, rows r and 64 + r of [A'; A']
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -786,7 +797,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
                            const float *beta, const GateParams &gp, const SeqInfo &s,
                            int64_t nchunks, int H, int Hk, char *pkg, uint32_t *err,
-                           cudaStream_t st) {
+                           cudaStream_t st, float *a_out) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -804,7 +815,7 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
   const int grid = (int)(nitems < slots ? nitems : slots);
   kern<<<grid, NT, SMEM_BYTES, st>>>(maps, static_cast<const __nv_bfloat16 *>(q),
                                      static_cast<const __nv_bfloat16 *>(k), x, beta, gp, s, nitems,
-                                     H, Hk, pkg, err);
+                                     H, Hk, pkg, a_out, err);
   return cudaGetLastError();
 }
 
