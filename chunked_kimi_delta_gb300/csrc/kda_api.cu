@@ -718,7 +718,7 @@ kda_status check_bwd(const kda_bwd_args *b) {
 struct BwdPlan {
   FwdPlan f;
   size_t off_h, off_vn, off_dhn, off_dvn, off_dqg, off_dw, off_dkg, off_dgc, off_palog, off_pdtb;
-  size_t off_himg, off_vnimg, off_dhimg, off_dvimg;  // bf16 tile images (tensor-core path)
+  size_t off_himg, off_vnimg, off_dhimg, off_dvimg, off_dwimg;  // bf16 tile images (tensor-core path)
   size_t off_dqv, off_dkv;
   size_t off_ainv;                                // A of every chunk (tensor-core recompute)
   size_t off_vf_init, off_vf_dfin, off_vf_dinit;  // K-first copies of V-first states
@@ -734,12 +734,13 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
   const size_t K = p.f.K, V = p.f.V;
   const bool tc = use_tc(&b->fwd);
   size_t o = tc ? tc_plan(p.f).total : p.f.total;
-  p.off_h = p.off_dhn = p.off_himg = p.off_vnimg = p.off_dhimg = p.off_dvimg = 0;
+  p.off_h = p.off_dhn = p.off_himg = p.off_vnimg = p.off_dhimg = p.off_dvimg = p.off_dwimg = 0;
   if (tc) {  // states and state gradients travel as bf16 operand-tile images
     p.off_himg = o;  o = align256(o + ch * 32768);
     p.off_vnimg = o; o = align256(o + ch * 16384);
     p.off_dhimg = o; o = align256(o + ch * 32768);
     p.off_dvimg = o; o = align256(o + ch * 16384);
+    p.off_dwimg = o; o = align256(o + ch * 16384);
   } else {
     p.off_h = o;     o = align256(o + 4 * ch * K * V);
     p.off_dhn = o;   o = align256(o + 4 * ch * K * V);
@@ -942,6 +943,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
       ba.dv_img = reinterpret_cast<uint8_t *>(ws + p.off_dvimg);
       ba.err = err;
       e = tcp::launch_tc_bwd_dh(ba, si, a->H, p.f.T_tot, st);
+      uint8_t *sa_dw_img = reinterpret_cast<uint8_t *>(ws + p.off_dwimg);
       if (e == cudaSuccess) {  // the state-contraction terms on the tensor cores
         tcp::BwdStateArgs sa{};
         sa.h_img = reinterpret_cast<const uint8_t *>(ws + p.off_himg);
@@ -950,11 +952,34 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
         sa.dv_img = ba.dv_img;
         sa.d_out = b->d_out;
         sa.dqg = l.dqg; sa.dw = l.dw; sa.dkg = l.dkg; sa.dgc = l.dgc;
+        sa.dw_img = reinterpret_cast<uint8_t *>(ws + p.off_dwimg);
         sa.err = err;
         e = tcp::launch_tc_bwd_state(sa, si, p.f.nchunks, a->H, st);
       }
+      if (e == cudaSuccess) {  // the intra-chunk backward on the tensor cores
+        const bool grouped = p.f.Hk != p.f.H;
+        tcp::TcIntraArgs ia{};
+        ia.q = a->q; ia.k = a->k; ia.v = a->v; ia.g = a->g; ia.beta = a->beta;
+        ia.a_in = l.a_in;
+        ia.dqg = l.dqg; ia.dkg = l.dkg; ia.dgc = l.dgc;
+        ia.d_out = b->d_out;
+        ia.dv_img = ba.dv_img;
+        ia.dw_img = sa_dw_img;
+        ia.vn_img = reinterpret_cast<const uint8_t *>(ws + p.off_vnimg);
+        ia.dq = grouped ? static_cast<void *>(l.dqv) : b->dq;
+        ia.dk = grouped ? static_cast<void *>(l.dkv) : b->dk;
+        ia.dq_is_f32 = grouped;
+        ia.dv = b->dv; ia.dg = b->dg; ia.dbeta = b->dbeta;
+        ia.part_alog = l.part_alog; ia.part_dtb = l.part_dtb;
+        ia.err = err;
+        e = tcp::launch_tc_bwd_intra(ia, si, p.f.nchunks, a->H, p.f.Hk, gp, st);
+        if (e == cudaSuccess && grouped)
+          e = launch_bwd_group_sum(a->qkv_dtype, p.f.T_tot, a->H, p.f.Hk, a->dk, l.dqv, l.dkv, b->dq, b->dk,
+                                   st);
+      }
+    } else {
+      e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st);
     }
-    if (e == cudaSuccess) e = launch_generic_bwd(a->qkv_dtype, a->dk, a->dv, l, st, !tc, !tc);
   }
   if (e == cudaSuccess)
     e = launch_bwd_param_reduce(p.f.nchunks, p.f.H, p.f.K, f32(p.off_palog), f32(p.off_pdtb), b->da_log,

@@ -738,6 +738,19 @@ cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaSt
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_bwd_group_sum(kda_dtype dt, int64_t rows, int H, int Hk, int K, const float *dqv,
+                                 const float *dkv, void *dq, void *dk, cudaStream_t st) {
+  const int64_t n = rows * Hk * K;
+  if (n == 0) return cudaSuccess;
+  if (dt == KDA_F32)
+    bwd_group_sum_kernel<float><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+        rows, H, Hk, K, dqv, dkv, static_cast<float *>(dq), static_cast<float *>(dk));
+  else
+    bwd_group_sum_kernel<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+        rows, H, Hk, K, dqv, dkv, static_cast<__nv_bfloat16 *>(dq), static_cast<__nv_bfloat16 *>(dk));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_param_reduce(int64_t nchunks, int H, int K, const float *part_alog,
                                     const float *part_dtb, float *da_log, float *ddt_bias,
                                     cudaStream_t st) {

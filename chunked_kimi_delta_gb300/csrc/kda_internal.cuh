@@ -196,6 +196,9 @@ cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, c
                                bool with_dh = true, bool with_state = true);
 // The reverse state-gradient chain alone (dhn / dvn may be null: not written).
 cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
+// dq, dk of each key head = the sum over the value heads of its group.
+cudaError_t launch_bwd_group_sum(kda_dtype dt, int64_t rows, int H, int Hk, int K, const float *dqv,
+                                 const float *dkv, void *dq, void *dk, cudaStream_t st);
 cudaError_t launch_bwd_param_reduce(int64_t nchunks, int H, int K, const float *part_alog,
                                     const float *part_dtb, float *da_log, float *ddt_bias,
                                     cudaStream_t st);

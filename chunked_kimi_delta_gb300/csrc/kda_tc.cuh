@@ -202,9 +202,29 @@ struct BwdChainArgs {
 struct BwdStateArgs {
   const uint8_t *h_img, *vn_img, *dh_img, *dv_img;
   const void *d_out;            // bf16 [T_tot, H, V] or null (zeros)
-  float *dqg, *dw, *dkg, *dgc;
+  float *dqg, *dw, *dkg, *dgc;  // dw fp32 unless dw_img
+  uint8_t *dw_img;              // or dw as a bf16 tile image (16 KB per (chunk, head),
+                                // rows past the chunk end zero)
   uint32_t *err;
 };
+
+// Intra-chunk backward on the tensor cores (kda_tc_bwd_intra.cu).
+struct TcIntraArgs {
+  const void *q, *k, *v;        // bf16 inputs (q, k with Hk heads)
+  const float *g, *beta;        // raw gate input / natural-log g, beta (logits or beta)
+  const float *a_in;            // [nchunks, H, 64, 64] A = (I + L)^-1 from the prep
+  const float *dqg, *dkg, *dgc; // from the state kernel
+  const void *d_out;            // bf16 [T_tot, H, V] or null
+  const uint8_t *dv_img, *dw_img, *vn_img;  // -dv_new, dw, v_new tile images
+  void *dq, *dk;                // [T_tot, H, K]: bf16, or fp32 per value head (dq_is_f32)
+  void *dv;                     // bf16 [T_tot, H, V]
+  float *dg, *dbeta;
+  float *part_alog, *part_dtb;  // [nchunks, H], [nchunks, H, K]
+  uint32_t *err;
+  bool dq_is_f32;
+};
+cudaError_t launch_tc_bwd_intra(const TcIntraArgs &a, const SeqInfo &s, int64_t nchunks, int H, int Hk,
+                                const GateParams &gp, cudaStream_t st);
 cudaError_t launch_tc_bwd_state(const BwdStateArgs &a, const SeqInfo &s, int64_t nchunks, int H,
                                 cudaStream_t st);
 cudaError_t launch_tc_bwd_dh(const BwdChainArgs &a, const SeqInfo &s, int H, int64_t T_tot,

@@ -441,7 +441,30 @@ tc_bwd_state_kernel(const __grid_constant__ CUtensorMap map_do, BwdStateArgs a, 
   __syncwarp();
   ok = !*abort_flag && __all_sync(0xffffffffu, wait_or_flag(bar2, 0, a.err));
   if (!ok) *abort_flag = 1;
-  else {
+  else if (a.dw_img) {  // dw as a bf16 tile image, every row (zeros past the chunk end)
+    tc::tc_fence_after();
+    uint8_t *img = a.dw_img + item * 16384;
+    const int r = 16 * q4 + lane;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float d[16];
+      __syncwarp();
+      tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
+      tc::tmem_ld_wait();
+      if (lane < 16) {
+        const int col = 64 * hf + 16 * cc;
+        const bool in = r < len;
+        *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col)) =
+            in ? make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                            pack_bf16(d[6], d[7]))
+               : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col + 8)) =
+            in ? make_uint4(pack_bf16(d[8], d[9]), pack_bf16(d[10], d[11]), pack_bf16(d[12], d[13]),
+                            pack_bf16(d[14], d[15]))
+               : make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else {
     tc::tc_fence_after();
     readout(tmem, a.dw, false);
   }

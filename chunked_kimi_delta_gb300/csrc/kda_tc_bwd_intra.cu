@@ -1,0 +1,624 @@
+// kda_tc_bwd_intra.cu - intra-chunk backward on the tensor cores (bf16
+// inputs, d_k = d_v = 128).
+//
+// "KDA Chunk Backward - TPU/Pallas Kernel Design" section 2.3: the WY backward
+// (from v_new = u - w h, u = A (v.beta), w = A (k^.beta.e^G) to q, k, v, beta,
+// g and A), the intra-chunk attention backward (A_qk and the L of
+// A = (I + L)^-1) and the reverse cumulative sum over the chunk, then the
+// gate, L2-norm and sigmoid backward.  One CTA per (chunk, head).  Every
+// contraction is a tcgen05 MMA on bf16 operands with fp32 accumulation in
+// TMEM; the CUDA cores build operands and do the elementwise chain rule:
+//   M1  dA    = [dv_new | dw] [v.beta | k^.beta.e^G]^T         (64 x 64, K = 256)
+//   M2  [dvb | dkb] = A^T [dv_new | dw]                        (64 x 256, K = 64)
+//   M4  dA_qk = dO v_new^T                                     (64 x 64, K = 128)
+//   M3  T = A^T dA,  dL = -T A^T                               (64 x 64, K = 64)
+//   M5  row side of the pairwise terms: for row i in 16-token block I,
+//       sum_j Q_ij k^_jc e^{G_ic - G_jc} and sum_j dL_ij (...), with
+//       e^{G_i - G_j} = e^{G_i - G_rI} e^{G_rI - G_j} (rI = 16 I) and the
+//       blocks' right operands stacked along K (16 + 32 + 48 + 64 = 160)
+//   M6  column side: for row j in block J, sum_i (beta_i dL_ij k^_ic + Q_ij q^_ic)
+//       e^{G_ic - G_jc}, references at the blocks' last tokens, segments of
+//       64 + 48 + 32 + 16 = 160 rows, the dL and Q parts accumulated
+// (Q = scale dA_qk on j <= i, dL on j < i.)  The sub-block reference decays
+// are those of the forward's A_kk / A_qk (the same section's 3.7): every
+// factor off the diagonal blocks is <= 1, inside a block at most 16 tokens of
+// decay.
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace tcp {
+namespace {
+
+constexpr int NT = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t S_G = 0;            // fp32 G [64][128], log2 units (chunk-local cumsum)
+constexpr uint32_t S_QR = 32768;       // bf16 raw q rows [64][128]
+constexpr uint32_t S_KR = 49152;       // bf16 raw k rows [64][128]
+constexpr uint32_t S_QF = 65536;       // fp32 Q [64][65]
+constexpr uint32_t S_DF = 82176;       // fp32 dL [64][65]
+constexpr uint32_t S_MISC = 98816;
+constexpr uint32_t M_BETA = S_MISC;          // fp32 [64]
+constexpr uint32_t M_RQ = S_MISC + 256;      // fp32 [64] rstd of q
+constexpr uint32_t M_RK = S_MISC + 512;      // fp32 [64] rstd of k
+constexpr uint32_t M_DB = S_MISC + 768;      // fp32 [64][4] dbeta parts
+constexpr uint32_t M_RED = S_MISC + 1792;    // fp32 [2][128] reductions
+constexpr uint32_t M_SRED = S_MISC + 2816;   // fp32 [8]
+constexpr uint32_t M_BAR = S_MISC + 2880;    // mbarriers
+constexpr uint32_t M_TSLOT = S_MISC + 2944;
+constexpr uint32_t S_R = 103424;       // reused region (120 KB)
+// phase A / B tiles (offsets from S_R)
+constexpr uint32_t R_DVN = 0, R_DW = 16384, R_VB = 32768, R_KB = 49152, R_AT = 65536;
+constexpr uint32_t R_DO = 73728, R_VN = 90112, R_DA = 106496, R_TT = 114688;
+// phase C / D tiles
+constexpr uint32_t R_AQ = 0, R_AD = 24576, R_BB = 49152;  // M5: A rows (Q, dL), stacked B
+constexpr uint32_t R_AP = 0, R_BP = 24576;                // M6: A, stacked B (one part at a time)
+// final phase (fp32 [64][128] each)
+constexpr uint32_t R_FG = 0, R_FQ = 32768, R_FK = 65536;
+constexpr uint32_t SMEM_BYTES = S_R + 122880 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+// TMEM columns
+constexpr uint32_t C_D2 = 0;      // [-dvb | dkb] (256); later D6Q in 0..127
+constexpr uint32_t C_D1 = 256;    // dA, then T, then D6D (128 from 256)
+constexpr uint32_t C_D5 = 320;    // dA_qk, then dL
+constexpr uint32_t C_D7 = 384;    // column side (128)
+constexpr uint32_t KB_BIG = 160;  // stacked segments
+
+__device__ __forceinline__ int seg_off_row(int I) { return 8 * I * (I + 1); }        // 0, 16, 48, 96
+__device__ __forceinline__ int seg_off_col(int J) { return 64 * J - 8 * J * (J - 1); } // 0, 64, 112, 144
+
+__device__ __forceinline__ float softplus_f(float z) { return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z))); }
+
+// bf16 K-major / MN-major SW128 element stores
+__device__ __forceinline__ void st_bf16x8(uint8_t *tile, uint32_t off, const float (&x)[8]) {
+  *reinterpret_cast<uint4 *>(tile + off) =
+      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+
+template <typename Tdq>
+__global__ void __launch_bounds__(NT, 1)
+tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, SeqInfo s, int H, int Hk,
+                    GateParams gp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *sG = reinterpret_cast<float *>(sm + S_G);
+  const __nv_bfloat16 *sQR = reinterpret_cast<const __nv_bfloat16 *>(sm + S_QR);
+  const __nv_bfloat16 *sKR = reinterpret_cast<const __nv_bfloat16 *>(sm + S_KR);
+  float *sQF = reinterpret_cast<float *>(sm + S_QF);
+  float *sDF = reinterpret_cast<float *>(sm + S_DF);
+  float *sB = reinterpret_cast<float *>(sm + M_BETA);
+  float *sRq = reinterpret_cast<float *>(sm + M_RQ);
+  float *sRk = reinterpret_cast<float *>(sm + M_RK);
+  float *sDB = reinterpret_cast<float *>(sm + M_DB);
+  float *sSRed = reinterpret_cast<float *>(sm + M_SRED);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + M_BAR);  // [0] loads, [1..6] MMA groups
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + M_TSLOT);
+  volatile uint32_t *abort_flag = tslot + 1;
+  uint8_t *R = sm + S_R;
+
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y;
+  int n, len;
+  int64_t t0;
+  if (!chunk_lookup(s, c, n, t0, len)) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q4 = warp & 3, hf = warp >> 2;
+  const int hk = h / (H / Hk);
+  const bool gate = (gp.flags & KDA_GATE_IN_KERNEL) != 0;
+  const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
+  const bool l2n = (gp.flags & KDA_L2NORM_QK) != 0;
+  const bool has_do = a.d_out != nullptr;
+  const float A_h = gate ? expf(gp.a_log[h]) : 0.f;
+  const float scale = gp.scale;
+  const size_t item = (size_t)(c * H + h);
+  auto tok = [&](int r, int heads, int head, int D) { return ((t0 + r) * heads + head) * (int64_t)D; };
+
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int x = 0; x < 7; ++x) tc::mbar_init(bar + x, 1);
+    tc::mbar_fence_init();
+    *abort_flag = 0;
+    // images of -dv_new, dw, v_new and the dO tile
+    tc::mbar_arrive_expect_tx(bar, has_do ? 65536u : 49152u);
+    bulk_load(R + R_DVN, a.dv_img + item * 16384, 16384, bar);
+    bulk_load(R + R_DW, a.dw_img + item * 16384, 16384, bar);
+    bulk_load(R + R_VN, a.vn_img + item * 16384, 16384, bar);
+    if (has_do) {
+      tma_load_3d(R + R_DO, &map_do, bar, 0, h, (int32_t)t0);
+      tma_load_3d(R + R_DO + 8192, &map_do, bar, 64, h, (int32_t)t0);
+    }
+  }
+
+  // ---- 0. raw q, k (bf16 rows), natural-log gate -> G (log2 units), beta
+  for (int i = tid; i < BT * 16; i += NT) {  // 16-byte groups of 8 channels
+    const int r = i >> 4, c8 = (i & 15) * 8;
+    uint4 qv = make_uint4(0, 0, 0, 0), kv = qv;
+    if (r < len) {
+      qv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + tok(r, Hk, hk, K) + c8);
+      kv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.k) + tok(r, Hk, hk, K) + c8);
+    }
+    *reinterpret_cast<uint4 *>(sm + S_QR + r * 256 + c8 * 2) = qv;
+    *reinterpret_cast<uint4 *>(sm + S_KR + r * 256 + c8 * 2) = kv;
+  }
+  for (int i = tid; i < BT * K; i += NT) {
+    const int r = i >> 7, cc = i & 127;
+    float gv = 0.f;
+    if (r < len) {
+      gv = a.g[tok(r, H, h, K) + cc];
+      if (gate) gv = -A_h * softplus_f(gv + (gp.dt_bias ? gp.dt_bias[h * K + cc] : 0.f));
+    }
+    sG[r * K + cc] = gv * kLog2e;
+  }
+  if (tid < BT) {
+    float b = 0.f;
+    if (tid < len) {
+      b = a.beta[(t0 + tid) * H + h];
+      if (sig) b = 1.f / (1.f + expf(-b));
+    }
+    sB[tid] = b;
+  }
+  __syncthreads();
+  for (int r = warp; r < BT; r += 8) {  // row norms
+    float sq = 0.f, sk = 0.f;
+    for (int cc = lane; cc < K; cc += 32) {
+      const float x = __bfloat162float(sQR[r * K + cc]), y = __bfloat162float(sKR[r * K + cc]);
+      sq = fmaf(x, x, sq);
+      sk = fmaf(y, y, sk);
+    }
+    for (int o = 16; o; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (lane == 0) {
+      sRq[r] = l2n ? rsqrtf(sq + gp.eps) : 1.f;
+      sRk[r] = l2n ? rsqrtf(sk + gp.eps) : 1.f;
+    }
+  }
+  if (tid < K) {  // chunk-local inclusive cumsum (rows past the end add zero)
+    float acc = 0.f;
+    for (int r = 0; r < BT; ++r) {
+      acc += sG[r * K + tid];
+      sG[r * K + tid] = acc;
+    }
+  }
+  __syncthreads();
+  auto qhat = [&](int r, int cc) { return __bfloat162float(sQR[r * K + cc]) * sRq[r]; };
+  auto khat = [&](int r, int cc) { return __bfloat162float(sKR[r * K + cc]) * sRk[r]; };
+
+  // ---- operands of M1 / M2: -v.beta, k^.beta.e^G (K-major [token][channel]),
+  //      A (bf16, K-major [i][j])
+  for (int i = tid; i < BT * 16; i += NT) {
+    const int r = i >> 4, c8 = (i & 15) * 8;
+    float vb[8], kb[8];
+    uint4 vv = make_uint4(0, 0, 0, 0);
+    if (r < len) vv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.v) + tok(r, H, h, V) + c8);
+    const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vw[e]));
+      vb[2 * e] = -sB[r] * f.x;
+      vb[2 * e + 1] = -sB[r] * f.y;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      kb[e] = r < len ? khat(r, c8 + e) * sB[r] * tc::ex2(sG[r * K + c8 + e]) : 0.f;
+    st_bf16x8(R + R_VB, kmaj_off(64, r, c8), vb);
+    st_bf16x8(R + R_KB, kmaj_off(64, r, c8), kb);
+  }
+  for (int i = tid; i < BT * 8; i += NT) {
+    const int r = i >> 3, j8 = (i & 7) * 8;
+    float av[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) av[e] = (r < len) ? a.a_in[item * (BT * BT) + r * BT + j8 + e] : 0.f;
+    st_bf16x8(R + R_AT, kmaj_off(64, r, j8), av);
+  }
+  tc::fence_proxy_async_smem();
+  bool ok = wait_or_flag(bar, 0, a.err);
+  if (!ok) *abort_flag = 1;
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  int issued = 0;  // MMA groups started (thread 0), for the drain
+
+  // ---- phase A: M1, M2, M4
+  if (!*abort_flag && tid == 0) {
+    const uint32_t dvn = tc::smem_u32(R + R_DVN), dw = tc::smem_u32(R + R_DW);
+    const uint32_t vb = tc::smem_u32(R + R_VB), kb = tc::smem_u32(R + R_KB);
+    const uint32_t at = tc::smem_u32(R + R_AT);
+    const uint32_t i64 = tc::idesc_bf16_f32(64, 64, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {  // M1: dA (both products negated in the V half)
+      const uint32_t ab = kk < 8 ? dvn : dw, bb = kk < 8 ? vb : kb, k8 = kk & 7;
+      tc::mma_bf16(tmem + C_D1, tc::smem_desc_sw128(ab + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024),
+                   tc::smem_desc_sw128(bb + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024), i64, kk > 0);
+    }
+    const uint32_t i256 = tc::idesc_bf16_f32(64, 256, true, true);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)  // M2: A^T [-dv_new | dw]
+      tc::mma_bf16(tmem + C_D2, tc::smem_desc_sw128(at + kk * 2048, 8192, 1024),
+                   tc::smem_desc_sw128(dvn + kk * 2048, 8192, 1024), i256, kk > 0);
+    if (has_do) {
+      const uint32_t o0 = tc::smem_u32(R + R_DO), v0 = tc::smem_u32(R + R_VN);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // M4: dO v_new^T
+        tc::mma_bf16(tmem + C_D5, tc::smem_desc_sw128(o0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                     tc::smem_desc_sw128(v0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), i64, kk > 0);
+    }
+    tc::mma_commit(bar + 1);
+    issued = 1;
+  }
+  // M=64 readout: row r = 16 q4 + lane (lanes < 16), columns in 16-column loads
+  const int rr = 16 * q4 + lane;
+  const bool rv = lane < 16;
+  auto wait_mma = [&](int k) -> bool {
+    __syncwarp();
+    const bool w = !*abort_flag && __all_sync(0xffffffffu, wait_or_flag(bar + k, 0, a.err));
+    if (!w) *abort_flag = 1;
+    tc::tc_fence_after();
+    return w;
+  };
+  if (wait_mma(1)) {
+    // dA (j < i) -> bf16 MN-major B tile of M3a [i][j]; Q -> sQF; -dvb -> dv, dbeta part
+    {
+      float d[16];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int j0 = 32 * hf + 16 * cc;
+        __syncwarp();
+        tc::tmem_ld16(tmem + C_D1 + ((uint32_t)(32 * q4) << 16) + j0, d);
+        tc::tmem_ld_wait();
+        if (rv) {
+          float x[8], y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            x[e] = (j0 + e < rr && rr < len) ? d[e] : 0.f;
+            y[e] = (j0 + 8 + e < rr && rr < len) ? d[8 + e] : 0.f;
+          }
+          st_bf16x8(R + R_DA, mnmaj_off(64, rr, j0), x);
+          st_bf16x8(R + R_DA, mnmaj_off(64, rr, j0 + 8), y);
+        }
+        __syncwarp();
+        if (has_do) {
+          tc::tmem_ld16(tmem + C_D5 + ((uint32_t)(32 * q4) << 16) + j0, d);
+          tc::tmem_ld_wait();
+        }
+        if (rv)
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            sQF[rr * 65 + j0 + e] = (has_do && j0 + e <= rr && rr < len) ? scale * d[e] : 0.f;
+      }
+      float pb = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int v0 = 64 * hf + 16 * cc;
+        __syncwarp();
+        tc::tmem_ld16(tmem + C_D2 + ((uint32_t)(32 * q4) << 16) + v0, d);
+        tc::tmem_ld_wait();
+        if (rv && rr < len) {
+          const __nv_bfloat16 *vr = static_cast<const __nv_bfloat16 *>(a.v) + tok(rr, H, h, V) + v0;
+          const float br = sB[rr];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float dvb0 = -d[e], dvb1 = -d[e + 1];
+            const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(vr + e));
+            pb = fmaf(dvb0, vf.x, fmaf(dvb1, vf.y, pb));
+            *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(a.dv) + tok(rr, H, h, V) + v0 + e) =
+                __floats2bfloat162_rn(br * dvb0, br * dvb1);
+          }
+        }
+      }
+      if (rv) sDB[rr * 4 + hf] = pb;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+
+  // ---- phase B: T = A^T dA, then dL = -T A^T
+  if (!*abort_flag && tid == 0) {
+    tc::tc_fence_after();
+    const uint32_t at = tc::smem_u32(R + R_AT), da = tc::smem_u32(R + R_DA);
+    const uint32_t id = tc::idesc_bf16_f32(64, 64, true, true);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      tc::mma_bf16(tmem + C_D1, tc::smem_desc_sw128(at + kk * 2048, 8192, 1024),
+                   tc::smem_desc_sw128(da + kk * 2048, 8192, 1024), id, kk > 0);
+    tc::mma_commit(bar + 2);
+    issued = 2;
+  }
+  if (wait_mma(2)) {
+    float d[16];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int q0 = 32 * hf + 16 * cc;
+      __syncwarp();
+      tc::tmem_ld16(tmem + C_D1 + ((uint32_t)(32 * q4) << 16) + q0, d);
+      tc::tmem_ld_wait();
+      if (rv) {
+        float x[8], y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { x[e] = d[e]; y[e] = d[8 + e]; }
+        st_bf16x8(R + R_TT, kmaj_off(64, rr, q0), x);
+        st_bf16x8(R + R_TT, kmaj_off(64, rr, q0 + 8), y);
+      }
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (!*abort_flag && tid == 0) {
+    tc::tc_fence_after();
+    const uint32_t tt = tc::smem_u32(R + R_TT), at = tc::smem_u32(R + R_AT);
+    const uint32_t id = tc::idesc_bf16_f32(64, 64, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      tc::mma_bf16(tmem + C_D5, tc::smem_desc_sw128(tt + kk * 32, 16, 1024),
+                   tc::smem_desc_sw128(at + kk * 32, 16, 1024), id, kk > 0);
+    tc::mma_commit(bar + 3);
+    issued = 3;
+  }
+  if (wait_mma(3)) {
+    float d[16];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int j0 = 32 * hf + 16 * cc;
+      __syncwarp();
+      tc::tmem_ld16(tmem + C_D5 + ((uint32_t)(32 * q4) << 16) + j0, d);
+      tc::tmem_ld_wait();
+      if (rv)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sDF[rr * 65 + j0 + e] = (j0 + e < rr && rr < len) ? -d[e] : 0.f;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+
+  // ---- phase C: row side.  A rows (K-major, K = 160 stacked segments) and
+  //      the stacked right operand k^_j e^{G_rI - G_j} (MN-major, N = channels)
+  if (!*abort_flag) {
+    for (int i = tid; i < BT * 24; i += NT) {  // [row][192 / 8] 16-byte groups, Q and dL rows
+      const int r = i / 24, g8 = (i % 24) * 8, I = r >> 4, o = seg_off_row(I);
+      float xq[8], xd[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = g8 + e - o;  // token of this K slot in row r's segment
+        const bool in = j >= 0 && j < 16 * (I + 1);
+        xq[e] = in ? sQF[r * 65 + j] : 0.f;   // zero past the row (Q_ij = 0 for j > i)
+        xd[e] = in ? sDF[r * 65 + j] : 0.f;
+      }
+      st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
+      st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
+    }
+    for (int i = tid; i < KB_BIG * 16; i += NT) {  // [160 rows][128 / 8]
+      const int kr = i >> 4, c8 = (i & 15) * 8;
+      const int I = kr < 16 ? 0 : (kr < 48 ? 1 : (kr < 96 ? 2 : 3));
+      const int j = kr - seg_off_row(I), ref = 16 * I;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        x[e] = j < len ? khat(j, c8 + e) * tc::ex2(fminf(sG[ref * K + c8 + e] - sG[j * K + c8 + e], 126.f)) : 0.f;
+      st_bf16x8(R + R_BB, mnmaj_off(KB_BIG, kr, c8), x);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (!*abort_flag && tid == 0) {
+    tc::tc_fence_after();
+    const uint32_t aq = tc::smem_u32(R + R_AQ), ad = tc::smem_u32(R + R_AD), bb = tc::smem_u32(R + R_BB);
+    const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 10; ++kk) {
+      const uint64_t bd = tc::smem_desc_sw128(bb + kk * 2048, KB_BIG * 128, 1024);
+      tc::mma_bf16(tmem + C_D2, tc::smem_desc_sw128(aq + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
+                   kk > 0);
+      tc::mma_bf16(tmem + C_D1, tc::smem_desc_sw128(ad + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
+                   kk > 0);
+    }
+    tc::mma_commit(bar + 4);
+    issued = 4;
+  }
+  wait_mma(4);  // the operand region is rewritten below
+  tc::tc_fence_before();
+  __syncthreads();
+
+  // ---- phase D: column side, the dL part then the Q part (same region)
+  for (int part = 0; part < 2; ++part) {
+    if (!*abort_flag) {
+      for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8]
+        const int j = i / 24, g8 = (i % 24) * 8, J = j >> 4, o = seg_off_col(J);
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
+          const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len;
+          float val = 0.f;
+          if (in) val = part == 0 ? (ii > j ? sB[ii] * sDF[ii * 65 + j] : 0.f) : (ii >= j ? sQF[ii * 65 + j] : 0.f);
+          x[e] = val;
+        }
+        st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
+      }
+      for (int i = tid; i < KB_BIG * 16; i += NT) {  // B: [160 rows][128 / 8]
+        const int kr = i >> 4, c8 = (i & 15) * 8;
+        const int J = kr < 64 ? 0 : (kr < 112 ? 1 : (kr < 144 ? 2 : 3));
+        const int ii = kr - seg_off_col(J) + 16 * J, ref = 16 * J + 15;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float f = tc::ex2(fminf(sG[ii * K + c8 + e] - sG[ref * K + c8 + e], 126.f));
+          x[e] = ii < len ? (part == 0 ? khat(ii, c8 + e) : qhat(ii, c8 + e)) * f : 0.f;
+        }
+        st_bf16x8(R + R_BP, mnmaj_off(KB_BIG, kr, c8), x);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (!*abort_flag && tid == 0) {
+      tc::tc_fence_after();
+      const uint32_t ap = tc::smem_u32(R + R_AP), bp = tc::smem_u32(R + R_BP);
+      const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 10; ++kk)
+        tc::mma_bf16(tmem + C_D7, tc::smem_desc_sw128(ap + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                     tc::smem_desc_sw128(bp + kk * 2048, KB_BIG * 128, 1024), id, part > 0 || kk > 0);
+      tc::mma_commit(bar + 5 + part);
+      issued = 5 + part;
+    }
+    wait_mma(5 + part);
+    tc::tc_fence_before();
+    __syncthreads();
+  }
+
+  // ---- final readout: row r, 64 columns per thread; dq^, dk^, dG (natural
+  //      log units) and the dkg.kg parts into shared memory, dbeta parts
+  float *fG = reinterpret_cast<float *>(R + R_FG), *fQ = reinterpret_cast<float *>(R + R_FQ);
+  float *fK = reinterpret_cast<float *>(R + R_FK), *fP = sQF;  // fP [64][128] over sQF / sDF
+  if (!*abort_flag) {
+    float pb = 0.f;
+    const int rI = 16 * (rr >> 4), rJ = 16 * (rr >> 4) + 15;
+    const float br = rv ? sB[rr] : 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      const int c0 = 64 * hf + 16 * cc;
+      float dq6[16], dd6[16], d7[16], dkb[16];
+      const uint32_t lanes = (uint32_t)(32 * q4) << 16;
+      __syncwarp();
+      tc::tmem_ld16(tmem + C_D2 + lanes + c0, dq6);        // row side, Q rows
+      tc::tmem_ld16(tmem + C_D1 + lanes + c0, dd6);        // row side, dL rows
+      tc::tmem_ld16(tmem + C_D7 + lanes + c0, d7);         // column side
+      tc::tmem_ld16(tmem + C_D2 + 128 + lanes + c0, dkb);  // A^T dw (kept from phase A)
+      tc::tmem_ld_wait();
+      if (rv) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int cc2 = c0 + e;
+          float oq = 0.f, ok = 0.f, og = 0.f, op = 0.f;
+          if (rr < len) {
+            const float G = sG[rr * K + cc2], GC = sG[(len - 1) * K + cc2];
+            const float fq = tc::ex2(G - sG[rI * K + cc2]);                 // <= 1
+            const float fc = tc::ex2(fminf(sG[rJ * K + cc2] - G, 0.f));     // <= 1
+            const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
+            const float qh = qhat(rr, cc2), kh = khat(rr, cc2);
+            const float aq = fq * dq6[e], akr = br * fq * dd6[e], akc = fc * d7[e];
+            const int64_t off = tok(rr, H, h, K) + cc2;
+            const float dqg = a.dqg[off], dkg = a.dkg[off];
+            const float kbf = br * eG;
+            oq = aq + dqg * scale * eG;
+            ok = akr + akc + dkb[e] * kbf + dkg * ekg;
+            og = qh * aq + kh * akr - kh * akc + dkb[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
+            op = dkg * kh * ekg;
+            pb = fmaf(dkb[e], kh * eG, fmaf(kh, fq * dd6[e], pb));
+          }
+          fQ[rr * K + cc2] = oq;
+          fK[rr * K + cc2] = ok;
+          fG[rr * K + cc2] = og;
+          fP[rr * K + cc2] = op;
+        }
+      }
+    }
+    if (rv) sDB[rr * 4 + 2 + hf] = pb;
+  }
+  __syncthreads();
+
+  // ---- L2-norm backward: dx = r (dx^ - x^ (x^ . dx^)), one warp per row
+  if (!*abort_flag)
+    for (int r = warp; r < len; r += 8) {
+      float pq = 0.f, pk = 0.f;
+      for (int c2 = lane; c2 < K; c2 += 32) {
+        pq = fmaf(qhat(r, c2), fQ[r * K + c2], pq);
+        pk = fmaf(khat(r, c2), fK[r * K + c2], pk);
+      }
+      for (int o = 16; o; o >>= 1) {
+        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        pk += __shfl_xor_sync(0xffffffffu, pk, o);
+      }
+      if (!l2n) pq = pk = 0.f;
+      const float rq = sRq[r], rk = sRk[r];
+      for (int c2 = lane; c2 < K; c2 += 32) {
+        const float xq = rq * (fQ[r * K + c2] - qhat(r, c2) * pq);
+        const float xk = rk * (fK[r * K + c2] - khat(r, c2) * pk);
+        const int64_t off = tok(r, H, h, K) + c2;  // per value head (summed over the group later)
+        static_cast<Tdq *>(a.dq)[off] = from_f32<Tdq>(xq);
+        static_cast<Tdq *>(a.dk)[off] = from_f32<Tdq>(xk);
+      }
+    }
+
+  // ---- reverse cumsum over the chunk (dG_C onto every row), gate backward
+  float dtb = 0.f, alog = 0.f;
+  if (!*abort_flag && tid < K) {
+    const float GC = sG[(len - 1) * K + tid];
+    float run = a.dgc[item * K + tid] * tc::ex2(GC);
+    for (int r = 0; r < len; ++r) run += fP[r * K + tid];
+    for (int r = len - 1; r >= 0; --r) {
+      run += fG[r * K + tid];
+      const int64_t off = tok(r, H, h, K) + tid;
+      if (gate) {
+        const float z = a.g[off] + (gp.dt_bias ? gp.dt_bias[h * K + tid] : 0.f);
+        const float sgm = 1.f / (1.f + expf(-z));
+        const float dz = -A_h * sgm * run;
+        a.dg[off] = dz;
+        dtb += dz;
+        alog = fmaf(-A_h * softplus_f(z), run, alog);
+      } else {
+        a.dg[off] = run;
+      }
+    }
+  }
+  if (gate && tid < K) {
+    for (int o = 16; o; o >>= 1) alog += __shfl_xor_sync(0xffffffffu, alog, o);
+    if (lane == 0) sSRed[warp] = alog;
+  }
+  __syncthreads();
+  if (!*abort_flag && gate && tid < K) {
+    a.part_dtb[item * K + tid] = dtb;
+    if (tid == 0) a.part_alog[item] = sSRed[0] + sSRed[1] + sSRed[2] + sSRed[3];
+  }
+  // ---- beta: parts from -v.beta (phase A) and the final readout; sigmoid backward
+  if (!*abort_flag && tid < len) {
+    const float d = sDB[tid * 4] + sDB[tid * 4 + 1] + sDB[tid * 4 + 2] + sDB[tid * 4 + 3];
+    const float b = sB[tid];
+    a.dbeta[(t0 + tid) * H + h] = sig ? d * b * (1.f - b) : d;
+  }
+  if (*abort_flag && tid == 0) {  // bounded drain of the loads and MMAs this CTA started
+    drain_wait(bar, 0);
+    for (int x = 1; x <= issued; ++x) drain_wait(bar + x, 0);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd_intra(const TcIntraArgs &a, const SeqInfo &s, int64_t nchunks, int H, int Hk,
+                                const GateParams &gp, cudaStream_t st) {
+  if (nchunks == 0 || H == 0) return cudaSuccess;
+  CUtensorMap map_do;
+  memset(&map_do, 0, sizeof(map_do));  // not read without d_out
+  if (a.d_out && (s.T_tot <= 0 || !make_value_map(a.d_out, s.T_tot, H, map_do))) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)nchunks, (unsigned)H);
+  cudaError_t e;
+  if (a.dq_is_f32) {
+    e = cudaFuncSetAttribute(tc_bwd_intra_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    tc_bwd_intra_kernel<float><<<grid, NT, SMEM_BYTES, st>>>(map_do, a, s, H, Hk, gp);
+  } else {
+    e = cudaFuncSetAttribute(tc_bwd_intra_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    tc_bwd_intra_kernel<__nv_bfloat16><<<grid, NT, SMEM_BYTES, st>>>(map_do, a, s, H, Hk, gp);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tcp
+}  // namespace kda
