@@ -19,7 +19,15 @@
 //   M6  column side: for row j in block J, sum_i (beta_i dL_ij k^_ic + Q_ij q^_ic)
 //       e^{G_ic - G_jc}, references at the blocks' last tokens, segments of
 //       64 + 48 + 32 + 16 = 160 rows, the dL and Q parts accumulated
-// (Q = scale dA_qk on j <= i, dL on j < i.)  The sub-block reference decays
+// (Q = scale dA_qk on j <= i, dL on j < i.)  Every pair (i, j) enters dG_i
+// from the row side and -dG_j from the column side; after the reverse cumsum
+// the two cancel in dg_r for r <= j, so both sides must round a pair alike:
+// the left operands (Q, dL) are the same bf16 values on both sides, the
+// right operands (k^ and q^ with their decay factors) are split into
+// bf16 hi + lo parts (two accumulating MMAs), and the diagonal of Q, whose
+// two terms cancel exactly in dG, stays out of M5 / M6 and enters dq^ and
+// dk^ in fp32 ("dg ... where cumulative contributions nearly cancel",
+// section 3.2 of the same design).  The sub-block reference decays
 // are those of the forward's A_kk / A_qk (the same section's 3.7): every
 // factor off the diagonal blocks is <= 1, inside a block at most 16 tokens of
 // decay.
@@ -46,10 +54,11 @@ constexpr uint32_t M_BETA = S_MISC;          // fp32 [64]
 constexpr uint32_t M_RQ = S_MISC + 256;      // fp32 [64] rstd of q
 constexpr uint32_t M_RK = S_MISC + 512;      // fp32 [64] rstd of k
 constexpr uint32_t M_DB = S_MISC + 768;      // fp32 [64][4] dbeta parts
-constexpr uint32_t M_RED = S_MISC + 1792;    // fp32 [2][128] reductions
+constexpr uint32_t M_QD = S_MISC + 1792;     // fp32 [64] diagonal of Q
 constexpr uint32_t M_SRED = S_MISC + 2816;   // fp32 [8]
-constexpr uint32_t M_BAR = S_MISC + 2880;    // mbarriers
-constexpr uint32_t M_TSLOT = S_MISC + 2944;
+constexpr uint32_t M_BAR = S_MISC + 2880;    // 10 mbarriers
+constexpr uint32_t M_TSLOT = S_MISC + 3008;
+constexpr int NBAR = 10;
 constexpr uint32_t S_R = 103424;       // reused region (120 KB)
 // phase A / B tiles (offsets from S_R)
 constexpr uint32_t R_DVN = 0, R_DW = 16384, R_VB = 32768, R_KB = 49152, R_AT = 65536;
@@ -95,7 +104,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   float *sRk = reinterpret_cast<float *>(sm + M_RK);
   float *sDB = reinterpret_cast<float *>(sm + M_DB);
   float *sSRed = reinterpret_cast<float *>(sm + M_SRED);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + M_BAR);  // [0] loads, [1..6] MMA groups
+  float *sQD = reinterpret_cast<float *>(sm + M_QD);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + M_BAR);  // [0] loads, [1..9] MMA groups
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + M_TSLOT);
   volatile uint32_t *abort_flag = tslot + 1;
   uint8_t *R = sm + S_R;
@@ -122,7 +132,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int x = 0; x < 7; ++x) tc::mbar_init(bar + x, 1);
+    for (int x = 0; x < NBAR; ++x) tc::mbar_init(bar + x, 1);
     tc::mbar_fence_init();
     *abort_flag = 0;
     // images of -dv_new, dw, v_new and the dO tile
@@ -320,6 +330,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (tid < BT) sQD[tid] = sQF[tid * 65 + tid];
 
   // ---- phase B: T = A^T dA, then dL = -T A^T
   if (!*abort_flag && tid == 0) {
@@ -381,70 +392,82 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   __syncthreads();
 
   // ---- phase C: row side.  A rows (K-major, K = 160 stacked segments) and
-  //      the stacked right operand k^_j e^{G_rI - G_j} (MN-major, N = channels)
-  if (!*abort_flag) {
-    for (int i = tid; i < BT * 24; i += NT) {  // [row][192 / 8] 16-byte groups, Q and dL rows
-      const int r = i / 24, g8 = (i % 24) * 8, I = r >> 4, o = seg_off_row(I);
-      float xq[8], xd[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = g8 + e - o;  // token of this K slot in row r's segment
-        const bool in = j >= 0 && j < 16 * (I + 1);
-        xq[e] = in ? sQF[r * 65 + j] : 0.f;   // zero past the row (Q_ij = 0 for j > i)
-        xd[e] = in ? sDF[r * 65 + j] : 0.f;
-      }
-      st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
-      st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
-    }
-    for (int i = tid; i < KB_BIG * 16; i += NT) {  // [160 rows][128 / 8]
-      const int kr = i >> 4, c8 = (i & 15) * 8;
-      const int I = kr < 16 ? 0 : (kr < 48 ? 1 : (kr < 96 ? 2 : 3));
-      const int j = kr - seg_off_row(I), ref = 16 * I;
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        x[e] = j < len ? khat(j, c8 + e) * tc::ex2(fminf(sG[ref * K + c8 + e] - sG[j * K + c8 + e], 126.f)) : 0.f;
-      st_bf16x8(R + R_BB, mnmaj_off(KB_BIG, kr, c8), x);
-    }
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  if (!*abort_flag && tid == 0) {
-    tc::tc_fence_after();
-    const uint32_t aq = tc::smem_u32(R + R_AQ), ad = tc::smem_u32(R + R_AD), bb = tc::smem_u32(R + R_BB);
-    const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
-#pragma unroll
-    for (int kk = 0; kk < 10; ++kk) {
-      const uint64_t bd = tc::smem_desc_sw128(bb + kk * 2048, KB_BIG * 128, 1024);
-      tc::mma_bf16(tmem + C_D2, tc::smem_desc_sw128(aq + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
-                   kk > 0);
-      tc::mma_bf16(tmem + C_D1, tc::smem_desc_sw128(ad + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
-                   kk > 0);
-    }
-    tc::mma_commit(bar + 4);
-    issued = 4;
-  }
-  wait_mma(4);  // the operand region is rewritten below
-  tc::tc_fence_before();
-  __syncthreads();
-
-  // ---- phase D: column side, the dL part then the Q part (same region)
-  for (int part = 0; part < 2; ++part) {
+  //      the stacked right operand k^_j e^{G_rI - G_j} (MN-major, N = channels),
+  //      its bf16 hi part then its lo part
+  auto split = [](float x, bool lo) {
+    const float hi = __bfloat162float(__float2bfloat16_rn(x));
+    return lo ? x - hi : x;
+  };
+  for (int sub = 0; sub < 2; ++sub) {
     if (!*abort_flag) {
-      for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8]
-        const int j = i / 24, g8 = (i % 24) * 8, J = j >> 4, o = seg_off_col(J);
+      if (sub == 0)
+        for (int i = tid; i < BT * 24; i += NT) {  // [row][192 / 8] 16-byte groups, Q and dL rows
+          const int r = i / 24, g8 = (i % 24) * 8, I = r >> 4, o = seg_off_row(I);
+          float xq[8], xd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = g8 + e - o;  // token of this K slot in row r's segment
+            const bool in = j >= 0 && j < 16 * (I + 1);
+            xq[e] = (in && j < r) ? sQF[r * 65 + j] : 0.f;  // strictly below the diagonal
+            xd[e] = in ? sDF[r * 65 + j] : 0.f;
+          }
+          st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
+          st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
+        }
+      for (int i = tid; i < KB_BIG * 16; i += NT) {  // [160 rows][128 / 8]
+        const int kr = i >> 4, c8 = (i & 15) * 8;
+        const int I = kr < 16 ? 0 : (kr < 48 ? 1 : (kr < 96 ? 2 : 3));
+        const int j = kr - seg_off_row(I), ref = 16 * I;
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
-          const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len;
-          float val = 0.f;
-          if (in) val = part == 0 ? (ii > j ? sB[ii] * sDF[ii * 65 + j] : 0.f) : (ii >= j ? sQF[ii * 65 + j] : 0.f);
-          x[e] = val;
-        }
-        st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
+        for (int e = 0; e < 8; ++e)
+          x[e] = j < len ? split(khat(j, c8 + e) * tc::ex2(fminf(sG[ref * K + c8 + e] - sG[j * K + c8 + e], 126.f)),
+                                 sub == 1)
+                         : 0.f;
+        st_bf16x8(R + R_BB, mnmaj_off(KB_BIG, kr, c8), x);
       }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (!*abort_flag && tid == 0) {
+      tc::tc_fence_after();
+      const uint32_t aq = tc::smem_u32(R + R_AQ), ad = tc::smem_u32(R + R_AD), bb = tc::smem_u32(R + R_BB);
+      const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 10; ++kk) {
+        const uint64_t bd = tc::smem_desc_sw128(bb + kk * 2048, KB_BIG * 128, 1024);
+        tc::mma_bf16(tmem + C_D2, tc::smem_desc_sw128(aq + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
+                     sub > 0 || kk > 0);
+        tc::mma_bf16(tmem + C_D1, tc::smem_desc_sw128(ad + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
+                     sub > 0 || kk > 0);
+      }
+      tc::mma_commit(bar + 4 + sub);
+      issued = 4 + sub;
+    }
+    wait_mma(4 + sub);  // the operand region is rewritten next
+    tc::tc_fence_before();
+    __syncthreads();
+  }
+
+  // ---- phase D: column side, the dL part then the Q part, each with the hi
+  //      and lo parts of its right operand (the left one is rebuilt per part)
+  for (int step = 0; step < 4; ++step) {
+    const int part = step >> 1;
+    const bool lo = (step & 1) != 0;
+    if (!*abort_flag) {
+      if (!lo)
+        for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8]
+          const int j = i / 24, g8 = (i % 24) * 8, J = j >> 4, o = seg_off_col(J);
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
+            const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len && ii > j;
+            x[e] = in ? (part == 0 ? sDF[ii * 65 + j] : sQF[ii * 65 + j]) : 0.f;
+          }
+          st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
+        }
       for (int i = tid; i < KB_BIG * 16; i += NT) {  // B: [160 rows][128 / 8]
         const int kr = i >> 4, c8 = (i & 15) * 8;
         const int J = kr < 64 ? 0 : (kr < 112 ? 1 : (kr < 144 ? 2 : 3));
@@ -453,7 +476,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float f = tc::ex2(fminf(sG[ii * K + c8 + e] - sG[ref * K + c8 + e], 126.f));
-          x[e] = ii < len ? (part == 0 ? khat(ii, c8 + e) : qhat(ii, c8 + e)) * f : 0.f;
+          x[e] = ii < len ? split((part == 0 ? sB[ii] * khat(ii, c8 + e) : qhat(ii, c8 + e)) * f, lo) : 0.f;
         }
         st_bf16x8(R + R_BP, mnmaj_off(KB_BIG, kr, c8), x);
       }
@@ -468,11 +491,11 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
 #pragma unroll
       for (int kk = 0; kk < 10; ++kk)
         tc::mma_bf16(tmem + C_D7, tc::smem_desc_sw128(ap + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                     tc::smem_desc_sw128(bp + kk * 2048, KB_BIG * 128, 1024), id, part > 0 || kk > 0);
-      tc::mma_commit(bar + 5 + part);
-      issued = 5 + part;
+                     tc::smem_desc_sw128(bp + kk * 2048, KB_BIG * 128, 1024), id, step > 0 || kk > 0);
+      tc::mma_commit(bar + 6 + step);
+      issued = 6 + step;
     }
-    wait_mma(5 + part);
+    wait_mma(6 + step);
     tc::tc_fence_before();
     __syncthreads();
   }
@@ -510,9 +533,9 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
             const float aq = fq * dq6[e], akr = br * fq * dd6[e], akc = fc * d7[e];
             const int64_t off = tok(rr, H, h, K) + cc2;
             const float dqg = a.dqg[off], dkg = a.dkg[off];
-            const float kbf = br * eG;
-            oq = aq + dqg * scale * eG;
-            ok = akr + akc + dkb[e] * kbf + dkg * ekg;
+            const float kbf = br * eG, qd = sQD[rr];
+            oq = aq + qd * kh + dqg * scale * eG;
+            ok = akr + akc + qd * qh + dkb[e] * kbf + dkg * ekg;
             og = qh * aq + kh * akr - kh * akc + dkb[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
             op = dkg * kh * ekg;
             pb = fmaf(dkb[e], kh * eG, fmaf(kh, fq * dd6[e], pb));
