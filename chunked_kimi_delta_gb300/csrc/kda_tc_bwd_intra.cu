@@ -44,12 +44,16 @@ constexpr int NT = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // shared memory (bytes from a 1024-aligned base)
-constexpr uint32_t S_G = 0;            // fp32 G [64][128], log2 units (chunk-local cumsum)
-constexpr uint32_t S_QR = 32768;       // bf16 raw q rows [64][128]
-constexpr uint32_t S_KR = 49152;       // bf16 raw k rows [64][128]
-constexpr uint32_t S_QF = 65536;       // fp32 Q [64][65]
-constexpr uint32_t S_DF = 82176;       // fp32 dL [64][65]
-constexpr uint32_t S_MISC = 98816;
+// Row strides padded so that the 16 rows a warp's readout lanes hold fall in
+// different banks.
+constexpr int GS = 129;                // floats per row of G and of the final fp32 arrays
+constexpr int QS = 132;                // bf16 per row of the raw q / k copies (264 bytes)
+constexpr uint32_t S_G = 0;            // fp32 G [64][GS], log2 units (chunk-local cumsum)
+constexpr uint32_t S_QR = 33280;       // bf16 raw q rows [64][QS]
+constexpr uint32_t S_KR = 50176;       // bf16 raw k rows [64][QS]
+constexpr uint32_t S_QF = 67072;       // fp32 Q [64][65]
+constexpr uint32_t S_DF = 83712;       // fp32 dL [64][65]
+constexpr uint32_t S_MISC = 100352;
 constexpr uint32_t M_BETA = S_MISC;          // fp32 [64]
 constexpr uint32_t M_RQ = S_MISC + 256;      // fp32 [64] rstd of q
 constexpr uint32_t M_RK = S_MISC + 512;      // fp32 [64] rstd of k
@@ -65,10 +69,13 @@ constexpr uint32_t R_DVN = 0, R_DW = 16384, R_VB = 32768, R_KB = 49152, R_AT = 6
 constexpr uint32_t R_DO = 73728, R_VN = 90112, R_DA = 106496, R_TT = 114688;
 // phase C / D tiles
 constexpr uint32_t R_AQ = 0, R_AD = 24576, R_BB = 49152;  // M5: A rows (Q, dL), stacked B
-constexpr uint32_t R_AP = 0, R_BP = 24576;                // M6: A, stacked B (one part at a time)
-// final phase (fp32 [64][128] each)
-constexpr uint32_t R_FG = 0, R_FQ = 32768, R_FK = 65536;
+constexpr uint32_t R_AP = 0, R_BP = 24576, R_BPL = 65536;  // M6: A, stacked B hi, lo (one part at a time)
+// final phase (fp32 [64][GS] each)
+constexpr uint32_t R_FG = 0, R_FQ = 33024, R_FK = 66048;
 constexpr uint32_t SMEM_BYTES = S_R + 122880 + 1024;
+static_assert(S_G + 64 * GS * 4 <= S_QR && S_QR + 64 * QS * 2 <= S_KR && S_KR + 64 * QS * 2 <= S_QF &&
+                  S_QF + 64 * GS * 4 <= S_MISC && S_MISC + 3072 <= S_R && R_FK + 64 * GS * 4 <= 122880,
+              "shared memory layout");
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns
 constexpr uint32_t C_D2 = 0;      // [-dvb | dkb] (256); later D6Q in 0..127
@@ -154,17 +161,31 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       qv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + tok(r, Hk, hk, K) + c8);
       kv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.k) + tok(r, Hk, hk, K) + c8);
     }
-    *reinterpret_cast<uint4 *>(sm + S_QR + r * 256 + c8 * 2) = qv;
-    *reinterpret_cast<uint4 *>(sm + S_KR + r * 256 + c8 * 2) = kv;
+    uint2 *dq2 = reinterpret_cast<uint2 *>(sm + S_QR + r * (QS * 2) + c8 * 2);
+    uint2 *dk2 = reinterpret_cast<uint2 *>(sm + S_KR + r * (QS * 2) + c8 * 2);
+    dq2[0] = make_uint2(qv.x, qv.y);
+    dq2[1] = make_uint2(qv.z, qv.w);
+    dk2[0] = make_uint2(kv.x, kv.y);
+    dk2[1] = make_uint2(kv.z, kv.w);
   }
-  for (int i = tid; i < BT * K; i += NT) {
-    const int r = i >> 7, cc = i & 127;
-    float gv = 0.f;
-    if (r < len) {
-      gv = a.g[tok(r, H, h, K) + cc];
-      if (gate) gv = -A_h * softplus_f(gv + (gp.dt_bias ? gp.dt_bias[h * K + cc] : 0.f));
+  {  // the gate: all of a thread's loads first, then the activation
+    float4 gx[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int i = tid + NT * it, r = i >> 5, c4 = (i & 31) * 4;
+      gx[it] = r < len ? *reinterpret_cast<const float4 *>(a.g + tok(r, H, h, K) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    sG[r * K + cc] = gv * kLog2e;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int i = tid + NT * it, r = i >> 5, c4 = (i & 31) * 4;
+      const float xs[4] = {gx[it].x, gx[it].y, gx[it].z, gx[it].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float gv = xs[e];
+        if (gate && r < len) gv = -A_h * softplus_f(gv + (gp.dt_bias ? gp.dt_bias[h * K + c4 + e] : 0.f));
+        sG[r * GS + c4 + e] = gv * kLog2e;
+      }
+    }
   }
   if (tid < BT) {
     float b = 0.f;
@@ -178,7 +199,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   for (int r = warp; r < BT; r += 8) {  // row norms
     float sq = 0.f, sk = 0.f;
     for (int cc = lane; cc < K; cc += 32) {
-      const float x = __bfloat162float(sQR[r * K + cc]), y = __bfloat162float(sKR[r * K + cc]);
+      const float x = __bfloat162float(sQR[r * QS + cc]), y = __bfloat162float(sKR[r * QS + cc]);
       sq = fmaf(x, x, sq);
       sk = fmaf(y, y, sk);
     }
@@ -194,13 +215,13 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   if (tid < K) {  // chunk-local inclusive cumsum (rows past the end add zero)
     float acc = 0.f;
     for (int r = 0; r < BT; ++r) {
-      acc += sG[r * K + tid];
-      sG[r * K + tid] = acc;
+      acc += sG[r * GS + tid];
+      sG[r * GS + tid] = acc;
     }
   }
   __syncthreads();
-  auto qhat = [&](int r, int cc) { return __bfloat162float(sQR[r * K + cc]) * sRq[r]; };
-  auto khat = [&](int r, int cc) { return __bfloat162float(sKR[r * K + cc]) * sRk[r]; };
+  auto qhat = [&](int r, int cc) { return __bfloat162float(sQR[r * QS + cc]) * sRq[r]; };
+  auto khat = [&](int r, int cc) { return __bfloat162float(sKR[r * QS + cc]) * sRk[r]; };
 
   // ---- operands of M1 / M2: -v.beta, k^.beta.e^G (K-major [token][channel]),
   //      A (bf16, K-major [i][j])
@@ -218,7 +239,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      kb[e] = r < len ? khat(r, c8 + e) * sB[r] * tc::ex2(sG[r * K + c8 + e]) : 0.f;
+      kb[e] = r < len ? khat(r, c8 + e) * sB[r] * tc::ex2(sG[r * GS + c8 + e]) : 0.f;
     st_bf16x8(R + R_VB, kmaj_off(64, r, c8), vb);
     st_bf16x8(R + R_KB, kmaj_off(64, r, c8), kb);
   }
@@ -421,7 +442,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          x[e] = j < len ? split(khat(j, c8 + e) * tc::ex2(fminf(sG[ref * K + c8 + e] - sG[j * K + c8 + e], 126.f)),
+          x[e] = j < len ? split(khat(j, c8 + e) * tc::ex2(fminf(sG[ref * GS + c8 + e] - sG[j * GS + c8 + e], 126.f)),
                                  sub == 1)
                          : 0.f;
         st_bf16x8(R + R_BB, mnmaj_off(KB_BIG, kr, c8), x);
@@ -450,35 +471,35 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     __syncthreads();
   }
 
-  // ---- phase D: column side, the dL part then the Q part, each with the hi
-  //      and lo parts of its right operand (the left one is rebuilt per part)
-  for (int step = 0; step < 4; ++step) {
-    const int part = step >> 1;
-    const bool lo = (step & 1) != 0;
+  // ---- phase D: column side, the dL part then the Q part; the right
+  //      operand's hi and lo parts are built together
+  for (int part = 0; part < 2; ++part) {
     if (!*abort_flag) {
-      if (!lo)
-        for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8]
-          const int j = i / 24, g8 = (i % 24) * 8, J = j >> 4, o = seg_off_col(J);
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
-            const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len && ii > j;
-            x[e] = in ? (part == 0 ? sDF[ii * 65 + j] : sQF[ii * 65 + j]) : 0.f;
-          }
-          st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
-        }
-      for (int i = tid; i < KB_BIG * 16; i += NT) {  // B: [160 rows][128 / 8]
-        const int kr = i >> 4, c8 = (i & 15) * 8;
-        const int J = kr < 64 ? 0 : (kr < 112 ? 1 : (kr < 144 ? 2 : 3));
-        const int ii = kr - seg_off_col(J) + 16 * J, ref = 16 * J + 15;
+      for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8]
+        const int j = i / 24, g8 = (i % 24) * 8, J = j >> 4, o = seg_off_col(J);
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float f = tc::ex2(fminf(sG[ii * K + c8 + e] - sG[ref * K + c8 + e], 126.f));
-          x[e] = ii < len ? split((part == 0 ? sB[ii] * khat(ii, c8 + e) : qhat(ii, c8 + e)) * f, lo) : 0.f;
+          const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
+          const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len && ii > j;
+          x[e] = in ? (part == 0 ? sDF[ii * 65 + j] : sQF[ii * 65 + j]) : 0.f;
         }
-        st_bf16x8(R + R_BP, mnmaj_off(KB_BIG, kr, c8), x);
+        st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
+      }
+      for (int i = tid; i < KB_BIG * 16; i += NT) {  // B hi and lo: [160 rows][128 / 8]
+        const int kr = i >> 4, c8 = (i & 15) * 8;
+        const int J = kr < 64 ? 0 : (kr < 112 ? 1 : (kr < 144 ? 2 : 3));
+        const int ii = kr - seg_off_col(J) + 16 * J, ref = 16 * J + 15;
+        float xh[8], xl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float f = tc::ex2(fminf(sG[ii * GS + c8 + e] - sG[ref * GS + c8 + e], 126.f));
+          const float x = ii < len ? (part == 0 ? sB[ii] * khat(ii, c8 + e) : qhat(ii, c8 + e)) * f : 0.f;
+          xh[e] = x;
+          xl[e] = split(x, true);
+        }
+        st_bf16x8(R + R_BP, mnmaj_off(KB_BIG, kr, c8), xh);
+        st_bf16x8(R + R_BPL, mnmaj_off(KB_BIG, kr, c8), xl);
       }
     }
     tc::fence_proxy_async_smem();
@@ -486,16 +507,19 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     __syncthreads();
     if (!*abort_flag && tid == 0) {
       tc::tc_fence_after();
-      const uint32_t ap = tc::smem_u32(R + R_AP), bp = tc::smem_u32(R + R_BP);
+      const uint32_t ap = tc::smem_u32(R + R_AP), bh = tc::smem_u32(R + R_BP), bl = tc::smem_u32(R + R_BPL);
       const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
 #pragma unroll
-      for (int kk = 0; kk < 10; ++kk)
-        tc::mma_bf16(tmem + C_D7, tc::smem_desc_sw128(ap + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                     tc::smem_desc_sw128(bp + kk * 2048, KB_BIG * 128, 1024), id, step > 0 || kk > 0);
-      tc::mma_commit(bar + 6 + step);
-      issued = 6 + step;
+      for (int kk = 0; kk < 20; ++kk) {
+        const uint32_t k10 = kk % 10;
+        tc::mma_bf16(tmem + C_D7, tc::smem_desc_sw128(ap + (k10 >> 2) * 8192 + (k10 & 3) * 32, 16, 1024),
+                     tc::smem_desc_sw128((kk < 10 ? bh : bl) + k10 * 2048, KB_BIG * 128, 1024), id,
+                     part > 0 || kk > 0);
+      }
+      tc::mma_commit(bar + 6 + part);
+      issued = 6 + part;
     }
-    wait_mma(6 + step);
+    wait_mma(6 + part);
     tc::tc_fence_before();
     __syncthreads();
   }
@@ -518,6 +542,17 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       tc::tmem_ld16(tmem + C_D1 + lanes + c0, dd6);        // row side, dL rows
       tc::tmem_ld16(tmem + C_D7 + lanes + c0, d7);         // column side
       tc::tmem_ld16(tmem + C_D2 + 128 + lanes + c0, dkb);  // A^T dw (kept from phase A)
+      float dqgv[16], dkgv[16];
+      if (rv && rr < len) {
+        const float4 *pq = reinterpret_cast<const float4 *>(a.dqg + tok(rr, H, h, K) + c0);
+        const float4 *pk = reinterpret_cast<const float4 *>(a.dkg + tok(rr, H, h, K) + c0);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float4 u = pq[x], w = pk[x];
+          dqgv[4 * x] = u.x; dqgv[4 * x + 1] = u.y; dqgv[4 * x + 2] = u.z; dqgv[4 * x + 3] = u.w;
+          dkgv[4 * x] = w.x; dkgv[4 * x + 1] = w.y; dkgv[4 * x + 2] = w.z; dkgv[4 * x + 3] = w.w;
+        }
+      }
       tc::tmem_ld_wait();
       if (rv) {
 #pragma unroll
@@ -525,14 +560,13 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           const int cc2 = c0 + e;
           float oq = 0.f, ok = 0.f, og = 0.f, op = 0.f;
           if (rr < len) {
-            const float G = sG[rr * K + cc2], GC = sG[(len - 1) * K + cc2];
-            const float fq = tc::ex2(G - sG[rI * K + cc2]);                 // <= 1
-            const float fc = tc::ex2(fminf(sG[rJ * K + cc2] - G, 0.f));     // <= 1
+            const float G = sG[rr * GS + cc2], GC = sG[(len - 1) * GS + cc2];
+            const float fq = tc::ex2(G - sG[rI * GS + cc2]);                 // <= 1
+            const float fc = tc::ex2(fminf(sG[rJ * GS + cc2] - G, 0.f));     // <= 1
             const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
             const float qh = qhat(rr, cc2), kh = khat(rr, cc2);
             const float aq = fq * dq6[e], akr = br * fq * dd6[e], akc = fc * d7[e];
-            const int64_t off = tok(rr, H, h, K) + cc2;
-            const float dqg = a.dqg[off], dkg = a.dkg[off];
+            const float dqg = dqgv[e], dkg = dkgv[e];
             const float kbf = br * eG, qd = sQD[rr];
             oq = aq + qd * kh + dqg * scale * eG;
             ok = akr + akc + qd * qh + dkb[e] * kbf + dkg * ekg;
@@ -540,10 +574,10 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
             op = dkg * kh * ekg;
             pb = fmaf(dkb[e], kh * eG, fmaf(kh, fq * dd6[e], pb));
           }
-          fQ[rr * K + cc2] = oq;
-          fK[rr * K + cc2] = ok;
-          fG[rr * K + cc2] = og;
-          fP[rr * K + cc2] = op;
+          fQ[rr * GS + cc2] = oq;
+          fK[rr * GS + cc2] = ok;
+          fG[rr * GS + cc2] = og;
+          fP[rr * GS + cc2] = op;
         }
       }
     }
@@ -556,8 +590,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     for (int r = warp; r < len; r += 8) {
       float pq = 0.f, pk = 0.f;
       for (int c2 = lane; c2 < K; c2 += 32) {
-        pq = fmaf(qhat(r, c2), fQ[r * K + c2], pq);
-        pk = fmaf(khat(r, c2), fK[r * K + c2], pk);
+        pq = fmaf(qhat(r, c2), fQ[r * GS + c2], pq);
+        pk = fmaf(khat(r, c2), fK[r * GS + c2], pk);
       }
       for (int o = 16; o; o >>= 1) {
         pq += __shfl_xor_sync(0xffffffffu, pq, o);
@@ -566,43 +600,85 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       if (!l2n) pq = pk = 0.f;
       const float rq = sRq[r], rk = sRk[r];
       for (int c2 = lane; c2 < K; c2 += 32) {
-        const float xq = rq * (fQ[r * K + c2] - qhat(r, c2) * pq);
-        const float xk = rk * (fK[r * K + c2] - khat(r, c2) * pk);
+        const float xq = rq * (fQ[r * GS + c2] - qhat(r, c2) * pq);
+        const float xk = rk * (fK[r * GS + c2] - khat(r, c2) * pk);
         const int64_t off = tok(r, H, h, K) + c2;  // per value head (summed over the group later)
         static_cast<Tdq *>(a.dq)[off] = from_f32<Tdq>(xq);
         static_cast<Tdq *>(a.dk)[off] = from_f32<Tdq>(xk);
       }
     }
 
-  // ---- reverse cumsum over the chunk (dG_C onto every row), gate backward
-  float dtb = 0.f, alog = 0.f;
+  // ---- reverse cumsum over the chunk (dG_C onto every row): fG <- the
+  //      gradient of the natural-log gate g of each token
   if (!*abort_flag && tid < K) {
-    const float GC = sG[(len - 1) * K + tid];
+    const float GC = sG[(len - 1) * GS + tid];
     float run = a.dgc[item * K + tid] * tc::ex2(GC);
-    for (int r = 0; r < len; ++r) run += fP[r * K + tid];
+    for (int r = 0; r < len; ++r) run += fP[r * GS + tid];
     for (int r = len - 1; r >= 0; --r) {
-      run += fG[r * K + tid];
-      const int64_t off = tok(r, H, h, K) + tid;
-      if (gate) {
-        const float z = a.g[off] + (gp.dt_bias ? gp.dt_bias[h * K + tid] : 0.f);
-        const float sgm = 1.f / (1.f + expf(-z));
-        const float dz = -A_h * sgm * run;
-        a.dg[off] = dz;
-        dtb += dz;
-        alog = fmaf(-A_h * softplus_f(z), run, alog);
-      } else {
-        a.dg[off] = run;
-      }
+      run += fG[r * GS + tid];
+      fG[r * GS + tid] = run;
     }
   }
-  if (gate && tid < K) {
+  __syncthreads();
+  // ---- gate backward, all threads (4 channels x every 8th row each):
+  //      dz = -exp(a_log) sigmoid(z) dg, z = x + dt_bias; dA_log, ddt_bias parts
+  float alog = 0.f;
+  float *sPart = fQ;  // [8][128] ddt_bias parts (fQ is free after the norm backward)
+  {
+    const int c4 = (tid & 31) * 4, rg = tid >> 5;
+    float dtb[4] = {0.f, 0.f, 0.f, 0.f}, bias[4] = {0.f, 0.f, 0.f, 0.f};
+    if (gate && gp.dt_bias)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bias[e] = gp.dt_bias[h * K + c4 + e];
+    if (!*abort_flag) {
+      float4 gx[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int r = rg + 8 * m;
+        gx[m] = (gate && r < len) ? *reinterpret_cast<const float4 *>(a.g + tok(r, H, h, K) + c4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int r = rg + 8 * m;
+        if (r < len) {
+          const float xs[4] = {gx[m].x, gx[m].y, gx[m].z, gx[m].w};
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float dgn = fG[r * GS + c4 + e];
+            if (gate) {
+              const float z = xs[e] + bias[e];
+              const float dz = -A_h * dgn / (1.f + expf(-z));
+              o[e] = dz;
+              dtb[e] += dz;
+              alog = fmaf(-A_h * softplus_f(z), dgn, alog);
+            } else {
+              o[e] = dgn;
+            }
+          }
+          *reinterpret_cast<float4 *>(a.dg + tok(r, H, h, K) + c4) = make_float4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    if (gate)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sPart[rg * K + c4 + e] = dtb[e];
+  }
+  if (gate) {
     for (int o = 16; o; o >>= 1) alog += __shfl_xor_sync(0xffffffffu, alog, o);
     if (lane == 0) sSRed[warp] = alog;
   }
   __syncthreads();
   if (!*abort_flag && gate && tid < K) {
-    a.part_dtb[item * K + tid] = dtb;
-    if (tid == 0) a.part_alog[item] = sSRed[0] + sSRed[1] + sSRed[2] + sSRed[3];
+    float d = 0.f;
+    for (int x = 0; x < 8; ++x) d += sPart[x * K + tid];
+    a.part_dtb[item * K + tid] = d;
+    if (tid == 0) {
+      float al = 0.f;
+      for (int x = 0; x < 8; ++x) al += sSRed[x];
+      a.part_alog[item] = al;
+    }
   }
   // ---- beta: parts from -v.beta (phase A) and the final readout; sigmoid backward
   if (!*abort_flag && tid < len) {
