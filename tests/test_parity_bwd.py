@@ -59,9 +59,9 @@ def test_bwd_ragged_small(cuda_lib, dtype, dk, dv, T):
     _compare(got, ref, cfg, dtype)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_bwd_precomputed_gate_and_beta_without_l2norm(cuda_lib, dtype):
-    cfg = KdaConfig("bwd_pre", B=1, T=150, H=2, dk=64, dv=64, dtype=dtype, gate_in_kernel=False,
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 64), ("bf16", 128)])
+def test_bwd_precomputed_gate_and_beta_without_l2norm(cuda_lib, dtype, d):
+    cfg = KdaConfig("bwd_pre", B=1, T=150, H=2, dk=d, dv=d, dtype=dtype, gate_in_kernel=False,
                     beta_sigmoid=False, l2norm=False, initial_state=True, seed=5)
     inp = make(cfg)
     inp["k"] = (inp["k"].float() * 0.1).to(inp["k"].dtype)  # keep the unnormalised rule contractive
@@ -69,13 +69,14 @@ def test_bwd_precomputed_gate_and_beta_without_l2norm(cuda_lib, dtype):
     _compare(got, ref, cfg, dtype)
 
 
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
 @pytest.mark.parametrize("which", ["d_out only", "d_final only"])
-def test_bwd_one_cotangent(cuda_lib, which):
-    cfg = KdaConfig("bwd_one", B=1, T=100, H=2, dk=64, dv=64, dtype="f32", initial_state=True,
+def test_bwd_one_cotangent(cuda_lib, which, dtype, d):
+    cfg = KdaConfig("bwd_one", B=1, T=200, H=2, dk=d, dv=d, dtype=dtype, initial_state=True,
                     seed=3)
     got, ref = _run(cuda_lib, cfg, with_dout=(which == "d_out only"),
                     with_dfin=(which == "d_final only"))
-    _compare(got, ref, cfg, "f32")
+    _compare(got, ref, cfg, dtype)
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
