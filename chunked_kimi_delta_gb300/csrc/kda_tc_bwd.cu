@@ -324,8 +324,8 @@ tc_bwd_state_kernel(const __grid_constant__ CUtensorMap map_do, BwdStateArgs a, 
   uint64_t *bar1 = full + 1, *bar2 = full + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(full + 3);
   volatile uint32_t *abort_flag = tslot + 1;
-  const int64_t c = blockIdx.x;
-  const int h = blockIdx.y;
+  const int64_t c = (int64_t)blockIdx.x / H;  // head fastest: adjacent CTAs share tokens
+  const int h = (int)(blockIdx.x % H);
   int n, len;
   int64_t t0;
   if (!chunk_lookup(s, c, n, t0, len)) return;
@@ -489,7 +489,7 @@ cudaError_t launch_tc_bwd_state(const BwdStateArgs &a, const SeqInfo &s, int64_t
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)T_SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)nchunks, (unsigned)H);
+  dim3 grid((unsigned)(nchunks * H));
   tc_bwd_state_kernel<<<grid, NT, T_SMEM, st>>>(map_do, a, s, H);
   return cudaGetLastError();
 }

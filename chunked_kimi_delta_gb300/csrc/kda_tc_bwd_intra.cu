@@ -117,8 +117,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   volatile uint32_t *abort_flag = tslot + 1;
   uint8_t *R = sm + S_R;
 
-  const int64_t c = blockIdx.x;
-  const int h = blockIdx.y;
+  const int64_t c = (int64_t)blockIdx.x / H;  // head fastest: adjacent CTAs share tokens
+  const int h = (int)(blockIdx.x % H);
   int n, len;
   int64_t t0;
   if (!chunk_lookup(s, c, n, t0, len)) return;
@@ -703,7 +703,7 @@ cudaError_t launch_tc_bwd_intra(const TcIntraArgs &a, const SeqInfo &s, int64_t 
   CUtensorMap map_do;
   memset(&map_do, 0, sizeof(map_do));  // not read without d_out
   if (a.d_out && (s.T_tot <= 0 || !make_value_map(a.d_out, s.T_tot, H, map_do))) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)nchunks, (unsigned)H);
+  dim3 grid((unsigned)(nchunks * H));
   cudaError_t e;
   if (a.dq_is_f32) {
     e = cudaFuncSetAttribute(tc_bwd_intra_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
