@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from chunked_kimi_delta_gb300.inputs import KdaConfig, make_cotangents
-from kda_testutil import check, fwd_kwargs, gpu_fwd, make, oracle_problem, to_cuda
+from kda_testutil import check, fwd_kwargs, gpu_fwd, make, oracle_problem, rel_l2, to_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -114,3 +114,53 @@ def test_summaries_head_major(cuda_lib):
                                            to_hm(cot["d_out"], False), sb, head_major=True, **kw)
     torch.cuda.synchronize()
     assert torch.equal(M_h, M_t) and torch.equal(S_h, S_t) and torch.equal(E_h, E_t)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_all_boundary_options_together(cuda_lib, dtype, d):
+    """Packed sequences in NTD (head-major) layout, V-first states and two
+    key heads for four value heads, forward and backward, against the plain
+    token-major K-first run on q/k expanded to the value heads: the
+    conversions are exact, so o, the states and every per-value-head gradient
+    agree bit for bit; dq, dk agree with the group sums of the expanded run."""
+    lens = (1, 64, 0, 65, 130)
+    H, Hk = 4, 2
+    cfg = KdaConfig("combo", dtype=dtype, H=H, dk=d, dv=d, seq_lens=lens, initial_state=True,
+                    seed=23)
+    inp = to_cuda(make(cfg))
+    cot = to_cuda(make_cotangents(cfg, inp))
+    T = sum(lens)
+    small, wide = dict(inp), dict(inp)
+    for n in ("q", "k"):
+        x = inp[n][:, :Hk].contiguous()
+        small[n] = x
+        wide[n] = x.repeat_interleave(H // Hk, dim=1).contiguous()
+    kw = fwd_kwargs(cfg, inp)
+    o_w, f_w = cuda_lib.kda_chunk_fwd(wide["q"], wide["k"], wide["v"], wide["g"], wide["beta"], **kw)
+    g_w = cuda_lib.kda_chunk_bwd(wide["q"], wide["k"], wide["v"], wide["g"], wide["beta"], cot["d_out"],
+                                 d_final_state=cot["d_final_state"], want_d_initial_state=True, **kw)
+    hm = {n: to_hm(small[n], True) for n in ("q", "k", "v", "g", "beta")}
+    kv = dict(kw)
+    kv["initial_state"] = inp["initial_state"].transpose(-1, -2).contiguous()
+    o_c, f_c = cuda_lib.kda_chunk_fwd(hm["q"], hm["k"], hm["v"], hm["g"], hm["beta"], head_major=True,
+                                      state_v_first=True, **kv)
+    g_c = cuda_lib.kda_chunk_bwd(hm["q"], hm["k"], hm["v"], hm["g"], hm["beta"], to_hm(cot["d_out"], True),
+                                 d_final_state=cot["d_final_state"].transpose(-1, -2).contiguous(),
+                                 want_d_initial_state=True, head_major=True, state_v_first=True, **kv)
+    torch.cuda.synchronize()
+    assert torch.equal(o_c, to_hm(o_w, True))
+    assert torch.equal(f_c, f_w.transpose(-1, -2))
+    for name in ("dv", "dg", "dbeta"):
+        assert torch.equal(g_c[name], to_hm(g_w[name], True)), name
+    for name in ("da_log", "ddt_bias"):
+        assert torch.equal(g_c[name], g_w[name]), name
+    assert torch.equal(g_c["d_initial_state"], g_w["d_initial_state"].transpose(-1, -2))
+    for name in ("dq", "dk"):
+        # the library sums the value heads' fp32 gradients and rounds once;
+        # the expanded run rounds each head's gradient to the input dtype
+        want = g_w[name].float().reshape(T, Hk, H // Hk, d).sum(dim=2)
+        got = g_c[name].float().transpose(0, 1)
+        if dtype == "bf16":
+            assert rel_l2(got.cpu().numpy(), want.cpu().numpy()) <= 1e-2, name
+        else:
+            torch.testing.assert_close(got, want, rtol=1e-5, atol=1e-5)
