@@ -42,6 +42,7 @@ namespace {
 
 constexpr int NT = 256;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // shared memory (bytes from a 1024-aligned base)
 // Row strides padded so that the 16 rows a warp's readout lanes hold fall in
@@ -74,7 +75,7 @@ constexpr uint32_t R_AP = 0, R_BP = 24576, R_BPL = 65536;  // M6: A, stacked B h
 constexpr uint32_t R_FG = 0, R_FQ = 33024, R_FK = 66048;
 constexpr uint32_t SMEM_BYTES = S_R + 122880 + 1024;
 static_assert(S_G + 64 * GS * 4 <= S_QR && S_QR + 64 * QS * 2 <= S_KR && S_KR + 64 * QS * 2 <= S_QF &&
-                  S_QF + 64 * GS * 4 <= S_MISC && S_MISC + 3072 <= S_R && R_FK + 64 * GS * 4 <= 122880,
+                  S_QF + 64 * GS * 4 <= S_MISC && S_MISC + 3072 <= S_R && R_FK + 64 * GS * 4 + 2048 <= 122880,
               "shared memory layout");
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns
@@ -87,7 +88,12 @@ constexpr uint32_t KB_BIG = 160;  // stacked segments
 __device__ __forceinline__ int seg_off_row(int I) { return 8 * I * (I + 1); }        // 0, 16, 48, 96
 __device__ __forceinline__ int seg_off_col(int J) { return 64 * J - 8 * J * (J - 1); } // 0, 64, 112, 144
 
-__device__ __forceinline__ float softplus_f(float z) { return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z))); }
+
+// Bulk prefetch into L2 (16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
 
 // bf16 K-major / MN-major SW128 element stores
 __device__ __forceinline__ void st_bf16x8(uint8_t *tile, uint32_t off, const float (&x)[8]) {
@@ -129,7 +135,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
   const bool l2n = (gp.flags & KDA_L2NORM_QK) != 0;
   const bool has_do = a.d_out != nullptr;
-  const float A_h = gate ? expf(gp.a_log[h]) : 0.f;
+  const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
   const float scale = gp.scale;
   const size_t item = (size_t)(c * H + h);
   auto tok = [&](int r, int heads, int head, int D) { return ((t0 + r) * heads + head) * (int64_t)D; };
@@ -153,71 +159,116 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     }
   }
 
-  // ---- 0. raw q, k (bf16 rows), natural-log gate -> G (log2 units), beta
-  for (int i = tid; i < BT * 16; i += NT) {  // 16-byte groups of 8 channels
-    const int r = i >> 4, c8 = (i & 15) * 8;
-    uint4 qv = make_uint4(0, 0, 0, 0), kv = qv;
+  // ---- 0. every global load of the phase first (q, k, v rows; the gate
+  //      input; A; beta), then the raw q, k rows to shared memory with their
+  //      norms, and the gate in log2 units with its chunk-local inclusive
+  //      cumsum (8-row groups in registers, then the groups' prefix)
+  const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(a.q);
+  const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(a.k);
+  const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(a.v);
+  const int gc4 = 4 * lane;  // gate layout: rows 8 warp .. 8 warp + 7, channels gc4 .. gc4 + 3
+  uint4 qv[4], kv[4], vv[4];
+  float4 gx[8], av[4];
+  float bload = 0.f;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {  // 16-byte groups of 8 channels: row (tid + 256 it) / 16
+    const int i = tid + NT * it, r = i >> 4, c8 = (i & 15) * 8;
+    qv[it] = kv[it] = vv[it] = make_uint4(0, 0, 0, 0);
     if (r < len) {
-      qv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + tok(r, Hk, hk, K) + c8);
-      kv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.k) + tok(r, Hk, hk, K) + c8);
+      qv[it] = *reinterpret_cast<const uint4 *>(qin + tok(r, Hk, hk, K) + c8);
+      kv[it] = *reinterpret_cast<const uint4 *>(kin + tok(r, Hk, hk, K) + c8);
+      vv[it] = *reinterpret_cast<const uint4 *>(vin + tok(r, H, h, V) + c8);
     }
+  }
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const int r = 8 * warp + x;
+    gx[x] = r < len ? *reinterpret_cast<const float4 *>(a.g + tok(r, H, h, K) + gc4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {  // A rows: 8 consecutive entries per thread and step
+    const int i = tid + NT * it, r = i >> 3, j8 = (i & 7) * 8;
+    av[2 * it] = av[2 * it + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < len) {
+      const float4 *p = reinterpret_cast<const float4 *>(a.a_in + item * (BT * BT) + r * BT + j8);
+      av[2 * it] = p[0];
+      av[2 * it + 1] = p[1];
+    }
+  }
+  if (tid < BT && tid < len) bload = a.beta[(t0 + tid) * H + h];
+
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int i = tid + NT * it, r = i >> 4, c8 = (i & 15) * 8;
     uint2 *dq2 = reinterpret_cast<uint2 *>(sm + S_QR + r * (QS * 2) + c8 * 2);
     uint2 *dk2 = reinterpret_cast<uint2 *>(sm + S_KR + r * (QS * 2) + c8 * 2);
-    dq2[0] = make_uint2(qv.x, qv.y);
-    dq2[1] = make_uint2(qv.z, qv.w);
-    dk2[0] = make_uint2(kv.x, kv.y);
-    dk2[1] = make_uint2(kv.z, kv.w);
-  }
-  {  // the gate: all of a thread's loads first, then the activation
-    float4 gx[8];
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int i = tid + NT * it, r = i >> 5, c4 = (i & 31) * 4;
-      gx[it] = r < len ? *reinterpret_cast<const float4 *>(a.g + tok(r, H, h, K) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int i = tid + NT * it, r = i >> 5, c4 = (i & 31) * 4;
-      const float xs[4] = {gx[it].x, gx[it].y, gx[it].z, gx[it].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float gv = xs[e];
-        if (gate && r < len) gv = -A_h * softplus_f(gv + (gp.dt_bias ? gp.dt_bias[h * K + c4 + e] : 0.f));
-        sG[r * GS + c4 + e] = gv * kLog2e;
-      }
-    }
-  }
-  if (tid < BT) {
-    float b = 0.f;
-    if (tid < len) {
-      b = a.beta[(t0 + tid) * H + h];
-      if (sig) b = 1.f / (1.f + expf(-b));
-    }
-    sB[tid] = b;
-  }
-  __syncthreads();
-  for (int r = warp; r < BT; r += 8) {  // row norms
+    dq2[0] = make_uint2(qv[it].x, qv[it].y);
+    dq2[1] = make_uint2(qv[it].z, qv[it].w);
+    dk2[0] = make_uint2(kv[it].x, kv[it].y);
+    dk2[1] = make_uint2(kv[it].z, kv[it].w);
+    // sums of squares over the row's 16 groups, held by 16 adjacent lanes
+    const uint32_t qw[4] = {qv[it].x, qv[it].y, qv[it].z, qv[it].w};
+    const uint32_t kw[4] = {kv[it].x, kv[it].y, kv[it].z, kv[it].w};
     float sq = 0.f, sk = 0.f;
-    for (int cc = lane; cc < K; cc += 32) {
-      const float x = __bfloat162float(sQR[r * QS + cc]), y = __bfloat162float(sKR[r * QS + cc]);
-      sq = fmaf(x, x, sq);
-      sk = fmaf(y, y, sk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[e]));
+      const float2 fk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kw[e]));
+      sq = fmaf(fq.x, fq.x, fmaf(fq.y, fq.y, sq));
+      sk = fmaf(fk.x, fk.x, fmaf(fk.y, fk.y, sk));
     }
-    for (int o = 16; o; o >>= 1) {
+#pragma unroll
+    for (int o = 8; o; o >>= 1) {
       sq += __shfl_xor_sync(0xffffffffu, sq, o);
       sk += __shfl_xor_sync(0xffffffffu, sk, o);
     }
-    if (lane == 0) {
+    if ((i & 15) == 0) {
       sRq[r] = l2n ? rsqrtf(sq + gp.eps) : 1.f;
       sRk[r] = l2n ? rsqrtf(sk + gp.eps) : 1.f;
     }
   }
-  if (tid < K) {  // chunk-local inclusive cumsum (rows past the end add zero)
-    float acc = 0.f;
-    for (int r = 0; r < BT; ++r) {
-      acc += sG[r * GS + tid];
-      sG[r * GS + tid] = acc;
+  float Gl[8][4];
+  {
+    float dbl[4];  // dt_bias in log2 units
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dbl[e] = (gate && gp.dt_bias) ? gp.dt_bias[h * K + gc4 + e] * kLog2e : 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const int r = 8 * warp + x;
+      const float xs[4] = {gx[x].x, gx[x].y, gx[x].z, gx[x].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float g = xs[e] * kLog2e;
+        if (gate) {
+          // -exp(a_log) softplus(x + dt_bias), in log2 units
+          const float z = fmaf(xs[e], kLog2e, dbl[e]);
+          g = -A_h * (fmaxf(z, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z))));
+        }
+        if (r >= len) g = 0.f;
+        acc[e] += g;
+        Gl[x][e] = acc[e];
+      }
     }
+    *reinterpret_cast<float4 *>(R + R_DA + (warp * 128 + gc4) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  }
+  if (tid < BT) {
+    float b = bload;
+    if (sig && tid < len) b = 1.f / (1.f + expf(-b));
+    sB[tid] = b;
+  }
+  __syncthreads();
+  {  // add the totals of the earlier 8-row groups
+    const float *tot = reinterpret_cast<const float *>(R + R_DA);
+    float pre[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int w2 = 0; w2 < warp; ++w2) {
+      const float4 t = *reinterpret_cast<const float4 *>(tot + w2 * 128 + gc4);
+      pre[0] += t.x; pre[1] += t.y; pre[2] += t.z; pre[3] += t.w;
+    }
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sG[(8 * warp + x) * GS + gc4 + e] = Gl[x][e] + pre[e];
   }
   __syncthreads();
   auto qhat = [&](int r, int cc) { return __bfloat162float(sQR[r * QS + cc]) * sRq[r]; };
@@ -225,30 +276,30 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
 
   // ---- operands of M1 / M2: -v.beta, k^.beta.e^G (K-major [token][channel]),
   //      A (bf16, K-major [i][j])
-  for (int i = tid; i < BT * 16; i += NT) {
-    const int r = i >> 4, c8 = (i & 15) * 8;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int i = tid + NT * it, r = i >> 4, c8 = (i & 15) * 8;
     float vb[8], kb[8];
-    uint4 vv = make_uint4(0, 0, 0, 0);
-    if (r < len) vv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.v) + tok(r, H, h, V) + c8);
-    const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+    const uint32_t vw[4] = {vv[it].x, vv[it].y, vv[it].z, vv[it].w};
+    const float br = sB[r];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vw[e]));
-      vb[2 * e] = -sB[r] * f.x;
-      vb[2 * e + 1] = -sB[r] * f.y;
+      vb[2 * e] = -br * f.x;
+      vb[2 * e + 1] = -br * f.y;
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      kb[e] = r < len ? khat(r, c8 + e) * sB[r] * tc::ex2(sG[r * GS + c8 + e]) : 0.f;
+      kb[e] = r < len ? khat(r, c8 + e) * br * tc::ex2(sG[r * GS + c8 + e]) : 0.f;
     st_bf16x8(R + R_VB, kmaj_off(64, r, c8), vb);
     st_bf16x8(R + R_KB, kmaj_off(64, r, c8), kb);
   }
-  for (int i = tid; i < BT * 8; i += NT) {
-    const int r = i >> 3, j8 = (i & 7) * 8;
-    float av[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) av[e] = (r < len) ? a.a_in[item * (BT * BT) + r * BT + j8 + e] : 0.f;
-    st_bf16x8(R + R_AT, kmaj_off(64, r, j8), av);
+  for (int it = 0; it < 2; ++it) {
+    const int i = tid + NT * it, r = i >> 3, j8 = (i & 7) * 8;
+    const float x[8] = {av[2 * it].x, av[2 * it].y, av[2 * it].z, av[2 * it].w,
+                        av[2 * it + 1].x, av[2 * it + 1].y, av[2 * it + 1].z, av[2 * it + 1].w};
+    st_bf16x8(R + R_AT, kmaj_off(64, r, j8), x);
   }
   tc::fence_proxy_async_smem();
   bool ok = wait_or_flag(bar, 0, a.err);
@@ -471,6 +522,14 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     __syncthreads();
   }
 
+  // the fp32 rows the final readout reads (dq_g, dk_g), and the gate input
+  // the gate backward reads again: fetched into L2 one phase ahead
+  if (tid < len) {
+    prefetch_l2(a.dqg + tok(tid, H, h, K), K * 4);
+    prefetch_l2(a.dkg + tok(tid, H, h, K), K * 4);
+    if (gate) prefetch_l2(a.g + tok(tid, H, h, K), K * 4);
+  }
+
   // ---- phase D: column side, the dL part then the Q part; the right
   //      operand's hi and lo parts are built together
   for (int part = 0; part < 2; ++part) {
@@ -585,38 +644,82 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   }
   __syncthreads();
 
-  // ---- L2-norm backward: dx = r (dx^ - x^ (x^ . dx^)), one warp per row
+  // ---- L2-norm backward: dx = r (dx^ - x^ (x^ . dx^)), one warp per row,
+  //      two rows (r, r + 8) at a time
   if (!*abort_flag)
-    for (int r = warp; r < len; r += 8) {
-      float pq = 0.f, pk = 0.f;
-      for (int c2 = lane; c2 < K; c2 += 32) {
-        pq = fmaf(qhat(r, c2), fQ[r * GS + c2], pq);
-        pk = fmaf(khat(r, c2), fK[r * GS + c2], pk);
+    for (int r0 = warp; r0 < len; r0 += 16) {
+      float pq[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
+#pragma unroll
+      for (int y = 0; y < 2; ++y) {
+        const int r = r0 + 8 * y;
+        if (r < len)
+#pragma unroll
+          for (int c2 = lane; c2 < K; c2 += 32) {
+            pq[y] = fmaf(qhat(r, c2), fQ[r * GS + c2], pq[y]);
+            pk[y] = fmaf(khat(r, c2), fK[r * GS + c2], pk[y]);
+          }
       }
-      for (int o = 16; o; o >>= 1) {
-        pq += __shfl_xor_sync(0xffffffffu, pq, o);
-        pk += __shfl_xor_sync(0xffffffffu, pk, o);
-      }
-      if (!l2n) pq = pk = 0.f;
-      const float rq = sRq[r], rk = sRk[r];
-      for (int c2 = lane; c2 < K; c2 += 32) {
-        const float xq = rq * (fQ[r * GS + c2] - qhat(r, c2) * pq);
-        const float xk = rk * (fK[r * GS + c2] - khat(r, c2) * pk);
-        const int64_t off = tok(r, H, h, K) + c2;  // per value head (summed over the group later)
-        static_cast<Tdq *>(a.dq)[off] = from_f32<Tdq>(xq);
-        static_cast<Tdq *>(a.dk)[off] = from_f32<Tdq>(xk);
+#pragma unroll
+      for (int o = 16; o; o >>= 1)
+#pragma unroll
+        for (int y = 0; y < 2; ++y) {
+          pq[y] += __shfl_xor_sync(0xffffffffu, pq[y], o);
+          pk[y] += __shfl_xor_sync(0xffffffffu, pk[y], o);
+        }
+#pragma unroll
+      for (int y = 0; y < 2; ++y) {
+        const int r = r0 + 8 * y;
+        if (r >= len) continue;
+        const float sq = l2n ? pq[y] : 0.f, sk = l2n ? pk[y] : 0.f;
+        const float rq = sRq[r], rk = sRk[r];
+#pragma unroll
+        for (int c2 = lane; c2 < K; c2 += 32) {
+          const float xq = rq * (fQ[r * GS + c2] - qhat(r, c2) * sq);
+          const float xk = rk * (fK[r * GS + c2] - khat(r, c2) * sk);
+          const int64_t off = tok(r, H, h, K) + c2;  // per value head (summed over the group later)
+          static_cast<Tdq *>(a.dq)[off] = from_f32<Tdq>(xq);
+          static_cast<Tdq *>(a.dk)[off] = from_f32<Tdq>(xk);
+        }
       }
     }
 
   // ---- reverse cumsum over the chunk (dG_C onto every row): fG <- the
-  //      gradient of the natural-log gate g of each token
-  if (!*abort_flag && tid < K) {
-    const float GC = sG[(len - 1) * GS + tid];
-    float run = a.dgc[item * K + tid] * tc::ex2(GC);
-    for (int r = 0; r < len; ++r) run += fP[r * GS + tid];
-    for (int r = len - 1; r >= 0; --r) {
-      run += fG[r * GS + tid];
-      fG[r * GS + tid] = run;
+  //      gradient of the natural-log gate g of each token.  Thread = (channel,
+  //      half of the chunk); the halves exchange their sums of fP and fG.
+  {
+    float *sHalf = reinterpret_cast<float *>(R + R_FK + 64 * GS * 4);  // [2 halves][fP, fG][128]
+    const int cch = tid & 127, hb = tid >> 7, rb = 32 * hb;
+    float gv[32];
+    float sp = 0.f, sg = 0.f, dgc0 = 0.f, GC = 0.f;
+    if (!*abort_flag) {
+      if (hb == 0) {
+        dgc0 = a.dgc[item * K + cch];
+        GC = sG[(len - 1) * GS + cch];
+      }
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const bool in = rb + x < len;
+        gv[x] = in ? fG[(rb + x) * GS + cch] : 0.f;
+        sp += in ? fP[(rb + x) * GS + cch] : 0.f;
+      }
+#pragma unroll
+      for (int x = 0; x < 32; ++x) sg += gv[x];
+      sHalf[(2 * hb) * 128 + cch] = sp;
+      sHalf[(2 * hb + 1) * 128 + cch] = sg;
+    }
+    __syncthreads();
+    if (!*abort_flag) {
+      if (hb == 1) {
+        dgc0 = a.dgc[item * K + cch];
+        GC = sG[(len - 1) * GS + cch];
+      }
+      float run = dgc0 * tc::ex2(GC) + sHalf[cch] + sHalf[256 + cch];
+      if (hb == 0) run += sHalf[384 + cch];  // fG of the later half
+#pragma unroll
+      for (int x = 31; x >= 0; --x) {
+        run += gv[x];
+        if (rb + x < len) fG[(rb + x) * GS + cch] = run;
+      }
     }
   }
   __syncthreads();
@@ -648,11 +751,16 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           for (int e = 0; e < 4; ++e) {
             const float dgn = fG[r * GS + c4 + e];
             if (gate) {
+              // t = e^{-|z|}: sigmoid(z) = (z >= 0 ? 1 : t) / (1 + t),
+              // softplus(z) = max(z, 0) + ln(1 + t)
               const float z = xs[e] + bias[e];
-              const float dz = -A_h * dgn / (1.f + expf(-z));
+              const float t = tc::ex2(-fabsf(z) * kLog2e);
+              const float sgm = __fdividef(z >= 0.f ? 1.f : t, 1.f + t);
+              const float spl = fmaxf(z, 0.f) + tc::lg2(1.f + t) * kLn2;
+              const float dz = -A_h * dgn * sgm;
               o[e] = dz;
               dtb[e] += dz;
-              alog = fmaf(-A_h * softplus_f(z), dgn, alog);
+              alog = fmaf(-A_h * spl, dgn, alog);
             } else {
               o[e] = dgn;
             }
