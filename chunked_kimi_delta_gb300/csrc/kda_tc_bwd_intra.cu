@@ -588,9 +588,13 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   float *fG = reinterpret_cast<float *>(R + R_FG), *fQ = reinterpret_cast<float *>(R + R_FQ);
   float *fK = reinterpret_cast<float *>(R + R_FK), *fP = sQF;  // fP [64][128] over sQF / sDF
   if (!*abort_flag) {
+    // every lane works: lane l < 16 and lane l + 16 share row 16 q4 + l, the
+    // upper lane taking columns 8..15 of each 16-column load
+    const int row = 16 * q4 + (lane & 15), up = lane >> 4, s8 = 8 * up;
     float pb = 0.f;
-    const int rI = 16 * (rr >> 4), rJ = 16 * (rr >> 4) + 15;
-    const float br = rv ? sB[rr] : 0.f;
+    const int rI = 16 * (row >> 4), rJ = rI + 15;
+    const float br = sB[row], qd = sQD[row];
+    const bool live = row < len;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int c0 = 64 * hf + 16 * cc;
@@ -601,46 +605,57 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       tc::tmem_ld16(tmem + C_D1 + lanes + c0, dd6);        // row side, dL rows
       tc::tmem_ld16(tmem + C_D7 + lanes + c0, d7);         // column side
       tc::tmem_ld16(tmem + C_D2 + 128 + lanes + c0, dkb);  // A^T dw (kept from phase A)
-      float dqgv[16], dkgv[16];
-      if (rv && rr < len) {
-        const float4 *pq = reinterpret_cast<const float4 *>(a.dqg + tok(rr, H, h, K) + c0);
-        const float4 *pk = reinterpret_cast<const float4 *>(a.dkg + tok(rr, H, h, K) + c0);
+      float dqgv[8], dkgv[8];
+      if (live) {
+        const float4 *pq = reinterpret_cast<const float4 *>(a.dqg + tok(row, H, h, K) + c0 + s8);
+        const float4 *pk = reinterpret_cast<const float4 *>(a.dkg + tok(row, H, h, K) + c0 + s8);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
+        for (int x = 0; x < 2; ++x) {
           const float4 u = pq[x], w = pk[x];
           dqgv[4 * x] = u.x; dqgv[4 * x + 1] = u.y; dqgv[4 * x + 2] = u.z; dqgv[4 * x + 3] = u.w;
           dkgv[4 * x] = w.x; dkgv[4 * x + 1] = w.y; dkgv[4 * x + 2] = w.z; dkgv[4 * x + 3] = w.w;
         }
       }
       tc::tmem_ld_wait();
-      if (rv) {
+      float mq[8], md[8], m7[8], mk[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int cc2 = c0 + e;
-          float oq = 0.f, ok = 0.f, og = 0.f, op = 0.f;
-          if (rr < len) {
-            const float G = sG[rr * GS + cc2], GC = sG[(len - 1) * GS + cc2];
-            const float fq = tc::ex2(G - sG[rI * GS + cc2]);                 // <= 1
-            const float fc = tc::ex2(fminf(sG[rJ * GS + cc2] - G, 0.f));     // <= 1
-            const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
-            const float qh = qhat(rr, cc2), kh = khat(rr, cc2);
-            const float aq = fq * dq6[e], akr = br * fq * dd6[e], akc = fc * d7[e];
-            const float dqg = dqgv[e], dkg = dkgv[e];
-            const float kbf = br * eG, qd = sQD[rr];
-            oq = aq + qd * kh + dqg * scale * eG;
-            ok = akr + akc + qd * qh + dkb[e] * kbf + dkg * ekg;
-            og = qh * aq + kh * akr - kh * akc + dkb[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
-            op = dkg * kh * ekg;
-            pb = fmaf(dkb[e], kh * eG, fmaf(kh, fq * dd6[e], pb));
-          }
-          fQ[rr * GS + cc2] = oq;
-          fK[rr * GS + cc2] = ok;
-          fG[rr * GS + cc2] = og;
-          fP[rr * GS + cc2] = op;
+      for (int e = 0; e < 8; ++e) {
+        const float tq = __shfl_sync(0xffffffffu, dq6[8 + e], lane & 15);
+        const float td = __shfl_sync(0xffffffffu, dd6[8 + e], lane & 15);
+        const float t7 = __shfl_sync(0xffffffffu, d7[8 + e], lane & 15);
+        const float tk = __shfl_sync(0xffffffffu, dkb[8 + e], lane & 15);
+        mq[e] = up ? tq : dq6[e];
+        md[e] = up ? td : dd6[e];
+        m7[e] = up ? t7 : d7[e];
+        mk[e] = up ? tk : dkb[e];
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int cc2 = c0 + s8 + e;
+        float oq = 0.f, ok = 0.f, og = 0.f, op = 0.f;
+        if (live) {
+          const float G = sG[row * GS + cc2], GC = sG[(len - 1) * GS + cc2];
+          const float fq = tc::ex2(G - sG[rI * GS + cc2]);                 // <= 1
+          const float fc = tc::ex2(fminf(sG[rJ * GS + cc2] - G, 0.f));     // <= 1
+          const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
+          const float qh = qhat(row, cc2), kh = khat(row, cc2);
+          const float aq = fq * mq[e], akr = br * fq * md[e], akc = fc * m7[e];
+          const float dqg = dqgv[e], dkg = dkgv[e];
+          const float kbf = br * eG;
+          oq = aq + qd * kh + dqg * scale * eG;
+          ok = akr + akc + qd * qh + mk[e] * kbf + dkg * ekg;
+          og = qh * aq + kh * akr - kh * akc + mk[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
+          op = dkg * kh * ekg;
+          pb = fmaf(mk[e], kh * eG, fmaf(kh, fq * md[e], pb));
         }
+        fQ[row * GS + cc2] = oq;
+        fK[row * GS + cc2] = ok;
+        fG[row * GS + cc2] = og;
+        fP[row * GS + cc2] = op;
       }
     }
-    if (rv) sDB[rr * 4 + 2 + hf] = pb;
+    pb += __shfl_xor_sync(0xffffffffu, pb, 16);
+    if (!up) sDB[row * 4 + 2 + hf] = pb;
   }
   __syncthreads();
 
