@@ -474,7 +474,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     if (!*abort_flag) {
       if (sub == 0)
         for (int i = tid; i < BT * 24; i += NT) {  // [row][192 / 8] 16-byte groups, Q and dL rows
-          const int r = i / 24, g8 = (i % 24) * 8, I = r >> 4, o = seg_off_row(I);
+          // lanes run over rows: their reads of one column fall in different banks
+          const int r = (i & 31) + 32 * ((i >> 5) & 1), g8 = (i >> 6) * 8, I = r >> 4, o = seg_off_row(I);
           float xq[8], xd[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -486,8 +487,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
           st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
         }
-      for (int i = tid; i < KB_BIG * 16; i += NT) {  // [160 rows][128 / 8]
-        const int kr = i >> 4, c8 = (i & 15) * 8;
+      for (int i = tid; i < KB_BIG * 16; i += NT) {  // [160 rows][128 / 8], lanes over rows
+        const int kr = (i & 31) + 32 * ((i >> 5) % 5), c8 = ((i >> 5) / 5) * 8;
         const int I = kr < 16 ? 0 : (kr < 48 ? 1 : (kr < 96 ? 2 : 3));
         const int j = kr - seg_off_row(I), ref = 16 * I;
         float x[8];
@@ -534,8 +535,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   //      operand's hi and lo parts are built together
   for (int part = 0; part < 2; ++part) {
     if (!*abort_flag) {
-      for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8]
-        const int j = i / 24, g8 = (i % 24) * 8, J = j >> 4, o = seg_off_col(J);
+      for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8], lanes over rows
+        const int j = (i & 31) + 32 * ((i >> 5) & 1), g8 = (i >> 6) * 8, J = j >> 4, o = seg_off_col(J);
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -545,8 +546,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         }
         st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
       }
-      for (int i = tid; i < KB_BIG * 16; i += NT) {  // B hi and lo: [160 rows][128 / 8]
-        const int kr = i >> 4, c8 = (i & 15) * 8;
+      for (int i = tid; i < KB_BIG * 16; i += NT) {  // B hi and lo: [160 rows][128 / 8], lanes over rows
+        const int kr = (i & 31) + 32 * ((i >> 5) % 5), c8 = ((i >> 5) / 5) * 8;
         const int J = kr < 64 ? 0 : (kr < 112 ? 1 : (kr < 144 ? 2 : 3));
         const int ii = kr - seg_off_col(J) + 16 * J, ref = 16 * J + 15;
         float xh[8], xl[8];
