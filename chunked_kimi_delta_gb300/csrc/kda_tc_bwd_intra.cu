@@ -70,12 +70,14 @@ constexpr uint32_t R_DVN = 0, R_DW = 16384, R_VB = 32768, R_KB = 49152, R_AT = 6
 constexpr uint32_t R_DO = 73728, R_VN = 90112, R_DA = 106496, R_TT = 114688;
 // phase C / D tiles
 constexpr uint32_t R_AQ = 0, R_AD = 24576, R_BB = 49152;  // M5: A rows (Q, dL), stacked B
+constexpr uint32_t R_BLO = 90112;  // M5: lo part of stacked B rows 0..127 (128-row MN-major tile)
 constexpr uint32_t R_AP = 0, R_BP = 24576, R_BPL = 65536;  // M6: A, stacked B hi, lo (one part at a time)
 // final phase (fp32 [64][GS] each)
 constexpr uint32_t R_FG = 0, R_FQ = 33024, R_FK = 66048;
 constexpr uint32_t SMEM_BYTES = S_R + 122880 + 1024;
 static_assert(S_G + 64 * GS * 4 <= S_QR && S_QR + 64 * QS * 2 <= S_KR && S_KR + 64 * QS * 2 <= S_QF &&
-                  S_QF + 64 * GS * 4 <= S_MISC && S_MISC + 3072 <= S_R && R_FK + 64 * GS * 4 + 2048 <= 122880,
+                  S_QF + 64 * GS * 4 <= S_MISC && S_MISC + 3072 <= S_R && R_FK + 64 * GS * 4 + 2048 <= 122880 &&
+                  R_BB + 160 * 256 <= R_BLO && R_BLO + 128 * 256 <= 122880,
               "shared memory layout");
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns
@@ -377,27 +379,48 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           for (int e = 0; e < 16; ++e)
             sQF[rr * 65 + j0 + e] = (has_do && j0 + e <= rr && rr < len) ? scale * d[e] : 0.f;
       }
-      float pb = 0.f;
+      // -dv_new.beta: every lane works (lane l + 16 takes columns 8..15 of each
+      // 16-column load of row 16 q4 + l); v rows loaded before the TMEM reads
+      {
+        const int row = 16 * q4 + (lane & 15), up = lane >> 4, s8 = 8 * up;
+        const bool live = row < len;
+        uint4 vraw[4];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int v0 = 64 * hf + 16 * cc;
-        __syncwarp();
-        tc::tmem_ld16(tmem + C_D2 + ((uint32_t)(32 * q4) << 16) + v0, d);
-        tc::tmem_ld_wait();
-        if (rv && rr < len) {
-          const __nv_bfloat16 *vr = static_cast<const __nv_bfloat16 *>(a.v) + tok(rr, H, h, V) + v0;
-          const float br = sB[rr];
+        for (int cc = 0; cc < 4; ++cc)
+          vraw[cc] = live ? *reinterpret_cast<const uint4 *>(vin + tok(row, H, h, V) + 64 * hf + 16 * cc + s8)
+                          : make_uint4(0, 0, 0, 0);
+        const float br = sB[row];
+        float pb = 0.f;
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float dvb0 = -d[e], dvb1 = -d[e + 1];
-            const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(vr + e));
-            pb = fmaf(dvb0, vf.x, fmaf(dvb1, vf.y, pb));
-            *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(a.dv) + tok(rr, H, h, V) + v0 + e) =
-                __floats2bfloat162_rn(br * dvb0, br * dvb1);
+        for (int cc = 0; cc < 4; ++cc) {
+          const int v0 = 64 * hf + 16 * cc;
+          __syncwarp();
+          tc::tmem_ld16(tmem + C_D2 + ((uint32_t)(32 * q4) << 16) + v0, d);
+          tc::tmem_ld_wait();
+          float m[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float t = __shfl_sync(0xffffffffu, d[8 + e], lane & 15);
+            m[e] = up ? t : d[e];
+          }
+          if (live) {
+            const uint32_t vw[4] = {vraw[cc].x, vraw[cc].y, vraw[cc].z, vraw[cc].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float dvb0 = -m[2 * e], dvb1 = -m[2 * e + 1];
+              const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vw[e]));
+              pb = fmaf(dvb0, vf.x, fmaf(dvb1, vf.y, pb));
+              const __nv_bfloat162 ob = __floats2bfloat162_rn(br * dvb0, br * dvb1);
+              o[e] = *reinterpret_cast<const uint32_t *>(&ob);
+            }
+            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) + tok(row, H, h, V) + v0 + s8) =
+                make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        pb += __shfl_xor_sync(0xffffffffu, pb, 16);
+        if (!up) sDB[row * 4 + hf] = pb;
       }
-      if (rv) sDB[rr * 4 + hf] = pb;
     }
   }
   tc::tc_fence_before();
@@ -487,17 +510,28 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
           st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
         }
-      for (int i = tid; i < KB_BIG * 16; i += NT) {  // [160 rows][128 / 8], lanes over rows
-        const int kr = (i & 31) + 32 * ((i >> 5) % 5), c8 = ((i >> 5) / 5) * 8;
+      // stacked right operand: the first pass stores the hi part of all 160
+      // rows and the lo part of rows 0..127 (to R_BLO); the second pass only
+      // writes the lo part of rows 128..159 over the hi tile
+      auto build_b = [&](int kr, int c8) {
         const int I = kr < 16 ? 0 : (kr < 48 ? 1 : (kr < 96 ? 2 : 3));
         const int j = kr - seg_off_row(I), ref = 16 * I;
-        float x[8];
+        float x[8], lo[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          x[e] = j < len ? split(khat(j, c8 + e) * tc::ex2(fminf(sG[ref * GS + c8 + e] - sG[j * GS + c8 + e], 126.f)),
-                                 sub == 1)
-                         : 0.f;
+        for (int e = 0; e < 8; ++e) {
+          const float v = j < len ? khat(j, c8 + e) * tc::ex2(fminf(sG[ref * GS + c8 + e] - sG[j * GS + c8 + e], 126.f))
+                                  : 0.f;
+          lo[e] = split(v, true);
+          x[e] = sub ? lo[e] : v;
+        }
         st_bf16x8(R + R_BB, mnmaj_off(KB_BIG, kr, c8), x);
+        if (sub == 0 && kr < 128) st_bf16x8(R + R_BLO, mnmaj_off(128, kr, c8), lo);
+      };
+      if (sub == 0) {
+        for (int i = tid; i < KB_BIG * 16; i += NT)  // [160 rows][128 / 8], lanes over rows
+          build_b((i & 31) + 32 * ((i >> 5) % 5), ((i >> 5) / 5) * 8);
+      } else {
+        for (int i = tid; i < 32 * 16; i += NT) build_b(128 + (i & 31), (i >> 5) * 8);
       }
     }
     tc::fence_proxy_async_smem();
@@ -507,9 +541,11 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       tc::tc_fence_after();
       const uint32_t aq = tc::smem_u32(R + R_AQ), ad = tc::smem_u32(R + R_AD), bb = tc::smem_u32(R + R_BB);
       const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
+      const uint32_t blo = tc::smem_u32(R + R_BLO);
 #pragma unroll
       for (int kk = 0; kk < 10; ++kk) {
-        const uint64_t bd = tc::smem_desc_sw128(bb + kk * 2048, KB_BIG * 128, 1024);
+        const uint64_t bd = (sub == 1 && kk < 8) ? tc::smem_desc_sw128(blo + kk * 2048, 128 * 128, 1024)
+                                                 : tc::smem_desc_sw128(bb + kk * 2048, KB_BIG * 128, 1024);
         tc::mma_bf16(tmem + C_D2, tc::smem_desc_sw128(aq + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
                      sub > 0 || kk > 0);
         tc::mma_bf16(tmem + C_D1, tc::smem_desc_sw128(ad + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), bd, id,
