@@ -222,6 +222,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--bwd-config", default=None,
+                    help="named workload of the bwd line (default: the forward's workload)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -347,7 +349,16 @@ def main():
     if rank == 0 and not args.no_decode:
         result["decode"] = bench_decode(kda, dev, stream, hbm_peak)
     if rank == 0 and not args.no_bwd:
-        result["bwd"] = bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak)
+        if args.bwd_config and args.bwd_config != cfg.name:
+            from chunked_kimi_delta_gb300.inputs import CONFIGS, make_inputs
+            bcfg = CONFIGS[args.bwd_config]
+            if bcfg.seq_lens or bcfg.varlen_count or bcfg.dtype != "bf16":
+                raise SystemExit("--bwd-config takes a fixed-length bf16 workload")
+            binp = make_inputs(bcfg, device=dev)
+            result["bwd"] = bench_bwd(kda, lib, bcfg, binp, binp.get("initial_state"), dev, stream, hbm_peak)
+            del binp
+        else:
+            result["bwd"] = bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak)
     if rank == 0 and not args.no_bwd and not args.no_segment:
         result["segment_mode_bwd"] = bench_segment_bwd(kda, dev, stream)
     if not args.no_e2e:
@@ -440,9 +451,9 @@ def bwd_alg_bytes_per_token_head(dk, dv):
 
 
 def bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak, steps=5, warmup=3):
-    """Backward of the same workload (B=4, T=8192, H=32, d=128, bf16): all
-    gradients (q, k, v, gate input, beta logits, a_log, dt_bias, initial
-    state) of <d_out, o> + <d_final, final_state>."""
+    """Backward of a workload (by default the forward's: B=4, T=8192, H=32,
+    d=128, bf16): all gradients (q, k, v, gate input, beta logits, a_log,
+    dt_bias, initial state) of <d_out, o> + <d_final, final_state>."""
     import torch
     from chunked_kimi_delta_gb300.inputs import make_cotangents
     cot = make_cotangents(cfg, inp, device=dev)
@@ -471,12 +482,15 @@ def bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak, steps=5, warmup=3):
     ms = statistics.median(a.elapsed_time(e) for a, e in evs)
     th = cfg.B * cfg.T * H
     nbytes = bwd_alg_bytes_per_token_head(K, V) * th + 3 * 4 * K * V * cfg.B * H
+    in_bytes = sum(t.numel() * t.element_size() for t in (inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                                          cot["d_out"]))
     gbs = nbytes / (ms / 1e3) / 1e9
     return {"workload": f"{cfg.name} backward: B={cfg.B} T={cfg.T} H={H} d={K}, bf16 q/k/v/d_out and "
                         f"dq/dk/dv, fp32 gate/beta gradients, dA_log, ddt_bias, initial-state gradient",
             "tokens_per_s": cfg.B * cfg.T / (ms / 1e3), "ms_per_step": ms, "steps": steps,
             "launches_per_step": 6,
-            "l2_policy": "inputs (1.6 GB) larger than L2 (129 MB); no flush",
+            "l2_policy": f"inputs ({in_bytes / 1e9:.2f} GB) " + ("larger than L2 (129 MB); no flush"
+                                                                 if in_bytes > 129e6 else "fit in L2: no flush"),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "alg_bytes_per_launch": nbytes,
                          "scope": "whole backward call"}}

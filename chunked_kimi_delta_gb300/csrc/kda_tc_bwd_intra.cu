@@ -45,16 +45,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // shared memory (bytes from a 1024-aligned base)
-// Row strides padded so that the 16 rows a warp's readout lanes hold fall in
-// different banks.
-constexpr int GS = 129;                // floats per row of G and of the final fp32 arrays
+// Row strides: fp32 rows of 132 floats (528 bytes, 16-byte aligned) are read
+// eight columns at a time by lanes that run over rows, which puts the eight
+// lanes of each 128-bit access phase in different banks; the bf16 rows of
+// 132 elements (264 bytes) are read as 8-byte vectors.
+constexpr int GS = 132;                // floats per row of G and of the final fp32 arrays
 constexpr int QS = 132;                // bf16 per row of the raw q / k copies (264 bytes)
+constexpr int FS = 66;                 // floats per row of Q and dL (two rows = one GS row)
 constexpr uint32_t S_G = 0;            // fp32 G [64][GS], log2 units (chunk-local cumsum)
-constexpr uint32_t S_QR = 33280;       // bf16 raw q rows [64][QS]
-constexpr uint32_t S_KR = 50176;       // bf16 raw k rows [64][QS]
-constexpr uint32_t S_QF = 67072;       // fp32 Q [64][65]
-constexpr uint32_t S_DF = 83712;       // fp32 dL [64][65]
-constexpr uint32_t S_MISC = 100352;
+constexpr uint32_t S_QR = 33792;       // bf16 raw q rows [64][QS]
+constexpr uint32_t S_KR = 50688;       // bf16 raw k rows [64][QS]
+constexpr uint32_t S_QF = 67584;       // fp32 Q [64][FS]
+constexpr uint32_t S_DF = 84480;       // fp32 dL [64][FS]
+constexpr uint32_t S_MISC = 101376;
 constexpr uint32_t M_BETA = S_MISC;          // fp32 [64]
 constexpr uint32_t M_RQ = S_MISC + 256;      // fp32 [64] rstd of q
 constexpr uint32_t M_RK = S_MISC + 512;      // fp32 [64] rstd of k
@@ -64,7 +67,7 @@ constexpr uint32_t M_SRED = S_MISC + 2816;   // fp32 [8]
 constexpr uint32_t M_BAR = S_MISC + 2880;    // 10 mbarriers
 constexpr uint32_t M_TSLOT = S_MISC + 3008;
 constexpr int NBAR = 10;
-constexpr uint32_t S_R = 103424;       // reused region (120 KB)
+constexpr uint32_t S_R = 104448;       // reused region (120 KB)
 // phase A / B tiles (offsets from S_R)
 constexpr uint32_t R_DVN = 0, R_DW = 16384, R_VB = 32768, R_KB = 49152, R_AT = 65536;
 constexpr uint32_t R_DO = 73728, R_VN = 90112, R_DA = 106496, R_TT = 114688;
@@ -73,12 +76,15 @@ constexpr uint32_t R_AQ = 0, R_AD = 24576, R_BB = 49152;  // M5: A rows (Q, dL),
 constexpr uint32_t R_BLO = 90112;  // M5: lo part of stacked B rows 0..127 (128-row MN-major tile)
 constexpr uint32_t R_AP = 0, R_BP = 24576, R_BPL = 65536;  // M6: A, stacked B hi, lo (one part at a time)
 // final phase (fp32 [64][GS] each)
-constexpr uint32_t R_FG = 0, R_FQ = 33024, R_FK = 66048;
+constexpr uint32_t R_FG = 0, R_FQ = 33792, R_FK = 67584;
 constexpr uint32_t SMEM_BYTES = S_R + 122880 + 1024;
 static_assert(S_G + 64 * GS * 4 <= S_QR && S_QR + 64 * QS * 2 <= S_KR && S_KR + 64 * QS * 2 <= S_QF &&
-                  S_QF + 64 * GS * 4 <= S_MISC && S_MISC + 3072 <= S_R && R_FK + 64 * GS * 4 + 2048 <= 122880 &&
+                  S_QF + 64 * FS * 4 == S_DF && S_DF + 64 * FS * 4 <= S_MISC && 2 * FS == GS &&
+                  S_MISC + 3072 <= S_R && S_R % 1024 == 0 && R_FQ >= 64 * GS * 4 &&
+                  R_FK >= R_FQ + 64 * GS * 4 && R_FK + 64 * GS * 4 + 2048 <= 122880 &&
                   R_BB + 160 * 256 <= R_BLO && R_BLO + 128 * 256 <= 122880,
               "shared memory layout");
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory of one CTA");
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns
 constexpr uint32_t C_D2 = 0;      // [-dvb | dkb] (256); later D6Q in 0..127
@@ -95,6 +101,27 @@ __device__ __forceinline__ int seg_off_col(int J) { return 64 * J - 8 * J * (J -
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                : "memory");
+}
+
+// Eight consecutive fp32 (16-byte aligned) / bf16 (8-byte aligned) shared
+// memory values.
+__device__ __forceinline__ void lds_f8(const float *p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void sts_f8(float *p, const float (&x)[8]) {
+  reinterpret_cast<float4 *>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4 *>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+__device__ __forceinline__ void lds_bf8(const __nv_bfloat16 *p, float (&x)[8]) {
+  const uint2 a = reinterpret_cast<const uint2 *>(p)[0], b = reinterpret_cast<const uint2 *>(p)[1];
+  const uint32_t w[4] = {a.x, a.y, b.x, b.y};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
+  }
 }
 
 // bf16 K-major / MN-major SW128 element stores
@@ -269,8 +296,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     }
 #pragma unroll
     for (int x = 0; x < 8; ++x)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sG[(8 * warp + x) * GS + gc4 + e] = Gl[x][e] + pre[e];
+      *reinterpret_cast<float4 *>(sG + (8 * warp + x) * GS + gc4) =
+          make_float4(Gl[x][0] + pre[0], Gl[x][1] + pre[1], Gl[x][2] + pre[2], Gl[x][3] + pre[3]);
   }
   __syncthreads();
   auto qhat = [&](int r, int cc) { return __bfloat162float(sQR[r * QS + cc]) * sRq[r]; };
@@ -290,9 +317,12 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       vb[2 * e] = -br * f.x;
       vb[2 * e + 1] = -br * f.y;
     }
+    float kr8[8], g8v[8];
+    lds_bf8(sKR + r * QS + c8, kr8);
+    lds_f8(sG + r * GS + c8, g8v);
+    const float rk = sRk[r];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      kb[e] = r < len ? khat(r, c8 + e) * br * tc::ex2(sG[r * GS + c8 + e]) : 0.f;
+    for (int e = 0; e < 8; ++e) kb[e] = r < len ? kr8[e] * rk * br * tc::ex2(g8v[e]) : 0.f;
     st_bf16x8(R + R_VB, kmaj_off(64, r, c8), vb);
     st_bf16x8(R + R_KB, kmaj_off(64, r, c8), kb);
   }
@@ -377,7 +407,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         if (rv)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            sQF[rr * 65 + j0 + e] = (has_do && j0 + e <= rr && rr < len) ? scale * d[e] : 0.f;
+            sQF[rr * FS + j0 + e] = (has_do && j0 + e <= rr && rr < len) ? scale * d[e] : 0.f;
       }
       // -dv_new.beta: every lane works (lane l + 16 takes columns 8..15 of each
       // 16-column load of row 16 q4 + l); v rows loaded before the TMEM reads
@@ -425,7 +455,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (tid < BT) sQD[tid] = sQF[tid * 65 + tid];
+  if (tid < BT) sQD[tid] = sQF[tid * FS + tid];
 
   // ---- phase B: T = A^T dA, then dL = -T A^T
   if (!*abort_flag && tid == 0) {
@@ -480,7 +510,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       tc::tmem_ld_wait();
       if (rv)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sDF[rr * 65 + j0 + e] = (j0 + e < rr && rr < len) ? -d[e] : 0.f;
+        for (int e = 0; e < 16; ++e) sDF[rr * FS + j0 + e] = (j0 + e < rr && rr < len) ? -d[e] : 0.f;
     }
   }
   tc::tc_fence_before();
@@ -504,8 +534,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           for (int e = 0; e < 8; ++e) {
             const int j = g8 + e - o;  // token of this K slot in row r's segment
             const bool in = j >= 0 && j < 16 * (I + 1);
-            xq[e] = (in && j < r) ? sQF[r * 65 + j] : 0.f;  // strictly below the diagonal
-            xd[e] = in ? sDF[r * 65 + j] : 0.f;
+            xq[e] = (in && j < r) ? sQF[r * FS + j] : 0.f;  // strictly below the diagonal
+            xd[e] = in ? sDF[r * FS + j] : 0.f;
           }
           st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
           st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
@@ -516,11 +546,14 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       auto build_b = [&](int kr, int c8) {
         const int I = kr < 16 ? 0 : (kr < 48 ? 1 : (kr < 96 ? 2 : 3));
         const int j = kr - seg_off_row(I), ref = 16 * I;
-        float x[8], lo[8];
+        float x[8], lo[8], kr8[8], gr[8], gj[8];
+        lds_bf8(sKR + j * QS + c8, kr8);
+        lds_f8(sG + ref * GS + c8, gr);
+        lds_f8(sG + j * GS + c8, gj);
+        const float rk = sRk[j];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float v = j < len ? khat(j, c8 + e) * tc::ex2(fminf(sG[ref * GS + c8 + e] - sG[j * GS + c8 + e], 126.f))
-                                  : 0.f;
+          const float v = j < len ? kr8[e] * rk * tc::ex2(fminf(gr[e] - gj[e], 126.f)) : 0.f;
           lo[e] = split(v, true);
           x[e] = sub ? lo[e] : v;
         }
@@ -578,7 +611,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         for (int e = 0; e < 8; ++e) {
           const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
           const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len && ii > j;
-          x[e] = in ? (part == 0 ? sDF[ii * 65 + j] : sQF[ii * 65 + j]) : 0.f;
+          x[e] = in ? (part == 0 ? sDF[ii * FS + j] : sQF[ii * FS + j]) : 0.f;
         }
         st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
       }
@@ -586,11 +619,15 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         const int kr = (i & 31) + 32 * ((i >> 5) % 5), c8 = ((i >> 5) / 5) * 8;
         const int J = kr < 64 ? 0 : (kr < 112 ? 1 : (kr < 144 ? 2 : 3));
         const int ii = kr - seg_off_col(J) + 16 * J, ref = 16 * J + 15;
-        float xh[8], xl[8];
+        float xh[8], xl[8], raw[8], gi[8], gr[8];
+        lds_bf8((part == 0 ? sKR : sQR) + ii * QS + c8, raw);
+        lds_f8(sG + ii * GS + c8, gi);
+        lds_f8(sG + ref * GS + c8, gr);
+        const float rs = part == 0 ? sRk[ii] : sRq[ii], bs = sB[ii];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float f = tc::ex2(fminf(sG[ii * GS + c8 + e] - sG[ref * GS + c8 + e], 126.f));
-          const float x = ii < len ? (part == 0 ? sB[ii] * khat(ii, c8 + e) : qhat(ii, c8 + e)) * f : 0.f;
+          const float f = tc::ex2(fminf(gi[e] - gr[e], 126.f));
+          const float x = ii < len ? (part == 0 ? bs * (raw[e] * rs) : raw[e] * rs) * f : 0.f;
           xh[e] = x;
           xl[e] = split(x, true);
         }
@@ -667,28 +704,47 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         mk[e] = up ? tk : dkb[e];
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int cc2 = c0 + s8 + e;
-        float oq = 0.f, ok = 0.f, og = 0.f, op = 0.f;
+      for (int e4 = 0; e4 < 8; e4 += 4) {
+        const int cb = c0 + s8 + e4;  // first of this step's four columns
+        float oq[4] = {0.f, 0.f, 0.f, 0.f}, ok[4] = {0.f, 0.f, 0.f, 0.f};
+        float og[4] = {0.f, 0.f, 0.f, 0.f}, op[4] = {0.f, 0.f, 0.f, 0.f};
         if (live) {
-          const float G = sG[row * GS + cc2], GC = sG[(len - 1) * GS + cc2];
-          const float fq = tc::ex2(G - sG[rI * GS + cc2]);                 // <= 1
-          const float fc = tc::ex2(fminf(sG[rJ * GS + cc2] - G, 0.f));     // <= 1
-          const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
-          const float qh = qhat(row, cc2), kh = khat(row, cc2);
-          const float aq = fq * mq[e], akr = br * fq * md[e], akc = fc * m7[e];
-          const float dqg = dqgv[e], dkg = dkgv[e];
-          const float kbf = br * eG;
-          oq = aq + qd * kh + dqg * scale * eG;
-          ok = akr + akc + qd * qh + mk[e] * kbf + dkg * ekg;
-          og = qh * aq + kh * akr - kh * akc + mk[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
-          op = dkg * kh * ekg;
-          pb = fmaf(mk[e], kh * eG, fmaf(kh, fq * md[e], pb));
+          const float4 G4 = *reinterpret_cast<const float4 *>(sG + row * GS + cb);
+          const float4 C4 = *reinterpret_cast<const float4 *>(sG + (len - 1) * GS + cb);
+          const float4 I4 = *reinterpret_cast<const float4 *>(sG + rI * GS + cb);
+          const float4 J4 = *reinterpret_cast<const float4 *>(sG + rJ * GS + cb);
+          const uint2 qr = *reinterpret_cast<const uint2 *>(sQR + row * QS + cb);
+          const uint2 kr = *reinterpret_cast<const uint2 *>(sKR + row * QS + cb);
+          const float Gv[4] = {G4.x, G4.y, G4.z, G4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
+          const float Iv[4] = {I4.x, I4.y, I4.z, I4.w}, Jv[4] = {J4.x, J4.y, J4.z, J4.w};
+          const float2 q01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr.x));
+          const float2 q23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr.y));
+          const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.x));
+          const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.y));
+          const float qv[4] = {q01.x, q01.y, q23.x, q23.y}, kv4[4] = {k01.x, k01.y, k23.x, k23.y};
+          const float rq = sRq[row], rk = sRk[row];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int e = e4 + x;
+            const float G = Gv[x], GC = Cv[x];
+            const float fq = tc::ex2(G - Iv[x]);                 // <= 1
+            const float fc = tc::ex2(fminf(Jv[x] - G, 0.f));     // <= 1
+            const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
+            const float qh = qv[x] * rq, kh = kv4[x] * rk;
+            const float aq = fq * mq[e], akr = br * fq * md[e], akc = fc * m7[e];
+            const float dqg = dqgv[e], dkg = dkgv[e];
+            const float kbf = br * eG;
+            oq[x] = aq + qd * kh + dqg * scale * eG;
+            ok[x] = akr + akc + qd * qh + mk[e] * kbf + dkg * ekg;
+            og[x] = qh * aq + kh * akr - kh * akc + mk[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
+            op[x] = dkg * kh * ekg;
+            pb = fmaf(mk[e], kh * eG, fmaf(kh, fq * md[e], pb));
+          }
         }
-        fQ[row * GS + cc2] = oq;
-        fK[row * GS + cc2] = ok;
-        fG[row * GS + cc2] = og;
-        fP[row * GS + cc2] = op;
+        *reinterpret_cast<float4 *>(fQ + row * GS + cb) = make_float4(oq[0], oq[1], oq[2], oq[3]);
+        *reinterpret_cast<float4 *>(fK + row * GS + cb) = make_float4(ok[0], ok[1], ok[2], ok[3]);
+        *reinterpret_cast<float4 *>(fG + row * GS + cb) = make_float4(og[0], og[1], og[2], og[3]);
+        *reinterpret_cast<float4 *>(fP + row * GS + cb) = make_float4(op[0], op[1], op[2], op[3]);
       }
     }
     pb += __shfl_xor_sync(0xffffffffu, pb, 16);
@@ -799,9 +855,11 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         if (r < len) {
           const float xs[4] = {gx[m].x, gx[m].y, gx[m].z, gx[m].w};
           float o[4];
+          const float4 dg4 = *reinterpret_cast<const float4 *>(fG + r * GS + c4);
+          const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float dgn = fG[r * GS + c4 + e];
+            const float dgn = dgv[e];
             if (gate) {
               // t = e^{-|z|}: sigmoid(z) = (z >= 0 ? 1 : t) / (1 + t),
               // softplus(z) = max(z, 0) + ln(1 + t)
