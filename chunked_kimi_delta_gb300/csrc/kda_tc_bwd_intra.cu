@@ -124,6 +124,14 @@ __device__ __forceinline__ void lds_bf8(const __nv_bfloat16 *p, float (&x)[8]) {
   }
 }
 
+// Four consecutive outputs (16-byte aligned fp32 / 8-byte aligned bf16).
+__device__ __forceinline__ void st4(float *p, const float (&x)[4]) {
+  *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, const float (&x)[4]) {
+  *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]));
+}
+
 // bf16 K-major / MN-major SW128 element stores
 __device__ __forceinline__ void st_bf16x8(uint8_t *tile, uint32_t off, const float (&x)[8]) {
   *reinterpret_cast<uint4 *>(tile + off) =
@@ -752,20 +760,46 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   }
   __syncthreads();
 
-  // ---- L2-norm backward: dx = r (dx^ - x^ (x^ . dx^)), one warp per row,
-  //      two rows (r, r + 8) at a time
-  if (!*abort_flag)
+  // global inputs of the last two passes, loaded ahead of them: the chunk-end
+  // gate gradient term of this thread's channel and the gate input rows
+  const int gc4b = (tid & 31) * 4, grg = tid >> 5;  // gate pass: channels gc4b .., rows grg + 8 m
+  float dgc0 = 0.f;
+  float4 gxg[8];
+  {
+    const bool go = !*abort_flag;
+    if (go) dgc0 = a.dgc[item * K + (tid & 127)];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int r = grg + 8 * m;
+      gxg[m] = (go && gate && r < len) ? *reinterpret_cast<const float4 *>(a.g + tok(r, H, h, K) + gc4b)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  // ---- L2-norm backward: dx = r (dx^ - x^ (x^ . dx^)), one warp per row
+  //      (lane = four consecutive channels), two rows (r, r + 8) at a time
+  if (!*abort_flag) {
+    const int c4n = 4 * lane;
     for (int r0 = warp; r0 < len; r0 += 16) {
-      float pq[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
+      float xq[2][4], xk[2][4], gq[2][4], gk[2][4], pq[2], pk[2];
 #pragma unroll
       for (int y = 0; y < 2; ++y) {
-        const int r = r0 + 8 * y;
-        if (r < len)
-#pragma unroll
-          for (int c2 = lane; c2 < K; c2 += 32) {
-            pq[y] = fmaf(qhat(r, c2), fQ[r * GS + c2], pq[y]);
-            pk[y] = fmaf(khat(r, c2), fK[r * GS + c2], pk[y]);
-          }
+        const int r = r0 + 8 * y < len ? r0 + 8 * y : r0;  // a row past the end reads row r0 (unused)
+        const uint2 qr = *reinterpret_cast<const uint2 *>(sQR + r * QS + c4n);
+        const uint2 kr = *reinterpret_cast<const uint2 *>(sKR + r * QS + c4n);
+        const float4 fq4 = *reinterpret_cast<const float4 *>(fQ + r * GS + c4n);
+        const float4 fk4 = *reinterpret_cast<const float4 *>(fK + r * GS + c4n);
+        const float2 q01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr.x));
+        const float2 q23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr.y));
+        const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.x));
+        const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.y));
+        const float rq = sRq[r], rk = sRk[r];
+        xq[y][0] = q01.x * rq; xq[y][1] = q01.y * rq; xq[y][2] = q23.x * rq; xq[y][3] = q23.y * rq;
+        xk[y][0] = k01.x * rk; xk[y][1] = k01.y * rk; xk[y][2] = k23.x * rk; xk[y][3] = k23.y * rk;
+        gq[y][0] = fq4.x; gq[y][1] = fq4.y; gq[y][2] = fq4.z; gq[y][3] = fq4.w;
+        gk[y][0] = fk4.x; gk[y][1] = fk4.y; gk[y][2] = fk4.z; gk[y][3] = fk4.w;
+        pq[y] = fmaf(xq[y][3], gq[y][3], fmaf(xq[y][2], gq[y][2], fmaf(xq[y][1], gq[y][1], xq[y][0] * gq[y][0])));
+        pk[y] = fmaf(xk[y][3], gk[y][3], fmaf(xk[y][2], gk[y][2], fmaf(xk[y][1], gk[y][1], xk[y][0] * gk[y][0])));
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1)
@@ -780,16 +814,18 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         if (r >= len) continue;
         const float sq = l2n ? pq[y] : 0.f, sk = l2n ? pk[y] : 0.f;
         const float rq = sRq[r], rk = sRk[r];
+        float oq[4], ok[4];
 #pragma unroll
-        for (int c2 = lane; c2 < K; c2 += 32) {
-          const float xq = rq * (fQ[r * GS + c2] - qhat(r, c2) * sq);
-          const float xk = rk * (fK[r * GS + c2] - khat(r, c2) * sk);
-          const int64_t off = tok(r, H, h, K) + c2;  // per value head (summed over the group later)
-          static_cast<Tdq *>(a.dq)[off] = from_f32<Tdq>(xq);
-          static_cast<Tdq *>(a.dk)[off] = from_f32<Tdq>(xk);
+        for (int x = 0; x < 4; ++x) {
+          oq[x] = rq * (gq[y][x] - xq[y][x] * sq);
+          ok[x] = rk * (gk[y][x] - xk[y][x] * sk);
         }
+        const int64_t off = tok(r, H, h, K) + c4n;  // per value head (summed over the group later)
+        st4(static_cast<Tdq *>(a.dq) + off, oq);
+        st4(static_cast<Tdq *>(a.dk) + off, ok);
       }
     }
+  }
 
   // ---- reverse cumsum over the chunk (dG_C onto every row): fG <- the
   //      gradient of the natural-log gate g of each token.  Thread = (channel,
@@ -798,12 +834,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     float *sHalf = reinterpret_cast<float *>(R + R_FK + 64 * GS * 4);  // [2 halves][fP, fG][128]
     const int cch = tid & 127, hb = tid >> 7, rb = 32 * hb;
     float gv[32];
-    float sp = 0.f, sg = 0.f, dgc0 = 0.f, GC = 0.f;
+    float sp = 0.f, sg = 0.f;
     if (!*abort_flag) {
-      if (hb == 0) {
-        dgc0 = a.dgc[item * K + cch];
-        GC = sG[(len - 1) * GS + cch];
-      }
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
         const bool in = rb + x < len;
@@ -817,10 +849,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     }
     __syncthreads();
     if (!*abort_flag) {
-      if (hb == 1) {
-        dgc0 = a.dgc[item * K + cch];
-        GC = sG[(len - 1) * GS + cch];
-      }
+      const float GC = sG[(len - 1) * GS + cch];
       float run = dgc0 * tc::ex2(GC) + sHalf[cch] + sHalf[256 + cch];
       if (hb == 0) run += sHalf[384 + cch];  // fG of the later half
 #pragma unroll
@@ -836,24 +865,17 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   float alog = 0.f;
   float *sPart = fQ;  // [8][128] ddt_bias parts (fQ is free after the norm backward)
   {
-    const int c4 = (tid & 31) * 4, rg = tid >> 5;
+    const int c4 = gc4b, rg = grg;
     float dtb[4] = {0.f, 0.f, 0.f, 0.f}, bias[4] = {0.f, 0.f, 0.f, 0.f};
     if (gate && gp.dt_bias)
 #pragma unroll
       for (int e = 0; e < 4; ++e) bias[e] = gp.dt_bias[h * K + c4 + e];
     if (!*abort_flag) {
-      float4 gx[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int r = rg + 8 * m;
-        gx[m] = (gate && r < len) ? *reinterpret_cast<const float4 *>(a.g + tok(r, H, h, K) + c4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         const int r = rg + 8 * m;
         if (r < len) {
-          const float xs[4] = {gx[m].x, gx[m].y, gx[m].z, gx[m].w};
+          const float xs[4] = {gxg[m].x, gxg[m].y, gxg[m].z, gxg[m].w};
           float o[4];
           const float4 dg4 = *reinterpret_cast<const float4 *>(fG + r * GS + c4);
           const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
