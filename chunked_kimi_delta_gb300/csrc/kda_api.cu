@@ -735,20 +735,21 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
   const bool tc = use_tc(&b->fwd);
   size_t o = tc ? tc_plan(p.f).total : p.f.total;
   p.off_h = p.off_dhn = p.off_himg = p.off_vnimg = p.off_dhimg = p.off_dvimg = p.off_dwimg = 0;
+  p.off_vn = p.off_dvn = p.off_dw = 0;
   if (tc) {  // states and state gradients travel as bf16 operand-tile images
     p.off_himg = o;  o = align256(o + ch * 32768);
     p.off_vnimg = o; o = align256(o + ch * 16384);
     p.off_dhimg = o; o = align256(o + ch * 32768);
     p.off_dvimg = o; o = align256(o + ch * 16384);
     p.off_dwimg = o; o = align256(o + ch * 16384);
-  } else {
+  } else {  // fp32 states, state gradients, v_new and its gradient, dw (CUDA-core path only)
     p.off_h = o;     o = align256(o + 4 * ch * K * V);
     p.off_dhn = o;   o = align256(o + 4 * ch * K * V);
+    p.off_vn = o;    o = align256(o + 4 * th * V);
+    p.off_dvn = o;   o = align256(o + 4 * th * V);
+    p.off_dw = o;    o = align256(o + 4 * th * K);
   }
-  p.off_vn = o;    o = align256(o + 4 * th * V);
-  p.off_dvn = o;   o = align256(o + 4 * th * V);
   p.off_dqg = o;   o = align256(o + 4 * th * K);
-  p.off_dw = o;    o = align256(o + 4 * th * K);
   p.off_dkg = o;   o = align256(o + 4 * th * K);
   p.off_dgc = o;   o = align256(o + 4 * ch * K);
   p.off_palog = o; o = align256(o + 4 * ch);
@@ -887,7 +888,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
       tcp::ChainArgs ca{};
       ca.pkg = pkg;
       ca.initial_state = init;
-      ca.v_new_out = f32(p.off_vn);
+      ca.v_new_out = nullptr;  // v_new travels as the bf16 tile image
       ca.h_img = reinterpret_cast<uint8_t *>(ws + p.off_himg);
       ca.vn_img = reinterpret_cast<uint8_t *>(ws + p.off_vnimg);
       ca.err = err;
@@ -922,9 +923,11 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
       l.aqk = f32(p.f.off_aqk); l.gc = f32(p.f.off_gc);
     }
     l.h = tc ? nullptr : f32(p.off_h);
-    l.vn = f32(p.off_vn);
+    l.vn = tc ? nullptr : f32(p.off_vn);
     l.dhn = tc ? nullptr : f32(p.off_dhn);
-    l.dvn = f32(p.off_dvn); l.dqg = f32(p.off_dqg); l.dw = f32(p.off_dw);
+    l.dvn = tc ? nullptr : f32(p.off_dvn);
+    l.dw = tc ? nullptr : f32(p.off_dw);
+    l.dqg = f32(p.off_dqg);
     l.dkg = f32(p.off_dkg); l.dgc = f32(p.off_dgc);
     l.part_alog = f32(p.off_palog); l.part_dtb = f32(p.off_pdtb);
     l.dqv = p.off_dqv ? f32(p.off_dqv) : nullptr;
