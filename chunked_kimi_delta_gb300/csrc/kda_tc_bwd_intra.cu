@@ -103,15 +103,11 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
                : "memory");
 }
 
-// Eight consecutive fp32 (16-byte aligned) / bf16 (8-byte aligned) shared
-// memory values.
+// Eight consecutive fp32 (16-byte aligned) / bf16 (8-byte aligned) values
+// from shared memory.
 __device__ __forceinline__ void lds_f8(const float *p, float (&x)[8]) {
   const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void sts_f8(float *p, const float (&x)[8]) {
-  reinterpret_cast<float4 *>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
-  reinterpret_cast<float4 *>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
 __device__ __forceinline__ void lds_bf8(const __nv_bfloat16 *p, float (&x)[8]) {
   const uint2 a = reinterpret_cast<const uint2 *>(p)[0], b = reinterpret_cast<const uint2 *>(p)[1];
