@@ -96,7 +96,6 @@ constexpr uint32_t KB_BIG = 160;  // stacked segments
 __device__ __forceinline__ int seg_off_row(int I) { return 8 * I * (I + 1); }        // 0, 16, 48, 96
 __device__ __forceinline__ int seg_off_col(int J) { return 64 * J - 8 * J * (J - 1); } // 0, 64, 112, 144
 
-
 // Bulk prefetch into L2 (16-byte aligned address, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
