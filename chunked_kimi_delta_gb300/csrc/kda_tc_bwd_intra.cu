@@ -409,8 +409,10 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         }
         if (rv)
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            sQF[rr * FS + j0 + e] = (has_do && j0 + e <= rr && rr < len) ? scale * d[e] : 0.f;
+          for (int e = 0; e < 16; e += 2)  // rows of FS floats are 8-byte aligned
+            *reinterpret_cast<float2 *>(sQF + rr * FS + j0 + e) =
+                make_float2((has_do && j0 + e <= rr && rr < len) ? scale * d[e] : 0.f,
+                            (has_do && j0 + e + 1 <= rr && rr < len) ? scale * d[e + 1] : 0.f);
       }
       // -dv_new.beta: every lane works (lane l + 16 takes columns 8..15 of each
       // 16-column load of row 16 q4 + l); v rows loaded before the TMEM reads
@@ -513,7 +515,9 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       tc::tmem_ld_wait();
       if (rv)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sDF[rr * FS + j0 + e] = (j0 + e < rr && rr < len) ? -d[e] : 0.f;
+        for (int e = 0; e < 16; e += 2)
+          *reinterpret_cast<float2 *>(sDF + rr * FS + j0 + e) =
+              make_float2((j0 + e < rr && rr < len) ? -d[e] : 0.f, (j0 + e + 1 < rr && rr < len) ? -d[e + 1] : 0.f);
     }
   }
   tc::tc_fence_before();
@@ -533,12 +537,23 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           // lanes run over rows: their reads of one column fall in different banks
           const int r = (i & 31) + 32 * ((i >> 5) & 1), g8 = (i >> 6) * 8, I = r >> 4, o = seg_off_row(I);
           float xq[8], xd[8];
+          // tokens g8 - o .. g8 - o + 7 of row r's segment: the whole group lies
+          // inside the segment or outside it (o and the segment length are
+          // multiples of 8)
+          const int jb = g8 - o;
+          if (jb >= 0 && jb < 16 * (I + 1)) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = g8 + e - o;  // token of this K slot in row r's segment
-            const bool in = j >= 0 && j < 16 * (I + 1);
-            xq[e] = (in && j < r) ? sQF[r * FS + j] : 0.f;  // strictly below the diagonal
-            xd[e] = in ? sDF[r * FS + j] : 0.f;
+            for (int e = 0; e < 8; e += 2) {
+              const float2 qv2 = *reinterpret_cast<const float2 *>(sQF + r * FS + jb + e);
+              const float2 dv2 = *reinterpret_cast<const float2 *>(sDF + r * FS + jb + e);
+              xq[e] = jb + e < r ? qv2.x : 0.f;  // strictly below the diagonal
+              xq[e + 1] = jb + e + 1 < r ? qv2.y : 0.f;
+              xd[e] = dv2.x;
+              xd[e + 1] = dv2.y;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xq[e] = xd[e] = 0.f;
           }
           st_bf16x8(R + R_AQ, kmaj_off(64, r, g8), xq);
           st_bf16x8(R + R_AD, kmaj_off(64, r, g8), xd);
