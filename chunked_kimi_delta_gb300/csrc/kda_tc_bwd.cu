@@ -312,15 +312,20 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
 // v_new / -dv_new tiles (K = tokens) and the TMA dO tile as K-major A.
 // ---------------------------------------------------------------------------
 constexpr uint32_t T_H = 0, T_DH = 32768, T_DV = 65536, T_VN = 81920, T_DO = 98304;
-constexpr uint32_t T_BAR = 114688;
-constexpr uint32_t T_SMEM = T_BAR + 64 + 1024;
+constexpr uint32_t T_TILES = 114688;
+// Two CTAs per SM: 2 x (dynamic + 1 KB reserved) must fit the SM's 228 KB, so
+// the dynamic size is the tiles plus the 1 KB alignment allowance only; the
+// 64 bytes of barriers go below the 1024-aligned tiles when the alignment gap
+// holds them, else above the tiles (then the gap is under 64 bytes).
+constexpr uint32_t T_SMEM = T_TILES + 1024;
+static_assert(2 * (T_SMEM + 1024) <= 233472, "two CTAs per SM");
 constexpr uint32_t T_TMEM = 256;
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT, 2)
 tc_bwd_state_kernel(const __grid_constant__ CUtensorMap map_do, BwdStateArgs a, SeqInfo s, int H) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(sm + T_BAR);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm - smem_raw >= 64 ? sm - 64 : sm + T_TILES);
   uint64_t *bar1 = full + 1, *bar2 = full + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(full + 3);
   volatile uint32_t *abort_flag = tslot + 1;
