@@ -172,6 +172,22 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _on_device(*ts):
+    """The calls that launch kernels dereference every pointer on the GPU:
+    their tensors must be CUDA tensors of one device (a host pointer there
+    would fault the device)."""
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("this call takes CUDA tensors (host tensors: kda_chunk_fwd_host)")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors of a call must be on one CUDA device")
+
+
 def _heads(x, head_major=False):
     """Head count of a [.., heads, D] (token-major) or [.., heads, T, D]
     (head-major) tensor."""
@@ -210,6 +226,11 @@ def _state_shape(N, q, v, v_first=False, head_major=False):
     return (N, H, V, K) if v_first else (N, H, K, V)
 
 
+# keyword arguments of make_fwd_args that are tensors
+_FWD_TENSOR_KW = ("a_log", "dt_bias", "initial_state", "cu_seqlens", "out", "final_state", "h_out",
+                  "v_new_out")
+
+
 def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias=None,
                   initial_state=None, cu_seqlens=None, l2norm_qk=True, beta_sigmoid=False,
                   gate_in_kernel=False, use_exp2=False, state_v_first=False, head_major=False,
@@ -217,7 +238,8 @@ def make_fwd_args(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
                   v_new_out=None) -> kda_fwd_args:
     """Fills a ``kda_fwd_args`` from tensors (BSND [B,T,H,D], or TND [T,H,D]
     with ``cu_seqlens``).  q and k may carry fewer heads than v (grouped key
-    heads, Hk dividing H): value head h reads key head h // (H // Hk)."""
+    heads, Hk dividing H): value head h reads key head h // (H // Hk).
+    Marshalling only: the calls that launch check where the tensors live."""
     _contig(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state,
             h_out, v_new_out)
     a = kda_fwd_args()
@@ -291,6 +313,8 @@ def kda_chunk_fwd(q, k, v, g, beta, *, scale=None, eps=1e-6, a_log=None, dt_bias
                       beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
                       state_v_first=state_v_first, head_major=head_major, extra_flags=extra_flags, out=out, final_state=final_state, h_out=h_out,
                       v_new_out=v_new_out)
+    _on_device(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state, h_out,
+               v_new_out, workspace)
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     _check(lib.kda_chunk_fwd(ctypes.byref(a), _stream(stream)), "kda_chunk_fwd")
@@ -367,6 +391,7 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_lo
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
                       beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
                       state_v_first=state_v_first, out=out, final_state=final_state)
+    _on_device(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state)
     _check(lib.kda_chunk_fwd_static_scratch(ctypes.byref(a), _stream(stream)),
            "kda_chunk_fwd_static_scratch")
     return out, final_state
@@ -389,6 +414,7 @@ def prepare_chunk_fwd(q, k, v, g, beta, *, output_final_state=True, workspace=No
                                        kw.get("head_major", False)),
                           dtype=torch.float32, device=q.device)
     a = make_fwd_args(q, k, v, g, beta, out=out, final_state=fin, **kw)
+    _on_device(q, k, v, g, beta, out, fin, workspace, *[kw.get(n) for n in _FWD_TENSOR_KW])
     ws = _workspace(lib.kda_chunk_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     return a, out, fin, ws
@@ -407,6 +433,7 @@ def prepare_segment_summary(q, k, v, g, beta, seg_bounds, *, M=None, S_tilde=Non
     if S_tilde is None:
         S_tilde = torch.empty(S, H, K, V, dtype=torch.float32, device=q.device)
     a = make_fwd_args(q, k, v, g, beta, **kw)
+    _on_device(q, k, v, g, beta, seg_bounds, M, S_tilde, workspace, *[kw.get(n) for n in _FWD_TENSOR_KW])
     ws = _workspace(lib.kda_segment_summary_workspace_size(ctypes.byref(a), S), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     return a, M, S_tilde, ws
@@ -460,6 +487,7 @@ def _segment_summary(q, k, v, g, beta, seg_bounds, *, scale=None, eps=1e-6, a_lo
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid,
                       gate_in_kernel=gate_in_kernel, use_exp2=use_exp2, head_major=head_major)
+    _on_device(q, k, v, g, beta, seg_bounds, M, S_tilde, a_log, dt_bias, workspace)
     ws = _workspace(lib.kda_segment_summary_workspace_size(ctypes.byref(a), S), q.device, workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     _check(lib.kda_segment_summary(ctypes.byref(a), seg_bounds.data_ptr(), S, M.data_ptr(),
@@ -481,6 +509,7 @@ def kda_state_prefix_scan(M, S_tilde, S0=None, *, S_in=None, S_final=None, strea
     if S_final is None:
         S_final = torch.empty(*(() if one else (C,)), H, K, V, dtype=torch.float32, device=M.device)
     _contig(M, S_tilde, S0, S_in, S_final)
+    _on_device(M, S_tilde, S0, S_in, S_final)
     _check(lib.kda_state_prefix_scan(_ptr(M), _ptr(S_tilde), _ptr(S0), C, S, H, K, V, _ptr(S_in),
                                      _ptr(S_final), _stream(stream)), "kda_state_prefix_scan")
     return S_in, S_final
@@ -518,6 +547,7 @@ def kda_state_gather(cache, idx, flags=None, *, packed=None, stream=None):
     _contig(idx, flags, packed)
     if flags is not None and flags.dtype != torch.bool:
         raise TypeError("flags must be bool")
+    _on_device(cache, idx, flags, packed)
     _check(lib.kda_state_gather(_ptr(cache), _dtype_code(cache), n_rows, stride, payload, _ptr(idx),
                                 _idx_code(idx), _ptr(flags), n, _ptr(packed), _stream(stream)),
            "kda_state_gather")
@@ -529,6 +559,7 @@ def kda_state_scatter(cache, idx, packed, *, stream=None):
     lib = load_library()
     n_rows, stride, payload = _rows(cache)
     _contig(idx, packed)
+    _on_device(cache, idx, packed)
     _check(lib.kda_state_scatter(_ptr(cache), _dtype_code(cache), n_rows, stride, payload,
                                  _ptr(idx), _idx_code(idx), _ptr(packed), _dtype_code(packed),
                                  idx.numel(), _stream(stream)), "kda_state_scatter")
@@ -553,6 +584,7 @@ def kda_recurrent_step(q, k, v, g, beta, cache, idx, init_flags=None, *, scale=N
     if out is None:
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     _contig(out)
+    _on_device(q, k, v, g, beta, cache, idx, init_flags, a_log, dt_bias, out)
     n_rows, stride, _ = _rows(cache)
     a = kda_decode_args()
     _check_shapes(q, k, v, g, beta, out)
@@ -609,6 +641,8 @@ def prepare_chunk_bwd(q, k, v, g, beta, d_out, *, d_final_state=None, initial_st
                                      dtype=torch.float32, device=dev)
                          if want_d_initial_state else None),
     )
+    _on_device(q, k, v, g, beta, d_out, d_final_state, initial_state, workspace,
+               *[kw.get(n) for n in _FWD_TENSOR_KW])
     b = kda_bwd_args()
     b.fwd = make_fwd_args(q, k, v, g, beta, initial_state=initial_state, **kw)
     b.d_out, b.d_final_state = _ptr(d_out), _ptr(d_final_state)
@@ -655,6 +689,7 @@ def kda_segment_bwd_summary(q, k, v, g, beta, d_out, seg_bounds, *, E=None, work
     kw.pop("initial_state", None)
     kw.pop("cu_seqlens", None)
     a = make_fwd_args(q, k, v, g, beta, **kw)
+    _on_device(q, k, v, g, beta, d_out, seg_bounds, E, workspace, *[kw.get(n) for n in _FWD_TENSOR_KW])
     ws = _workspace(lib.kda_segment_bwd_summary_workspace_size(ctypes.byref(a), S), q.device,
                     workspace)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
@@ -678,6 +713,7 @@ def kda_state_grad_scan(M, E, dS_final=None, *, dS_out=None, dS_initial=None, st
     if dS_initial is None:
         dS_initial = torch.empty(*(() if one else (C,)), H, K, V, dtype=torch.float32, device=M.device)
     _contig(M, E, dS_final, dS_out, dS_initial)
+    _on_device(M, E, dS_final, dS_out, dS_initial)
     _check(lib.kda_state_grad_scan(_ptr(M), _ptr(E), _ptr(dS_final), C, S, H, K, V, _ptr(dS_out),
                                    _ptr(dS_initial), _stream(stream)), "kda_state_grad_scan")
     return dS_out, dS_initial

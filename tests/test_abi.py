@@ -302,3 +302,35 @@ def test_binding_head_major_shapes():
     cu = torch.tensor([0, 3, 7], dtype=torch.int32)
     a = kda.make_fwd_args(q[0], q[0], v[0], g[0], beta[0], head_major=True, cu_seqlens=cu)
     assert (a.B, a.T, a.num_seqs) == (1, T, 2)
+
+
+def test_launching_calls_reject_host_tensors(lib):
+    """Every binding call that launches kernels refuses host tensors before
+    reaching the library (the kernels would dereference host pointers);
+    mixed devices are refused too."""
+    import torch
+    T, H, D = 64, 2, 64
+    q = torch.randn(T, H, D)
+    v = torch.randn(T, H, D)
+    g = torch.randn(T, H, D)
+    beta = torch.rand(T, H)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_chunk_fwd(q, q, v, g, beta)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_chunk_bwd(q, q, v, g, beta, v)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_segment_summary(q, q, v, g, beta, torch.tensor([0, T], dtype=torch.int32))
+    M, St = torch.zeros(1, H, D, D), torch.zeros(1, H, D, D)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_state_prefix_scan(M, St)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_state_grad_scan(M, St)
+    pool = torch.zeros(4, H, D, D)
+    idx = torch.tensor([1, 2], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_state_gather(pool, idx)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_state_scatter(pool, idx, torch.zeros(2, H, D, D))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda.kda_recurrent_step(q[None, :1], q[None, :1], v[None, :1], g[None, :1], beta[None, :1],
+                               pool, idx[:1])
