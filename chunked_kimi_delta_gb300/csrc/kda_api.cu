@@ -22,7 +22,7 @@ inline bool mis16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) &
 constexpr uint32_t kKnownFlags = KDA_L2NORM_QK | KDA_BETA_SIGMOID | KDA_GATE_IN_KERNEL |
                                  KDA_USE_EXP2 | KDA_REUSE_PREP | KDA_SAFE_GATE |
                                  KDA_ALLOW_NEG_EIGVAL | KDA_STATE_V_FIRST |
-                                 KDA_LAYOUT_HEAD_MAJOR;
+                                 KDA_LAYOUT_HEAD_MAJOR | KDA_TEST_WAIT_TIMEOUT;
 constexpr uint32_t kRejectedFlags = KDA_SAFE_GATE | KDA_ALLOW_NEG_EIGVAL;
 
 inline bool v_first(const kda_fwd_args *a) { return (a->flags & KDA_STATE_V_FIRST) != 0; }
@@ -84,17 +84,25 @@ bool use_tc(const kda_fwd_args *a) {
   return a->qkv_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128 && (int64_t)a->B * a->T > 0;
 }
 
-// Tensor-core workspace: error word, chunk offsets, one package per (chunk, head).
+// Tensor-core workspace: error word (and, 64 bytes in, the count of the
+// strong-decay list), chunk offsets, the strong-decay list, one package per
+// (chunk, head).
+constexpr size_t kFlagCountOff = 64;
 struct TcPlan {
-  size_t off_chunk_off, off_pkg, total;
+  size_t off_chunk_off, off_flags, off_pkg, total;
 };
 TcPlan tc_plan(const FwdPlan &p) {
   TcPlan t{};
   size_t o = 256;
   t.off_chunk_off = o; o = align256(o + sizeof(int32_t) * (size_t)(p.N + 1));
+  t.off_flags = o; o = align256(o + sizeof(uint32_t) * (size_t)p.nchunks * p.H);
   t.off_pkg = o; o = align256(o + (size_t)p.nchunks * p.H * tcp::PK_BYTES);
   t.total = o;
   return t;
+}
+inline uint32_t *flag_count(char *ws) { return reinterpret_cast<uint32_t *>(ws + kFlagCountOff); }
+inline uint32_t *flag_list(char *ws, const FwdPlan &p) {
+  return reinterpret_cast<uint32_t *>(ws + tc_plan(p).off_flags);
 }
 
 // K-first copies of the caller's V-first states (initial, final, h_out),
@@ -321,8 +329,8 @@ static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEve
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess && !reuse) e = mark();
     if (e == cudaSuccess && !reuse)
-      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H,
-                              p.Hk, pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p.nchunks,
+                              a->H, p.Hk, pkg, err, flag_count(ws), flag_list(ws, p), st);
     if (e == cudaSuccess) e = mark();
     if (e == cudaSuccess) {
       tcp::ChainArgs ca{};
@@ -333,6 +341,7 @@ static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEve
       ca.h_out = a->h_out;
       ca.v_new_out = a->v_new_out;
       ca.err = err;
+      ca.test_wait_timeout = (a->flags & KDA_TEST_WAIT_TIMEOUT) != 0;
       e = tcp::launch_tc_chain(ca, si, a->H, st);
     }
   } else {
@@ -598,8 +607,8 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     char *pkg = ws + tc_plan(p).off_pkg;
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess)
-      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H,
-                              p.Hk, pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p.nchunks,
+                              a->H, p.Hk, pkg, err, flag_count(ws), flag_list(ws, p), st);
     if (e == cudaSuccess) e = tcp::launch_tc_summary(pkg, S_tilde, M, si, a->H, err, st);
   } else {
     if (e == cudaSuccess)
@@ -882,8 +891,8 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   // recompute: the per-chunk intermediates, the state entering every chunk, v_new
   if (tc) {
     if (e == cudaSuccess)
-      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gp, si, p.f.nchunks, a->H, p.f.Hk, pkg,
-                              err, st, f32(p.off_ainv));
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->v, a->g, a->beta, gp, si, p.f.nchunks, a->H, p.f.Hk,
+                              pkg, err, flag_count(ws), flag_list(ws, p.f), st, f32(p.off_ainv));
     if (e == cudaSuccess) {
       tcp::ChainArgs ca{};
       ca.pkg = pkg;
@@ -976,6 +985,10 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
         ia.part_alog = l.part_alog; ia.part_dtb = l.part_dtb;
         ia.err = err;
         e = tcp::launch_tc_bwd_intra(ia, si, p.f.nchunks, a->H, p.f.Hk, gp, st);
+        // the chunks the prep listed under strong decay, again, exactly
+        if (e == cudaSuccess)
+          e = launch_bwd_intra_list(l, ba.dv_img, ia.vn_img, sa_dw_img, flag_count(ws), flag_list(ws, p.f),
+                                    st);
         if (e == cudaSuccess && grouped)
           e = launch_bwd_group_sum(a->qkv_dtype, p.f.T_tot, a->H, p.f.Hk, a->dk, l.dqv, l.dkv, b->dq, b->dk,
                                    st);
@@ -1051,8 +1064,8 @@ kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
     char *pkg = ws + tc_plan(p).off_pkg;
     uint32_t *err = reinterpret_cast<uint32_t *>(ws);
     if (e == cudaSuccess)
-      e = tcp::launch_tc_prep(maps, a->q, a->k, a->g, a->beta, gate_params(a), si, p.nchunks, a->H, p.Hk,
-                              pkg, err, st);
+      e = tcp::launch_tc_prep(maps, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p.nchunks, a->H,
+                              p.Hk, pkg, err, flag_count(ws), flag_list(ws, p), st);
     if (e == cudaSuccess) {
       tcp::BwdChainArgs ba{};
       ba.pkg = pkg;

@@ -27,6 +27,7 @@
 // All gates are natural-log here (the base-2 form of the forward is only a
 // change of base, section 3.1).
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -208,7 +209,25 @@ struct IntraSmem {
   static constexpr int total = oRedS + 8;
 };
 
-template <typename Tin, typename Tdq, int K, int V>
+// The tensor-core path's bf16 tile images of -dv_new, v_new and dw (16 KB
+// per (chunk, head), [token][column] in the 64-row MN-major SW128 layout),
+// and the list of the items to process, for the list mode of
+// bwd_intra_kernel; unused (null) otherwise.
+struct ImgSrc {
+  const uint8_t *dvn_neg, *vn, *dw;
+  const uint32_t *count, *list;
+};
+
+__device__ __forceinline__ float img_at(const uint8_t *img, int64_t item, int r, int col) {
+  return __bfloat162float(
+      *reinterpret_cast<const __nv_bfloat16 *>(img + item * 16384 + tcp::mnmaj_off(64, r, col)));
+}
+
+// LIST = false: one CTA per (chunk, head) of the grid, fp32 intermediates.
+// LIST = true: the CTAs loop over the items of img.list (chunk * H + head)
+// and read dv_new, v_new and dw from img's tile images - the exact pass over
+// the chunks the tensor-core kernel cannot take (strong decay).
+template <typename Tin, typename Tdq, int K, int V, bool LIST = false>
 __global__ void __launch_bounds__(256, 1)
 bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta, GateParams gp,
@@ -219,7 +238,7 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
                  Tdq *__restrict__ dq_out, Tdq *__restrict__ dk_out, Tin *__restrict__ dv_out,
                  float *__restrict__ dg_out, float *__restrict__ dbeta_out,
                  float *__restrict__ part_alog, float *__restrict__ part_dtb,
-                 const float *__restrict__ a_in) {
+                 const float *__restrict__ a_in, ImgSrc img) {
   using L = IntraSmem<K, V>;
   constexpr int KP = L::KP, XP = L::XP;
   constexpr int NP = 256 / K, NR = BT / NP;  // channel mapping: rows part + NP m
@@ -232,11 +251,15 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
   float *sRedV = smem + L::oRedV, *sRedK = smem + L::oRedK, *sRedC = smem + L::oRedC;
   float *sRedS = smem + L::oRedS;
 
-  const int64_t c = blockIdx.x;
-  const int h = blockIdx.y;
+  const uint32_t n_list = LIST ? *img.count : 1u;
+  for (uint32_t li = LIST ? blockIdx.x : 0u; li < n_list; li += LIST ? gridDim.x : 1u) {
+  if (LIST) __syncthreads();  // the previous item is done with shared memory
+  const int64_t c = LIST ? (int64_t)(img.list[li] / (uint32_t)H) : (int64_t)blockIdx.x;
+  const int h = LIST ? (int)(img.list[li] % (uint32_t)H) : (int)blockIdx.y;
+  const int64_t item = c * H + h;
   int n, len;
   int64_t t0;
-  if (!chunk_lookup(s, c, n, t0, len)) return;
+  if (!chunk_lookup(s, c, n, t0, len)) continue;  // uniform over the CTA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hk = h / (H / Hk);
   const bool gate = (gp.flags & KDA_GATE_IN_KERNEL) != 0;
@@ -346,7 +369,7 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
   for (int i = tid; i < BT * V; i += 256) {
     const int r = i / V, cv = i % V;
     const bool in = r < len;
-    X[r * XP + cv] = in ? dvn[row_off(r, H, h, V) + cv] : 0.f;
+    X[r * XP + cv] = in ? (LIST ? -img_at(img.dvn_neg, item, r, cv) : dvn[row_off(r, H, h, V) + cv]) : 0.f;
     Y[r * XP + cv] = in ? to_f32(v[row_off(r, H, h, V) + cv]) : 0.f;
   }
   __syncthreads();
@@ -377,7 +400,7 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
   //     dkb = A^T dw -> dk^, dbeta, dG
   for (int i = tid; i < BT * K; i += 256) {
     const int r = i / K, c2 = i % K;
-    X[r * XP + c2] = r < len ? dw[row_off(r, H, h, K) + c2] : 0.f;
+    X[r * XP + c2] = r < len ? (LIST ? img_at(img.dw, item, r, c2) : dw[row_off(r, H, h, K) + c2]) : 0.f;
     Y[r * XP + c2] = sK[r * KP + c2] * sB[r] * expf(sG[r * KP + c2]);
   }
   __syncthreads();
@@ -434,7 +457,7 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
     const int r = i / V, cv = i % V;
     const bool in = r < len;
     X[r * XP + cv] = (in && d_out) ? to_f32(d_out[row_off(r, H, h, V) + cv]) : 0.f;
-    Y[r * XP + cv] = in ? vn[row_off(r, H, h, V) + cv] : 0.f;
+    Y[r * XP + cv] = in ? (LIST ? img_at(img.vn, item, r, cv) : vn[row_off(r, H, h, V) + cv]) : 0.f;
   }
   __syncthreads();
   {
@@ -600,6 +623,7 @@ bwd_intra_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
     const float b = sB[tid];
     dbeta_out[(t0 + tid) * H + h] = sig ? d * b * (1.f - b) : d;
   }
+  }  // items
 }
 
 // ---------------------------------------------------------------------------
@@ -689,7 +713,7 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, bool with_state, cuda
       kern<<<grid, 256, smem, st>>>(
           static_cast<const Tin *>(b.q), static_cast<const Tin *>(b.k), static_cast<const Tin *>(b.v),
           b.g, b.beta, b.gp, s, H, Hk, dO, b.dvn, b.vn, b.dqg, b.dw, b.dkg, b.dgc, b.dqv, b.dkv,
-          static_cast<Tin *>(b.dv), b.dg, b.dbeta, b.part_alog, b.part_dtb, b.a_in);
+          static_cast<Tin *>(b.dv), b.dg, b.dbeta, b.part_alog, b.part_dtb, b.a_in, ImgSrc{});
     } else {
       auto kern = bwd_intra_kernel<Tin, Tin, K, V>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -698,7 +722,7 @@ cudaError_t bwd_dispatch(const BwdLaunch &b, bool with_dh, bool with_state, cuda
           static_cast<const Tin *>(b.q), static_cast<const Tin *>(b.k), static_cast<const Tin *>(b.v),
           b.g, b.beta, b.gp, s, H, Hk, dO, b.dvn, b.vn, b.dqg, b.dw, b.dkg, b.dgc,
           static_cast<Tin *>(b.dq), static_cast<Tin *>(b.dk), static_cast<Tin *>(b.dv), b.dg, b.dbeta,
-          b.part_alog, b.part_dtb, b.a_in);
+          b.part_alog, b.part_dtb, b.a_in, ImgSrc{});
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (grouped) {
@@ -725,6 +749,43 @@ cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, c
   }
 #undef KDA_BWD
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_intra_list(const BwdLaunch &b, const uint8_t *dvn_neg_img, const uint8_t *vn_img,
+                                  const uint8_t *dw_img, const uint32_t *count, const uint32_t *list,
+                                  cudaStream_t st) {
+  constexpr int K = 128, V = 128;
+  using Tin = __nv_bfloat16;
+  const int64_t nitems = b.nchunks * b.H;
+  if (nitems == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  const size_t smem = sizeof(float) * IntraSmem<K, V>::total;
+  const ImgSrc img{dvn_neg_img, vn_img, dw_img, count, list};
+  const int grid = (int)(nitems < sms ? nitems : sms);
+  const Tin *dO = static_cast<const Tin *>(b.d_out);
+  cudaError_t e;
+  if (b.Hk != b.H) {
+    auto kern = bwd_intra_kernel<Tin, float, K, V, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 256, smem, st>>>(
+        static_cast<const Tin *>(b.q), static_cast<const Tin *>(b.k), static_cast<const Tin *>(b.v), b.g,
+        b.beta, b.gp, b.s, b.H, b.Hk, dO, nullptr, nullptr, b.dqg, nullptr, b.dkg, b.dgc, b.dqv, b.dkv,
+        static_cast<Tin *>(b.dv), b.dg, b.dbeta, b.part_alog, b.part_dtb, b.a_in, img);
+  } else {
+    auto kern = bwd_intra_kernel<Tin, Tin, K, V, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 256, smem, st>>>(
+        static_cast<const Tin *>(b.q), static_cast<const Tin *>(b.k), static_cast<const Tin *>(b.v), b.g,
+        b.beta, b.gp, b.s, b.H, b.Hk, dO, nullptr, nullptr, b.dqg, nullptr, b.dkg, b.dgc,
+        static_cast<Tin *>(b.dq), static_cast<Tin *>(b.dk), static_cast<Tin *>(b.dv), b.dg, b.dbeta,
+        b.part_alog, b.part_dtb, b.a_in, img);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st) {

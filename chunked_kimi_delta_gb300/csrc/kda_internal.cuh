@@ -194,6 +194,14 @@ struct BwdLaunch {
 // with_state = false: dqg, dw, dkg, dgc from the tensor-core state kernel.
 cudaError_t launch_generic_bwd(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st,
                                bool with_dh = true, bool with_state = true);
+// The intra-chunk backward of the (chunk, head) items in list (count on the
+// device) on the CUDA cores, bf16 d_k = d_v = 128, from the tensor-core
+// path's tile images of -dv_new, v_new and dw (b.dvn, b.vn, b.dw unused):
+// the exact pass for the chunks under strong decay, written over what the
+// tensor-core kernel left for them.
+cudaError_t launch_bwd_intra_list(const BwdLaunch &b, const uint8_t *dvn_neg_img, const uint8_t *vn_img,
+                                  const uint8_t *dw_img, const uint32_t *count, const uint32_t *list,
+                                  cudaStream_t st);
 // The reverse state-gradient chain alone (dhn / dvn may be null: not written).
 cudaError_t launch_bwd_dh(kda_dtype dt, int K, int V, const BwdLaunch &b, cudaStream_t st);
 // dq, dk of each key head = the sum over the value heads of its group.

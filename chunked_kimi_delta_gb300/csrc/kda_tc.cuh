@@ -71,15 +71,16 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-// Wait for an mbarrier phase; on timeout record the device error word and
-// return false.
-__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, uint32_t *err) {
+// Wait for an mbarrier phase; on timeout (limit_ns) record the device error
+// word and return false.
+__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, uint32_t *err,
+                                             unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 256; ++i)
       if (tc::mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       atomicOr(err, DEV_ERR_TIMEOUT);
       return false;
     }
@@ -156,12 +157,30 @@ struct TcMaps {
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
                      int H, int Hk, TcMaps &maps);
 
-cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
-                           const float *beta, const GateParams &gp, const SeqInfo &s,
-                           int64_t nchunks, int H, int Hk, char *pkg, uint32_t *err,
+// Strong decay: an item in which some channel's chunk-local gate (log2
+// units) moves by more than this inside one 16-token sub-block is computed
+// by the exact CUDA-core kernel of kda_tc_exact.cu instead of the factored
+// tensor-core products (whose factors then stay inside [2^-96, 2^96]).
+constexpr float STRONG_DECAY_LOG2 = 96.f;
+
+// The prep of every (chunk, head), then the exact recomputation of the items
+// it listed under strong decay.  flag_count (one word, cleared here) and
+// flag_list ([nchunks * H] entries, item = chunk * H + head) are scratch the
+// caller keeps for the backward, which reads the same list.
+cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const void *v,
+                           const float *x, const float *beta, const GateParams &gp,
+                           const SeqInfo &s, int64_t nchunks, int H, int Hk, char *pkg,
+                           uint32_t *err, uint32_t *flag_count, uint32_t *flag_list,
                            cudaStream_t st, float *a_out = nullptr);
 // a_out: when given, [nchunks, H, 64, 64] fp32 receives A = (I + L)^-1 of
 // every item (the backward's intra-chunk stage reuses it).
+
+// The exact recomputation alone (kda_tc_exact.cu): overwrites the package
+// (and a_out) of each of the *flag_count items in flag_list.
+cudaError_t launch_tc_prep_exact(const void *q, const void *k, const void *v, const float *x,
+                                 const float *beta, const GateParams &gp, const SeqInfo &s,
+                                 int64_t nitems, int H, int Hk, const uint32_t *flag_count,
+                                 const uint32_t *flag_list, char *pkg, float *a_out, cudaStream_t st);
 
 struct ChainArgs {
   const char *pkg;
@@ -175,6 +194,9 @@ struct ChainArgs {
   // channels), v_new (16 KB, MN-major K = 64 tokens)
   uint8_t *h_img, *vn_img;
   uint32_t *err;
+  // test only: one extra wait, on a barrier nothing completes, with a 1 ms
+  // limit (the failure path of the bounded waits, without a hang)
+  bool test_wait_timeout;
 };
 
 cudaError_t launch_tc_chain(const ChainArgs &a, const SeqInfo &s, int H, cudaStream_t st);

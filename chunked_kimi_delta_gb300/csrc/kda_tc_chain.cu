@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   uint64_t *vn_ready = fullA + 7;  // v_new of the chunk is in shared memory (4 warp arrivals)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(fullA + 8);
   volatile uint32_t *abort_flag = tslot + 1;
+  uint64_t *bar_never = fullA + 16;  // test only: a barrier nothing completes
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hf = warp >> 2;
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     tc::mbar_init(bar_mc, 1);
     tc::mbar_init(bar_mb, 1);
     tc::mbar_init(vn_ready, 4);
+    tc::mbar_init(bar_never, 1);
     tc::mbar_fence_init();
     *abort_flag = 0;
   }
@@ -176,6 +178,9 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     bool ok = wait_or_flag(fullA + b, (uint32_t)((c >> 1) & 1), a.err);
     if (!ok) *abort_flag = 1;
     else if (tid == LEAD) a_done = c + 1;
+    // test only: give up on a wait with the next copies still in flight
+    if (a.test_wait_timeout && c == 0 && tid == LEAD && !wait_or_flag(bar_never, 0, a.err, 1000000ull))
+      *abort_flag = 1;
     if (a.h_out) {
       float4 *dst = reinterpret_cast<float4 *>(a.h_out + (((c0 + c) * H + h) * K + kr) * V + 64 * hf);
 #pragma unroll

@@ -15,9 +15,12 @@
 // at the end of sub-block R-1 (b_0 = 0).  Row r of sub-block R carries
 // 2^{G_r - b_R} <= 1; column j is stored once per later sub-block R' as
 // 2^{b_R' - G_j} <= 1 (off-diagonal blocks) and once with its own block's
-// reference, 2^{b_R(j) - G_j} (diagonal blocks, bounded by 16 tokens of
-// decay; clamped at 2^126, i.e. exact unless the gate falls below about
-// -5.5 nats per token for 16 tokens in a row).  One M=128 x N=160 x K=128
+// reference, 2^{b_R(j) - G_j} (diagonal blocks, bounded by the decay of the
+// block's own 16 tokens).  An item in which some channel's gate moves by more
+// than STRONG_DECAY_LOG2 inside one sub-block is put on a list instead, and
+// kda_tc_exact.cu recomputes it from exact gate differences; every factor
+// this kernel builds for the other items lies inside [2^-96, 2^96], where
+// bf16 and fp32 represent it without flush or overflow.  One M=128 x N=160 x K=128
 // tcgen05 MMA then yields every needed block of both A_kk and A_qk:
 //   A rows  0..63 : k^_r 2^{G_r - b_R}      A rows 64..127: q^_r 2^{G_r - b_R}
 //   B rows  0..15 : k^_j 2^{b_1 - G_j}, j < 16
@@ -170,7 +173,8 @@ __global__ void __launch_bounds__(NT, 2)
 tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restrict__ qg_in,
                const __nv_bfloat16 *__restrict__ kg_in, const float *__restrict__ xg_in,
                const float *__restrict__ beta, GateParams gp, SeqInfo s, int64_t nitems, int H,
-               int Hk, char *__restrict__ pkg, float *__restrict__ a_out, uint32_t *err) {
+               int Hk, char *__restrict__ pkg, float *__restrict__ a_out, uint32_t *err,
+               uint32_t *__restrict__ flag_count, uint32_t *__restrict__ flag_list) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *rq = reinterpret_cast<float *>(sm + M_RQ);
@@ -356,6 +360,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     __syncthreads();  // group totals, rstd and beta published
 
     // ---- phase 2: operand tiles and the elementwise package parts
+    bool strong = false;
     {
       // b_RR = gate sum before sub-block RR, G_C = sum over the chunk
       float bAll[4][4], GC[4], prev[4];
@@ -381,6 +386,16 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
           for (int j = 0; j < 4; ++j) Gl[rr][j] += prev[j];
+      }
+      // strong decay: the largest move of the gate inside this thread's
+      // sub-block, relative to the sub-block's reference
+      {
+        float gm = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) gm = fmaxf(gm, fabsf(Gl[rr][j]));
+        strong = gm > STRONG_DECAY_LOG2;
       }
       float eb[4], egc[4], cR[4][4];
 #pragma unroll
@@ -439,7 +454,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       }
     }
     tc::fence_proxy_async_smem();
-    __syncthreads();
+    // an item under strong decay goes on the list of kda_tc_exact.cu, which
+    // overwrites its package later (this pass still runs it, uniformly)
+    if (__syncthreads_or(strong) && tid == 0) flag_list[atomicAdd(flag_count, 1u)] = (uint32_t)w;
 
     // ---- MMA 1: [kE; qE] x B1^T -> D1 (128 x 160)
     if (tid == 0) {
@@ -794,9 +811,10 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 
 }  // namespace
 
-cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const float *x,
-                           const float *beta, const GateParams &gp, const SeqInfo &s,
-                           int64_t nchunks, int H, int Hk, char *pkg, uint32_t *err,
+cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const void *v,
+                           const float *x, const float *beta, const GateParams &gp,
+                           const SeqInfo &s, int64_t nchunks, int H, int Hk, char *pkg,
+                           uint32_t *err, uint32_t *flag_count, uint32_t *flag_list,
                            cudaStream_t st, float *a_out) {
   static int sms = 0;
   if (sms == 0) {
@@ -811,12 +829,18 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
   if (e != cudaSuccess) return e;
   const int64_t nitems = nchunks * H;
   if (nitems == 0) return cudaSuccess;
+  if (nitems > (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // list entries are 32-bit
+  if ((e = cudaMemsetAsync(flag_count, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
   const int64_t slots = 2 * (int64_t)sms;
   const int grid = (int)(nitems < slots ? nitems : slots);
   kern<<<grid, NT, SMEM_BYTES, st>>>(maps, static_cast<const __nv_bfloat16 *>(q),
                                      static_cast<const __nv_bfloat16 *>(k), x, beta, gp, s, nitems,
-                                     H, Hk, pkg, a_out, err);
-  return cudaGetLastError();
+                                     H, Hk, pkg, a_out, err, flag_count, flag_list);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the listed items again, exactly (a few CTAs that find an empty list
+  // return at once)
+  return launch_tc_prep_exact(q, k, v, x, beta, gp, s, nitems, H, Hk, flag_count, flag_list, pkg,
+                              a_out, st);
 }
 
 }  // namespace tcp

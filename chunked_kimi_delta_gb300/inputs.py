@@ -7,7 +7,8 @@ oracle, so both see identical bytes.
 Distributions (per the workload descriptions): q, k, v ~ N(0,1), rounded to
 bf16 where the workload is bf16 (q and k are L2-normalised by the method);
 beta logits b ~ N(0,1) (the method applies the sigmoid); raw gate input
-x ~ N(0,1), a_log ~ U(-4, 0) per head, dt_bias ~ N(0, 0.1) per (head,
+x ~ N(0,1), a_log ~ U(-4, 0) per head (another range for the strong-decay
+cases), dt_bias ~ N(0, 0.1) per (head,
 channel) (the method applies g = -exp(a_log) softplus(x + dt_bias));
 initial states ~ N(0, 0.1).  Draw order from one generator: sequence lengths
 (varlen only), q, k, v, x, b, a_log, dt_bias, initial state, then pool rows,
@@ -43,6 +44,7 @@ class KdaConfig:
     num_segments: int = 0            # segment mode: equal segments per sequence
     pool_rows: int = 0               # state pool size for gather/scatter
     a_log_const: Optional[float] = None   # slow-decay variant
+    a_log_range: tuple = (-4.0, 0.0)      # a_log ~ U(lo, hi) per head otherwise
     beta_logit_mean: float = 0.0
     seed: int = 0
 
@@ -135,7 +137,8 @@ def make_inputs(cfg: KdaConfig, device="cpu", seed: Optional[int] = None) -> dic
         a_log = torch.full((H,), cfg.a_log_const, dtype=f32, device=device)
         _ = rand(H)  # keep the draw order
     else:
-        a_log = rand(H) * 4.0 - 4.0
+        lo, hi = cfg.a_log_range
+        a_log = rand(H) * (hi - lo) + lo
     dt_bias = randn(H, dk, std=0.1)
     S0 = randn(N, H, dk, dv, std=0.1) if cfg.initial_state else None
     out = dict(q=q, k=k, v=v, g=g, beta=beta, a_log=a_log, dt_bias=dt_bias,

@@ -90,7 +90,17 @@ enum {
    * kernels work token-major; the library converts at the boundary through
    * workspace copies (included in the workspace sizes).  Rejected with
    * KDA_ERR_UNSUPPORTED by kda_chunk_fwd_host and kda_recurrent_step. */
-  KDA_LAYOUT_HEAD_MAJOR = 1u << 11
+  KDA_LAYOUT_HEAD_MAJOR = 1u << 11,
+  /* Test only (no counterpart on the pages): exercises the device-side
+   * failure path without faulting or hanging the GPU.  In a kda_chunk_fwd
+   * (or kda_chunk_fwd_static_scratch) that runs the tensor-core chain, the
+   * chain kernel also waits, once, on a barrier that nothing completes,
+   * with a 1 ms limit; it then records KDA_ERR_DEVICE_TIMEOUT in the
+   * workspace's error word, lets the copies it started land, releases its
+   * tensor memory and returns.  The call itself returns KDA_OK; its outputs
+   * are undefined; kda_get_device_status (kda_static_scratch_status) then
+   * reports the timeout.  Ignored by the CUDA-core path (no waits there). */
+  KDA_TEST_WAIT_TIMEOUT = 1u << 30
 };
 
 /*
@@ -148,6 +158,12 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
 
 /* The chunked KDA forward: out, and final_state / h_out / v_new_out when
  * given.  N = B without cu_seqlens, num_seqs with it.
+ * Arithmetic: bf16 inputs with dk = dv = 128 run on the tensor cores (bf16
+ * operands, fp32 accumulation, inverse and state); a chunk in which some
+ * channel's gate falls by more than 96 log2 units (about 66 nats) inside one
+ * of its 16-token sub-blocks is recomputed from exact gate differences in
+ * fp32 on the CUDA cores, so strong decay costs time, not accuracy.  fp32
+ * inputs and the other head sizes run in fp32 on the CUDA cores.
  * With no tokens (B*T == 0, or only empty sequences) the final state is the
  * initial state; q/k/v/g/beta/out may then be NULL.
  * Errors: KDA_ERR_INVALID_ARG (null q/k/v/g/beta/out with tokens, B or H < 1,
@@ -179,10 +195,22 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  *    before any stream capture.
  *  - All calls share the one array: calls that overlap on the GPU (e.g. on
  *    two streams) race and must be serialised by the caller.  Leftover
- *    contents of earlier calls do not affect results.
+ *    contents of earlier calls do not affect results: every call rewrites
+ *    what it reads, and KDA_REUSE_PREP (which would read an earlier call's
+ *    preparation back) is refused with KDA_ERR_UNSUPPORTED.
+ *  - A device-side wait that gave up is recorded in the array's error word:
+ *    read it with kda_static_scratch_status after the call and before the
+ *    next one (each call clears the word when it starts).
  *  - Other errors as kda_chunk_fwd; KDA_ERR_CUDA if the address lookup fails.
  */
 kda_status kda_chunk_fwd_static_scratch(const kda_fwd_args *args, kda_stream_t stream);
+
+/* kda_get_device_status for the static scratch array of the current device
+ * (the callers of kda_chunk_fwd_static_scratch never see its address):
+ * synchronises `stream`, returns KDA_ERR_DEVICE_TIMEOUT if a bounded wait of
+ * the last call gave up (and clears the word), else KDA_OK.  Copies 4 bytes
+ * to a host variable; allocates nothing. */
+kda_status kda_static_scratch_status(kda_stream_t stream);
 
 /* Tokens per block of kda_chunk_fwd_host. */
 #define KDA_HOST_BLOCK_TOKENS 1024
@@ -390,8 +418,11 @@ typedef struct {
  * dk*dv*4 bytes per chunk and head each), and per-token fp32 scratch. */
 size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *args);
 
-/* The chunked KDA backward (fp32 arithmetic on CUDA cores for every dtype and
- * head size).  Deterministic: no atomics; every sum runs in a fixed order.
+/* The chunked KDA backward.  bf16 inputs with dk = dv = 128 run on the
+ * tensor cores (bf16 operands, fp32 accumulation and state; chunks under
+ * strong gate decay are recomputed on the CUDA cores in fp32); fp32 inputs
+ * and the other head sizes run in fp32 on the CUDA cores.  Deterministic:
+ * every sum runs in a fixed order.
  * Errors: those of kda_chunk_fwd for `fwd` (except that out may be NULL),
  * KDA_ERR_INVALID_ARG (null dq/dk/dv/dg/dbeta with tokens),
  * KDA_ERR_UNSUPPORTED (KDA_REUSE_PREP), KDA_ERR_ALIGNMENT,
