@@ -29,6 +29,9 @@ KDA_SAFE_GATE = 1 << 8
 KDA_ALLOW_NEG_EIGVAL = 1 << 9
 KDA_STATE_V_FIRST = 1 << 10
 KDA_LAYOUT_HEAD_MAJOR = 1 << 11
+KDA_TEST_WAIT_TIMEOUT = 1 << 30   # test only: see include/kda.h
+KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_ALIGNMENT = 1, 2, 3
+KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_DEVICE_TIMEOUT = 4, 5, 6
 CHUNK = 64
 
 
@@ -111,6 +114,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kda_get_device_status": ([vp, vp], ctypes.c_int),
         "kda_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "kda_chunk_fwd_static_scratch": ([P, vp], ctypes.c_int),
+        "kda_static_scratch_status": ([vp], ctypes.c_int),
         "kda_chunk_fwd_host_workspace_size": ([P], ctypes.c_size_t),
         "kda_chunk_fwd_host": ([P, vp], ctypes.c_int),
         "kda_recurrent_step": ([ctypes.POINTER(kda_decode_args), vp], ctypes.c_int),
@@ -172,20 +176,34 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
-def _on_device(*ts):
-    """The calls that launch kernels dereference every pointer on the GPU:
-    their tensors must be CUDA tensors of one device (a host pointer there
-    would fault the device)."""
+def _check_devices(devices, current: int):
+    """``devices``: the torch devices of a call's tensors (None entries
+    skipped).  They must all be the current CUDA device ``current``: the
+    library launches on the current device and stream, and a pointer to
+    another GPU's memory (or to host memory) would fault the device."""
     dev = None
-    for t in ts:
-        if t is None:
+    for d in devices:
+        if d is None:
             continue
-        if not t.is_cuda:
+        if d.type != "cuda":
             raise ValueError("this call takes CUDA tensors (host tensors: kda_chunk_fwd_host)")
         if dev is None:
-            dev = t.device
-        elif t.device != dev:
+            dev = d
+        elif d != dev:
             raise ValueError("all tensors of a call must be on one CUDA device")
+    if dev is not None and dev.index != current:
+        raise ValueError(f"the tensors are on {dev} but cuda:{current} is the current device: "
+                         f"call under torch.cuda.device({dev.index})")
+
+
+def _on_device(*ts):
+    """The calls that launch kernels dereference every pointer on the
+    current GPU: their tensors must be CUDA tensors of the current device."""
+    devs = [None if t is None else t.device for t in ts]
+    if any(d is not None and d.type != "cuda" for d in devs):
+        raise ValueError("this call takes CUDA tensors (host tensors: kda_chunk_fwd_host)")
+    if any(d is not None for d in devs):
+        _check_devices(devs, _torch().cuda.current_device())
 
 
 def _heads(x, head_major=False):
@@ -369,13 +387,16 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_lo
                                  dt_bias=None, initial_state=None, cu_seqlens=None,
                                  l2norm_qk=True, beta_sigmoid=False, gate_in_kernel=False,
                                  use_exp2=False, output_final_state=True, out=None,
-                                 final_state=None, state_v_first=False, stream=None):
+                                 final_state=None, state_v_first=False, head_major=False,
+                                 extra_flags=0, stream=None):
     """The forward for callers that cannot allocate device memory: same
     arguments and results as :func:`kda_chunk_fwd`, but no workspace; the
     library's fixed scratch array is used instead (problems whose workspace
-    exceeds ``KDA_STATIC_SCRATCH_BYTES`` raise KdaError(KDA_ERR_WORKSPACE)).
-    Output tensors are allocated here only when not supplied.  Calls sharing a
-    GPU must not overlap in time."""
+    exceeds ``KDA_STATIC_SCRATCH_BYTES`` raise KdaError(KDA_ERR_WORKSPACE);
+    KDA_REUSE_PREP raises KdaError(KDA_ERR_UNSUPPORTED)).  Output tensors are
+    allocated here only when not supplied.  Calls sharing a GPU must not
+    overlap in time; :func:`kda_static_scratch_status` reads the error word of
+    the last call."""
     torch = _torch()
     lib = load_library()
     if cu_seqlens is not None:
@@ -385,16 +406,25 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, *, scale=None, eps=1e-6, a_lo
     if out is None:
         out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     if output_final_state and final_state is None:
-        final_state = torch.empty(_state_shape(N, q, v, state_v_first), dtype=torch.float32,
-                                  device=q.device)
+        final_state = torch.empty(_state_shape(N, q, v, state_v_first, head_major),
+                                  dtype=torch.float32, device=q.device)
     a = make_fwd_args(q, k, v, g, beta, scale=scale, eps=eps, a_log=a_log, dt_bias=dt_bias,
                       initial_state=initial_state, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk,
                       beta_sigmoid=beta_sigmoid, gate_in_kernel=gate_in_kernel, use_exp2=use_exp2,
-                      state_v_first=state_v_first, out=out, final_state=final_state)
+                      state_v_first=state_v_first, head_major=head_major, extra_flags=extra_flags,
+                      out=out, final_state=final_state)
     _on_device(q, k, v, g, beta, a_log, dt_bias, initial_state, cu_seqlens, out, final_state)
     _check(lib.kda_chunk_fwd_static_scratch(ctypes.byref(a), _stream(stream)),
            "kda_chunk_fwd_static_scratch")
     return out, final_state
+
+
+def kda_static_scratch_status(stream=None) -> int:
+    """The device status of the last kda_chunk_fwd_static_scratch call on
+    the current device (synchronises ``stream``): KDA_OK, or
+    KDA_ERR_DEVICE_TIMEOUT when a bounded device wait gave up (the word is
+    cleared)."""
+    return load_library().kda_static_scratch_status(_stream(stream))
 
 
 def prepare_chunk_fwd(q, k, v, g, beta, *, output_final_state=True, workspace=None, **kw):

@@ -11,8 +11,12 @@
 // library is used on.  All calls share it, so calls that run at the same
 // time on the GPU (for example on two streams) race; callers serialise them.
 // The forward rewrites every scratch byte it later reads (the device error
-// word is cleared at the start of each call), so leftovers of an earlier
-// call do not matter.
+// word and the strong-decay list count are cleared at the start of each
+// call), so leftovers of an earlier call do not matter.  That is why
+// KDA_REUSE_PREP, which reads an earlier call's chunk preparation back from
+// the scratch, is refused here.  The device error word (a bounded wait that
+// gave up) sits at the start of the array; kda_static_scratch_status reads
+// and clears it, and the next forward clears it too.
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -48,6 +52,8 @@ extern "C" kda_status kda_chunk_fwd_static_scratch(const kda_fwd_args *args, kda
   if (!args) return KDA_ERR_INVALID_ARG;
   const size_t need = kda_chunk_fwd_workspace_size(args);
   if (need == 0) return kda_chunk_fwd(args, stream);  // invalid arguments: same error as kda_chunk_fwd
+  // the shared array holds whatever the last call left: nothing may be reused
+  if (args->flags & KDA_REUSE_PREP) return KDA_ERR_UNSUPPORTED;
   if (need > (size_t)KDA_STATIC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
   void *ws = nullptr;
   const kda_status s = scratch_for_current_device(&ws);
@@ -56,4 +62,11 @@ extern "C" kda_status kda_chunk_fwd_static_scratch(const kda_fwd_args *args, kda
   a.workspace = ws;
   a.workspace_bytes = (size_t)KDA_STATIC_SCRATCH_BYTES;
   return kda_chunk_fwd(&a, stream);
+}
+
+extern "C" kda_status kda_static_scratch_status(kda_stream_t stream) {
+  void *ws = nullptr;
+  const kda_status s = scratch_for_current_device(&ws);
+  if (s != KDA_OK) return s;
+  return kda_get_device_status(ws, stream);
 }

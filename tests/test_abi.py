@@ -334,3 +334,18 @@ def test_launching_calls_reject_host_tensors(lib):
     with pytest.raises(ValueError, match="CUDA tensors"):
         kda.kda_recurrent_step(q[None, :1], q[None, :1], v[None, :1], g[None, :1], beta[None, :1],
                                pool, idx[:1])
+
+
+def test_device_check_refuses_other_gpus_and_mixtures():
+    """The library launches on the current device: tensors of another GPU,
+    or of several devices, are refused before any launch (checked on device
+    objects, so it runs without a GPU)."""
+    import torch
+    d0, d1 = torch.device("cuda", 0), torch.device("cuda", 1)
+    kda._check_devices([d0, None, d0], 0)  # all on the current device: accepted
+    with pytest.raises(ValueError, match="current device"):
+        kda._check_devices([d1, d1], 0)
+    with pytest.raises(ValueError, match="one CUDA device"):
+        kda._check_devices([d0, d1], 0)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kda._check_devices([d0, torch.device("cpu")], 0)
