@@ -6,11 +6,14 @@
 // and "Hyper-Parallel Chunk KDA current implementation design" sections 5.3
 // and 6.3 compose forward summaries in time (rank) order, in fp32.
 //
-// One CTA per (chain, head, 32-column tile of the state): the columns of S
+// One CTA per (chain, head, 16-column tile of the state): the columns of S
 // evolve independently (every M_j acts on the left).  The segment loop is
-// sequential; each step is a K x K by K x 32 product on CUDA cores in fp32,
-// with M_j staged in shared memory and the running state held in registers
-// (each warp owns K/8 rows of the tile, one column per lane).
+// sequential.  Thread (half, r) owns state row r and the 8 columns of its
+// half of the tile in registers; per segment it reads its own row of M_j
+// (its column, in the reverse form) straight from L2 four entries at a time
+// and the tile's rows from shared memory as warp-wide broadcasts (every lane
+// of a warp reads the same row), so one M entry feeds 8 FMAs and one
+// broadcast feeds 4 x 8 - in fp32 on the CUDA cores throughout.
 //
 // The reverse form is the backward twin ("Hyper-Parallel Chunk KDA current
 // implementation design" section 5.2; "KDA Chunk Backward - TPU/Pallas Kernel
@@ -22,68 +25,85 @@ namespace kda {
 
 namespace {
 
-template <int K>
-__global__ void __launch_bounds__(256)
+constexpr int CT = 16;  // state columns per CTA
+
+template <int K, bool REVERSE>
+__global__ void __launch_bounds__(2 * K)
 prefix_scan_kernel(const float *__restrict__ M, const float *__restrict__ St,
                    const float *__restrict__ S0, int S, int H, int V, float *__restrict__ S_in,
-                   float *__restrict__ S_final, bool reverse) {
-  constexpr int R = K / 8;  // rows of the tile per warp
-  extern __shared__ float smem[];
-  float *sM = smem;                // [K][K+1]
-  float *sS = sM + K * (K + 1);    // [K][32]
+                   float *__restrict__ S_final) {
+  __shared__ __align__(16) float sS[K * CT];  // the state tile entering the step
   const int ch = blockIdx.x / H, h = blockIdx.x % H;
-  const int tid = threadIdx.x, j = tid & 31, rb = tid >> 5;
-  const int col = blockIdx.y * 32 + j;
+  const int tid = threadIdx.x;
+  const int r = tid % K, half = tid / K;  // a warp shares `half`: broadcast reads
+  const int col0 = blockIdx.y * CT + 8 * half;
   const int64_t st0 = (int64_t)ch * H + h;
 
-  float reg[R];
+  float acc[8];
+  if (S0) {
+    const float4 *src = reinterpret_cast<const float4 *>(S0 + (st0 * K + r) * V + col0);
+    const float4 a = src[0], b = src[1];
+    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+  } else {
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int r = rb + 8 * i;
-    reg[i] = S0 ? S0[(st0 * K + r) * V + col] : 0.f;
+    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
   }
   for (int step = 0; step < S; ++step) {
-    const int seg = reverse ? S - 1 - step : step;
+    const int seg = REVERSE ? S - 1 - step : step;
     const int64_t u = ((int64_t)ch * S + seg) * H + h;
-    __syncthreads();  // previous step done with sM / sS
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int r = rb + 8 * i;
-      sS[r * 32 + j] = reg[i];
-      S_in[(u * K + r) * V + col] = reg[i];
+    float4 *sin = reinterpret_cast<float4 *>(S_in + (u * K + r) * V + col0);
+    sin[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    sin[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncthreads();  // the previous step is done reading sS
+    float4 *mine = reinterpret_cast<float4 *>(sS + r * CT + 8 * half);
+    mine[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    mine[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncthreads();
+    {
+      const float4 *st = reinterpret_cast<const float4 *>(St + (u * K + r) * V + col0);
+      const float4 a = st[0], b = st[1];
+      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+      acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
     }
     const float *Mu = M + u * K * K;
-    if (reverse)  // sM = M^T
-      for (int x = tid; x < K * K; x += 256) sM[(x % K) * (K + 1) + (x / K)] = Mu[x];
-    else
-      for (int x = tid; x < K * K; x += 256) sM[(x / K) * (K + 1) + (x % K)] = Mu[x];
-    __syncthreads();
+#pragma unroll 8
+    for (int m0 = 0; m0 < K; m0 += 4) {
+      float mv[4];
+      if (REVERSE) {  // row r of M^T = column r of M: lanes read consecutive entries
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int r = rb + 8 * i;
-      float acc = St[(u * K + r) * V + col];
-      for (int m = 0; m < K; ++m) acc = fmaf(sM[r * (K + 1) + m], sS[m * 32 + j], acc);
-      reg[i] = acc;
+        for (int i = 0; i < 4; ++i) mv[i] = __ldg(Mu + (m0 + i) * K + r);
+      } else {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(Mu + r * K + m0));
+        mv[0] = t.x; mv[1] = t.y; mv[2] = t.z; mv[3] = t.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 a = *reinterpret_cast<const float4 *>(sS + (m0 + i) * CT + 8 * half);
+        const float4 b = *reinterpret_cast<const float4 *>(sS + (m0 + i) * CT + 8 * half + 4);
+        acc[0] = fmaf(mv[i], a.x, acc[0]); acc[1] = fmaf(mv[i], a.y, acc[1]);
+        acc[2] = fmaf(mv[i], a.z, acc[2]); acc[3] = fmaf(mv[i], a.w, acc[3]);
+        acc[4] = fmaf(mv[i], b.x, acc[4]); acc[5] = fmaf(mv[i], b.y, acc[5]);
+        acc[6] = fmaf(mv[i], b.z, acc[6]); acc[7] = fmaf(mv[i], b.w, acc[7]);
+      }
     }
   }
   if (S_final) {
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int r = rb + 8 * i;
-      S_final[(st0 * K + r) * V + col] = reg[i];
-    }
+    float4 *dst = reinterpret_cast<float4 *>(S_final + (st0 * K + r) * V + col0);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
 template <int K>
 cudaError_t scan_dispatch(const float *M, const float *St, const float *S0, int C, int S, int H,
                           int V, float *S_in, float *S_final, cudaStream_t st, bool reverse) {
-  const size_t smem = sizeof(float) * (K * (K + 1) + K * 32);
-  auto kern = prefix_scan_kernel<K>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((int64_t)C * H), V / 32);
-  kern<<<grid, 256, smem, st>>>(M, St, S0, S, H, V, S_in, S_final, reverse);
+  if (V % CT != 0) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)((int64_t)C * H), V / CT);
+  if (reverse)
+    prefix_scan_kernel<K, true><<<grid, 2 * K, 0, st>>>(M, St, S0, S, H, V, S_in, S_final);
+  else
+    prefix_scan_kernel<K, false><<<grid, 2 * K, 0, st>>>(M, St, S0, S, H, V, S_in, S_final);
   return cudaGetLastError();
 }
 
