@@ -168,36 +168,68 @@ def cpu_oracle_sample(cfg, inp_cpu, units, ntokens, nthreads=0):
     return time.perf_counter() - t, ntokens * H, threads
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                name = ln.split(":", 1)[1].strip()
+                if name and not name.isdigit():
+                    return name
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def run_reference(args, rank):
+    """The oracle timed on the host cores on the same sample as the GPU line's
+    cpu_baseline: one step = one whole sequence of the workload (all H heads
+    x T tokens, OpenMP over the heads)."""
     if rank != 0:
         return
-    import torch
     from chunked_kimi_delta_gb300.inputs import CONFIGS, make_inputs
     cfg = CONFIGS[WORKLOAD]
-    small = cfg.replace(T=2048)
-    inp = make_inputs(small, device="cpu")
-    units = [(0, h) for h in range(8)]
+    one = cfg.replace(B=1)   # one sequence of the workload's shape and distributions
+    inp = make_inputs(one, device="cpu")
+    units = [(0, h) for h in range(cfg.H)]
     for _ in range(args.warmup):
-        cpu_oracle_sample(small, inp, units[:2], 256)
+        cpu_oracle_sample(one, inp, units[:2], 256)
     secs, th, threads = 0.0, 0, 1
     for _ in range(args.steps):
-        s, n, threads = cpu_oracle_sample(small, inp, units, 2048)
+        s, n, threads = cpu_oracle_sample(one, inp, units, cfg.T)
         secs += s
         th += n
-    tok_s = th / secs / cfg.H   # tokens/s of the full 32-head workload
+    tok_s = th / secs / cfg.H   # tokens/s of the full H-head workload
     tflops = th * alg_flops_per_token_head(cfg.dk, cfg.dv) / secs / 1e12
-    sample = (f"fp64 oracle, {len(units)} heads x 2048 tokens of batch row 0 per step "
-              f"(token-heads/s divided by H={cfg.H})")
+    sample = (f"fp64 oracle, one whole sequence per step: all {cfg.H} heads x {cfg.T} tokens "
+              f"(token-heads/s divided by H={cfg.H}); the GPU line's cpu_baseline times the same "
+              f"unit on the batch's own sequences")
     line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_desc(cfg), "tflops": tflops,
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model(), "nproc": os.cpu_count()},
             "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def step_stats(ms_list):
+    """median / min / p90 / mean of per-step times (ms)."""
+    xs = sorted(ms_list)
+    p90 = xs[min(len(xs) - 1, int(round(0.9 * (len(xs) - 1))))]
+    return {"median": statistics.median(xs), "min": xs[0], "p90": p90,
+            "mean": sum(xs) / len(xs), "n": len(xs)}
 
 
 def config_desc(cfg):
@@ -214,7 +246,7 @@ def config_desc(cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -222,6 +254,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the lines of the mid and varlen workloads")
     ap.add_argument("--bwd-config", default=None,
                     help="named workload of the bwd line (default: the forward's workload)")
     args = ap.parse_args()
@@ -292,9 +326,12 @@ def main():
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t0.record(stream)
     for i in range(args.steps):
+        step_ev[i].record(stream)
         step(ev_sets[i])
+    step_ev[args.steps].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -341,6 +378,7 @@ def main():
                      "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": stage_avg[dom],
                      "peak_source": peak_src},
         "stages_ms": dict(zip(stages, stage_avg)),
+        "step_ms": step_stats([step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]),
         "gpu_launches": args.steps * (len(stages) + 2),
         "clocks": clk,
     }
@@ -361,6 +399,9 @@ def main():
             result["bwd"] = bench_bwd(kda, lib, cfg, inp, S0, dev, stream, hbm_peak)
     if rank == 0 and not args.no_bwd and not args.no_segment:
         result["segment_mode_bwd"] = bench_segment_bwd(kda, dev, stream)
+    if rank == 0 and not args.no_configs:
+        result["config_lines"] = {name: bench_workload(kda, lib, CONFIGS[name], dev, stream, hbm_peak, tc_peak)
+                                  for name in ("mid_bf16", "varlen_bf16")}
     if not args.no_e2e:
         result["e2e"] = bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world)
     if rank == 0 and not args.no_cpu_baseline:
@@ -372,11 +413,17 @@ def main():
             b = nseq % cfg.B
             s_, n_, threads = cpu_oracle_sample(cfg, inp_cpu, [(b, h) for h in range(H)], cfg.T)
             secs, th, nseq = secs + s_, th + n_, nseq + 1
+        # single-threaded: 4 heads of one sequence, whole length (~1 s)
+        s1, n1, _ = cpu_oracle_sample(cfg, inp_cpu, [(0, h) for h in range(4)], cfg.T, nthreads=1)
         result["cpu_baseline"] = {
             "value": th / secs / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle on {nseq} whole sequences of the batch (rows 0..{cfg.B - 1} in "
                       f"turn), all {H} heads x {cfg.T} tokens each ({th} token-heads, {secs:.1f} s); "
-                      f"tokens/s = token-heads/s / H"}
+                      f"tokens/s = token-heads/s / H",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "single_thread": {"value": n1 / s1 / H, "unit": "tokens/s", "cores": 1,
+                              "sample": f"4 heads x {cfg.T} tokens of sequence 0 ({s1:.1f} s), "
+                                        f"token-heads/s / H"}}
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -398,6 +445,91 @@ def load_traffic(kernel):
         return ent["bytes"]
     except Exception:
         return None
+
+
+def bench_workload(kda, lib, cfg, dev, stream, hbm_peak, tc_peak, steps=50, warmup=5):
+    """One forward workload other than the headline: mid_bf16 (B=2, T=4096,
+    H=16, no initial state) or varlen_bf16 (64 packed sequences with states
+    gathered from and scattered back to a 512-row pool, ~10% invalid rows).
+    A 256 MiB buffer is written between steps (L2 flush); each step is timed
+    with CUDA events, kernel durations from events between the stages."""
+    import torch
+    from chunked_kimi_delta_gb300.inputs import make_inputs
+    inp = make_inputs(cfg, device=dev)
+    H, K, V = cfg.H, cfg.dk, cfg.dv
+    kw = dict(scale=float(K ** -0.5), a_log=inp["a_log"], dt_bias=inp["dt_bias"], l2norm_qk=cfg.l2norm,
+              beta_sigmoid=cfg.beta_sigmoid, gate_in_kernel=cfg.gate_in_kernel, use_exp2=cfg.use_exp2)
+    cu = inp["cu_seqlens"]
+    pool = inp.get("pool")
+    N = (cu.numel() - 1) if cu is not None else cfg.B
+    S0 = torch.empty(N, H, K, V, device=dev) if pool is not None else inp["initial_state"]
+    fa, out, fin, ws = kda.prepare_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                             cu_seqlens=cu, initial_state=S0, **kw)
+    stages = kda.kda_chunk_fwd_stages(fa)
+    sp = stream.cuda_stream
+
+    def step(events=None):
+        if pool is not None:
+            kda.kda_state_gather(pool, inp["idx"], flags=inp["flags"], packed=S0, stream=stream)
+        if events is not None:
+            kda.kda_chunk_fwd_profiled(fa, events, stream=stream)
+        else:
+            st = lib.kda_chunk_fwd(ctypes.byref(fa), sp)
+            if st:
+                raise kda.KdaError(st, "kda_chunk_fwd")
+        if pool is not None:
+            kda.kda_state_scatter(pool, inp["idx"], fin, stream=stream)
+
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(steps)]
+    se = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for es in ev:  # the library records them by handle: create them first
+        for e in es:
+            e.record(stream)
+    for i in range(steps):
+        flush.zero_()
+        se[i][0].record(stream)
+        step(ev[i])
+        se[i][1].record(stream)
+    torch.cuda.synchronize()
+    status = kda.kda_get_device_status(ws)
+    if status:
+        raise kda.KdaError(status, "device status")
+    st = step_stats([a.elapsed_time(b) for a, b in se])
+    stage_avg = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / steps for j in range(len(stages))]
+    tokens = int(inp["q"].numel() // (inp["q"].shape[-2] * K))
+    th = tokens * H
+    n_init = N if S0 is not None else 0               # states read by the forward
+    state_bytes = 4 * K * V * H * (n_init + N)        # + final states written
+    dom = max(range(len(stages)), key=lambda i: stage_avg[i])
+    name = stages[dom]
+    if name.startswith("intra") or name == "tc_prep":
+        dom_bytes = intra_alg_bytes_per_token_head(K, V) * th
+    elif name.startswith("inter") or name == "tc_chain":
+        dom_bytes = 2 * V * th + state_bytes
+    else:
+        dom_bytes = alg_bytes_per_token_head(K, V) * th
+    fwd_bytes = alg_bytes_per_token_head(K, V) * th + state_bytes
+    ms = st["median"]
+    desc = (f"{cfg.name}: B={cfg.B} T={cfg.T} H={H} d={K} bf16" if cu is None else
+            f"{cfg.name}: {N} packed sequences, {tokens} tokens (lengths U{{{cfg.len_lo}..{cfg.len_hi}}}), "
+            f"H={H} d={K} bf16, states gathered from / scattered to a {cfg.pool_rows}-row fp32 pool")
+    res = {"workload": desc, "tokens": tokens, "tokens_per_s": tokens / (ms / 1e3), "step_ms": st,
+           "tflops": th * alg_flops_per_token_head(K, V) / (ms / 1e3) / 1e12,
+           "hbm_frac_step": fwd_bytes / (ms / 1e3) / 1e9 / hbm_peak,
+           "stages_ms": dict(zip(stages, stage_avg)),
+           "l2_policy": "256 MiB buffer written between steps (flush)",
+           "roofline": {"bound": "hbm", "kernel": name, "achieved": dom_bytes / (stage_avg[dom] / 1e3) / 1e9,
+                        "peak": hbm_peak, "unit": "GB/s",
+                        "frac": dom_bytes / (stage_avg[dom] / 1e3) / 1e9 / hbm_peak,
+                        "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": stage_avg[dom]}}
+    res["tensor_peak_frac"] = res["tflops"] / tc_peak
+    del inp, fa, out, fin, ws, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode(kda, dev, stream, hbm_peak, steps=50, warmup=5):
@@ -657,8 +789,26 @@ def bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world, st
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
+    # the host link of this machine, measured with plain copies of the same sizes
+    # (one page-locked source / destination of each direction)
+    dev_buf = torch.empty(h2d, dtype=torch.uint8, device=inp["q"].device)
+    hbuf = torch.empty(h2d, dtype=torch.uint8, pin_memory=True)
+    link = {}
+    for name, dst, src, nbytes in (("h2d", dev_buf, hbuf, h2d), ("d2h", hbuf[:d2h], dev_buf[:d2h], d2h)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        link[name + "_gbs"] = nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+    link_ms = 1e3 * (h2d / (link["h2d_gbs"] * 1e9) + d2h / (link["d2h_gbs"] * 1e9))
+    del dev_buf, hbuf
     return {"value": cfg.B * cfg.T * world / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "host_link": {**link, "serial_copy_ms": link_ms,
+                          "note": "plain copies of the step's bytes on this box, one direction at a time"},
             "api": "kda_chunk_fwd_host (host q/k/v/gate/beta/o, page-locked)"}
 
 
