@@ -68,6 +68,7 @@ constexpr uint32_t M_TOT = S_MISC + 768;    // fp32 [8][128] row-group gate tota
 constexpr uint32_t M_BAR = S_MISC + 4864;   // bar_v, bar_mma
 constexpr uint32_t M_TSLOT = S_MISC + 4880;
 constexpr uint32_t M_ABORT = S_MISC + 4884;
+constexpr uint32_t M_STRONG = S_MISC + 4888;  // some warp saw strong decay in this item
 constexpr uint32_t M_ITEM = S_MISC + 4896;  // 2 x ItemSlot
 constexpr uint32_t SMEM_BYTES = S_MISC + 4960 + 1024;
 
@@ -185,6 +186,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   uint64_t *bar_mma = bar_v + 1;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + M_TSLOT);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + M_ABORT);
+  uint32_t *strong_flag = reinterpret_cast<uint32_t *>(sm + M_STRONG);
   ItemSlot *slots = reinterpret_cast<ItemSlot *>(sm + M_ITEM);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -205,6 +207,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     tc::mbar_init(bar_mma, 1);
     tc::mbar_fence_init();
     *abort_flag = 0;
+    *strong_flag = 0;
     tc::tma_prefetch_desc(&maps.v);
   }
   tc::tc_fence_before();
@@ -387,15 +390,15 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
           for (int j = 0; j < 4; ++j) Gl[rr][j] += prev[j];
       }
-      // strong decay: the largest move of the gate inside this thread's
-      // sub-block, relative to the sub-block's reference
-      {
-        float gm = 0.f;
+      // strong decay: the gate decays (g <= 0), so it moves furthest inside
+      // a sub-block over the whole sub-block: warp 0 compares the four
+      // sub-block totals of its channels (every warp holds the same ones)
+      if (warp == 0) {
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) gm = fmaxf(gm, fabsf(Gl[rr][j]));
-        strong = gm > STRONG_DECAY_LOG2;
+          for (int RR = 0; RR < 4; ++RR)
+            strong |= (bAll[RR][j] - (RR < 3 ? bAll[RR + 1][j] : GC[j])) > STRONG_DECAY_LOG2;
       }
       float eb[4], egc[4], cR[4][4];
 #pragma unroll
@@ -455,8 +458,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     }
     tc::fence_proxy_async_smem();
     // an item under strong decay goes on the list of kda_tc_exact.cu, which
-    // overwrites its package later (this pass still runs it, uniformly)
-    if (__syncthreads_or(strong) && tid == 0) flag_list[atomicAdd(flag_count, 1u)] = (uint32_t)w;
+    // overwrites its package later (this pass still runs it, uniformly):
+    // the warps that see it mark the item, thread 0 lists it after the next
+    // barrier
+    if (__any_sync(0xffffffffu, strong) && lane == 0) atomicOr(strong_flag, 1u);
+    __syncthreads();
 
     // ---- MMA 1: [kE; qE] x B1^T -> D1 (128 x 160)
     if (tid == 0) {
@@ -479,6 +485,10 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     tc::tc_fence_after();
     __syncthreads();
     if (*abort_flag) break;
+    if (tid == 0 && *strong_flag) {  // read before the barriers ahead of the next item's marks
+      flag_list[atomicAdd(flag_count, 1u)] = (uint32_t)w;
+      *strong_flag = 0;
+    }
 
     // ---- read D1: L (k rows) to shared fp32, Aqk (q rows) to the package;
     //      zero the inverse buffer
