@@ -126,6 +126,45 @@ __device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
   return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
+// fp32 x rounded to tf32 (to nearest), as the bits an MMA operand takes.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// d += a b for one m16n8k8 tf32 tile (warp-level MMA, fp32 accumulate).
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                                 const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc += X[0:16, 0:KK] Y[0:KK, 0:8] for one warp (X, Y fp32 in shared
+// memory, row strides ldx, ldy; g = lane / 4, t = lane % 4), as m16n8k8
+// tf32 MMAs with fp32 accumulation; acc holds rows g, g + 8 and columns
+// 2 t, 2 t + 1 of the 16 x 8 result.  The operands are rounded to tf32
+// (relative 2^-11), finer than the bf16 (2^-9) in which the inverse leaves
+// for the second MMA.
+template <int KK>
+__device__ __forceinline__ void warp_mm_tf32(const float *X, int ldx, const float *Y, int ldy, int g,
+                                             int t, float (&acc)[4]) {
+#pragma unroll
+  for (int k0 = 0; k0 < KK; k0 += 8) {
+    uint32_t a[4], b[2];
+    a[0] = to_tf32(X[g * ldx + k0 + t]);
+    a[1] = to_tf32(X[(g + 8) * ldx + k0 + t]);
+    a[2] = to_tf32(X[g * ldx + k0 + t + 4]);
+    a[3] = to_tf32(X[(g + 8) * ldx + k0 + t + 4]);
+    b[0] = to_tf32(Y[(k0 + t) * ldy + g]);
+    b[1] = to_tf32(Y[(k0 + t + 4) * ldy + g]);
+    mma_m16n8k8_tf32(acc, a, b);
+  }
+}
+
 // Barrier over the 128 threads of one half of the CTA (ids 1, 2).
 __device__ __forceinline__ void half_sync(int half) {
   asm volatile("bar.sync %0, 128;" :: "r"(1 + half) : "memory");
@@ -609,80 +648,46 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       }
       // step (2) of a half reads only that half's diagonal blocks
       half_sync(warp >> 2);
-      // (2) 32 x 32 diagonal halves: X_10 = -X_1 (L_10 X_0), X_32 = -X_3 (L_32 X_2);
-      //     thread = (half, row, column pair)
+      // (2) 32 x 32 diagonal halves: X_10 = -X_1 (L_10 X_0), X_32 = -X_3 (L_32 X_2),
+      //     16 x 16 x 16 products as warp-level MMAs: in half pr, warps 0 and 1
+      //     of the half own the 8-column tiles of the 16 x 16 result
       {
-        const int pr = tid >> 7, ii = (tid >> 3) & 15, jc = 2 * (tid & 7);
+        const int pr = warp >> 2, wl = warp & 3;
         const int rI = 32 * pr + 16, cJ = 32 * pr;
+        const int g = lane >> 2, t = lane & 3;
         float *T2 = TT + pr * 16 * TTS;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-          const float4 l = *reinterpret_cast<const float4 *>(LF + (rI + ii) * LFS + cJ + m);
-          const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const float2 x = *reinterpret_cast<const float2 *>(AF + (cJ + m + mm) * LFS + cJ + jc);
-            a0 = fmaf(lv[mm], x.x, a0);
-            a1 = fmaf(lv[mm], x.y, a1);
-          }
+        if (wl < 2) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          warp_mm_tf32<16>(LF + rI * LFS + cJ, LFS, AF + cJ * LFS + cJ + 8 * wl, LFS, g, t, acc);
+          *reinterpret_cast<float2 *>(T2 + g * TTS + 8 * wl + 2 * t) = make_float2(acc[0], acc[1]);
+          *reinterpret_cast<float2 *>(T2 + (g + 8) * TTS + 8 * wl + 2 * t) = make_float2(acc[2], acc[3]);
         }
-        *reinterpret_cast<float2 *>(T2 + ii * TTS + jc) = make_float2(a0, a1);
         half_sync(pr);
-        a0 = a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-          const float4 l = *reinterpret_cast<const float4 *>(AF + (rI + ii) * LFS + rI + m);
-          const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const float2 x = *reinterpret_cast<const float2 *>(T2 + (m + mm) * TTS + jc);
-            a0 = fmaf(lv[mm], x.x, a0);
-            a1 = fmaf(lv[mm], x.y, a1);
-          }
+        if (wl < 2) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          warp_mm_tf32<16>(AF + rI * LFS + rI, LFS, T2 + 8 * wl, TTS, g, t, acc);
+          *reinterpret_cast<float2 *>(AF + (rI + g) * LFS + cJ + 8 * wl + 2 * t) = make_float2(-acc[0], -acc[1]);
+          *reinterpret_cast<float2 *>(AF + (rI + g + 8) * LFS + cJ + 8 * wl + 2 * t) =
+              make_float2(-acc[2], -acc[3]);
         }
-        *reinterpret_cast<float2 *>(AF + (rI + ii) * LFS + cJ + jc) = make_float2(-a0, -a1);
       }
       __syncthreads();
-      // (3) lower-left 32 x 32 block: A_21 = -A_2 (L_21 A_1); thread = 2 x 2
-      //     outputs (rows 2 i2, 2 i2 + 1; columns 2 j2, 2 j2 + 1)
+      // (3) lower-left 32 x 32 block: A_21 = -A_2 (L_21 A_1), both 32 x 32 x 32
+      //     products on the tensor cores with warp-level MMAs (operands and
+      //     results stay in registers, no tensor-memory round trip); warp w
+      //     owns the 16 x 8 output tile (rows 16 (w >> 2), columns 8 (w & 3))
       {
-        const int i2 = 2 * (tid >> 4), j2 = 2 * (tid & 15);
-        float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 32; m += 4) {
-          const float4 l0 = *reinterpret_cast<const float4 *>(LF + (32 + i2) * LFS + m);
-          const float4 l1 = *reinterpret_cast<const float4 *>(LF + (33 + i2) * LFS + m);
-          const float lv0[4] = {l0.x, l0.y, l0.z, l0.w}, lv1[4] = {l1.x, l1.y, l1.z, l1.w};
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const float2 x = *reinterpret_cast<const float2 *>(AF + (m + mm) * LFS + j2);
-            c00 = fmaf(lv0[mm], x.x, c00);
-            c01 = fmaf(lv0[mm], x.y, c01);
-            c10 = fmaf(lv1[mm], x.x, c10);
-            c11 = fmaf(lv1[mm], x.y, c11);
-          }
-        }
-        *reinterpret_cast<float2 *>(TT + i2 * TTS + j2) = make_float2(c00, c01);
-        *reinterpret_cast<float2 *>(TT + (i2 + 1) * TTS + j2) = make_float2(c10, c11);
+        const int rt = 16 * (warp >> 2), ct = 8 * (warp & 3);
+        const int g = lane >> 2, t = lane & 3;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_mm_tf32<32>(LF + (32 + rt) * LFS, LFS, AF + ct, LFS, g, t, acc);
+        *reinterpret_cast<float2 *>(TT + (rt + g) * TTS + ct + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2 *>(TT + (rt + g + 8) * TTS + ct + 2 * t) = make_float2(acc[2], acc[3]);
         __syncthreads();
-        c00 = c01 = c10 = c11 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 32; m += 4) {
-          const float4 l0 = *reinterpret_cast<const float4 *>(AF + (32 + i2) * LFS + 32 + m);
-          const float4 l1 = *reinterpret_cast<const float4 *>(AF + (33 + i2) * LFS + 32 + m);
-          const float lv0[4] = {l0.x, l0.y, l0.z, l0.w}, lv1[4] = {l1.x, l1.y, l1.z, l1.w};
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const float2 x = *reinterpret_cast<const float2 *>(TT + (m + mm) * TTS + j2);
-            c00 = fmaf(lv0[mm], x.x, c00);
-            c01 = fmaf(lv0[mm], x.y, c01);
-            c10 = fmaf(lv1[mm], x.x, c10);
-            c11 = fmaf(lv1[mm], x.y, c11);
-          }
-        }
-        *reinterpret_cast<float2 *>(AF + (32 + i2) * LFS + j2) = make_float2(-c00, -c01);
-        *reinterpret_cast<float2 *>(AF + (33 + i2) * LFS + j2) = make_float2(-c10, -c11);
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        warp_mm_tf32<32>(AF + (32 + rt) * LFS + 32, LFS, TT + ct, TTS, g, t, acc);
+        *reinterpret_cast<float2 *>(AF + (32 + rt + g) * LFS + ct + 2 * t) = make_float2(-acc[0], -acc[1]);
+        *reinterpret_cast<float2 *>(AF + (32 + rt + g + 8) * LFS + ct + 2 * t) = make_float2(-acc[2], -acc[3]);
       }
       __syncthreads();
       if (a_out) {  // A = (I + L)^-1 of the item in fp32, for a backward (rows past the end: 0)
