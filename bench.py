@@ -196,7 +196,7 @@ def run_reference(args, rank):
     if rank != 0:
         return
     from chunked_kimi_delta_gb300.inputs import CONFIGS, make_inputs
-    cfg = CONFIGS[WORKLOAD]
+    cfg = CONFIGS[args.workload]
     one = cfg.replace(B=1)   # one sequence of the workload's shape and distributions
     inp = make_inputs(one, device="cpu")
     units = [(0, h) for h in range(cfg.H)]
@@ -238,7 +238,8 @@ def config_desc(cfg):
                          f"initial states gathered from a 512-row fp32 pool, final states "
                          f"scattered back"),
             "B": cfg.B, "T": cfg.T, "H": cfg.H, "dk": cfg.dk, "dv": cfg.dv, "chunk": 64,
-            "l2_policy": "inputs (1.35 GB) larger than L2 (129 MB); no flush"}
+            "l2_policy": (f"inputs ({cfg.B * cfg.T * cfg.H * intra_alg_bytes_per_token_head(cfg.dk, cfg.dv) / 1e9:.2f}"
+                          f" GB) larger than L2 (129 MB); no flush")}
 
 
 # ---------------------------------------------------------------- our arm
@@ -256,6 +257,9 @@ def main():
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the lines of the mid and varlen workloads")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="fixed-length bf16 d=128 workload of the main line (default: the "
+                         "Kimi-shaped batch; a smaller one serves profiling)")
     ap.add_argument("--bwd-config", default=None,
                     help="named workload of the bwd line (default: the forward's workload)")
     args = ap.parse_args()
@@ -277,7 +281,9 @@ def main():
     dev = torch.device("cuda", local)
     hbm_peak, tc_peak, tc_sus, peak_src = load_peaks()
 
-    cfg = CONFIGS[WORKLOAD]
+    cfg = CONFIGS[args.workload]
+    if cfg.seq_lens or cfg.varlen_count or cfg.dtype != "bf16" or cfg.dk != 128 or cfg.num_segments:
+        raise SystemExit("--workload takes a fixed-length bf16 d=128 workload")
     inp = make_inputs(cfg, device=dev, seed=rank)
     H, K, V = cfg.H, cfg.dk, cfg.dv
     gen = torch.Generator(device=dev)
