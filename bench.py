@@ -408,6 +408,13 @@ def main():
     if rank == 0 and not args.no_configs:
         result["config_lines"] = {name: bench_workload(kda, lib, CONFIGS[name], dev, stream, hbm_peak, tc_peak)
                                   for name in ("mid_bf16", "varlen_bf16")}
+        # the same batch under strong gate decay (a_log ~ U(1, 3): about -2 to -60 nats per
+        # token), where the chunks whose 16-token sub-blocks decay past the factored range are
+        # recomputed exactly; reported with the share of such (chunk, head) items
+        strong = cfg.replace(name=cfg.name + "_strong_decay", a_log_range=(1.0, 3.0))
+        line = bench_workload(kda, lib, strong, dev, stream, hbm_peak, tc_peak)
+        line["strong_item_share"] = strong_item_share(strong, dev)
+        result["strong_decay"] = line
     if not args.no_e2e:
         result["e2e"] = bench_e2e(kda, lib, cfg, inp, pool, idx, fa, out, fin, S0, stream, world)
     if rank == 0 and not args.no_cpu_baseline:
@@ -536,6 +543,24 @@ def bench_workload(kda, lib, cfg, dev, stream, hbm_peak, tc_peak, steps=50, warm
     del inp, fa, out, fin, ws, flush
     torch.cuda.empty_cache()
     return res
+
+
+def strong_item_share(cfg, dev) -> float:
+    """Share of (chunk, head) items with a 16-token sub-block whose decay
+    exceeds 96 log2 units in some channel (the items the library recomputes
+    exactly), from the workload's own gate: g = -exp(a_log) softplus(x +
+    dt_bias), summed over each sub-block."""
+    import torch
+    from chunked_kimi_delta_gb300.inputs import make_inputs
+    inp = make_inputs(cfg, device=dev)
+    g = -torch.exp(inp["a_log"])[:, None] * torch.nn.functional.softplus(inp["g"] + inp["dt_bias"])
+    B, T, H, K = g.shape
+    sub = g.reshape(B, T // 16, 16, H, K).sum(2) * 1.4426950408889634   # [B, T/16, H, K]
+    strong_sub = (-sub > 96.0).any(-1)                                    # [B, T/16, H]
+    item = strong_sub.reshape(B, T // 64, 4, H).any(2)                    # [B, T/64, H]
+    share = float(item.float().mean())
+    del inp, g, sub
+    return share
 
 
 def bench_decode(kda, dev, stream, hbm_peak, steps=50, warmup=5):

@@ -157,16 +157,15 @@ struct TcMaps {
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
                      int H, int Hk, TcMaps &maps);
 
-// Strong decay: an item in which some channel's chunk-local gate (log2
-// units) moves by more than this inside one 16-token sub-block is computed
-// by the exact CUDA-core kernel of kda_tc_exact.cu instead of the factored
-// tensor-core products (whose factors then stay inside [2^-96, 2^96]).
+// Strong decay: in an item in which some channel's chunk-local gate (log2
+// units) moves by more than this inside one 16-token sub-block, the prep
+// computes the factored products' at-risk parts from exact gate differences
+// (for every other item the factors stay inside [2^-96, 2^96]).
 constexpr float STRONG_DECAY_LOG2 = 96.f;
 
-// The prep of every (chunk, head), then the exact recomputation of the items
-// it listed under strong decay.  flag_count (one word, cleared here) and
-// flag_list ([nchunks * H] entries, item = chunk * H + head) are scratch the
-// caller keeps for the backward, which reads the same list.
+// The prep of every (chunk, head).  flag_count (one word, cleared here) and
+// flag_list ([nchunks * H] entries, item = chunk * H + head) receive the
+// items under strong decay, for the backward's exact pass.
 cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, const void *v,
                            const float *x, const float *beta, const GateParams &gp,
                            const SeqInfo &s, int64_t nchunks, int H, int Hk, char *pkg,
@@ -174,13 +173,6 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
                            cudaStream_t st, float *a_out = nullptr);
 // a_out: when given, [nchunks, H, 64, 64] fp32 receives A = (I + L)^-1 of
 // every item (the backward's intra-chunk stage reuses it).
-
-// The exact recomputation alone (kda_tc_exact.cu): overwrites the package
-// (and a_out) of each of the *flag_count items in flag_list.
-cudaError_t launch_tc_prep_exact(const void *q, const void *k, const void *v, const float *x,
-                                 const float *beta, const GateParams &gp, const SeqInfo &s,
-                                 int64_t nitems, int H, int Hk, const uint32_t *flag_count,
-                                 const uint32_t *flag_list, char *pkg, float *a_out, cudaStream_t st);
 
 struct ChainArgs {
   const char *pkg;

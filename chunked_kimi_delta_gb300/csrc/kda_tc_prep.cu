@@ -16,11 +16,14 @@
 // 2^{G_r - b_R} <= 1; column j is stored once per later sub-block R' as
 // 2^{b_R' - G_j} <= 1 (off-diagonal blocks) and once with its own block's
 // reference, 2^{b_R(j) - G_j} (diagonal blocks, bounded by the decay of the
-// block's own 16 tokens).  An item in which some channel's gate moves by more
-// than STRONG_DECAY_LOG2 inside one sub-block is put on a list instead, and
-// kda_tc_exact.cu recomputes it from exact gate differences; every factor
-// this kernel builds for the other items lies inside [2^-96, 2^96], where
-// bf16 and fp32 represent it without flush or overflow.  One M=128 x N=160 x K=128
+// block's own 16 tokens).  Where some channel's gate moves by more than
+// STRONG_DECAY_LOG2 inside one sub-block, the affected threads rewrite their
+// off-diagonal column factors and kg from exact exponents, and the four
+// diagonal 16 x 16 blocks of L and A_qk are recomputed from exact gate
+// differences on the CUDA cores (every off-diagonal product has both factors
+// <= 1, so it stays exact up to terms below 2^-126); the item is listed for
+// the backward, which does the same for its own factored products.  For every
+// other item all factors lie inside [2^-96, 2^96].  One M=128 x N=160 x K=128
 // tcgen05 MMA then yields every needed block of both A_kk and A_qk:
 //   A rows  0..63 : k^_r 2^{G_r - b_R}      A rows 64..127: q^_r 2^{G_r - b_R}
 //   B rows  0..15 : k^_j 2^{b_1 - G_j}, j < 16
@@ -56,6 +59,9 @@ constexpr uint32_t S_TT = 51200;     // fp32 scratch [32][36]
 constexpr uint32_t S_AINV = 33792;
 // staging of package parts for bulk stores (regions free at that time):
 constexpr uint32_t S_STG_AQK = 73728;  // Aqk image (8192), written after MMA 1 (B1 dead)
+// strong decay, between the D1 readout and the inverse: one sub-block's raw
+// q, k (bf16) and chunk-local gate (fp32), 16 rows x 128 channels (B1 dead)
+constexpr uint32_t S_FIX = 56320;      // G [16][128] fp32, then q, k [16][128] bf16 (ends at 72704)
 constexpr uint32_t S_STG_W = 90112;    // w rows of WQ, 2 panels x 8192, after MMA 2 (B2A dead)
 constexpr uint32_t S_STG_U = 49152;    // U image (16384), after MMA 2 (B1 dead)
 // OPA holds nothing between items: phase 1 parks the raw q and k rows there,
@@ -203,6 +209,212 @@ __device__ __forceinline__ void bulk_store_hint(void *dst, const void *src, uint
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
                :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(tc::smem_u32(src)), "r"(bytes), "l"(pol)
                : "memory");
+}
+
+// Strong decay, per thread: its channels decay past the factored range
+// inside their sub-block, so the column factor k^ 2^{b_R - G} may be clamped;
+// its off-diagonal copies k^ 2^{b_R' - G} (B1) and kg = k^ 2^{G_C - G} (the
+// package), both <= 1, are rewritten from exact exponents.  k and the gate
+// input come again from global memory (OPA holds the scaled operand by now).
+// Out of line, so that the common path's registers do not carry it.
+__device__ __noinline__ void strong_factors_exact(uint8_t *sm, uint8_t *pk, const __nv_bfloat16 *kg_in,
+                                                  const float *xg_in, const GateParams &gp, int h, int len,
+                                                  int64_t base_h, int64_t base_k, int64_t rowH, int64_t rowHk,
+                                                  uint32_t kp160, uint32_t kp64, uint64_t pol_once,
+                                                  uint64_t pol_qk) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float *tot = reinterpret_cast<const float *>(sm + M_TOT);
+  const float *rk = reinterpret_cast<const float *>(sm + M_RK);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c0 = 4 * lane, R = warp >> 1;
+  const uint32_t ch16 = (uint32_t)((lane & 15) >> 1), cbyte = (uint32_t)(lane & 1) * 8u;
+  const bool gate = (gp.flags & KDA_GATE_IN_KERNEL) != 0;
+  float dl[4][4], dg[4], acc[4];
+  {
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, bA[4][4];
+#pragma unroll
+    for (int gg = 0; gg < 8; ++gg) {
+      const float4 t = *reinterpret_cast<const float4 *>(tot + gg * 128 + c0);
+      const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if ((gg & 1) == 0) bA[gg >> 1][j] = a[j];
+        if (gg == (warp | 1) - 1) acc[j] = (warp & 1) ? tv[j] : 0.f;  // gate before this group
+        a[j] += tv[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float bl = bA[0][j];
+#pragma unroll
+      for (int RR = 1; RR < 4; ++RR)
+        if (RR == R) bl = bA[RR][j];
+#pragma unroll
+      for (int RR = 1; RR < 4; ++RR) dl[RR][j] = bA[RR][j] - bl;
+      dg[j] = a[j] - bl;
+    }
+  }
+  const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
+  float dbl[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    dbl[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + j] * kLog2e : 0.f;
+#pragma unroll 1
+  for (int rr = 0; rr < 8; ++rr) {
+    const int r = 8 * warp + rr;
+    const uint32_t rowb = (uint32_t)r * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
+    float kn[4] = {0.f, 0.f, 0.f, 0.f}, xv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < len) {
+      const uint2 kraw = ldg_u2_hint(kg_in + base_k + r * rowHk + c0, pol_qk);
+      const float4 x4 = ldg_f4_hint(xg_in + base_h + r * rowH + c0, pol_once);
+      const float2 ka = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw.x));
+      const float2 kb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw.y));
+      const float sk = rk[r];
+      kn[0] = ka.x * sk; kn[1] = ka.y * sk; kn[2] = kb.x * sk; kn[3] = kb.y * sk;
+      xv[0] = x4.x; xv[1] = x4.y; xv[2] = x4.z; xv[3] = x4.w;
+    }
+    float G[4], x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // the gate as in phase 1, chunk-local from the sub-block start
+      float g;
+      if (gate) {
+        const float z = fmaf(xv[j], kLog2e, dbl[j]);
+        g = -A_h * (fmaxf(z, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z))));
+      } else {
+        g = xv[j] * kLog2e;
+      }
+      acc[j] += r < len ? g : 0.f;
+      G[j] = acc[j];
+    }
+#pragma unroll
+    for (int Rp = 1; Rp < 4; ++Rp)
+      if (Rp > R) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = kn[j] * tc::ex2(dl[Rp][j] - G[j]);
+        st_u64(sm + S_B1, kp160 + (uint32_t)b1_off(Rp) * 128u + rowb, pack4(x[0], x[1], x[2], x[3]));
+      }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = kn[j] * tc::ex2(dg[j] - G[j]);
+    stg_hint(pk, PK_KG + kp64 + rowb, pack4(x[0], x[1], x[2], x[3]), pol_once);
+  }
+}
+
+// Strong decay: the four 16 x 16 diagonal blocks of L and A_qk of the item
+// again, from exponentials of exact gate differences (every factor <= 1):
+//   L_rj = beta_r sum_c k^_rc k^_jc 2^{G_rc - G_jc} (j < r),
+//   Aqk_rj = scale sum_c q^_rc k^_jc 2^{G_rc - G_jc} (j <= r),
+// over the item's fp32 L (LFS-strided) and its bf16 A_qk image.  Per
+// sub-block the 256 threads load its 16 rows (raw q, k and the gate, the
+// gate summed from the sub-block start); warp w then takes rows 2w, 2w + 1,
+// a lane four channels, and a reduce-scatter over the warp's lanes leaves the
+// 32 sums of a row (16 of L, 16 of A_qk) one per lane.
+__device__ __noinline__ void diagonal_blocks_exact(uint8_t *sm, const __nv_bfloat16 *qg_in,
+                                                   const __nv_bfloat16 *kg_in, const float *xg_in,
+                                                   const GateParams &gp, int h, int len, int64_t base_h,
+                                                   int64_t base_k, int64_t rowH, int64_t rowHk) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float *FG = reinterpret_cast<float *>(sm + S_FIX);
+  __nv_bfloat16 *FQ = reinterpret_cast<__nv_bfloat16 *>(sm + S_FIX + 8192);
+  __nv_bfloat16 *FK = FQ + 16 * 128;
+  float *LF = reinterpret_cast<float *>(sm + S_LF);
+  const float *rq = reinterpret_cast<const float *>(sm + M_RQ);
+  const float *rk = reinterpret_cast<const float *>(sm + M_RK);
+  const float *sbeta = reinterpret_cast<const float *>(sm + M_BETA);
+  uint8_t *saqk = sm + S_STG_AQK;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool gate = (gp.flags & KDA_GATE_IN_KERNEL) != 0;
+#pragma unroll 1
+  for (int Rb = 0; Rb < 4; ++Rb) {
+    if (tid < 128) {  // thread = channel; the sub-block's 16 rows in order
+      const int c = tid;
+      const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
+      const float dbc = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c] * kLog2e : 0.f;
+      float acc = 0.f;
+#pragma unroll 1
+      for (int rl = 0; rl < 16; ++rl) {
+        const int r = 16 * Rb + rl;
+        __nv_bfloat16 qv = __float2bfloat16_rn(0.f), kv = qv;
+        float g = 0.f;
+        if (r < len) {
+          qv = qg_in[base_k + r * rowHk + c];
+          kv = kg_in[base_k + r * rowHk + c];
+          const float x = xg_in[base_h + r * rowH + c];
+          if (gate) {
+            const float z = fmaf(x, kLog2e, dbc);
+            g = -A_h * (fmaxf(z, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z))));
+          } else {
+            g = x * kLog2e;
+          }
+        }
+        acc += g;
+        FG[rl * 128 + c] = acc;
+        FQ[rl * 128 + c] = qv;
+        FK[rl * 128 + c] = kv;
+      }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int sub = 0; sub < 2; ++sub) {
+      const int rl = 2 * warp + sub, r = 16 * Rb + rl;
+      const int c4 = 4 * lane;
+      float qh[4], kh[4], Gr[4];
+      {
+        const float qs = rq[r], ks = rk[r];
+        const uint2 qq = *reinterpret_cast<const uint2 *>(FQ + rl * 128 + c4);
+        const uint2 kk = *reinterpret_cast<const uint2 *>(FK + rl * 128 + c4);
+        const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq.x));
+        const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq.y));
+        const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.x));
+        const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.y));
+        qh[0] = q0.x * qs; qh[1] = q0.y * qs; qh[2] = q1.x * qs; qh[3] = q1.y * qs;
+        kh[0] = k0.x * ks; kh[1] = k0.y * ks; kh[2] = k1.x * ks; kh[3] = k1.y * ks;
+        const float4 g4 = *reinterpret_cast<const float4 *>(FG + rl * 128 + c4);
+        Gr[0] = g4.x; Gr[1] = g4.y; Gr[2] = g4.z; Gr[3] = g4.w;
+      }
+      float v[32];  // v[j]: L sum with token j, v[16 + j]: A_qk sum
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        v[j] = 0.f;
+        v[16 + j] = 0.f;
+        if (j <= rl) {  // uniform over the warp
+          const float kjs = rk[16 * Rb + j];
+          const uint2 kk = *reinterpret_cast<const uint2 *>(FK + j * 128 + c4);
+          const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.x));
+          const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.y));
+          const float4 g4 = *reinterpret_cast<const float4 *>(FG + j * 128 + c4);
+          const float kj[4] = {k0.x * kjs, k0.y * kjs, k1.x * kjs, k1.y * kjs};
+          const float Gj[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float t = kj[x] * tc::ex2(Gr[x] - Gj[x]);
+            v[j] = fmaf(kh[x], t, v[j]);
+            v[16 + j] = fmaf(qh[x], t, v[16 + j]);
+          }
+        }
+      }
+      // reduce-scatter: after step s the lane keeps the half of its values
+      // selected by lane bit 4 - s; lane l ends with the total of value l
+#pragma unroll
+      for (int st = 0; st < 5; ++st) {
+        const int half = 16 >> st;
+        const bool up = (lane & half) != 0;
+#pragma unroll
+        for (int i2 = 0; i2 < half; ++i2) {
+          const float send = up ? v[i2] : v[i2 + half];
+          const float keep = up ? v[i2 + half] : v[i2];
+          v[i2] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        }
+      }
+      const int j = lane & 15;
+      if (lane < 16) {
+        LF[r * LFS + 16 * Rb + j] = j < rl ? sbeta[r] * v[0] : 0.f;
+      } else {
+        *reinterpret_cast<__nv_bfloat16 *>(saqk + kmaj_off(64, r, 16 * Rb + j)) =
+            __float2bfloat16_rn(j <= rl ? v[0] : 0.f);
+      }
+    }
+    __syncthreads();
+  }
 }
 
 // GROUPED: q, k have Hk < H heads (value head h reads key head h / (H / Hk));
@@ -429,16 +641,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
           for (int j = 0; j < 4; ++j) Gl[rr][j] += prev[j];
       }
-      // strong decay: the gate decays (g <= 0), so it moves furthest inside
-      // a sub-block over the whole sub-block: warp 0 compares the four
-      // sub-block totals of its channels (every warp holds the same ones)
-      if (warp == 0) {
+      // strong decay: the gate decays (g <= 0), so inside a sub-block it
+      // has moved furthest at the last row - of this thread's 8-row group,
+      // and of the sub-block at the second group's last row
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int RR = 0; RR < 4; ++RR)
-            strong |= (bAll[RR][j] - (RR < 3 ? bAll[RR + 1][j] : GC[j])) > STRONG_DECAY_LOG2;
-      }
+      for (int j = 0; j < 4; ++j) strong |= -Gl[7][j] > STRONG_DECAY_LOG2;
       float eb[4], egc[4], cR[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -495,11 +702,13 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
                pack4(kf[0] * egc[0], kf[1] * egc[1], kf[2] * egc[2], kf[3] * egc[3]), pol_once);
       }
     }
+    if (strong)
+      strong_factors_exact(sm, pk, kg_in, xg_in, gp, h, len, base_h, base_k, rowH, rowHk, kp160, kp64, pol_once,
+                           pol_qk);
     tc::fence_proxy_async_smem();
-    // an item under strong decay goes on the list of kda_tc_exact.cu, which
-    // overwrites its package later (this pass still runs it, uniformly):
-    // the warps that see it mark the item, thread 0 lists it after the next
-    // barrier
+    // an item under strong decay: the warps that see it mark it; after the
+    // first MMA its diagonal blocks are recomputed and thread 0 lists it for
+    // the backward
     if (__any_sync(0xffffffffu, strong) && lane == 0) atomicOr(strong_flag, 1u);
     __syncthreads();
 
@@ -524,10 +733,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     tc::tc_fence_after();
     __syncthreads();
     if (*abort_flag) break;
-    if (tid == 0 && *strong_flag) {  // read before the barriers ahead of the next item's marks
+    if (tid == 0 && *strong_flag)  // the backward recomputes these items exactly too
       flag_list[atomicAdd(flag_count, 1u)] = (uint32_t)w;
-      *strong_flag = 0;
-    }
 
     // ---- read D1: L (k rows) to shared fp32, Aqk (q rows) to the package;
     //      zero the inverse buffer
@@ -609,6 +816,12 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();
     __syncthreads();
+    if (*reinterpret_cast<volatile uint32_t *>(strong_flag)) {
+      diagonal_blocks_exact(sm, qg_in, kg_in, xg_in, gp, h, len, base_h, base_k, rowH, rowHk);
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) *strong_flag = 0;  // every thread has read it; the next item marks after barriers
+    }
     if (tid == 0) {
       bulk_store_hint(pk + PK_AQK, sm + S_STG_AQK, 8192, pol_once);
       bulk_commit();
@@ -851,11 +1064,7 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
   kern<<<grid, NT, SMEM_BYTES, st>>>(maps, static_cast<const __nv_bfloat16 *>(q),
                                      static_cast<const __nv_bfloat16 *>(k), x, beta, gp, s, nitems,
                                      H, Hk, pkg, a_out, err, flag_count, flag_list);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // the listed items again, exactly (a few CTAs that find an empty list
-  // return at once)
-  return launch_tc_prep_exact(q, k, v, x, beta, gp, s, nitems, H, Hk, flag_count, flag_list, pkg,
-                              a_out, st);
+  return cudaGetLastError();
 }
 
 }  // namespace tcp

@@ -159,11 +159,13 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
 /* The chunked KDA forward: out, and final_state / h_out / v_new_out when
  * given.  N = B without cu_seqlens, num_seqs with it.
  * Arithmetic: bf16 inputs with dk = dv = 128 run on the tensor cores (bf16
- * operands, fp32 accumulation, inverse and state); a chunk in which some
+ * operands, fp32 accumulation, inverse and state); in a chunk in which some
  * channel's gate falls by more than 96 log2 units (about 66 nats) inside one
- * of its 16-token sub-blocks is recomputed from exact gate differences in
- * fp32 on the CUDA cores, so strong decay costs time, not accuracy.  fp32
- * inputs and the other head sizes run in fp32 on the CUDA cores.
+ * of its 16-token sub-blocks, the parts of the decay-factored products that
+ * could leave the floating-point range are computed from exact gate
+ * differences in fp32 on the CUDA cores, so strong decay costs time, not
+ * accuracy.  fp32 inputs and the other head sizes run in fp32 on the CUDA
+ * cores.
  * With no tokens (B*T == 0, or only empty sequences) the final state is the
  * initial state; q/k/v/g/beta/out may then be NULL.
  * Errors: KDA_ERR_INVALID_ARG (null q/k/v/g/beta/out with tokens, B or H < 1,

@@ -6,8 +6,9 @@ gives lower_bound = -5 for the safe_gate option: decays of several nats per
 token are a regime the method meets.  The tensor-core path factors each
 decay 2^{G_r - G_j} around a reference gate per 16-token sub-block ("KDA Chunk
 Backward - TPU/Pallas Kernel Design", section 3.7); when a sub-block decays so
-fast that the factors leave the floating-point range, the prep lists the
-chunk and an exact CUDA-core pass recomputes it (forward and backward).
+fast that the factors could leave the floating-point range, the prep computes
+the at-risk parts (the diagonal blocks, the affected channels' factors) from
+exact gate differences, and lists the chunk for the backward's exact pass.
 These cases drive that path: a_log ~ U(1, 3), so e^{a_log} is 2.7 to 20 and
 the per-token decay runs from about -2 to -60 nats, and hand-built gates with
 a cliff inside a sub-block.  Each case first checks on the CPU that it really
@@ -23,8 +24,8 @@ from kda_testutil import check, fwd_kwargs, gpu_fwd, make, oracle_problem, to_cu
 pytestmark = pytest.mark.gpu
 
 LOG2E = 1.4426950408889634
-# sub-blocks whose chunk-local gate moves by more than this (log2 units) are
-# the ones the exact pass takes over
+# sub-blocks whose chunk-local gate moves by more than this (log2 units) take
+# the exact paths
 STRONG_LOG2 = 96.0
 
 
