@@ -63,6 +63,14 @@ def max_over_ranks(ms: float, world: int, device) -> float:
     return float(t.item())
 
 
+def rank_inputs(cfg, device, rank: int) -> dict:
+    """The inputs of one rank: the workload drawn with the rank as its seed,
+    so that the ranks process independent batches (weak scaling, no
+    data-path collective)."""
+    from chunked_kimi_delta_gb300.inputs import make_inputs
+    return make_inputs(cfg, device=device, seed=rank)
+
+
 def whole_job_rate(units_per_rank_step: float, world: int, steps: int, ms: float) -> float:
     """Units of all ranks per second over the slowest rank's time (weak scaling)."""
     return units_per_rank_step * world * steps / (ms / 1e3)
@@ -284,7 +292,7 @@ def main():
     cfg = CONFIGS[args.workload]
     if cfg.seq_lens or cfg.varlen_count or cfg.dtype != "bf16" or cfg.dk != 128 or cfg.num_segments:
         raise SystemExit("--workload takes a fixed-length bf16 d=128 workload")
-    inp = make_inputs(cfg, device=dev, seed=rank)
+    inp = rank_inputs(cfg, dev, rank)
     H, K, V = cfg.H, cfg.dk, cfg.dv
     gen = torch.Generator(device=dev)
     gen.manual_seed(1000 + rank)
