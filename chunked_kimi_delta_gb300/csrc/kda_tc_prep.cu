@@ -131,6 +131,16 @@ __device__ __forceinline__ void st_u64(uint8_t *base, uint32_t off, uint2 v) {
 __device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
   return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
+__device__ __forceinline__ uint2 pack4(float2 a, float2 b) {
+  return make_uint2(pack_bf16(a.x, a.y), pack_bf16(b.x, b.y));
+}
+
+// Paired fp32 arithmetic (one packed instruction for two lanes of values,
+// each rounded to nearest as the scalar operation would be).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 
 // fp32 x rounded to tf32 (to nearest), as the bits an MMA operand takes.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
@@ -586,27 +596,31 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, qv[rr]);
       }
 
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 acc[2] = {splat2(0.f), splat2(0.f)};
+      const float2 dbl2[2] = {make_float2(dbl[0], dbl[1]), make_float2(dbl[2], dbl[3])};
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = 8 * warp + rr;
-        const float xv[4] = {xs[rr].x, xs[rr].y, xs[rr].z, xs[rr].w};
+        const float2 xv[2] = {make_float2(xs[rr].x, xs[rr].y), make_float2(xs[rr].z, xs[rr].w)};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float g;
+        for (int p = 0; p < 2; ++p) {
+          float2 g;
           if (gate) {
             // softplus(z) log2 e = max(z, 0) log2 e + log2(1 + 2^{-|z| log2 e})
-            const float z = fmaf(xv[j], kLog2e, dbl[j]);
-            g = -A_h * (fmaxf(z, 0.f) + tc::lg2(1.f + tc::ex2(-fabsf(z))));
+            const float2 z = fma2(xv[p], splat2(kLog2e), dbl2[p]);
+            const float2 t = add2(splat2(1.f), make_float2(tc::ex2(-fabsf(z.x)), tc::ex2(-fabsf(z.y))));
+            g = mul2(splat2(-A_h), add2(make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)),
+                                        make_float2(tc::lg2(t.x), tc::lg2(t.y))));
           } else {
-            g = xv[j] * kLog2e;
+            g = mul2(xv[p], splat2(kLog2e));
           }
-          if (r >= len) g = 0.f;
-          acc[j] += g;
-          Gl[rr][j] = acc[j];
+          if (r >= len) g = splat2(0.f);
+          acc[p] = add2(acc[p], g);
+          Gl[rr][2 * p] = acc[p].x;
+          Gl[rr][2 * p + 1] = acc[p].y;
         }
       }
-      *reinterpret_cast<float4 *>(tot + warp * 128 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4 *>(tot + warp * 128 + c0) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
     }
     // the staging buffers of the previous item must be read out before this
     // item's operand tiles overwrite them
@@ -639,24 +653,37 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) Gl[rr][j] += prev[j];
+          for (int p = 0; p < 2; ++p) {
+            const float2 gs = add2(make_float2(Gl[rr][2 * p], Gl[rr][2 * p + 1]),
+                                   make_float2(prev[2 * p], prev[2 * p + 1]));
+            Gl[rr][2 * p] = gs.x;
+            Gl[rr][2 * p + 1] = gs.y;
+          }
       }
       // strong decay: the gate decays (g <= 0), so inside a sub-block it
       // has moved furthest at the last row - of this thread's 8-row group,
       // and of the sub-block at the second group's last row
 #pragma unroll
       for (int j = 0; j < 4; ++j) strong |= -Gl[7][j] > STRONG_DECAY_LOG2;
-      float eb[4], egc[4], cR[4][4];
+      float ebs[4], egcs[4], cRs[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float bR = bAll[0][j];
 #pragma unroll
         for (int RR = 1; RR < 4; ++RR)
           if (RR == R) bR = bAll[RR][j];
-        eb[j] = tc::ex2(bR);
-        egc[j] = tc::ex2(GC[j] - bR);
+        ebs[j] = tc::ex2(bR);
+        egcs[j] = tc::ex2(GC[j] - bR);
 #pragma unroll
-        for (int RR = 1; RR < 4; ++RR) cR[RR][j] = tc::ex2(fminf(bAll[RR][j] - bR, 0.f));
+        for (int RR = 1; RR < 4; ++RR) cRs[RR][j] = tc::ex2(fminf(bAll[RR][j] - bR, 0.f));
+      }
+      float2 eb[2], egc[2], cR[4][2];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        eb[p] = make_float2(ebs[2 * p], ebs[2 * p + 1]);
+        egc[p] = make_float2(egcs[2 * p], egcs[2 * p + 1]);
+#pragma unroll
+        for (int RR = 1; RR < 4; ++RR) cR[RR][p] = make_float2(cRs[RR][2 * p], cRs[RR][2 * p + 1]);
       }
       if (warp == 0)
         *reinterpret_cast<float4 *>(pk + PK_GC + c0 * 4) =
@@ -675,31 +702,32 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kraw);
         const float2 qa = __bfloat1622float2(q2[0]), qb = __bfloat1622float2(q2[1]);
         const float2 ka = __bfloat1622float2(k2[0]), kb = __bfloat1622float2(k2[1]);
-        const float qn[4] = {qa.x * sq, qa.y * sq, qb.x * sq, qb.y * sq};
-        const float kn[4] = {ka.x * sk, ka.y * sk, kb.x * sk, kb.y * sk};
-        float ke[4], kf[4], qe[4], kd[4], qg[4];
+        const float2 qn[2] = {mul2(qa, splat2(sq)), mul2(qb, splat2(sq))};
+        const float2 kn[2] = {mul2(ka, splat2(sk)), mul2(kb, splat2(sk))};
+        float2 ke[2], kf[2], qe[2], kd[2], qg[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float e = tc::ex2(Gl[rr][j]), f = tc::ex2(fminf(-Gl[rr][j], 126.f));
-          ke[j] = kn[j] * e;
-          kf[j] = kn[j] * f;
-          qe[j] = qn[j] * e;
-          kd[j] = ke[j] * eb[j];  // k^ 2^G, G from the chunk start
-          qg[j] = qe[j] * eb[j];  // scale q^ 2^G
+        for (int p = 0; p < 2; ++p) {
+          const float g0 = Gl[rr][2 * p], g1 = Gl[rr][2 * p + 1];
+          const float2 e = make_float2(tc::ex2(g0), tc::ex2(g1));
+          const float2 f = make_float2(tc::ex2(fminf(-g0, 126.f)), tc::ex2(fminf(-g1, 126.f)));
+          ke[p] = mul2(kn[p], e);
+          kf[p] = mul2(kn[p], f);
+          qe[p] = mul2(qn[p], e);
+          kd[p] = mul2(ke[p], eb[p]);  // k^ 2^G, G from the chunk start
+          qg[p] = mul2(qe[p], eb[p]);  // scale q^ 2^G
         }
-        st_u64(sm + S_OPA, kp128 + orow, pack4(ke[0], ke[1], ke[2], ke[3]));
-        st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, pack4(qe[0], qe[1], qe[2], qe[3]));
-        st_u64(sm + S_B1, kp160 + 96u * 128u + rowb, pack4(kf[0], kf[1], kf[2], kf[3]));
+        st_u64(sm + S_OPA, kp128 + orow, pack4(ke[0], ke[1]));
+        st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, pack4(qe[0], qe[1]));
+        st_u64(sm + S_B1, kp160 + 96u * 128u + rowb, pack4(kf[0], kf[1]));
 #pragma unroll
         for (int Rp = 1; Rp < 4; ++Rp)
           if (Rp > R)
             st_u64(sm + S_B1, kp160 + (uint32_t)b1_off(Rp) * 128u + rowb,
-                   pack4(kf[0] * cR[Rp][0], kf[1] * cR[Rp][1], kf[2] * cR[Rp][2], kf[3] * cR[Rp][3]));
-        st_u64(sm + S_B2A, kp64 + rowb, pack4(kd[0], kd[1], kd[2], kd[3]));
+                   pack4(mul2(kf[0], cR[Rp][0]), mul2(kf[1], cR[Rp][1])));
+        st_u64(sm + S_B2A, kp64 + rowb, pack4(kd[0], kd[1]));
         // package: qg = scale q^ 2^G (WQ rows 0..63), kg = k^ 2^{G_C - G} (KG)
-        stg_hint(pk, PK_WQ + kp128 + rowb, pack4(qg[0], qg[1], qg[2], qg[3]), pol_once);
-        stg_hint(pk, PK_KG + kp64 + rowb,
-               pack4(kf[0] * egc[0], kf[1] * egc[1], kf[2] * egc[2], kf[3] * egc[3]), pol_once);
+        stg_hint(pk, PK_WQ + kp128 + rowb, pack4(qg[0], qg[1]), pol_once);
+        stg_hint(pk, PK_KG + kp64 + rowb, pack4(mul2(kf[0], egc[0]), mul2(kf[1], egc[1])), pol_once);
       }
     }
     if (strong)
@@ -789,11 +817,13 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
           for (int x = 0; x < 16; x += 4) {
             const int j = j0 + x;
+            const float2 p0 = mul2(splat2(br), make_float2(d[cix][x], d[cix][x + 1]));
+            const float2 p1 = mul2(splat2(br), make_float2(d[cix][x + 2], d[cix][x + 3]));
             float4 l4;
-            l4.x = (!diag || j < r) ? br * d[cix][x] : 0.f;
-            l4.y = (!diag || j + 1 < r) ? br * d[cix][x + 1] : 0.f;
-            l4.z = (!diag || j + 2 < r) ? br * d[cix][x + 2] : 0.f;
-            l4.w = (!diag || j + 3 < r) ? br * d[cix][x + 3] : 0.f;
+            l4.x = (!diag || j < r) ? p0.x : 0.f;
+            l4.y = (!diag || j + 1 < r) ? p0.y : 0.f;
+            l4.z = (!diag || j + 2 < r) ? p1.x : 0.f;
+            l4.w = (!diag || j + 3 < r) ? p1.y : 0.f;
             *reinterpret_cast<float4 *>(LF + r * LFS + j) = l4;
           }
         } else {
@@ -922,9 +952,9 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 #pragma unroll
         for (int x = 0; x < 8; x += 2) {
           const int jj = 8 * g + x;
-          const float a0 = (jj <= r) ? AF[r * LFS + jj] * sbeta[jj] : 0.f;
-          const float a1 = (jj + 1 <= r) ? AF[r * LFS + jj + 1] * sbeta[jj + 1] : 0.f;
-          pkd[x / 2] = pack_bf16(a0, a1);
+          const float2 ab = mul2(*reinterpret_cast<const float2 *>(AF + r * LFS + jj),
+                                 *reinterpret_cast<const float2 *>(sbeta + jj));
+          pkd[x / 2] = pack_bf16((jj <= r) ? ab.x : 0.f, (jj + 1 <= r) ? ab.y : 0.f);
         }
         const uint4 av = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
         *reinterpret_cast<uint4 *>(sm + S_AINV + kmaj_off(128, r, 8 * g)) = av;
