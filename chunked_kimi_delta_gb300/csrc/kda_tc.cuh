@@ -147,6 +147,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Paired fp32 arithmetic: one packed instruction for two values, each
+// rounded to nearest exactly as the scalar operation would be.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+// a - b (the product b * -1 is exact, so this rounds as the subtraction does)
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+
 // Host side --------------------------------------------------------------------
 struct TcMaps {
   CUtensorMap q, k, v, x;

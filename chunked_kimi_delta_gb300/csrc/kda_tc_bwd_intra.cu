@@ -533,7 +533,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   for (int sub = 0; sub < 2; ++sub) {
     if (!*abort_flag) {
       if (sub == 0)
-        for (int i = tid; i < BT * 24; i += NT) {  // [row][192 / 8] 16-byte groups, Q and dL rows
+        for (int i = tid; i < BT * (KB_BIG / 8); i += NT) {  // [row][160 / 8] 16-byte groups, Q and dL rows
           // lanes run over rows: their reads of one column fall in different banks
           const int r = (i & 31) + 32 * ((i >> 5) & 1), g8 = (i >> 6) * 8, I = r >> 4, o = seg_off_row(I);
           float xq[8], xd[8];
@@ -570,10 +570,16 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         lds_f8(sG + j * GS + c8, gj);
         const float rk = sRk[j];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float v = j < len ? kr8[e] * rk * tc::ex2(fminf(gr[e] - gj[e], 126.f)) : 0.f;
-          lo[e] = split(v, true);
-          x[e] = sub ? lo[e] : v;
+        for (int e = 0; e < 8; e += 2) {
+          const float2 dg = sub2(make_float2(gr[e], gr[e + 1]), make_float2(gj[e], gj[e + 1]));
+          const float2 f = make_float2(tc::ex2(fminf(dg.x, 126.f)), tc::ex2(fminf(dg.y, 126.f)));
+          float2 v = mul2(mul2(make_float2(kr8[e], kr8[e + 1]), splat2(rk)), f);
+          if (j >= len) v = splat2(0.f);
+          const float2 l = sub2(v, __bfloat1622float2(__float22bfloat162_rn(v)));  // v - bf16(v)
+          lo[e] = l.x;
+          lo[e + 1] = l.y;
+          x[e] = sub ? l.x : v.x;
+          x[e + 1] = sub ? l.y : v.y;
         }
         st_bf16x8(R + R_BB, mnmaj_off(KB_BIG, kr, c8), x);
         if (sub == 0 && kr < 128) st_bf16x8(R + R_BLO, mnmaj_off(128, kr, c8), lo);
@@ -622,16 +628,26 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   //      operand's hi and lo parts are built together
   for (int part = 0; part < 2; ++part) {
     if (!*abort_flag) {
-      for (int i = tid; i < BT * 24; i += NT) {  // A: [row j][192 / 8], lanes over rows
-        const int j = (i & 31) + 32 * ((i >> 5) & 1), g8 = (i >> 6) * 8, J = j >> 4, o = seg_off_col(J);
+      // A, MN-major [K slot][row j]: slot ks of rows j8 .. j8 + 7 (one 16-row
+      // block J) holds token ii = ks - o + 16 J of their segment, i.e. eight
+      // consecutive entries of row ii of dL (or Q); lanes run over K slots
+      for (int i = tid; i < KB_BIG * 8; i += NT) {
+        const int ks = i % KB_BIG, j8 = (i / KB_BIG) * 8, J = j8 >> 4, o = seg_off_col(J);
+        const int ii = ks - o + 16 * J;
         float x[8];
+        if (ks >= o && ks < o + 64 - 16 * J && ii < len) {
+          const float *src = (part == 0 ? sDF : sQF) + ii * FS + j8;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int ii = g8 + e - o + 16 * J;  // token i of this K slot in row j's segment
-          const bool in = g8 + e >= o && g8 + e < o + 64 - 16 * J && ii < len && ii > j;
-          x[e] = in ? (part == 0 ? sDF[ii * FS + j] : sQF[ii * FS + j]) : 0.f;
+          for (int e = 0; e < 8; e += 2) {
+            const float2 v = *reinterpret_cast<const float2 *>(src + e);
+            x[e] = ii > j8 + e ? v.x : 0.f;  // strictly below the diagonal
+            x[e + 1] = ii > j8 + e + 1 ? v.y : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
-        st_bf16x8(R + R_AP, kmaj_off(64, j, g8), x);
+        st_bf16x8(R + R_AP, mnmaj_off(KB_BIG, ks, j8), x);
       }
       for (int i = tid; i < KB_BIG * 16; i += NT) {  // B hi and lo: [160 rows][128 / 8], lanes over rows
         const int kr = (i & 31) + 32 * ((i >> 5) % 5), c8 = ((i >> 5) / 5) * 8;
@@ -643,11 +659,18 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         lds_f8(sG + ref * GS + c8, gr);
         const float rs = part == 0 ? sRk[ii] : sRq[ii], bs = sB[ii];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float f = tc::ex2(fminf(gi[e] - gr[e], 126.f));
-          const float x = ii < len ? (part == 0 ? bs * (raw[e] * rs) : raw[e] * rs) * f : 0.f;
-          xh[e] = x;
-          xl[e] = split(x, true);
+        for (int e = 0; e < 8; e += 2) {
+          const float2 dg = sub2(make_float2(gi[e], gi[e + 1]), make_float2(gr[e], gr[e + 1]));
+          const float2 f = make_float2(tc::ex2(fminf(dg.x, 126.f)), tc::ex2(fminf(dg.y, 126.f)));
+          float2 xs = mul2(make_float2(raw[e], raw[e + 1]), splat2(rs));
+          if (part == 0) xs = mul2(splat2(bs), xs);
+          float2 x = mul2(xs, f);
+          if (ii >= len) x = splat2(0.f);
+          const float2 l = sub2(x, __bfloat1622float2(__float22bfloat162_rn(x)));  // x - bf16(x)
+          xh[e] = x.x;
+          xh[e + 1] = x.y;
+          xl[e] = l.x;
+          xl[e + 1] = l.y;
         }
         st_bf16x8(R + R_BP, mnmaj_off(KB_BIG, kr, c8), xh);
         st_bf16x8(R + R_BPL, mnmaj_off(KB_BIG, kr, c8), xl);
@@ -659,11 +682,11 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     if (!*abort_flag && tid == 0) {
       tc::tc_fence_after();
       const uint32_t ap = tc::smem_u32(R + R_AP), bh = tc::smem_u32(R + R_BP), bl = tc::smem_u32(R + R_BPL);
-      const uint32_t id = tc::idesc_bf16_f32(64, 128, false, true);
+      const uint32_t id = tc::idesc_bf16_f32(64, 128, true, true);
 #pragma unroll
       for (int kk = 0; kk < 20; ++kk) {
         const uint32_t k10 = kk % 10;
-        tc::mma_bf16(tmem + C_D7, tc::smem_desc_sw128(ap + (k10 >> 2) * 8192 + (k10 & 3) * 32, 16, 1024),
+        tc::mma_bf16(tmem + C_D7, tc::smem_desc_sw128(ap + k10 * 2048, KB_BIG * 128, 1024),
                      tc::smem_desc_sw128((kk < 10 ? bh : bl) + k10 * 2048, KB_BIG * 128, 1024), id,
                      part > 0 || kk > 0);
       }
@@ -683,7 +706,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     // every lane works: lane l < 16 and lane l + 16 share row 16 q4 + l, the
     // upper lane taking columns 8..15 of each 16-column load
     const int row = 16 * q4 + (lane & 15), up = lane >> 4, s8 = 8 * up;
-    float pb = 0.f;
+    float2 pb2 = splat2(0.f);
     const int rI = 16 * (row >> 4), rJ = rI + 15;
     const float br = sB[row], qd = sQD[row];
     const bool live = row < len;
@@ -742,21 +765,32 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
           const float qv[4] = {q01.x, q01.y, q23.x, q23.y}, kv4[4] = {k01.x, k01.y, k23.x, k23.y};
           const float rq = sRq[row], rk = sRk[row];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
+          for (int x = 0; x < 4; x += 2) {  // two columns at a time (paired fp32)
             const int e = e4 + x;
-            const float G = Gv[x], GC = Cv[x];
-            const float fq = tc::ex2(G - Iv[x]);                 // <= 1
-            const float fc = tc::ex2(fminf(Jv[x] - G, 0.f));     // <= 1
-            const float eG = tc::ex2(G), ekg = tc::ex2(GC - G);
-            const float qh = qv[x] * rq, kh = kv4[x] * rk;
-            const float aq = fq * mq[e], akr = br * fq * md[e], akc = fc * m7[e];
-            const float dqg = dqgv[e], dkg = dkgv[e];
-            const float kbf = br * eG;
-            oq[x] = aq + qd * kh + dqg * scale * eG;
-            ok[x] = akr + akc + qd * qh + mk[e] * kbf + dkg * ekg;
-            og[x] = qh * aq + kh * akr - kh * akc + mk[e] * kh * kbf + dqg * scale * qh * eG - dkg * kh * ekg;
-            op[x] = dkg * kh * ekg;
-            pb = fmaf(mk[e], kh * eG, fmaf(kh, fq * md[e], pb));
+            auto pr = [&](const float *v, int i) { return make_float2(v[i], v[i + 1]); };
+            const float2 G = pr(Gv, x);
+            const float2 dI = sub2(G, pr(Iv, x)), dJ = sub2(pr(Jv, x), G), dC = sub2(pr(Cv, x), G);
+            const float2 fq = make_float2(tc::ex2(dI.x), tc::ex2(dI.y));                        // <= 1
+            const float2 fc = make_float2(tc::ex2(fminf(dJ.x, 0.f)), tc::ex2(fminf(dJ.y, 0.f)));  // <= 1
+            const float2 eG = make_float2(tc::ex2(G.x), tc::ex2(G.y));
+            const float2 ekg = make_float2(tc::ex2(dC.x), tc::ex2(dC.y));
+            const float2 qh = mul2(pr(qv, x), splat2(rq)), kh = mul2(pr(kv4, x), splat2(rk));
+            const float2 mke = pr(mk, e), fmd = mul2(fq, pr(md, e));
+            const float2 aq = mul2(fq, pr(mq, e)), akr = mul2(splat2(br), fmd), akc = mul2(fc, pr(m7, e));
+            const float2 dqs = mul2(pr(dqgv, e), splat2(scale)), dkg = pr(dkgv, e);
+            const float2 kbf = mul2(splat2(br), eG);
+            const float2 dkh = mul2(dkg, kh);
+            const float2 vq = fma2(dqs, eG, fma2(splat2(qd), kh, aq));
+            const float2 vk = fma2(dkg, ekg, fma2(mke, kbf, fma2(splat2(qd), qh, add2(akr, akc))));
+            const float2 vp = mul2(dkh, ekg);
+            float2 vg = fma2(kh, sub2(akr, akc), mul2(qh, aq));
+            vg = fma2(mul2(dqs, qh), eG, fma2(mul2(mke, kh), kbf, vg));
+            vg = sub2(vg, vp);
+            pb2 = fma2(mke, mul2(kh, eG), fma2(kh, fmd, pb2));
+            oq[x] = vq.x; oq[x + 1] = vq.y;
+            ok[x] = vk.x; ok[x + 1] = vk.y;
+            og[x] = vg.x; og[x + 1] = vg.y;
+            op[x] = vp.x; op[x + 1] = vp.y;
           }
         }
         *reinterpret_cast<float4 *>(fQ + row * GS + cb) = make_float4(oq[0], oq[1], oq[2], oq[3]);
@@ -765,6 +799,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
         *reinterpret_cast<float4 *>(fP + row * GS + cb) = make_float4(op[0], op[1], op[2], op[3]);
       }
     }
+    float pb = pb2.x + pb2.y;
     pb += __shfl_xor_sync(0xffffffffu, pb, 16);
     if (!up) sDB[row * 4 + 2 + hf] = pb;
   }

@@ -135,13 +135,6 @@ __device__ __forceinline__ uint2 pack4(float2 a, float2 b) {
   return make_uint2(pack_bf16(a.x, a.y), pack_bf16(b.x, b.y));
 }
 
-// Paired fp32 arithmetic (one packed instruction for two lanes of values,
-// each rounded to nearest as the scalar operation would be).
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
-
 // fp32 x rounded to tf32 (to nearest), as the bits an MMA operand takes.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
