@@ -136,7 +136,7 @@ __device__ __forceinline__ void st_bf16x8(uint8_t *tile, uint32_t off, const flo
 template <typename Tdq>
 __global__ void __launch_bounds__(NT, 1)
 tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, SeqInfo s, int H, int Hk,
-                    GateParams gp) {
+                    GateParams gp, int64_t nitems) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *sG = reinterpret_cast<float *>(sm + S_G);
@@ -155,22 +155,16 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   volatile uint32_t *abort_flag = tslot + 1;
   uint8_t *R = sm + S_R;
 
-  const int64_t c = (int64_t)blockIdx.x / H;  // head fastest: adjacent CTAs share tokens
-  const int h = (int)(blockIdx.x % H);
-  int n, len;
-  int64_t t0;
-  if (!chunk_lookup(s, c, n, t0, len)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hf = warp >> 2;
-  const int hk = h / (H / Hk);
   const bool gate = (gp.flags & KDA_GATE_IN_KERNEL) != 0;
   const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
   const bool l2n = (gp.flags & KDA_L2NORM_QK) != 0;
   const bool has_do = a.d_out != nullptr;
-  const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
   const float scale = gp.scale;
-  const size_t item = (size_t)(c * H + h);
-  auto tok = [&](int r, int heads, int head, int D) { return ((t0 + r) * heads + head) * (int64_t)D; };
+  const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(a.q);
+  const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(a.k);
+  const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(a.v);
 
   if (warp == 0) {
     tc::tmem_alloc(tslot, TMEM_COLS);
@@ -180,6 +174,32 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     for (int x = 0; x < NBAR; ++x) tc::mbar_init(bar + x, 1);
     tc::mbar_fence_init();
     *abort_flag = 0;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  int issued = 0;    // MMA groups of the current item started (thread 0), for the drain
+  uint32_t par = 0;  // every barrier completes once per item: the item's parity
+
+  // One persistent CTA per SM walks the (chunk, head) items, head fastest
+  // (neighbouring CTAs share tokens); while it works on one item, the next
+  // one's inputs and tile images are fetched into L2.
+  for (int64_t w = blockIdx.x; w < nitems; w += gridDim.x, par ^= 1u) {
+  const int64_t c = w / H;
+  const int h = (int)(w % H);
+  int n, len;
+  int64_t t0;
+  if (!chunk_lookup(s, c, n, t0, len)) break;  // items past the last chunk are all invalid
+  const int hk = h / (H / Hk);
+  const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
+  const size_t item = (size_t)w;
+  auto tok = [&](int r, int heads, int head, int D) { return ((t0 + r) * heads + head) * (int64_t)D; };
+  issued = 0;
+
+  if (tid == 0) {
+    // the previous item's accesses to the tile region precede these copies
+    tc::fence_proxy_async_smem();
     // images of -dv_new, dw, v_new and the dO tile
     tc::mbar_arrive_expect_tx(bar, has_do ? 65536u : 49152u);
     bulk_load(R + R_DVN, a.dv_img + item * 16384, 16384, bar);
@@ -190,14 +210,36 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
       tma_load_3d(R + R_DO + 8192, &map_do, bar, 64, h, (int32_t)t0);
     }
   }
+  {  // the next item's q, k, v and gate rows (a thread each), A and images, into L2
+    const int64_t wn = w + gridDim.x;
+    int nn, lenn;
+    int64_t t0n;
+    if (wn < nitems && chunk_lookup(s, wn / H, nn, t0n, lenn)) {
+      const int hn = (int)(wn % H), hkn = hn / (H / Hk), r = tid & 63, which = tid >> 6;
+      if (r < lenn) {
+        const int64_t t = t0n + r;
+        if (which == 0) prefetch_l2(qin + (t * Hk + hkn) * K, K * 2);
+        else if (which == 1) prefetch_l2(kin + (t * Hk + hkn) * K, K * 2);
+        else if (which == 2) prefetch_l2(vin + (t * H + hn) * V, V * 2);
+        else prefetch_l2(a.g + (t * H + hn) * K, K * 4);
+      }
+      if (tid == 0) {
+        prefetch_l2(a.dv_img + (size_t)wn * 16384, 16384);
+        prefetch_l2(a.dw_img + (size_t)wn * 16384, 16384);
+        prefetch_l2(a.vn_img + (size_t)wn * 16384, 16384);
+        prefetch_l2(a.a_in + (size_t)wn * (BT * BT), BT * BT * 4);
+        if (has_do) {
+          tma_prefetch_l2_3d(&map_do, 0, hn, (int32_t)t0n);
+          tma_prefetch_l2_3d(&map_do, 64, hn, (int32_t)t0n);
+        }
+      }
+    }
+  }
 
   // ---- 0. every global load of the phase first (q, k, v rows; the gate
   //      input; A; beta), then the raw q, k rows to shared memory with their
   //      norms, and the gate in log2 units with its chunk-local inclusive
   //      cumsum (8-row groups in registers, then the groups' prefix)
-  const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(a.q);
-  const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(a.k);
-  const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(a.v);
   const int gc4 = 4 * lane;  // gate layout: rows 8 warp .. 8 warp + 7, channels gc4 .. gc4 + 3
   uint4 qv[4], kv[4], vv[4];
   float4 gx[8], av[4];
@@ -337,13 +379,11 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     st_bf16x8(R + R_AT, kmaj_off(64, r, j8), x);
   }
   tc::fence_proxy_async_smem();
-  bool ok = wait_or_flag(bar, 0, a.err);
+  bool ok = wait_or_flag(bar, par, a.err);
   if (!ok) *abort_flag = 1;
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = *tslot;
-  int issued = 0;  // MMA groups started (thread 0), for the drain
 
   // ---- phase A: M1, M2, M4
   if (!*abort_flag && tid == 0) {
@@ -377,10 +417,10 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
   const bool rv = lane < 16;
   auto wait_mma = [&](int k) -> bool {
     __syncwarp();
-    const bool w = !*abort_flag && __all_sync(0xffffffffu, wait_or_flag(bar + k, 0, a.err));
-    if (!w) *abort_flag = 1;
+    const bool ok = !*abort_flag && __all_sync(0xffffffffu, wait_or_flag(bar + k, par, a.err));
+    if (!ok) *abort_flag = 1;
     tc::tc_fence_after();
-    return w;
+    return ok;
   };
   if (wait_mma(1)) {
     // dA (j < i) -> bf16 MN-major B tile of M3a [i][j]; Q -> sQF; -dvb -> dv, dbeta part
@@ -971,9 +1011,14 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap map_do, TcIntraArgs a, S
     const float b = sB[tid];
     a.dbeta[(t0 + tid) * H + h] = sig ? d * b * (1.f - b) : d;
   }
-  if (*abort_flag && tid == 0) {  // bounded drain of the loads and MMAs this CTA started
-    drain_wait(bar, 0);
-    for (int x = 1; x <= issued; ++x) drain_wait(bar + x, 0);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) break;
+  }  // items
+
+  if (*abort_flag && tid == 0) {  // bounded drain of the loads and MMAs of the item given up on
+    drain_wait(bar, par);
+    for (int x = 1; x <= issued; ++x) drain_wait(bar + x, par);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -988,18 +1033,26 @@ cudaError_t launch_tc_bwd_intra(const TcIntraArgs &a, const SeqInfo &s, int64_t 
   CUtensorMap map_do;
   memset(&map_do, 0, sizeof(map_do));  // not read without d_out
   if (a.d_out && (s.T_tot <= 0 || !make_value_map(a.d_out, s.T_tot, H, map_do))) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)(nchunks * H));
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t nitems = nchunks * H;
+  dim3 grid((unsigned)(nitems < sms ? nitems : sms));  // persistent: one CTA per SM
   cudaError_t e;
   if (a.dq_is_f32) {
     e = cudaFuncSetAttribute(tc_bwd_intra_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    tc_bwd_intra_kernel<float><<<grid, NT, SMEM_BYTES, st>>>(map_do, a, s, H, Hk, gp);
+    tc_bwd_intra_kernel<float><<<grid, NT, SMEM_BYTES, st>>>(map_do, a, s, H, Hk, gp, nitems);
   } else {
     e = cudaFuncSetAttribute(tc_bwd_intra_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    tc_bwd_intra_kernel<__nv_bfloat16><<<grid, NT, SMEM_BYTES, st>>>(map_do, a, s, H, Hk, gp);
+    tc_bwd_intra_kernel<__nv_bfloat16><<<grid, NT, SMEM_BYTES, st>>>(map_do, a, s, H, Hk, gp, nitems);
   }
   return cudaGetLastError();
 }
