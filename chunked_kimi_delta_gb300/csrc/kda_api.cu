@@ -172,8 +172,151 @@ cudaError_t hm_inputs_in(const kda_fwd_args *a, char *ws, const HmPlan &m, kda_f
   return e;
 }
 
-size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p) {
-  const size_t base = vf_plan(a, p, use_tc(a) ? tc_plan(p).total : p.total).total;
+// Narrow heads (bf16, d_k or d_v = 64) on the tensor cores: the 128-wide
+// kernels run on zero-padded copies in the workspace.  Exact: a padded key
+// channel has zero q and k and no decay (gate input -1e30 through the
+// in-kernel softplus, or a zero log-decay), a padded value channel zero v, so
+// the padded rows and columns of every state stay zero and the real channels
+// see the unpadded problem; the padded outputs are dropped.
+bool narrow_tc(const kda_fwd_args *a) {
+  return a->qkv_dtype == KDA_BF16 && (a->dk != 128 || a->dv != 128) && (int64_t)a->B * a->T > 0;
+}
+kda_fwd_args wide_args(const kda_fwd_args *a) {
+  kda_fwd_args w = *a;
+  w.dk = w.dv = 128;
+  return w;
+}
+constexpr size_t kWideState = 128 * 128 * 4;  // one padded fp32 state
+
+// Padded q, k, v, gate input, dt_bias (and initial state) from offset o on.
+struct PadIn {
+  size_t off_q, off_k, off_v, off_g, off_dtb, off_init, end;
+};
+PadIn pad_in_plan(const kda_fwd_args *a, size_t o, bool with_init) {
+  PadIn m{};
+  const size_t tok = (size_t)a->B * a->T, Hk = key_heads(a);
+  m.off_q = o; o = align256(o + tok * Hk * 256);
+  m.off_k = o; o = align256(o + tok * Hk * 256);
+  m.off_v = o; o = align256(o + tok * a->H * 256);
+  m.off_g = o; o = align256(o + tok * a->H * 512);
+  if (a->dt_bias) { m.off_dtb = o; o = align256(o + (size_t)a->H * 512); }
+  if (with_init && a->initial_state) {
+    m.off_init = o;
+    o = align256(o + (size_t)fwd_plan(a).N * a->H * kWideState);
+  }
+  m.end = o;
+  return m;
+}
+
+// Rows of w elements (esz bytes) widened to 128 with `fill`, and back.
+cudaError_t widen_rows(const void *src, void *dst, int64_t rows, int w, int esz, uint32_t fill,
+                       cudaStream_t st) {
+  return launch_window_copy(src, dst, rows, 1, w * esz, 1, 128 * esz, fill, nullptr, 0, st);
+}
+cudaError_t narrow_rows(const void *src, void *dst, int64_t rows, int w, int esz, cudaStream_t st) {
+  return launch_window_copy(src, dst, rows, 1, 128 * esz, 1, w * esz, 0u, nullptr, 0, st);
+}
+// fp32 r x c states (the caller's state dimensions) in 128 x 128 ones, and back.
+cudaError_t widen_states(const float *src, float *dst, int64_t n, int r, int c, cudaStream_t st) {
+  return launch_window_copy(src, dst, n, r, c * 4, 128, 512, 0u, nullptr, 0, st);
+}
+cudaError_t narrow_states(const float *src, float *dst, int64_t n, int r, int c, const int32_t *count,
+                          int per_count, cudaStream_t st) {
+  return launch_window_copy(src, dst, n, 128, 512, r, c * 4, 0u, count, per_count, st);
+}
+
+// w's q, k, v, g, dt_bias moved onto 128-wide copies (copied when `copy`);
+// tensors that are 128 wide already are used in place.
+cudaError_t pad_inputs(const kda_fwd_args *a, char *ws, const PadIn &m, kda_fwd_args *w, bool copy,
+                       cudaStream_t st) {
+  const int64_t tok = (int64_t)a->B * a->T, Hk = key_heads(a);
+  float gfill = (a->flags & KDA_GATE_IN_KERNEL) ? -1e30f : 0.f;  // no decay on padded channels
+  uint32_t gbits;
+  memcpy(&gbits, &gfill, 4);
+  cudaError_t e = cudaSuccess;
+  if (a->dk != 128) {
+    w->q = ws + m.off_q;
+    w->k = ws + m.off_k;
+    w->g = reinterpret_cast<float *>(ws + m.off_g);
+    w->dt_bias = a->dt_bias ? reinterpret_cast<float *>(ws + m.off_dtb) : nullptr;
+    if (copy) {
+      e = widen_rows(a->q, ws + m.off_q, tok * Hk, a->dk, 2, 0u, st);
+      if (e == cudaSuccess) e = widen_rows(a->k, ws + m.off_k, tok * Hk, a->dk, 2, 0u, st);
+      if (e == cudaSuccess) e = widen_rows(a->g, ws + m.off_g, tok * a->H, a->dk, 4, gbits, st);
+      if (e == cudaSuccess && a->dt_bias) e = widen_rows(a->dt_bias, ws + m.off_dtb, a->H, a->dk, 4, 0u, st);
+    }
+  }
+  if (a->dv != 128) {
+    w->v = ws + m.off_v;
+    if (copy && e == cudaSuccess) e = widen_rows(a->v, ws + m.off_v, tok * a->H, a->dv, 2, 0u, st);
+  }
+  return e;
+}
+
+// Forward of a narrow-head problem: the wide forward's workspace, the padded
+// inputs (not with KDA_REUSE_PREP, which reads no input: the finish then fits
+// in the workspace of the segment summary that prepared its chunks), then
+// 128-wide outputs.
+struct PadFwd {
+  size_t inner;
+  PadIn in;
+  size_t off_fin, off_out, off_hout, off_vn, total;
+};
+PadFwd pad_fwd_plan(const kda_fwd_args *a) {
+  PadFwd f{};
+  const kda_fwd_args w = wide_args(a);
+  const FwdPlan pw = fwd_plan(&w);
+  f.inner = tc_plan(pw).total;
+  if (a->flags & KDA_REUSE_PREP) {
+    f.in = PadIn{};
+    f.in.end = f.inner;
+    if (a->initial_state) {
+      f.in.off_init = f.inner;
+      f.in.end = align256(f.inner + (size_t)pw.N * a->H * kWideState);
+    }
+  } else {
+    f.in = pad_in_plan(a, f.inner, true);
+  }
+  size_t o = f.in.end;
+  const size_t tok = (size_t)a->B * a->T;
+  if (a->final_state) { f.off_fin = o; o = align256(o + (size_t)pw.N * a->H * kWideState); }
+  f.off_out = o; o = align256(o + tok * a->H * 256);
+  if (a->h_out) { f.off_hout = o; o = align256(o + (size_t)pw.nchunks * a->H * kWideState); }
+  if (a->v_new_out) { f.off_vn = o; o = align256(o + tok * a->H * 512); }
+  f.total = o;
+  return f;
+}
+// Segment summary of a narrow-head problem: 128-wide M and S~.
+struct PadSum {
+  size_t inner;
+  PadIn in;
+  size_t off_M, off_St, total;
+};
+PadSum pad_sum_plan(const kda_fwd_args *a, int32_t S) {
+  PadSum f{};
+  const kda_fwd_args w = wide_args(a);
+  f.inner = tc_plan(summary_plan(&w, S)).total;
+  f.in = pad_in_plan(a, f.inner, false);
+  size_t o = f.in.end;
+  f.off_M = o; o = align256(o + (size_t)S * a->H * kWideState);
+  f.off_St = o; o = align256(o + (size_t)S * a->H * kWideState);
+  f.total = o;
+  return f;
+}
+
+// The forward's (nseg = 0) or the segment summary's (nseg segments) own
+// workspace, before the layout copies.
+size_t inner_bytes(const kda_fwd_args *a, const FwdPlan &p, int32_t nseg) {
+  if (narrow_tc(a)) return nseg > 0 ? pad_sum_plan(a, nseg).total : pad_fwd_plan(a).total;
+  return use_tc(a) ? tc_plan(p).total : p.total;
+}
+// Where the chunk offsets (and, for packed sequences, the chunk count) live.
+size_t chunk_off_pos(const kda_fwd_args *a, const FwdPlan &p) {
+  return (use_tc(a) || narrow_tc(a)) ? tc_plan(p).off_chunk_off : p.off_chunk_off;
+}
+
+size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p, int32_t nseg = 0) {
+  const size_t base = vf_plan(a, p, inner_bytes(a, p, nseg)).total;
   return head_major(a) ? hm_plan(a, true, base).total : base;
 }
 
@@ -219,7 +362,7 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *a) {
 
 size_t kda_segment_summary_workspace_size(const kda_fwd_args *a, int32_t num_segments) {
   if (check_common(a) != KDA_OK || num_segments < 1) return 0;
-  return plan_bytes(a, summary_plan(a, num_segments));
+  return plan_bytes(a, summary_plan(a, num_segments), num_segments);
 }
 
 // Launch sequence of the forward.  When events are given, events[i] is
@@ -263,7 +406,7 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
   const FwdPlan p = fwd_plan(a);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
   char *ws = static_cast<char *>(a->workspace);
-  const VfPlan v = vf_plan(a, p, use_tc(a) ? tc_plan(p).total : p.total);
+  const VfPlan v = vf_plan(a, p, inner_bytes(a, p, 0));
   kda_fwd_args b = *a;
   b.flags &= ~(uint32_t)KDA_STATE_V_FIRST;
   b.workspace_bytes = v.off_init ? v.off_init : (v.off_fin ? v.off_fin : (v.off_hout ? v.off_hout : v.total));
@@ -282,16 +425,52 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
                                 0, st);
   if (e == cudaSuccess && a->h_out) {
     // only the chunks that exist: their count is on the device for packed sequences
-    const int32_t *count = a->cu_seqlens ? reinterpret_cast<const int32_t *>(ws + (use_tc(a)
-                               ? tc_plan(p).off_chunk_off : p.off_chunk_off)) + p.N
-                                         : nullptr;
+    const int32_t *count =
+        a->cu_seqlens ? reinterpret_cast<const int32_t *>(ws + chunk_off_pos(a, p)) + p.N : nullptr;
     e = launch_transpose_states(b.h_out, a->h_out, p.nchunks * p.H, p.K, p.V, count, p.H, st);
   }
   return cuda_status(e);
 }
 
+// Narrow heads: the 128-wide forward on padded copies, outputs cut back.
+static kda_status run_fwd_narrow(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
+                                 int32_t nev, bool keep_err) {
+  const FwdPlan p = fwd_plan(a);
+  kda_status s = check_workspace(a, p);
+  if (s != KDA_OK) return s;
+  const PadFwd m = pad_fwd_plan(a);
+  char *ws = static_cast<char *>(a->workspace);
+  auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+  kda_fwd_args w = wide_args(a);
+  w.workspace_bytes = m.inner;
+  // with KDA_REUSE_PREP the packages are in place and the inputs are not read
+  cudaError_t e = (a->flags & KDA_REUSE_PREP) ? cudaSuccess : pad_inputs(a, ws, m.in, &w, true, st);
+  const int64_t tok = (int64_t)a->B * a->T, ns = (int64_t)p.N * a->H;
+  if (e == cudaSuccess && a->initial_state) {
+    w.initial_state = f32(m.in.off_init);
+    e = widen_states(a->initial_state, f32(m.in.off_init), ns, a->dk, a->dv, st);
+  }
+  w.out = a->dv == 128 ? a->out : ws + m.off_out;
+  w.final_state = a->final_state ? f32(m.off_fin) : nullptr;
+  w.h_out = a->h_out ? f32(m.off_hout) : nullptr;
+  w.v_new_out = a->v_new_out ? (a->dv == 128 ? a->v_new_out : f32(m.off_vn)) : nullptr;
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  if ((s = run_fwd_kfirst(&w, st, ev, nev, keep_err)) != KDA_OK) return s;
+  if (a->dv != 128) e = narrow_rows(w.out, a->out, tok * a->H, a->dv, 2, st);
+  if (e == cudaSuccess && a->final_state) e = narrow_states(w.final_state, a->final_state, ns, a->dk, a->dv, nullptr, 0, st);
+  if (e == cudaSuccess && a->h_out) {
+    const int32_t *count = a->cu_seqlens ? reinterpret_cast<const int32_t *>(ws + chunk_off_pos(a, p)) + p.N
+                                         : nullptr;
+    e = narrow_states(w.h_out, a->h_out, p.nchunks * a->H, a->dk, a->dv, count, a->H, st);
+  }
+  if (e == cudaSuccess && a->v_new_out && a->dv != 128)
+    e = narrow_rows(w.v_new_out, a->v_new_out, tok * a->H, a->dv, 4, st);
+  return cuda_status(e);
+}
+
 static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
                                  int32_t nev, bool keep_err) {
+  if (narrow_tc(a)) return run_fwd_narrow(a, st, ev, nev, keep_err);
   kda_status s;
   const FwdPlan p = fwd_plan(a);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
@@ -314,11 +493,11 @@ static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEve
   const bool tc = use_tc(a);
   const size_t off_co = tc ? tc_plan(p).off_chunk_off : p.off_chunk_off;
   si.chunk_off = reinterpret_cast<int32_t *>(ws + off_co);
-  tcp::TcMaps maps;
-  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps))
+  const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
+  tcp::TcMaps maps;  // the prep's input maps (no prep with KDA_REUSE_PREP)
+  if (tc && !reuse && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps))
     return KDA_ERR_CUDA;
 
-  const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
   cudaError_t e = keep_err ? cudaSuccess : cudaMemsetAsync(ws, 0, 4, st);  // device error word
   if (e == cudaSuccess && si.bounds && !reuse) {
     e = mark();
@@ -373,7 +552,7 @@ int32_t kda_chunk_fwd_stages(const kda_fwd_args *a, const char **names, int32_t 
   int32_t n = 0;
   const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
   if (a->cu_seqlens && !reuse) list[n++] = "chunk_map";
-  if (use_tc(a)) {
+  if (use_tc(a) || narrow_tc(a)) {
     if (!reuse) list[n++] = "tc_prep";
     list[n++] = "tc_chain";
   } else {
@@ -576,7 +755,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
   if (head_major(a) && (int64_t)a->B * a->T > 0) {  // token-major copies of the inputs
     kda_fwd_args b = *a;
     b.flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
-    const size_t base = plan_bytes(&b, summary_plan(&b, num_segments));
+    const size_t base = plan_bytes(&b, summary_plan(&b, num_segments), num_segments);
     const HmPlan m = hm_plan(a, false, base);
     if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
@@ -584,6 +763,22 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     if (hm_inputs_in(a, static_cast<char *>(a->workspace), m, &b, st0) != cudaSuccess) return KDA_ERR_CUDA;
     b.workspace_bytes = base;
     return kda_segment_summary(&b, seg_bounds, num_segments, M, S_tilde, stream);
+  }
+  if (narrow_tc(a)) {  // the 128-wide summary on padded copies, M and S~ cut back
+    const PadSum m = pad_sum_plan(a, num_segments);
+    if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(a->workspace);
+    kda_fwd_args w = wide_args(a);
+    w.workspace_bytes = m.inner;
+    if (pad_inputs(a, ws, m.in, &w, true, st0) != cudaSuccess) return KDA_ERR_CUDA;
+    float *Mw = reinterpret_cast<float *>(ws + m.off_M), *Sw = reinterpret_cast<float *>(ws + m.off_St);
+    if ((s = kda_segment_summary(&w, seg_bounds, num_segments, Mw, Sw, stream)) != KDA_OK) return s;
+    const int64_t n = (int64_t)num_segments * a->H;
+    cudaError_t e = narrow_states(Mw, M, n, a->dk, a->dk, nullptr, 0, st0);
+    if (e == cudaSuccess) e = narrow_states(Sw, S_tilde, n, a->dk, a->dv, nullptr, 0, st0);
+    return cuda_status(e);
   }
   const FwdPlan p = summary_plan(a, num_segments);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
@@ -781,6 +976,116 @@ BwdPlan bwd_plan(const kda_bwd_args *b) {
   return p;
 }
 
+// Backward of a narrow-head problem: the wide backward's workspace, the padded
+// inputs and cotangents, then 128-wide gradients.
+struct PadBwd {
+  size_t inner;
+  PadIn in;
+  size_t off_dfin, off_do, off_dq, off_dk, off_dv, off_dg, off_ddtb, off_dinit, total;
+};
+kda_bwd_args wide_bwd(const kda_bwd_args *b) {
+  kda_bwd_args c = *b;
+  c.fwd = wide_args(&b->fwd);
+  return c;
+}
+PadBwd pad_bwd_plan(const kda_bwd_args *b) {
+  PadBwd f{};
+  const kda_fwd_args *a = &b->fwd;
+  const kda_bwd_args c = wide_bwd(b);
+  f.inner = bwd_plan(&c).total;
+  f.in = pad_in_plan(a, f.inner, true);
+  size_t o = f.in.end;
+  const size_t tok = (size_t)a->B * a->T, Hk = key_heads(a), ns = (size_t)fwd_plan(a).N * a->H;
+  if (b->d_final_state) { f.off_dfin = o; o = align256(o + ns * kWideState); }
+  if (b->d_out) { f.off_do = o; o = align256(o + tok * a->H * 256); }
+  f.off_dq = o; o = align256(o + tok * Hk * 256);
+  f.off_dk = o; o = align256(o + tok * Hk * 256);
+  f.off_dv = o; o = align256(o + tok * a->H * 256);
+  f.off_dg = o; o = align256(o + tok * a->H * 512);
+  if (b->ddt_bias) { f.off_ddtb = o; o = align256(o + (size_t)a->H * 512); }
+  if (b->d_initial_state) { f.off_dinit = o; o = align256(o + ns * kWideState); }
+  f.total = o;
+  return f;
+}
+size_t bwd_total(const kda_bwd_args *b) {
+  return narrow_tc(&b->fwd) ? pad_bwd_plan(b).total : bwd_plan(b).total;
+}
+
+// Segment backward summary of a narrow-head problem: padded d_out, 128-wide E.
+struct PadSegBwd {
+  size_t inner;
+  PadIn in;
+  size_t off_do, off_E, total;
+};
+PadSegBwd pad_segbwd_plan(const kda_fwd_args *a, int32_t S) {
+  PadSegBwd f{};
+  const kda_fwd_args w = wide_args(a);
+  f.inner = tc_plan(summary_plan(&w, S)).total;
+  f.in = pad_in_plan(a, f.inner, false);
+  size_t o = f.in.end;
+  f.off_do = o; o = align256(o + (size_t)a->B * a->T * a->H * 256);
+  f.off_E = o; o = align256(o + (size_t)S * a->H * kWideState);
+  f.total = o;
+  return f;
+}
+size_t segbwd_total(const kda_fwd_args *a, int32_t S) {
+  if (narrow_tc(a)) return pad_segbwd_plan(a, S).total;
+  const FwdPlan p = summary_plan(a, S);  // packages or generic intermediates
+  return use_tc(a) ? tc_plan(p).total : p.total;
+}
+
+// Narrow heads: the 128-wide backward on padded copies, gradients cut back;
+// dbeta and dA_log (no head-width dimension) go to the caller's buffers.
+kda_status run_bwd_narrow(const kda_bwd_args *b, kda_stream_t stream) {
+  const kda_fwd_args *a = &b->fwd;
+  const PadBwd m = pad_bwd_plan(b);
+  if (!b->workspace || b->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(b->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(b->workspace);
+  auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+  kda_bwd_args c = wide_bwd(b);
+  c.workspace_bytes = m.inner;
+  const int64_t tok = (int64_t)a->B * a->T, Hk = key_heads(a), ns = (int64_t)fwd_plan(a).N * a->H;
+  const bool vf = v_first(a);
+  const int sr = vf ? a->dv : a->dk, sc = vf ? a->dk : a->dv;  // the caller's state dimensions
+  const bool nk = a->dk != 128, nv = a->dv != 128;
+  cudaError_t e = pad_inputs(a, ws, m.in, &c.fwd, true, st);
+  if (e == cudaSuccess && a->initial_state) {
+    c.fwd.initial_state = f32(m.in.off_init);
+    e = widen_states(a->initial_state, f32(m.in.off_init), ns, sr, sc, st);
+  }
+  if (e == cudaSuccess && b->d_final_state) {
+    c.d_final_state = f32(m.off_dfin);
+    e = widen_states(b->d_final_state, f32(m.off_dfin), ns, sr, sc, st);
+  }
+  if (e == cudaSuccess && b->d_out && nv) {
+    c.d_out = ws + m.off_do;
+    e = widen_rows(b->d_out, ws + m.off_do, tok * a->H, a->dv, 2, 0u, st);
+  }
+  if (nk) {
+    c.dq = ws + m.off_dq;
+    c.dk = ws + m.off_dk;
+    c.dg = f32(m.off_dg);
+    c.ddt_bias = b->ddt_bias ? f32(m.off_ddtb) : nullptr;
+  }
+  if (nv) c.dv = ws + m.off_dv;
+  c.d_initial_state = b->d_initial_state ? f32(m.off_dinit) : nullptr;
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  kda_status s = kda_chunk_bwd(&c, stream);
+  if (s != KDA_OK) return s;
+  if (nk) {
+    e = narrow_rows(c.dq, b->dq, tok * Hk, a->dk, 2, st);
+    if (e == cudaSuccess) e = narrow_rows(c.dk, b->dk, tok * Hk, a->dk, 2, st);
+    if (e == cudaSuccess) e = narrow_rows(c.dg, b->dg, tok * a->H, a->dk, 4, st);
+    if (e == cudaSuccess && b->ddt_bias) e = narrow_rows(c.ddt_bias, b->ddt_bias, a->H, a->dk, 4, st);
+  }
+  if (e == cudaSuccess && nv) e = narrow_rows(c.dv, b->dv, tok * a->H, a->dv, 2, st);
+  if (e == cudaSuccess && b->d_initial_state)
+    e = narrow_states(c.d_initial_state, b->d_initial_state, ns, sr, sc, nullptr, 0, st);
+  return cuda_status(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -809,7 +1114,7 @@ HmBwd hm_bwd_plan(const kda_bwd_args *b, size_t base) {
 
 size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *b) {
   if (check_bwd(b) != KDA_OK) return 0;
-  const size_t base = bwd_plan(b).total;
+  const size_t base = bwd_total(b);
   return head_major(&b->fwd) ? hm_bwd_plan(b, base).total : base;
 }
 
@@ -818,7 +1123,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   if (s != KDA_OK) return s;
   const kda_fwd_args *a = &b->fwd;
   if (head_major(a) && (int64_t)a->B * a->T > 0) {
-    const size_t base = bwd_plan(b).total;
+    const size_t base = bwd_total(b);
     const HmBwd m = hm_bwd_plan(b, base);
     if (!b->workspace || b->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(b->workspace) & 255u) return KDA_ERR_ALIGNMENT;
@@ -848,6 +1153,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
     if (e == cudaSuccess) e = launch_swap_token_head(c.dbeta, b->dbeta, B, a->H, T, 4, false, st0);
     return cuda_status(e);
   }
+  if (narrow_tc(a)) return run_bwd_narrow(b, stream);
   const BwdPlan p = bwd_plan(b);
   if (!b->workspace || b->workspace_bytes < p.total) return KDA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(b->workspace) & 255u) return KDA_ERR_ALIGNMENT;
@@ -1007,8 +1313,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
 
 size_t kda_segment_bwd_summary_workspace_size(const kda_fwd_args *a, int32_t num_segments) {
   if (check_common(a) != KDA_OK || num_segments < 1) return 0;
-  const FwdPlan p = summary_plan(a, num_segments);  // packages or generic intermediates
-  const size_t base = use_tc(a) ? tc_plan(p).total : p.total;
+  const size_t base = segbwd_total(a, num_segments);
   return head_major(a) ? hm_plan(a, true, base).total : base;  // + token-major inputs and d_out
 }
 
@@ -1023,8 +1328,7 @@ kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
   if (head_major(a) && (int64_t)a->B * a->T > 0) {  // token-major copies of the inputs, d_out
     kda_fwd_args b = *a;
     b.flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
-    const FwdPlan pb = summary_plan(&b, num_segments);
-    const size_t base = use_tc(&b) ? tc_plan(pb).total : pb.total;
+    const size_t base = segbwd_total(&b, num_segments);
     const HmPlan m = hm_plan(a, true, base);
     if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
@@ -1042,6 +1346,25 @@ kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     b.workspace_bytes = base;
     return kda_segment_bwd_summary(&b, dO, seg_bounds, num_segments, E, stream);
+  }
+  if (narrow_tc(a)) {  // the 128-wide reverse chain on padded copies, E cut back
+    const PadSegBwd m = pad_segbwd_plan(a, num_segments);
+    if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(a->workspace);
+    kda_fwd_args w = wide_args(a);
+    w.workspace_bytes = m.inner;
+    cudaError_t e = pad_inputs(a, ws, m.in, &w, true, st0);
+    const void *dO = d_out;
+    if (e == cudaSuccess && d_out && a->dv != 128) {
+      e = widen_rows(d_out, ws + m.off_do, (int64_t)a->B * a->T * a->H, a->dv, 2, 0u, st0);
+      dO = ws + m.off_do;
+    }
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    float *Ew = reinterpret_cast<float *>(ws + m.off_E);
+    if ((s = kda_segment_bwd_summary(&w, dO, seg_bounds, num_segments, Ew, stream)) != KDA_OK) return s;
+    return cuda_status(narrow_states(Ew, E, (int64_t)num_segments * a->H, a->dk, a->dv, nullptr, 0, st0));
   }
   const FwdPlan p = summary_plan(a, num_segments);
   const bool tc = use_tc(a);

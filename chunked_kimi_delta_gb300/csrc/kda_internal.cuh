@@ -142,6 +142,13 @@ cudaError_t launch_chunk_map(const SeqInfo &s, int32_t *chunk_off, cudaStream_t 
 
 // n fp32 matrices R x C -> C x R (kda_layout.cu); with count_ptr only the
 // first (*count_ptr) * per_count matrices.
+// dst[m] = the rows_dst x row_bytes_dst window of src[m] (rows_src x
+// row_bytes_src), `fill` (a 32-bit pattern) outside src; n matrices, row
+// bytes multiples of 16.  With count_ptr only matrices below
+// (*count_ptr) * per_count are written.
+cudaError_t launch_window_copy(const void *src, void *dst, int64_t n, int rows_src, int row_bytes_src,
+                               int rows_dst, int row_bytes_dst, uint32_t fill, const int32_t *count_ptr,
+                               int per_count, cudaStream_t st);
 cudaError_t launch_transpose_states(const float *src, float *dst, int64_t n, int R, int C,
                                     const int32_t *count_ptr, int per_count, cudaStream_t st);
 // [B, H, T, row] <-> [B, T, H, row] (row_bytes a multiple of 4).

@@ -10,7 +10,9 @@
 // TND [T, H, D] and the head-major BNSD [B, H, T, D], NTD [H, T, D].  The
 // kernels work token-major; head-major tensors are converted at the
 // boundary by swapping the token and head axes, row by row (a row is the D
-// elements of one (token, head)).
+// elements of one (token, head)).  Heads narrower than the tensor-core
+// kernels' 128 channels are widened into zero-padded copies and the outputs
+// cut back (window copies).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -69,7 +71,40 @@ swap_token_head_kernel(const Unit *__restrict__ src, Unit *__restrict__ dst, int
   }
 }
 
+// Window copy between stacks of matrices of different shapes, in 16-byte
+// units: dst[m][r][u] = src[m][r][u] where r < Rs and u < Us, else `fill`
+// (m < n; dst is Rd x Ud units per matrix).  With count_ptr only matrices
+// below (*count_ptr) * per_count are written.
+__global__ void __launch_bounds__(256)
+window_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int Rs, int Us, int Rd, int Ud,
+              uint4 fill, const int32_t *__restrict__ count_ptr, int per_count, int64_t total) {
+  const int64_t limit = count_ptr ? (int64_t)(*count_ptr) * per_count * Rd * Ud : total;
+  const int64_t end = limit < total ? limit : total;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < end;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int u = (int)(i % Ud);
+    const int64_t mr = i / Ud;
+    const int r = (int)(mr % Rd);
+    const int64_t m = mr / Rd;
+    dst[i] = (r < Rs && u < Us) ? src[(m * Rs + r) * Us + u] : fill;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_window_copy(const void *src, void *dst, int64_t n, int rows_src, int row_bytes_src,
+                               int rows_dst, int row_bytes_dst, uint32_t fill, const int32_t *count_ptr,
+                               int per_count, cudaStream_t st) {
+  if (row_bytes_src % 16 || row_bytes_dst % 16 || rows_src < 1 || rows_dst < 1) return cudaErrorInvalidValue;
+  const int64_t total = n * rows_dst * (row_bytes_dst / 16);
+  if (total == 0) return cudaSuccess;
+  const int64_t want = (total + 255) / 256;
+  const unsigned blocks = (unsigned)(want < 4096 ? want : 4096);
+  window_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), rows_src,
+                                        row_bytes_src / 16, rows_dst, row_bytes_dst / 16,
+                                        make_uint4(fill, fill, fill, fill), count_ptr, per_count, total);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_swap_token_head(const void *src, void *dst, int64_t B, int H, int64_t T,
                                    int row_bytes, bool to_token_major, cudaStream_t st) {
