@@ -5,13 +5,17 @@
 // ("Hyper-Parallel Chunk KDA current implementation design" section 5.1,
 // PreProcessFwd: H_out = M H_in + E; "KDA Context Parallelism (KCP)", "Les
 // notations").  Per chunk, with the prep kernel's package:
-//   P   = w X                          (tcgen05, M=64, N=256, K=128)
+//   P   = [w; w] X                     (tcgen05, M=128, N=256, K=128)
 //   V'  = [u - P_S~ | -P_M]            (the values of the two parts; bf16)
 //   U   = kg^T V'                      (tcgen05, M=128, N=256, K=64)
 //   X  <- e^{G_C} X + U                (fp32, registers)
 // Both parts share one CTA and one copy of each package; only the w rows,
 // u, kg and e^{G_C} of a package are loaded (qg and A_qk serve the output,
-// which a summary does not produce).
+// which a summary does not produce).  The w rows are stacked twice, so that
+// the product fills all 128 TMEM lanes (an M=64 product would leave half of
+// every warp's lanes idle in the readout) at no extra tensor time: the
+// warps of lane quarters 0, 1 and 2, 3 read the two copies and split the
+// columns.
 #include <cuda_bf16.h>
 
 #include "kda_tc.cuh"
@@ -22,18 +26,20 @@ namespace {
 
 constexpr int NT = 512;  // 16 warps: (TMEM lane quarter) x (64-column quarter of X)
 
-// One package buffer (bytes): w (K-major, two 64-channel panels of 64 rows),
-// u, kg (as in the package) and e^{G_C}.
+// One package buffer (bytes): [w; w] (K-major, two 64-channel panels of 128
+// rows), u, kg (as in the package) and e^{G_C}.
 constexpr uint32_t B_W = 0;
-constexpr uint32_t B_U = 16384;
-constexpr uint32_t B_KG = 32768;
-constexpr uint32_t B_GC = 49152;
-constexpr uint32_t B_BYTES = 49664;
-constexpr uint32_t BUF_STRIDE = 50176;           // 1024-aligned
+constexpr uint32_t B_U = 32768;
+constexpr uint32_t B_KG = 49152;
+constexpr uint32_t B_GC = 65536;
+constexpr uint32_t B_BYTES = 66048;
+constexpr uint32_t BUF_STRIDE = 66560;           // 1024-aligned
+constexpr uint32_t S_BAR = B_BYTES;              // full[2], bar_ma, bar_mc, tslot, abort: in the
+                                                 // alignment gap after buffer 0
 constexpr uint32_t S_XB = 2 * BUF_STRIDE;        // X bf16, MN-major (K = 128 channels, N = 256)
 constexpr uint32_t S_VN = S_XB + 65536;          // V' bf16, MN-major (K = 64 tokens, N = 256)
-constexpr uint32_t S_BAR = S_VN + 32768;         // full[2], bar_ma, bar_mc, tslot, abort
-constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
+constexpr uint32_t SMEM_BYTES = S_VN + 32768 + 1024;
+static_assert(S_BAR + 64 <= BUF_STRIDE && SMEM_BYTES <= 232448, "shared memory layout");
 constexpr uint32_t TMEM_COLS = 512;              // P (256, M=64 layout) and U (256)
 
 __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restrict__ pkg, float *S_tilde,
@@ -98,8 +104,11 @@ __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restric
     uint8_t *dst = sm + bb * BUF_STRIDE;
     const char *src = pkg + (size_t)((c0 + cc) * H + h) * PK_BYTES;
     tc::mbar_arrive_expect_tx(full + bb, B_BYTES);
-    bulk_load(dst + B_W, src + PK_WQ + 8192, 8192, full + bb);            // w rows, panel 0
-    bulk_load(dst + B_W + 8192, src + PK_WQ + 16384 + 8192, 8192, full + bb);  // panel 1
+    // the package's w rows (rows 64..127 of each [qg; w] panel; their swizzle
+    // phase repeats every 8 rows) into rows 0..63 and 64..127 of each panel
+    for (int pn = 0; pn < 2; ++pn)
+      for (int cp = 0; cp < 2; ++cp)
+        bulk_load(dst + B_W + pn * 16384 + cp * 8192, src + PK_WQ + pn * 16384 + 8192, 8192, full + bb);
     bulk_load(dst + B_U, src + PK_U, 16384, full + bb);
     bulk_load(dst + B_KG, src + PK_KG, 16384, full + bb);
     bulk_load(dst + B_GC, src + PK_GC, 512, full + bb);
@@ -117,14 +126,14 @@ __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restric
     __syncthreads();  // X (bf16) of this chunk and its package are in place
     if (*abort_flag) break;
 
-    // ---- P = w X; the buffer of chunk c - 1 takes chunk c + 1
+    // ---- P = [w; w] X; the buffer of chunk c - 1 takes chunk c + 1
     if (tid == 0) {
       tc::tc_fence_after();
-      const uint32_t idesc = tc::idesc_bf16_f32(64, 256, false, true);
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 256, false, true);
       const uint32_t a0 = tc::smem_u32(buf + B_W), b0 = tc::smem_u32(sm + S_XB);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc::mma_bf16(tP, tc::smem_desc_sw128(a0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+        tc::mma_bf16(tP, tc::smem_desc_sw128(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                      tc::smem_desc_sw128(b0 + kk * 2048, 16384, 1024), idesc, kk > 0);
       tc::mma_commit(bar_ma);
       ma_pending = true;
@@ -137,18 +146,19 @@ __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restric
     if (!ok) *abort_flag = 1;
     tc::tc_fence_after();
 
-    // ---- V' = [u - P | -P]: P row r (M=64 layout) in TMEM lane (r % 16) +
-    //      32 (r / 16), i.e. lanes 0..15 of each quarter
+    // ---- V' = [u - P | -P]: row r of P in TMEM lanes r and 64 + r; the
+    //      warps of lane quarters 0, 1 take the first 32 columns of their
+    //      64-column quarter, those of quarters 2, 3 the last 32
     if (ok) {
-      const int r = 16 * q4 + lane;  // valid for lane < 16
+      const int r = 32 * (q4 & 1) + lane;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         float d[16];
+        const int col = 64 * cq + 32 * (q4 >> 1) + 16 * cc;  // column of X
         __syncwarp();
-        tc::tmem_ld16(tP + ((uint32_t)(32 * q4) << 16) + 64 * cq + 16 * cc, d);
+        tc::tmem_ld16(tP + ((uint32_t)(32 * q4) << 16) + col, d);
         tc::tmem_ld_wait();
-        if (lane < 16) {
-          const int col = 64 * cq + 16 * cc;  // column of X
+        {
           float vn[16];
           if (cq >= 2) {
 #pragma unroll
