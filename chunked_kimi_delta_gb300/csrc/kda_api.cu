@@ -78,10 +78,11 @@ FwdPlan summary_plan(const kda_fwd_args *a, int32_t num_segments) {
   return p;
 }
 
-// The tensor-core path takes bf16 inputs with d_k = d_v = 128; every other
-// case runs on the CUDA-core path.
+// The tensor-core path takes bf16 inputs (d_k, d_v of 64 or 128: the
+// forward kernels read narrow heads with the extra channels held at zero);
+// fp32 inputs run on the CUDA-core path.
 bool use_tc(const kda_fwd_args *a) {
-  return a->qkv_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128 && (int64_t)a->B * a->T > 0;
+  return a->qkv_dtype == KDA_BF16 && (int64_t)a->B * a->T > 0;
 }
 
 // Tensor-core workspace: error word (and, 64 bytes in, the count of the
@@ -172,12 +173,13 @@ cudaError_t hm_inputs_in(const kda_fwd_args *a, char *ws, const HmPlan &m, kda_f
   return e;
 }
 
-// Narrow heads (bf16, d_k or d_v = 64) on the tensor cores: the 128-wide
-// kernels run on zero-padded copies in the workspace.  Exact: a padded key
-// channel has zero q and k and no decay (gate input -1e30 through the
-// in-kernel softplus, or a zero log-decay), a padded value channel zero v, so
-// the padded rows and columns of every state stay zero and the real channels
-// see the unpadded problem; the padded outputs are dropped.
+// Narrow heads (bf16, d_k or d_v = 64) in the backward and the backward
+// summary: their 128-wide tensor-core kernels run on zero-padded copies in
+// the workspace (the forward and the summary read narrow heads directly).
+// Exact: a padded key channel has zero q and k and no decay (gate input
+// -1e30 through the in-kernel softplus, or a zero log-decay), a padded value
+// channel zero v, so the padded rows and columns of every state stay zero and
+// the real channels see the unpadded problem; the padded outputs are dropped.
 bool narrow_tc(const kda_fwd_args *a) {
   return a->qkv_dtype == KDA_BF16 && (a->dk != 128 || a->dv != 128) && (int64_t)a->B * a->T > 0;
 }
@@ -253,70 +255,18 @@ cudaError_t pad_inputs(const kda_fwd_args *a, char *ws, const PadIn &m, kda_fwd_
   return e;
 }
 
-// Forward of a narrow-head problem: the wide forward's workspace, the padded
-// inputs (not with KDA_REUSE_PREP, which reads no input: the finish then fits
-// in the workspace of the segment summary that prepared its chunks), then
-// 128-wide outputs.
-struct PadFwd {
-  size_t inner;
-  PadIn in;
-  size_t off_fin, off_out, off_hout, off_vn, total;
-};
-PadFwd pad_fwd_plan(const kda_fwd_args *a) {
-  PadFwd f{};
-  const kda_fwd_args w = wide_args(a);
-  const FwdPlan pw = fwd_plan(&w);
-  f.inner = tc_plan(pw).total;
-  if (a->flags & KDA_REUSE_PREP) {
-    f.in = PadIn{};
-    f.in.end = f.inner;
-    if (a->initial_state) {
-      f.in.off_init = f.inner;
-      f.in.end = align256(f.inner + (size_t)pw.N * a->H * kWideState);
-    }
-  } else {
-    f.in = pad_in_plan(a, f.inner, true);
-  }
-  size_t o = f.in.end;
-  const size_t tok = (size_t)a->B * a->T;
-  if (a->final_state) { f.off_fin = o; o = align256(o + (size_t)pw.N * a->H * kWideState); }
-  f.off_out = o; o = align256(o + tok * a->H * 256);
-  if (a->h_out) { f.off_hout = o; o = align256(o + (size_t)pw.nchunks * a->H * kWideState); }
-  if (a->v_new_out) { f.off_vn = o; o = align256(o + tok * a->H * 512); }
-  f.total = o;
-  return f;
-}
-// Segment summary of a narrow-head problem: 128-wide M and S~.
-struct PadSum {
-  size_t inner;
-  PadIn in;
-  size_t off_M, off_St, total;
-};
-PadSum pad_sum_plan(const kda_fwd_args *a, int32_t S) {
-  PadSum f{};
-  const kda_fwd_args w = wide_args(a);
-  f.inner = tc_plan(summary_plan(&w, S)).total;
-  f.in = pad_in_plan(a, f.inner, false);
-  size_t o = f.in.end;
-  f.off_M = o; o = align256(o + (size_t)S * a->H * kWideState);
-  f.off_St = o; o = align256(o + (size_t)S * a->H * kWideState);
-  f.total = o;
-  return f;
-}
-
-// The forward's (nseg = 0) or the segment summary's (nseg segments) own
-// workspace, before the layout copies.
-size_t inner_bytes(const kda_fwd_args *a, const FwdPlan &p, int32_t nseg) {
-  if (narrow_tc(a)) return nseg > 0 ? pad_sum_plan(a, nseg).total : pad_fwd_plan(a).total;
+// The forward's or the segment summary's own workspace, before the layout
+// copies.
+size_t inner_bytes(const kda_fwd_args *a, const FwdPlan &p) {
   return use_tc(a) ? tc_plan(p).total : p.total;
 }
 // Where the chunk offsets (and, for packed sequences, the chunk count) live.
 size_t chunk_off_pos(const kda_fwd_args *a, const FwdPlan &p) {
-  return (use_tc(a) || narrow_tc(a)) ? tc_plan(p).off_chunk_off : p.off_chunk_off;
+  return use_tc(a) ? tc_plan(p).off_chunk_off : p.off_chunk_off;
 }
 
-size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p, int32_t nseg = 0) {
-  const size_t base = vf_plan(a, p, inner_bytes(a, p, nseg)).total;
+size_t plan_bytes(const kda_fwd_args *a, const FwdPlan &p) {
+  const size_t base = vf_plan(a, p, inner_bytes(a, p)).total;
   return head_major(a) ? hm_plan(a, true, base).total : base;
 }
 
@@ -333,6 +283,8 @@ GateParams gate_params(const kda_fwd_args *a) {
   gp.scale = a->scale;
   gp.eps = a->eps;
   gp.flags = a->flags;
+  gp.dk = a->dk;
+  gp.dv = a->dv;
   return gp;
 }
 
@@ -362,7 +314,7 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *a) {
 
 size_t kda_segment_summary_workspace_size(const kda_fwd_args *a, int32_t num_segments) {
   if (check_common(a) != KDA_OK || num_segments < 1) return 0;
-  return plan_bytes(a, summary_plan(a, num_segments), num_segments);
+  return plan_bytes(a, summary_plan(a, num_segments));
 }
 
 // Launch sequence of the forward.  When events are given, events[i] is
@@ -406,7 +358,7 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
   const FwdPlan p = fwd_plan(a);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
   char *ws = static_cast<char *>(a->workspace);
-  const VfPlan v = vf_plan(a, p, inner_bytes(a, p, 0));
+  const VfPlan v = vf_plan(a, p, inner_bytes(a, p));
   kda_fwd_args b = *a;
   b.flags &= ~(uint32_t)KDA_STATE_V_FIRST;
   b.workspace_bytes = v.off_init ? v.off_init : (v.off_fin ? v.off_fin : (v.off_hout ? v.off_hout : v.total));
@@ -432,45 +384,8 @@ static kda_status run_fwd(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t co
   return cuda_status(e);
 }
 
-// Narrow heads: the 128-wide forward on padded copies, outputs cut back.
-static kda_status run_fwd_narrow(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
-                                 int32_t nev, bool keep_err) {
-  const FwdPlan p = fwd_plan(a);
-  kda_status s = check_workspace(a, p);
-  if (s != KDA_OK) return s;
-  const PadFwd m = pad_fwd_plan(a);
-  char *ws = static_cast<char *>(a->workspace);
-  auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
-  kda_fwd_args w = wide_args(a);
-  w.workspace_bytes = m.inner;
-  // with KDA_REUSE_PREP the packages are in place and the inputs are not read
-  cudaError_t e = (a->flags & KDA_REUSE_PREP) ? cudaSuccess : pad_inputs(a, ws, m.in, &w, true, st);
-  const int64_t tok = (int64_t)a->B * a->T, ns = (int64_t)p.N * a->H;
-  if (e == cudaSuccess && a->initial_state) {
-    w.initial_state = f32(m.in.off_init);
-    e = widen_states(a->initial_state, f32(m.in.off_init), ns, a->dk, a->dv, st);
-  }
-  w.out = a->dv == 128 ? a->out : ws + m.off_out;
-  w.final_state = a->final_state ? f32(m.off_fin) : nullptr;
-  w.h_out = a->h_out ? f32(m.off_hout) : nullptr;
-  w.v_new_out = a->v_new_out ? (a->dv == 128 ? a->v_new_out : f32(m.off_vn)) : nullptr;
-  if (e != cudaSuccess) return KDA_ERR_CUDA;
-  if ((s = run_fwd_kfirst(&w, st, ev, nev, keep_err)) != KDA_OK) return s;
-  if (a->dv != 128) e = narrow_rows(w.out, a->out, tok * a->H, a->dv, 2, st);
-  if (e == cudaSuccess && a->final_state) e = narrow_states(w.final_state, a->final_state, ns, a->dk, a->dv, nullptr, 0, st);
-  if (e == cudaSuccess && a->h_out) {
-    const int32_t *count = a->cu_seqlens ? reinterpret_cast<const int32_t *>(ws + chunk_off_pos(a, p)) + p.N
-                                         : nullptr;
-    e = narrow_states(w.h_out, a->h_out, p.nchunks * a->H, a->dk, a->dv, count, a->H, st);
-  }
-  if (e == cudaSuccess && a->v_new_out && a->dv != 128)
-    e = narrow_rows(w.v_new_out, a->v_new_out, tok * a->H, a->dv, 4, st);
-  return cuda_status(e);
-}
-
 static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEvent_t const *ev,
                                  int32_t nev, bool keep_err) {
-  if (narrow_tc(a)) return run_fwd_narrow(a, st, ev, nev, keep_err);
   kda_status s;
   const FwdPlan p = fwd_plan(a);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
@@ -495,7 +410,8 @@ static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEve
   si.chunk_off = reinterpret_cast<int32_t *>(ws + off_co);
   const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
   tcp::TcMaps maps;  // the prep's input maps (no prep with KDA_REUSE_PREP)
-  if (tc && !reuse && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps))
+  if (tc && !reuse &&
+      !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->dk, a->dv, a->H, p.Hk, maps))
     return KDA_ERR_CUDA;
 
   cudaError_t e = keep_err ? cudaSuccess : cudaMemsetAsync(ws, 0, 4, st);  // device error word
@@ -520,6 +436,8 @@ static kda_status run_fwd_kfirst(const kda_fwd_args *a, cudaStream_t st, cudaEve
       ca.h_out = a->h_out;
       ca.v_new_out = a->v_new_out;
       ca.err = err;
+      ca.dk = a->dk;
+      ca.dv = a->dv;
       ca.test_wait_timeout = (a->flags & KDA_TEST_WAIT_TIMEOUT) != 0;
       e = tcp::launch_tc_chain(ca, si, a->H, st);
     }
@@ -552,7 +470,7 @@ int32_t kda_chunk_fwd_stages(const kda_fwd_args *a, const char **names, int32_t 
   int32_t n = 0;
   const bool reuse = (a->flags & KDA_REUSE_PREP) != 0;
   if (a->cu_seqlens && !reuse) list[n++] = "chunk_map";
-  if (use_tc(a) || narrow_tc(a)) {
+  if (use_tc(a)) {
     if (!reuse) list[n++] = "tc_prep";
     list[n++] = "tc_chain";
   } else {
@@ -755,7 +673,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
   if (head_major(a) && (int64_t)a->B * a->T > 0) {  // token-major copies of the inputs
     kda_fwd_args b = *a;
     b.flags &= ~(uint32_t)KDA_LAYOUT_HEAD_MAJOR;
-    const size_t base = plan_bytes(&b, summary_plan(&b, num_segments), num_segments);
+    const size_t base = plan_bytes(&b, summary_plan(&b, num_segments));
     const HmPlan m = hm_plan(a, false, base);
     if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
@@ -763,22 +681,6 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     if (hm_inputs_in(a, static_cast<char *>(a->workspace), m, &b, st0) != cudaSuccess) return KDA_ERR_CUDA;
     b.workspace_bytes = base;
     return kda_segment_summary(&b, seg_bounds, num_segments, M, S_tilde, stream);
-  }
-  if (narrow_tc(a)) {  // the 128-wide summary on padded copies, M and S~ cut back
-    const PadSum m = pad_sum_plan(a, num_segments);
-    if (!a->workspace || a->workspace_bytes < m.total) return KDA_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return KDA_ERR_ALIGNMENT;
-    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(a->workspace);
-    kda_fwd_args w = wide_args(a);
-    w.workspace_bytes = m.inner;
-    if (pad_inputs(a, ws, m.in, &w, true, st0) != cudaSuccess) return KDA_ERR_CUDA;
-    float *Mw = reinterpret_cast<float *>(ws + m.off_M), *Sw = reinterpret_cast<float *>(ws + m.off_St);
-    if ((s = kda_segment_summary(&w, seg_bounds, num_segments, Mw, Sw, stream)) != KDA_OK) return s;
-    const int64_t n = (int64_t)num_segments * a->H;
-    cudaError_t e = narrow_states(Mw, M, n, a->dk, a->dk, nullptr, 0, st0);
-    if (e == cudaSuccess) e = narrow_states(Sw, S_tilde, n, a->dk, a->dv, nullptr, 0, st0);
-    return cuda_status(e);
   }
   const FwdPlan p = summary_plan(a, num_segments);
   if ((s = check_workspace(a, p)) != KDA_OK) return s;
@@ -793,7 +695,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
   const bool tc = use_tc(a);
   si.chunk_off = reinterpret_cast<int32_t *>(ws + (tc ? tc_plan(p).off_chunk_off : p.off_chunk_off));
   tcp::TcMaps maps;
-  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps))
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->dk, a->dv, a->H, p.Hk, maps))
     return KDA_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
@@ -804,7 +706,7 @@ kda_status kda_segment_summary(const kda_fwd_args *a, const int32_t *seg_bounds,
     if (e == cudaSuccess)
       e = tcp::launch_tc_prep(maps, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p.nchunks,
                               a->H, p.Hk, pkg, err, flag_count(ws), flag_list(ws, p), st);
-    if (e == cudaSuccess) e = tcp::launch_tc_summary(pkg, S_tilde, M, si, a->H, err, st);
+    if (e == cudaSuccess) e = tcp::launch_tc_summary(pkg, S_tilde, M, si, a->H, a->dk, a->dv, err, st);
   } else {
     if (e == cudaSuccess)
       e = launch_generic_intra(a->qkv_dtype, a->q, a->k, a->v, a->g, a->beta, gate_params(a), si, p, ws, st);
@@ -1172,7 +1074,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *b, kda_stream_t stream) {
   uint32_t *err = reinterpret_cast<uint32_t *>(ws);
   char *pkg = ws + tc_plan(p.f).off_pkg;
   tcp::TcMaps maps;
-  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.f.T_tot, a->H, p.f.Hk, maps))
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.f.T_tot, a->dk, a->dv, a->H, p.f.Hk, maps))
     return KDA_ERR_CUDA;
 
   // V-first states: K-first copies in the workspace
@@ -1380,7 +1282,8 @@ kda_status kda_segment_bwd_summary(const kda_fwd_args *a, const void *d_out,
   si.T = a->T;
   si.N = num_segments;
   tcp::TcMaps maps;
-  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->H, p.Hk, maps)) return KDA_ERR_CUDA;
+  if (tc && !tcp::make_input_maps(a->q, a->k, a->v, a->g, p.T_tot, a->dk, a->dv, a->H, p.Hk, maps))
+    return KDA_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
   if (e == cudaSuccess) e = launch_chunk_map(si, const_cast<int32_t *>(si.chunk_off), st);
   if (tc) {  // the packages, then the reverse chain on the tensor cores

@@ -136,6 +136,9 @@ struct GateParams {
   const float *a_log, *dt_bias;
   float scale, eps;
   uint32_t flags;
+  // head widths of the call (the tensor-core kernels work 128 wide: narrower
+  // heads are read with the extra channels held at zero)
+  int32_t dk = 128, dv = 128;
 };
 
 cudaError_t launch_chunk_map(const SeqInfo &s, int32_t *chunk_off, cudaStream_t st);

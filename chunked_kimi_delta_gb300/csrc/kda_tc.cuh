@@ -161,10 +161,11 @@ struct TcMaps {
   CUtensorMap q, k, v, x;
 };
 
-// Encodes the four input tensor maps; false when the driver entry point is
-// unavailable or a map is rejected.
+// Encodes the four input tensor maps (q, k, gate input with dk channels, v
+// with dv); false when the driver entry point is unavailable or a map is
+// rejected.
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
-                     int H, int Hk, TcMaps &maps);
+                     int dk, int dv, int H, int Hk, TcMaps &maps);
 
 // Strong decay: in an item in which some channel's chunk-local gate (log2
 // units) moves by more than this inside one 16-token sub-block, the prep
@@ -185,11 +186,14 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
 
 struct ChainArgs {
   const char *pkg;
-  void *out;                    // bf16 [T_tot, H, V] or null (not written)
-  const float *initial_state;   // [N, H, K, V] or null
-  float *final_state;           // [N, H, K, V] or null
-  float *h_out;                 // [nchunks, H, K, V] or null
-  float *v_new_out;             // [T_tot, H, V] or null
+  void *out;                    // bf16 [T_tot, H, dv] or null (not written)
+  const float *initial_state;   // [N, H, dk, dv] or null
+  float *final_state;           // [N, H, dk, dv] or null
+  float *h_out;                 // [nchunks, H, dk, dv] or null
+  float *v_new_out;             // [T_tot, H, dv] or null
+  // head widths of the caller's tensors (64 or 128); the chain works 128
+  // wide (the packages of narrow heads carry zeros in the extra channels)
+  int dk = 128, dv = 128;
   // bf16 byte images of the chain's operand tiles, per (chunk, head), for
   // the backward (or null): h entering the chunk (32 KB, MN-major K = 128
   // channels), v_new (16 KB, MN-major K = 64 tokens)
@@ -256,10 +260,10 @@ cudaError_t launch_tc_bwd_dh(const BwdChainArgs &a, const SeqInfo &s, int H, int
 // TMA map of a bf16 [T_tot, H, 128] tensor in the forward's v-tile layout.
 bool make_value_map(const void *x, int64_t T_tot, int H, CUtensorMap &map);
 
-// Segment summary (kda_tc_summary.cu): M and S~ of every (segment, head)
-// from the packages of its chunks.
-cudaError_t launch_tc_summary(const char *pkg, float *S_tilde, float *M, const SeqInfo &s, int H,
-                              uint32_t *err, cudaStream_t st);
+// Segment summary (kda_tc_summary.cu): M [.., dk, dk] and S~ [.., dk, dv] of
+// every (segment, head) from the packages of its chunks.
+cudaError_t launch_tc_summary(const char *pkg, float *S_tilde, float *M, const SeqInfo &s, int H, int dk,
+                              int dv, uint32_t *err, cudaStream_t st);
 
 }  // namespace tcp
 }  // namespace kda

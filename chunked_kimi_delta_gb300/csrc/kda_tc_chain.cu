@@ -54,6 +54,10 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hf = warp >> 2;
   const int kr = 32 * q4 + lane;  // key channel (state row) owned by this thread
+  // the caller's state window: rows < dk, columns < dv (narrow heads: the rest
+  // of the 128 x 128 state stays zero and is not stored)
+  const int dk = a.dk, dv = a.dv;
+  const bool sown = kr < dk && 64 * hf < dv;
   const int n = blockIdx.x / H, h = blockIdx.x % H;
   int64_t t0, t1;
   seq_range(s, n, t0, t1);
@@ -81,8 +85,8 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 
   // initial state -> registers and the bf16 operand
   float hr[64];
-  if (a.initial_state) {
-    const float4 *src = reinterpret_cast<const float4 *>(a.initial_state + (unit * K + kr) * V + 64 * hf);
+  if (a.initial_state && sown) {
+    const float4 *src = reinterpret_cast<const float4 *>(a.initial_state + (unit * dk + kr) * dv + 64 * hf);
 #pragma unroll
     for (int x = 0; x < 16; ++x) {
       const float4 v = src[x];
@@ -158,9 +162,9 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
       __syncwarp();
       tc::tmem_ld16(tPp + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
       tc::tmem_ld_wait();
-      if (a.out && r < lenp) {
+      if (a.out && r < lenp && 64 * hf < dv) {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
-                                               ((tcp + r) * H + h) * V + 64 * hf + 16 * cc);
+                                               ((tcp + r) * H + h) * dv + 64 * hf + 16 * cc);
         dst[0] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
                             pack_bf16(d[6], d[7]));
         dst[1] = make_uint4(pack_bf16(d[8], d[9]), pack_bf16(d[10], d[11]), pack_bf16(d[12], d[13]),
@@ -181,8 +185,8 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     // test only: give up on a wait with the next copies still in flight
     if (a.test_wait_timeout && c == 0 && tid == LEAD && !wait_or_flag(bar_never, 0, a.err, 1000000ull))
       *abort_flag = 1;
-    if (a.h_out) {
-      float4 *dst = reinterpret_cast<float4 *>(a.h_out + (((c0 + c) * H + h) * K + kr) * V + 64 * hf);
+    if (a.h_out && sown) {
+      float4 *dst = reinterpret_cast<float4 *>(a.h_out + (((c0 + c) * H + h) * dk + kr) * dv + 64 * hf);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
     }
@@ -252,8 +256,8 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
           *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col)) = v0;
           *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col + 8)) = v1;
         }
-        if (a.v_new_out && r < len) {
-          float4 *dst = reinterpret_cast<float4 *>(a.v_new_out + ((tc0 + r) * H + h) * V + col);
+        if (a.v_new_out && r < len && col < dv) {
+          float4 *dst = reinterpret_cast<float4 *>(a.v_new_out + ((tc0 + r) * H + h) * dv + col);
 #pragma unroll
           for (int x = 0; x < 4; ++x) dst[x] = make_float4(vn[4 * x], vn[4 * x + 1], vn[4 * x + 2], vn[4 * x + 3]);
         }
@@ -334,8 +338,8 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   __syncthreads();
 
   if (*abort_flag == 0) {
-    if (a.final_state) {
-      float4 *dst = reinterpret_cast<float4 *>(a.final_state + (unit * K + kr) * V + 64 * hf);
+    if (a.final_state && sown) {
+      float4 *dst = reinterpret_cast<float4 *>(a.final_state + (unit * dk + kr) * dv + 64 * hf);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
     }

@@ -41,15 +41,15 @@ bool encode3(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void 
 }  // namespace
 
 bool make_input_maps(const void *q, const void *k, const void *v, const float *x, int64_t T_tot,
-                     int H, int Hk, TcMaps &maps) {
-  if (T_tot <= 0) return false;
-  return encode3(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, K, Hk, T_tot, 128,
+                     int dk, int dv, int H, int Hk, TcMaps &maps) {
+  if (T_tot <= 0 || (dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return false;
+  return encode3(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dk, Hk, T_tot, (uint32_t)dk,
                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode3(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, K, Hk, T_tot, 128,
+         encode3(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dk, Hk, T_tot, (uint32_t)dk,
                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode3(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, V, H, T_tot, 64,
+         encode3(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, H, T_tot, 64,
                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode3(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, K, H, T_tot, 128,
+         encode3(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, dk, H, T_tot, (uint32_t)dk,
                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 

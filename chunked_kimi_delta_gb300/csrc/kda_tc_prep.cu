@@ -109,11 +109,13 @@ __device__ __forceinline__ Item get_item(const SeqInfo &s, int H, int64_t w) {
   return it;
 }
 
+// v of an item: one 64-channel panel per TMA box (one box for heads of 64
+// channels; the second panel then stays zero)
 __device__ __forceinline__ void issue_v(const TcMaps &m, uint8_t *dst, uint64_t *bar,
-                                        const Item &it) {
-  tc::mbar_arrive_expect_tx(bar, 16384);
+                                        const Item &it, int dv) {
+  tc::mbar_arrive_expect_tx(bar, dv == 128 ? 16384u : 8192u);
   tma_load_3d(dst, &m.v, bar, 0, it.h, (int32_t)it.t0);
-  tma_load_3d(dst + 8192, &m.v, bar, 64, it.h, (int32_t)it.t0);
+  if (dv == 128) tma_load_3d(dst + 8192, &m.v, bar, 64, it.h, (int32_t)it.t0);
 }
 
 __device__ __forceinline__ void put_slot(ItemSlot &sl, const Item &it, bool ok) {
@@ -261,7 +263,7 @@ __device__ __noinline__ void strong_factors_exact(uint8_t *sm, uint8_t *pk, cons
   float dbl[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    dbl[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + j] * kLog2e : 0.f;
+    dbl[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * gp.dk + c0 + j] * kLog2e : 0.f;  // c0 < dk here
 #pragma unroll 1
   for (int rr = 0; rr < 8; ++rr) {
     const int r = 8 * warp + rr;
@@ -331,14 +333,15 @@ __device__ __noinline__ void diagonal_blocks_exact(uint8_t *sm, const __nv_bfloa
     if (tid < 128) {  // thread = channel; the sub-block's 16 rows in order
       const int c = tid;
       const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
-      const float dbc = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c] * kLog2e : 0.f;
+      const bool cin = c < gp.dk;  // channels past a narrow head: zero q, k and gate
+      const float dbc = (gate && gp.dt_bias && cin) ? gp.dt_bias[h * gp.dk + c] * kLog2e : 0.f;
       float acc = 0.f;
 #pragma unroll 1
       for (int rl = 0; rl < 16; ++rl) {
         const int r = 16 * Rb + rl;
         __nv_bfloat16 qv = __float2bfloat16_rn(0.f), kv = qv;
         float g = 0.f;
-        if (r < len) {
+        if (r < len && cin) {
           qv = qg_in[base_k + r * rowHk + c];
           kv = kg_in[base_k + r * rowHk + c];
           const float x = xg_in[base_h + r * rowH + c];
@@ -448,8 +451,10 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   const bool l2n = (gp.flags & KDA_L2NORM_QK) != 0;
   const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
   constexpr float kLog2e = 1.4426950408889634f;
-  const int64_t rowH = (int64_t)H * 128;    // elements between tokens of the gate input
-  const int64_t rowHk = GROUPED ? (int64_t)Hk * 128 : rowH;  // and of q, k
+  const int dk = gp.dk, dv = gp.dv;           // 64 or 128: narrow heads are read with the
+                                              // channels from dk on held at zero
+  const int64_t rowH = (int64_t)H * dk;       // elements between tokens of the gate input
+  const int64_t rowHk = GROUPED ? (int64_t)Hk * dk : rowH;  // and of q, k
   const int grp = GROUPED ? H / Hk : 1;                       // value heads per key head
 
   if (warp == 0) {
@@ -464,6 +469,11 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     *strong_flag = 0;
     tc::tma_prefetch_desc(&maps.v);
   }
+  if (dv < 128) {  // the v tile's second panel is never loaded: zero, for every item
+    reinterpret_cast<uint4 *>(sm + S_V + 8192)[tid] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4 *>(sm + S_V + 8192)[tid + NT] = make_uint4(0, 0, 0, 0);
+    tc::fence_proxy_async_smem();
+  }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -472,6 +482,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   // elementwise roles: lane = channel quad (channels c0 .. c0 + 3), warp =
   // row group (rows 8 warp .. 8 warp + 7) inside sub-block R = warp / 2
   const int c0 = 4 * lane, R = warp >> 1;
+  const bool cin = c0 < dk;  // this thread's channels exist (narrow heads: lanes 16..31 do not)
   const uint32_t ch16 = (uint32_t)((lane & 15) >> 1), cbyte = (uint32_t)(lane & 1) * 8u;
   const uint32_t pan = (uint32_t)(lane >> 4);
 
@@ -487,7 +498,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     const bool ok0 = blockIdx.x < nitems && it0.ok;
     put_slot(slots[0], it0, ok0);
     if (ok0) {
-      issue_v(maps, sm + S_V, bar_v, it0);
+      issue_v(maps, sm + S_V, bar_v, it0, dv);
       v_issued = 1;
     }
   }
@@ -501,8 +512,8 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     const int len = it.len, h = it.h;
     const int64_t t0 = it.t0;
     uint8_t *pk = reinterpret_cast<uint8_t *>(pkg + (size_t)(it.gc * H + h) * PK_BYTES);
-    const int64_t base_h = t0 * rowH + (int64_t)h * 128;           // (t0, h, 0) of the gate input
-    const int64_t base_k = t0 * rowHk + (int64_t)(GROUPED ? h / grp : h) * 128;  // (t0, h / grp, 0) of q, k
+    const int64_t base_h = t0 * rowH + (int64_t)h * dk;            // (t0, h, 0) of the gate input
+    const int64_t base_k = t0 * rowHk + (int64_t)(GROUPED ? h / grp : h) * dk;  // (t0, h / grp, 0) of q, k
     Item nx;
     bool okn = false;
     if (tid == 0) {
@@ -535,7 +546,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         qv[rr] = make_uint2(0, 0);
         kv[rr] = make_uint2(0, 0);
         xs[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < len) {
+        if (r < len && cin) {
           qv[rr] = ldg_u2_hint(qg_in + offk, pol_qk);
           kv[rr] = ldg_u2_hint(kg_in + offk, pol_qk);
           xs[rr] = ldg_f4_hint(xg_in + off, pol_once);
@@ -547,7 +558,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
       float dbl[4];  // dt_bias in log2 units
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        dbl[j] = (gate && gp.dt_bias) ? gp.dt_bias[h * 128 + c0 + j] * kLog2e : 0.f;
+        dbl[j] = (gate && gp.dt_bias && cin) ? gp.dt_bias[h * dk + c0 + j] * kLog2e : 0.f;
 
       float v[16];
 #pragma unroll
@@ -607,7 +618,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
           } else {
             g = mul2(xv[p], splat2(kLog2e));
           }
-          if (r >= len) g = splat2(0.f);
+          if (r >= len || !cin) g = splat2(0.f);
           acc[p] = add2(acc[p], g);
           Gl[rr][2 * p] = acc[p].x;
           Gl[rr][2 * p + 1] = acc[p].y;
@@ -990,7 +1001,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
 
     // v is free: fetch the next item's v
     if (tid == 0 && okn) {
-      issue_v(maps, sm + S_V, bar_v, nx);
+      issue_v(maps, sm + S_V, bar_v, nx, dv);
       ++v_issued;
     }
 

@@ -42,8 +42,14 @@ constexpr uint32_t SMEM_BYTES = S_VN + 32768 + 1024;
 static_assert(S_BAR + 64 <= BUF_STRIDE && SMEM_BYTES <= 232448, "shared memory layout");
 constexpr uint32_t TMEM_COLS = 512;              // P (256, M=64 layout) and U (256)
 
+// NARROW: heads of 64 channels (dk or dv), whose M and S~ are the windows
+// of the 128-wide ones (the 128-wide instantiation keeps constant addressing,
+// and so its registers).
+template <bool NARROW>
 __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restrict__ pkg, float *S_tilde,
-                                                           float *Mout, SeqInfo s, int H, uint32_t *err) {
+                                                           float *Mout, SeqInfo s, int H, int dk_arg,
+                                                           int dv_arg, uint32_t *err) {
+  const int dk = NARROW ? dk_arg : 128, dv = NARROW ? dv_arg : 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + S_BAR);  // [2]
@@ -225,12 +231,16 @@ __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restric
   }
   __syncthreads();
 
-  if (*abort_flag == 0) {
-    float *base = cq < 2 ? S_tilde + (unit * K + kr) * V + 64 * cq : Mout + (unit * K + kr) * K + 64 * (cq - 2);
+  // the caller's windows: S~ rows < dk, columns < dv; M rows and columns < dk
+  // (narrow heads: the padded channels' part of M is the identity, of S~ zero)
+  const int lim = cq < 2 ? dv : dk;  // columns of this thread's part
+  if (*abort_flag == 0 && kr < dk && 64 * (cq & 1) < lim) {
+    float *base = (cq < 2 ? S_tilde : Mout) + (unit * dk + kr) * lim + 64 * (cq & 1);
     float4 *dst = reinterpret_cast<float4 *>(base);
 #pragma unroll
     for (int x = 0; x < 16; ++x) dst[x] = make_float4(hr[4 * x], hr[4 * x + 1], hr[4 * x + 2], hr[4 * x + 3]);
-  } else if (tid == 0) {
+  }
+  if (*abort_flag != 0 && tid == 0) {
     // a wait gave up: let the MMAs and copies this CTA started finish (each
     // wait bounded) before its tensor and shared memory are released
     if (ma_pending) drain_wait(bar_ma, ma_par);
@@ -244,14 +254,14 @@ __global__ void __launch_bounds__(NT, 1) tc_summary_kernel(const char *__restric
 
 }  // namespace
 
-cudaError_t launch_tc_summary(const char *pkg, float *S_tilde, float *M, const SeqInfo &s, int H,
-                              uint32_t *err, cudaStream_t st) {
+cudaError_t launch_tc_summary(const char *pkg, float *S_tilde, float *M, const SeqInfo &s, int H, int dk,
+                              int dv, uint32_t *err, cudaStream_t st) {
   const int64_t units = (int64_t)s.N * H;
   if (units == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(tc_summary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
+  auto kern = (dk == 128 && dv == 128) ? tc_summary_kernel<false> : tc_summary_kernel<true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tc_summary_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(pkg, S_tilde, M, s, H, err);
+  kern<<<(unsigned)units, NT, SMEM_BYTES, st>>>(pkg, S_tilde, M, s, H, dk, dv, err);
   return cudaGetLastError();
 }
 

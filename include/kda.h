@@ -164,11 +164,11 @@ size_t kda_chunk_fwd_workspace_size(const kda_fwd_args *args);
  * of its 16-token sub-blocks, the parts of the decay-factored products that
  * could leave the floating-point range are computed from exact gate
  * differences in fp32 on the CUDA cores, so strong decay costs time, not
- * accuracy.  bf16 inputs with dk or dv = 64 run the same 128-wide kernels on
- * zero-padded copies of the narrow tensors in the workspace, with the
- * outputs cut back: exact, since a padded key channel has zero q and k and
- * no decay and a padded value channel zero v, so the padded state rows and
- * columns stay zero.  fp32 inputs run in fp32 on the CUDA cores.
+ * accuracy.  bf16 heads with dk or dv = 64 run the same 128-wide kernels,
+ * which read the narrow tensors directly and hold the missing channels at
+ * zero (zero q and k, no decay, zero v: the extra state rows and columns stay
+ * zero) and write only the caller's channels: exact.  fp32 inputs run in
+ * fp32 on the CUDA cores.
  * With no tokens (B*T == 0, or only empty sequences) the final state is the
  * initial state; q/k/v/g/beta/out may then be NULL.
  * Errors: KDA_ERR_INVALID_ARG (null q/k/v/g/beta/out with tokens, B or H < 1,
@@ -268,8 +268,8 @@ size_t kda_segment_summary_workspace_size(const kda_fwd_args *args, int32_t num_
  * a_log, dt_bias, beta, flags, sizes and workspace of args (q is not needed
  * by the math but is validated); ignores initial_state, cu_seqlens,
  * num_seqs, out, final_state, h_out, v_new_out.  Arithmetic as
- * kda_chunk_fwd (bf16 heads of 64 channels: M and S_tilde cut from the
- * padded problem's, whose M is blockdiag(M, I)).
+ * kda_chunk_fwd (bf16 heads of 64 channels: M and S_tilde are the windows of
+ * the 128-wide ones, whose M is blockdiag(M, I)).
  * seg_bounds: device int32 [num_segments+1], strictly increasing, within
  * [0, tokens].  Errors as kda_chunk_fwd, plus KDA_ERR_INVALID_ARG for
  * num_segments < 1 or a null M / S_tilde / seg_bounds. */
@@ -428,8 +428,9 @@ size_t kda_chunk_bwd_workspace_size(const kda_bwd_args *args);
 /* The chunked KDA backward.  bf16 inputs run on the tensor cores (bf16
  * operands, fp32 accumulation and state; chunks under strong gate decay are
  * recomputed on the CUDA cores in fp32), heads of 64 channels on zero-padded
- * 128-wide copies as in kda_chunk_fwd (gradients cut back; dbeta and dA_log
- * written directly); fp32 inputs run in fp32 on the CUDA cores.
+ * 128-wide copies in the workspace (exact for the reason given at
+ * kda_chunk_fwd; gradients cut back, dbeta and dA_log written directly);
+ * fp32 inputs run in fp32 on the CUDA cores.
  * Deterministic: every sum runs in a fixed order.
  * Errors: those of kda_chunk_fwd for `fwd` (except that out may be NULL),
  * KDA_ERR_INVALID_ARG (null dq/dk/dv/dg/dbeta with tokens),
