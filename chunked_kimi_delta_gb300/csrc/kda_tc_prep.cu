@@ -426,7 +426,9 @@ __device__ __noinline__ void diagonal_blocks_exact(uint8_t *sm, const __nv_bfloa
 // GROUPED: q, k have Hk < H heads (value head h reads key head h / (H / Hk));
 // the ungrouped instantiation shares the gate input's addressing, which keeps
 // its per-row address arithmetic out of the issue-bound load phase.
-template <bool GROUPED>
+// NARROW: d_k or d_v is 64 (gp.dk, gp.dv); the 128-wide instantiation keeps
+// the widths constant, and the masks out of its issue-bound phases.
+template <bool GROUPED, bool NARROW>
 __global__ void __launch_bounds__(NT, 2)
 tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restrict__ qg_in,
                const __nv_bfloat16 *__restrict__ kg_in, const float *__restrict__ xg_in,
@@ -451,7 +453,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   const bool l2n = (gp.flags & KDA_L2NORM_QK) != 0;
   const bool sig = (gp.flags & KDA_BETA_SIGMOID) != 0;
   constexpr float kLog2e = 1.4426950408889634f;
-  const int dk = gp.dk, dv = gp.dv;           // 64 or 128: narrow heads are read with the
+  const int dk = NARROW ? gp.dk : 128, dv = NARROW ? gp.dv : 128;  // narrow heads are read with the
                                               // channels from dk on held at zero
   const int64_t rowH = (int64_t)H * dk;       // elements between tokens of the gate input
   const int64_t rowHk = GROUPED ? (int64_t)Hk * dk : rowH;  // and of q, k
@@ -482,7 +484,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   // elementwise roles: lane = channel quad (channels c0 .. c0 + 3), warp =
   // row group (rows 8 warp .. 8 warp + 7) inside sub-block R = warp / 2
   const int c0 = 4 * lane, R = warp >> 1;
-  const bool cin = c0 < dk;  // this thread's channels exist (narrow heads: lanes 16..31 do not)
+  const bool cin = !NARROW || c0 < dk;  // this thread's channels exist (d_k = 64: lanes 16..31 do not)
   const uint32_t ch16 = (uint32_t)((lane & 15) >> 1), cbyte = (uint32_t)(lane & 1) * 8u;
   const uint32_t pan = (uint32_t)(lane >> 4);
 
@@ -1085,7 +1087,9 @@ cudaError_t launch_tc_prep(const TcMaps &maps, const void *q, const void *k, con
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  auto kern = Hk != H ? tc_prep_kernel<true> : tc_prep_kernel<false>;
+  const bool narrow = gp.dk != 128 || gp.dv != 128;
+  auto kern = Hk != H ? (narrow ? tc_prep_kernel<true, true> : tc_prep_kernel<true, false>)
+                      : (narrow ? tc_prep_kernel<false, true> : tc_prep_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
