@@ -109,15 +109,6 @@ __device__ __forceinline__ Item get_item(const SeqInfo &s, int H, int64_t w) {
   return it;
 }
 
-// v of an item: one 64-channel panel per TMA box (one box for heads of 64
-// channels; the second panel then stays zero)
-__device__ __forceinline__ void issue_v(const TcMaps &m, uint8_t *dst, uint64_t *bar,
-                                        const Item &it, int dv) {
-  tc::mbar_arrive_expect_tx(bar, dv == 128 ? 16384u : 8192u);
-  tma_load_3d(dst, &m.v, bar, 0, it.h, (int32_t)it.t0);
-  if (dv == 128) tma_load_3d(dst + 8192, &m.v, bar, 64, it.h, (int32_t)it.t0);
-}
-
 __device__ __forceinline__ void put_slot(ItemSlot &sl, const Item &it, bool ok) {
   sl.t0 = it.t0;
   sl.gc = it.gc;
@@ -214,6 +205,31 @@ __device__ __forceinline__ void bulk_store_hint(void *dst, const void *src, uint
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
                :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(tc::smem_u32(src)), "r"(bytes), "l"(pol)
                : "memory");
+}
+
+// Asynchronous global -> shared copies of 8 and 16 bytes (no registers held
+// while they are in flight); a row that is not valid copies nothing and reads
+// as zero (src-size 0; the source address is then not dereferenced, and a
+// valid one is passed anyway).
+__device__ __forceinline__ void cp_async8(uint8_t *dst, const void *src, bool valid, uint64_t pol) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2, %3;"
+               :: "r"(tc::smem_u32(dst)), "l"(src), "r"(valid ? 8 : 0), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint8_t *dst, const void *src, bool valid, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;"
+               :: "r"(tc::smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Where a thread's gate-input row rr (16 bytes, fp32 channels c0 .. c0 + 3)
+// waits for phase 1: rows 0..5 in the B1 region from S_XIN (dead from the
+// second MMA of the item before until the operand build), rows 6, 7 in the
+// first v panel (the item's v is requested only after phase 1).  Consecutive
+// threads take consecutive 16-byte slots.
+constexpr uint32_t S_XIN = 65536;
+__device__ __forceinline__ uint32_t x_slot(int rr, int tid) {
+  return rr < 6 ? S_XIN + (uint32_t)(rr * NT + tid) * 16u : S_V + (uint32_t)((rr - 6) * NT + tid) * 16u;
 }
 
 // Strong decay, per thread: its channels decay past the factored range
@@ -423,6 +439,35 @@ __device__ __noinline__ void diagonal_blocks_exact(uint8_t *sm, const __nv_bfloa
   }
 }
 
+// Phase-1 inputs of one item, copied asynchronously into shared memory: this
+// thread's 8 rows x 4 channels of q and k go straight to the positions of
+// the operand tile that phase 2 reads them from (raw bf16), the gate input
+// to the thread's x slots.  Rows past the item's end and channels past a
+// narrow head read as zero.  Only the issuing thread reads these copies
+// back, after its own wait.
+template <bool GROUPED>
+__device__ __forceinline__ void stage_rows(uint8_t *sm, const ItemSlot &it, const __nv_bfloat16 *qg_in,
+                                           const __nv_bfloat16 *kg_in, const float *xg_in, int dk,
+                                           int64_t rowH, int64_t rowHk, int grp, int warp, int c0, bool cin,
+                                           int tid, uint32_t kp128, int prow0, uint32_t ch16, uint32_t cbyte,
+                                           uint64_t pol_qk, uint64_t pol_once) {
+  const int len = it.len, h = it.h;
+  const int64_t base_h = it.t0 * rowH + (int64_t)h * dk;
+  const int64_t base_k = it.t0 * rowHk + (int64_t)(GROUPED ? h / grp : h) * dk;
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int r = 8 * warp + rr;
+    const bool ok = r < len && cin;
+    const int64_t off = ok ? base_h + r * rowH + c0 : 0;
+    const int64_t offk = GROUPED ? (ok ? base_k + r * rowHk + c0 : 0) : off;
+    const uint32_t orow = (uint32_t)(prow0 + rr) * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
+    cp_async8(sm + S_OPA + kp128 + orow, kg_in + offk, ok, pol_qk);
+    cp_async8(sm + S_OPA + kp128 + 64u * 128u + orow, qg_in + offk, ok, pol_qk);
+    cp_async16(sm + x_slot(rr, tid), xg_in + off, ok, pol_once);
+  }
+  cp_async_commit();
+}
+
 // GROUPED: q, k have Hk < H heads (value head h reads key head h / (H / Hk));
 // the ungrouped instantiation shares the gate input's addressing, which keeps
 // its per-row address arithmetic out of the issue-bound load phase.
@@ -495,16 +540,23 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   // thread 0 keeps count of the loads and MMAs it started, for the drain
   int64_t v_issued = 0, v_done = 0;
   bool mma_pending = false;
+  const uint32_t kp128 = pan * 128u * 128u, kp160 = pan * B1_PANEL, kp64 = pan * 64u * 128u;
+  const int prow0 = 16 * lane_block(R) + 8 * (warp & 1);  // OPA row of this thread's first row
   if (tid == 0) {
     Item it0 = get_item(s, H, blockIdx.x);
     const bool ok0 = blockIdx.x < nitems && it0.ok;
     put_slot(slots[0], it0, ok0);
-    if (ok0) {
-      issue_v(maps, sm + S_V, bar_v, it0, dv);
-      v_issued = 1;
-    }
   }
   __syncthreads();
+  // the first item's rows; every later item's are requested during the item
+  // before it, once that item's second MMA has finished, so that they arrive
+  // while it reads out w and u
+  float bnext = 0.f;
+  if (slots[0].ok) {
+    stage_rows<GROUPED>(sm, slots[0], qg_in, kg_in, xg_in, dk, rowH, rowHk, grp, warp, c0, cin, tid, kp128,
+                        prow0, ch16, cbyte, pol_qk, pol_once);
+    if (tid < 64 && tid < slots[0].len) bnext = beta[(slots[0].t0 + tid) * H + slots[0].h];
+  }
 
   uint32_t mma_phase = 0;
   int64_t i = 0;
@@ -535,27 +587,18 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     //      sums of its 8 rows), gate in log2 units and the cumulative sums
     //      of each 8-row group
     float Gl[8][4];
-    const uint32_t kp128 = pan * 128u * 128u, kp160 = pan * B1_PANEL, kp64 = pan * 64u * 128u;
-    const int prow0 = 16 * lane_block(R) + 8 * (warp & 1);  // OPA row of this thread's first row
     {
       uint2 qv[8], kv[8];
       float4 xs[8];
+      cp_async_wait_all();  // this thread's own copies: no barrier needed
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
-        const int r = 8 * warp + rr;
-        const int64_t off = base_h + r * rowH + c0;
-        const int64_t offk = GROUPED ? base_k + r * rowHk + c0 : off;
-        qv[rr] = make_uint2(0, 0);
-        kv[rr] = make_uint2(0, 0);
-        xs[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < len && cin) {
-          qv[rr] = ldg_u2_hint(qg_in + offk, pol_qk);
-          kv[rr] = ldg_u2_hint(kg_in + offk, pol_qk);
-          xs[rr] = ldg_f4_hint(xg_in + off, pol_once);
-        }
+        const uint32_t orow = (uint32_t)(prow0 + rr) * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
+        kv[rr] = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + orow);
+        qv[rr] = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + 64u * 128u + orow);
+        xs[rr] = *reinterpret_cast<const float4 *>(sm + x_slot(rr, tid));
       }
-      float bload = 0.f;
-      if (tid < 64 && tid < len) bload = beta[(t0 + tid) * H + h];
+      const float bload = bnext;
       const float A_h = gate ? tc::ex2(gp.a_log[h] * kLog2e) : 0.f;
       float dbl[4];  // dt_bias in log2 units
 #pragma unroll
@@ -595,12 +638,6 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         else rk[r] = nv;
       }
       if (tid < 64) sbeta[tid] = (sig && tid < len) ? 1.f / (1.f + tc::ex2(-bload * kLog2e)) : bload;
-#pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const uint32_t orow = (uint32_t)(prow0 + rr) * 128u + (((ch16 ^ (uint32_t)rr) << 4) | cbyte);
-        st_u64(sm + S_OPA, kp128 + orow, kv[rr]);
-        st_u64(sm + S_OPA, kp128 + 64u * 128u + orow, qv[rr]);
-      }
 
       float2 acc[2] = {splat2(0.f), splat2(0.f)};
       const float2 dbl2[2] = {make_float2(dbl[0], dbl[1]), make_float2(dbl[2], dbl[3])};
@@ -631,7 +668,15 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     // the staging buffers of the previous item must be read out before this
     // item's operand tiles overwrite them
     if (tid == 0) bulk_wait_read();
-    __syncthreads();  // group totals, rstd and beta published
+    __syncthreads();  // group totals, rstd and beta published; x slots read
+    // every thread has read its x slots: the item's v may land in the first panel
+    if (tid == 0) {
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive_expect_tx(bar_v, dv == 128 ? 16384u : 8192u);
+      tma_load_3d(sm + S_V, &maps.v, bar_v, 0, h, (int32_t)t0);
+      if (dv == 128) tma_load_3d(sm + S_V + 8192, &maps.v, bar_v, 64, h, (int32_t)t0);
+      ++v_issued;
+    }
 
     // ---- phase 2: operand tiles and the elementwise package parts
     bool strong = false;
@@ -1001,10 +1046,15 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
     __syncthreads();
     if (*abort_flag) break;
 
-    // v is free: fetch the next item's v
-    if (tid == 0 && okn) {
-      issue_v(maps, sm + S_V, bar_v, nx, dv);
-      ++v_issued;
+    // the second MMA and the read of the Aqk image are done: request the next
+    // item's rows
+    {
+      const ItemSlot itn = slots[(i + 1) & 1];
+      if (itn.ok) {
+        stage_rows<GROUPED>(sm, itn, qg_in, kg_in, xg_in, dk, rowH, rowHk, grp, warp, c0, cin, tid, kp128,
+                            prow0, ch16, cbyte, pol_qk, pol_once);
+        if (tid < 64 && tid < itn.len) bnext = beta[(itn.t0 + tid) * H + itn.h];
+      }
     }
 
     // ---- read D2: w (lanes 0..63 of columns 0..127) -> package WQ rows
@@ -1060,6 +1110,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
   // Drain after a timeout: wait (bounded) for the load and the MMA this CTA
   // started, so that nothing lands in memory it no longer owns.  On the
   // normal path every issued load has been consumed.
+  cp_async_wait_all();
   __syncthreads();
   if (tid == 0) {
     bulk_wait_all();  // package stores complete before the CTA exits
