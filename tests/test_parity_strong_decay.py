@@ -27,6 +27,7 @@ LOG2E = 1.4426950408889634
 # sub-blocks whose chunk-local gate moves by more than this (log2 units) take
 # the exact paths
 STRONG_LOG2 = 96.0
+GRADS = ["dq", "dk", "dv", "dg", "dbeta"]
 
 
 def _strong_and_weak(cfg, inp_c):
@@ -108,6 +109,82 @@ def test_fwd_gate_cliff_inside_a_sub_block(cuda_lib):
     _fwd_case(cuda_lib, cfg, inp, need_weak=False)
 
 
+def _chunk_gate_pattern(inp, cfg, kind):
+    """Precomputed natural-log gates whose chunk totals are large while the
+    16-token sub-blocks stay ordinary, or the other way round:
+      near_edge:    -2.05 nats per token on every channel: 189 log2 units per
+                    64-token chunk, 47 per sub-block
+      past_edge:    -2.2 nats per token: 203 per chunk, 51 per sub-block
+      cliff_inside: -0.01 per token and -80 nats at token 5 of every chunk on
+                    odd channels: 116 log2 units inside one sub-block (listed
+                    for the exact passes) in a chunk that moves little else
+      channel_mix:  even channels -2.05 per token, odd channels -2.4"""
+    g = torch.full_like(inp["g"], -0.01)
+    t = torch.arange(cfg.T)
+    if kind == "near_edge":
+        g[:] = -2.05
+    elif kind == "past_edge":
+        g[:] = -2.2
+    elif kind == "cliff_inside":
+        g[:, (t % 64) == 5, :, 1::2] = -80.0
+    elif kind == "channel_mix":
+        g[..., 0::2] = -2.05
+        g[..., 1::2] = -2.4
+    inp["g"] = g
+    return inp
+
+
+def _chunk_moves(cfg, inp_c):
+    """Largest move of the gate (log2 units) over any whole chunk, and over
+    any 16-token sub-block, from the oracle's gate."""
+    p = oracle_problem(cfg, inp_c)
+    g = oracle.preprocess(p)[3] * LOG2E
+    chunk = sub = 0.0
+    for n in range(len(p.cu) - 1):
+        for c0 in range(int(p.cu[n]), int(p.cu[n + 1]), 64):
+            c1 = min(c0 + 64, int(p.cu[n + 1]))
+            chunk = max(chunk, float(np.abs(g[c0:c1].sum(axis=0)).max()))
+            for b0 in range(c0, c1, 16):
+                sub = max(sub, float(np.abs(g[b0:min(b0 + 16, c1)].sum(axis=0)).max()))
+    return chunk, sub
+
+
+@pytest.mark.parametrize("kind", ["near_edge", "past_edge", "cliff_inside", "channel_mix"])
+def test_fwd_large_chunk_decay(cuda_lib, kind):
+    cfg = KdaConfig("ref_bound", B=2, T=200, H=2, dk=128, dv=128, dtype="bf16", gate_in_kernel=False,
+                    initial_state=True, seed=61)
+    inp_c = _chunk_gate_pattern(make(cfg), cfg, kind)
+    chunk, sub = _chunk_moves(cfg, inp_c)
+    if kind == "cliff_inside":
+        assert sub > STRONG_LOG2 and chunk < 120.0, (chunk, sub)
+    else:  # large chunk totals from sub-blocks that stay ordinary
+        assert chunk > 180.0 and sub <= STRONG_LOG2, (chunk, sub)
+    out, fin = gpu_fwd(cuda_lib, cfg, to_cuda(inp_c))
+    o_ref, f_ref = oracle.chunk_fwd(oracle_problem(cfg, inp_c), inp_c["initial_state"])
+    check(out.reshape(o_ref.shape), o_ref, cfg.dtype, "o")
+    check(fin, f_ref, cfg.dtype, "final_state")
+
+
+@pytest.mark.parametrize("kind", ["near_edge", "cliff_inside"])
+def test_bwd_large_chunk_decay(cuda_lib, kind):
+    """Backward on the same gate patterns: the cliff case's chunks go through
+    the backward's exact pass."""
+    cfg = KdaConfig("ref_bound_bwd", B=1, T=150, H=2, dk=128, dv=128, dtype="bf16",
+                    gate_in_kernel=False, initial_state=True, seed=62)
+    inp_c = _chunk_gate_pattern(make(cfg), cfg, kind)
+    cot = make_cotangents(cfg, inp_c)
+    inp = to_cuda(inp_c)
+    got = cuda_lib.kda_chunk_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                 cot["d_out"].cuda(), d_final_state=cot["d_final_state"].cuda(),
+                                 want_d_initial_state=True, **fwd_kwargs(cfg, inp))
+    torch.cuda.synchronize()
+    ref = oracle.chunk_bwd(oracle_problem(cfg, inp_c), inp_c["initial_state"], cot["d_out"],
+                           cot["d_final_state"])
+    for name in GRADS:
+        check(got[name].reshape(ref[name].shape), ref[name], "bf16", name)
+    check(got["d_initial_state"], ref["d_initial"], "bf16", "d_initial_state")
+
+
 def test_summary_scan_strong_decay(cuda_lib):
     cfg = KdaConfig("strong_seg", B=1, T=333, H=2, dk=128, dv=128, dtype="bf16", use_exp2=True,
                     initial_state=True, a_log_range=(1.0, 3.0), seed=12)
@@ -130,9 +207,6 @@ def test_summary_scan_strong_decay(cuda_lib):
     _, f_ref = oracle.chunk_fwd(p, inp_c["initial_state"])
     check(S_in, Si_ref, "bf16", "S_in")
     check(S_fin, f_ref[0], "bf16", "scanned final state")
-
-
-GRADS = ["dq", "dk", "dv", "dg", "dbeta"]
 
 
 @pytest.mark.parametrize("case", ["a_log U(1,3)", "channel mix, varlen"])
