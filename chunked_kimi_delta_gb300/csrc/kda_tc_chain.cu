@@ -38,7 +38,16 @@ constexpr uint32_t SMEM_BYTES = 198656 + 1024;
 constexpr uint32_t BUF_STRIDE = S_BUF1 - S_BUF0;
 constexpr uint32_t TMEM_COLS = 512;          // P (two buffers) and U
 
+// EXTRAS: the optional outputs (per-chunk states and v_new, the backward's
+// tile images, the test-only wait); the instantiation without them keeps the
+// per-chunk loops free of their branches.
+template <bool EXTRAS>
 __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s, int H) {
+  if (!EXTRAS) {
+    a.h_out = a.v_new_out = nullptr;
+    a.h_img = a.vn_img = nullptr;
+    a.test_wait_timeout = false;
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *fullA = reinterpret_cast<uint64_t *>(sm + S_BAR);  // [2] WQ, U of a buffer
@@ -362,10 +371,11 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
 cudaError_t launch_tc_chain(const ChainArgs &a, const SeqInfo &s, int H, cudaStream_t st) {
   const int64_t units = (int64_t)s.N * H;
   if (units == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
+  const bool extras = a.h_out || a.v_new_out || a.h_img || a.vn_img || a.test_wait_timeout;
+  auto kern = extras ? tc_chain_kernel<true> : tc_chain_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tc_chain_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(a, s, H);
+  kern<<<(unsigned)units, NT, SMEM_BYTES, st>>>(a, s, H);
   return cudaGetLastError();
 }
 
