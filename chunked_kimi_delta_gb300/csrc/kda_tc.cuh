@@ -259,6 +259,9 @@ cudaError_t launch_tc_bwd_dh(const BwdChainArgs &a, const SeqInfo &s, int H, int
 
 // TMA map of a bf16 [T_tot, H, 128] tensor in the forward's v-tile layout.
 bool make_value_map(const void *x, int64_t T_tot, int H, CUtensorMap &map);
+// The chain's output o, bf16 [T_tot, H, dv]: boxes of 64 channels x 64 tokens
+// of one head, 128-byte swizzle (the layout of the chain's staging tile).
+bool make_out_map(const void *o, int64_t T_tot, int H, int dv, CUtensorMap &map);
 
 // Segment summary (kda_tc_summary.cu): M [.., dk, dk] and S~ [.., dk, dv] of
 // every (segment, head) from the packages of its chunks.

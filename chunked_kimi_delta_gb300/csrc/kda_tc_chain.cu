@@ -21,6 +21,7 @@
 // the MMAs of chunk c - 1 have finished.
 //
 #include <cuda_bf16.h>
+#include <string.h>
 
 #include "kda_tc.cuh"
 
@@ -34,15 +35,37 @@ constexpr uint32_t S_BAR = PK_BYTES;         // mbarriers in the gap before buff
 constexpr uint32_t S_BUF1 = 74752;           // 1024-aligned
 constexpr uint32_t S_HB = 149504;            // h bf16, MN-major (K = 128 channels)
 constexpr uint32_t S_VN = 182272;            // v_new bf16, MN-major (K = 64 tokens)
-constexpr uint32_t SMEM_BYTES = 198656 + 1024;
+constexpr uint32_t S_OST = 198656;           // o of a full chunk, bf16, staged for the TMA store
+constexpr uint32_t SMEM_BYTES = S_OST + 16384 + 1024;
+static_assert(S_OST % 1024 == 0 && SMEM_BYTES <= 232448, "shared memory layout");
 constexpr uint32_t BUF_STRIDE = S_BUF1 - S_BUF0;
 constexpr uint32_t TMEM_COLS = 512;          // P (two buffers) and U
+
+// 3-D TMA store of a staged tile (coordinates: channel, head, token), tracked
+// by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int32_t x, int32_t y,
+                                             int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// Barrier over the 128 threads of the o warps (lane quarters 0 and 1), the
+// AND of their flags returned to each.
+__device__ __forceinline__ bool o_warps_and(bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
+               "selp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r) : "r"((uint32_t)v) : "memory");
+  return r != 0;
+}
 
 // EXTRAS: the optional outputs (per-chunk states and v_new, the backward's
 // tile images, the test-only wait); the instantiation without them keeps the
 // per-chunk loops free of their branches.
 template <bool EXTRAS>
-__global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s, int H) {
+__global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__ CUtensorMap map_o,
+                                                         ChainArgs a, SeqInfo s, int H, bool o_tma) {
   if (!EXTRAS) {
     a.h_out = a.v_new_out = nullptr;
     a.h_img = a.vn_img = nullptr;
@@ -156,10 +179,19 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
   }
 
   // o of a finished chunk: P rows 0..63 of its buffer, by the warps of lane
-  // quarters 0 and 1 once Aqk v_new has landed (Mb completion number cp)
+  // quarters 0 and 1 once Aqk v_new has landed (Mb completion number cp).  A
+  // full chunk goes out through the shared staging tile and one TMA store
+  // per 64 columns (whole 128-byte lines); a shorter one (the end of a
+  // sequence: the rows after it belong to the next) row by row.
   auto read_o = [&](int64_t cp, int lenp) {
-    // tcgen05.ld needs the whole warp: act on a warp-uniform verdict
-    const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar_mb, (uint32_t)(cp & 1), a.err));
+    // tcgen05.ld needs the whole warp, the staging tile all four o warps: act
+    // on a verdict shared by the four
+    bool ok = __all_sync(0xffffffffu, wait_or_flag(bar_mb, (uint32_t)(cp & 1), a.err));
+    const bool staged = o_tma && a.out && lenp == BT;
+    if (staged) {
+      if (tid == 0) bulk_wait_read();  // the previous tile's store has read the staging buffer
+      ok = o_warps_and(ok);
+    }
     if (!ok) { *abort_flag = 1; return; }
     tc::tc_fence_after();
     const uint32_t tPp = tmem + 128u * (uint32_t)(cp & 1);
@@ -171,13 +203,27 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
       __syncwarp();
       tc::tmem_ld16(tPp + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
       tc::tmem_ld_wait();
-      if (a.out && r < lenp && 64 * hf < dv) {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
-                                               ((tcp + r) * H + h) * dv + 64 * hf + 16 * cc);
-        dst[0] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
-                            pack_bf16(d[6], d[7]));
-        dst[1] = make_uint4(pack_bf16(d[8], d[9]), pack_bf16(d[10], d[11]), pack_bf16(d[12], d[13]),
-                            pack_bf16(d[14], d[15]));
+      const uint4 o0 = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                                  pack_bf16(d[6], d[7]));
+      const uint4 o1 = make_uint4(pack_bf16(d[8], d[9]), pack_bf16(d[10], d[11]), pack_bf16(d[12], d[13]),
+                                  pack_bf16(d[14], d[15]));
+      const int col = 64 * hf + 16 * cc;
+      if (staged) {
+        *reinterpret_cast<uint4 *>(sm + S_OST + mnmaj_off(64, r, col)) = o0;
+        *reinterpret_cast<uint4 *>(sm + S_OST + mnmaj_off(64, r, col + 8)) = o1;
+      } else if (a.out && r < lenp && 64 * hf < dv) {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + ((tcp + r) * H + h) * dv + col);
+        dst[0] = o0;
+        dst[1] = o1;
+      }
+    }
+    if (staged) {
+      tc::fence_proxy_async_smem();  // the tile's generic writes, before the TMA reads it
+      o_warps_and(true);
+      if (tid == 0) {
+        tma_store_3d(&map_o, sm + S_OST, 0, h, (int32_t)tcp);
+        if (dv == 128) tma_store_3d(&map_o, sm + S_OST + 8192, 64, h, (int32_t)tcp);
+        bulk_commit();
       }
     }
   };
@@ -235,23 +281,36 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     }
     if (ok && q4 >= 2) {
       const int r = 32 * (q4 - 2) + lane;
+      constexpr int PER = 4;  // TMEM loads per wait (all four, then one wait)
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float d[16];
-        __syncwarp();
-        tc::tmem_ld16(tP + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * cc, d);
-        tc::tmem_ld_wait();
+      for (int cg = 0; cg < 4; cg += PER) {
+      float dd[PER][16];
+      uint4 uu[PER][2];
+      __syncwarp();
+#pragma unroll
+      for (int x = 0; x < PER; ++x)
+        tc::tmem_ld16(tP + ((uint32_t)(32 * q4) << 16) + 64 * hf + 16 * (cg + x), dd[x]);
+#pragma unroll
+      for (int x = 0; x < PER; ++x) {
+        const int colx = 64 * hf + 16 * (cg + x);
+        uu[x][0] = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, colx));
+        uu[x][1] = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, colx + 8));
+      }
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int x = 0; x < PER; ++x) {
+        const int cc = cg + x;
+        const float *d = dd[x];
         const int col = 64 * hf + 16 * cc;
         float vn[16];
         {
-          const uint4 ua = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, col));
-          const uint4 ub = *reinterpret_cast<const uint4 *>(buf + PK_U + u_offset(r, col + 8));
+          const uint4 ua = uu[x][0], ub = uu[x][1];
           const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const float2 u2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[x]));
-            vn[2 * x] = u2.x - d[2 * x];
-            vn[2 * x + 1] = u2.y - d[2 * x + 1];
+          for (int x2 = 0; x2 < 8; ++x2) {
+            const float2 u2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[x2]));
+            vn[2 * x2] = u2.x - d[2 * x2];
+            vn[2 * x2 + 1] = u2.y - d[2 * x2 + 1];
           }
         }
         const uint4 v0 = make_uint4(pack_bf16(vn[0], vn[1]), pack_bf16(vn[2], vn[3]),
@@ -268,8 +327,9 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
         if (a.v_new_out && r < len && col < dv) {
           float4 *dst = reinterpret_cast<float4 *>(a.v_new_out + ((tc0 + r) * H + h) * dv + col);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) dst[x] = make_float4(vn[4 * x], vn[4 * x + 1], vn[4 * x + 2], vn[4 * x + 3]);
+          for (int x3 = 0; x3 < 4; ++x3) dst[x3] = make_float4(vn[4 * x3], vn[4 * x3 + 1], vn[4 * x3 + 2], vn[4 * x3 + 3]);
         }
+      }
       }
     }
     if (q4 >= 2) {
@@ -361,6 +421,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(ChainArgs a, SeqInfo s,
     for (int64_t c = a_done; c < a_issued; ++c) drain_wait(fullA + (c & 1), (uint32_t)((c >> 1) & 1));
     for (int64_t c = b_done; c < b_issued; ++c) drain_wait(fullB + (c & 1), (uint32_t)((c >> 1) & 1));
   }
+  if (tid == 0) bulk_wait_all();  // the TMA stores of o are complete before the CTA ends
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
@@ -375,7 +436,13 @@ cudaError_t launch_tc_chain(const ChainArgs &a, const SeqInfo &s, int H, cudaStr
   auto kern = extras ? tc_chain_kernel<true> : tc_chain_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)units, NT, SMEM_BYTES, st>>>(a, s, H);
+  // o of full chunks by TMA: [T_tot, H, dv] bf16 with 16-byte aligned rows
+  // (without a map the rows are stored one by one)
+  CUtensorMap map_o;
+  memset(&map_o, 0, sizeof(map_o));
+  const bool o_tma = a.out && (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 &&
+                     make_out_map(a.out, s.T_tot, H, a.dv, map_o);
+  kern<<<(unsigned)units, NT, SMEM_BYTES, st>>>(map_o, a, s, H, o_tma);
   return cudaGetLastError();
 }
 

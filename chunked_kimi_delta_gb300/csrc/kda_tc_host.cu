@@ -53,6 +53,11 @@ bool make_input_maps(const void *q, const void *k, const void *v, const float *x
                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool make_out_map(const void *o, int64_t T_tot, int H, int dv, CUtensorMap &map) {
+  if (T_tot <= 0 || (dv != 64 && dv != 128)) return false;
+  return encode3(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o, dv, H, T_tot, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool make_value_map(const void *x, int64_t T_tot, int H, CUtensorMap &map) {
   if (T_tot <= 0) return false;
   return encode3(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, V, H, T_tot, 64,
