@@ -31,8 +31,10 @@
 //   B rows 48..95 : k^_j 2^{b_3 - G_j}, j < 48
 //   B rows 96..159: k^_j 2^{b_R(j) - G_j}, j < 64 (own block)
 //
-// One persistent CTA per SM loops over (chunk, head) items; TMA brings the
-// next item's q, k, gate input and v while the current one computes.
+// Two persistent CTAs per SM loop over (chunk, head) items.  Once an item's
+// second MMA has finished, cp.async brings the next item's q, k and gate input
+// into shared memory while the current one reads out w and u; the item's v
+// arrives by TMA during its own operand build.
 #include <cuda_bf16.h>
 
 #include "kda_tc.cuh"
@@ -64,7 +66,7 @@ constexpr uint32_t S_STG_AQK = 73728;  // Aqk image (8192), written after MMA 1 
 constexpr uint32_t S_FIX = 56320;      // G [16][128] fp32, then q, k [16][128] bf16 (ends at 72704)
 constexpr uint32_t S_STG_W = 90112;    // w rows of WQ, 2 panels x 8192, after MMA 2 (B2A dead)
 constexpr uint32_t S_STG_U = 49152;    // U image (16384), after MMA 2 (B1 dead)
-// OPA holds nothing between items: phase 1 parks the raw q and k rows there,
+// OPA holds nothing between items: the next item's raw q and k rows land there,
 // at the positions phase 2 overwrites with the scaled operands.
 constexpr uint32_t S_MISC = 106496;
 constexpr uint32_t M_RQ = S_MISC;           // fp32 [64] scale x rstd q
@@ -746,7 +748,7 @@ tc_prep_kernel(const __grid_constant__ TcMaps maps, const __nv_bfloat16 *__restr
         const uint32_t rowb = (uint32_t)r * 128u + xo;
         const uint32_t orow = (uint32_t)(prow0 + rr) * 128u + xo;
         const float sq = rq[r], sk = rk[r];
-        // raw rows parked by this thread in phase 1
+        // raw rows this thread copied in (cp.async) and read in phase 1
         const uint2 qraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + 64u * 128u + orow);
         const uint2 kraw = *reinterpret_cast<const uint2 *>(sm + S_OPA + kp128 + orow);
         const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw);
