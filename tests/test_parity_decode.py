@@ -127,3 +127,44 @@ def test_decode_layouts_agree_bit_for_bit(cuda_lib):
     o2 = cuda_lib.kda_recurrent_step(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], pool2, idx, **kw)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(pool, pool2)
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128)])
+def test_decode_many_states_against_oracle(cuda_lib, dk, dv):
+    """More states than the GPU holds CTAs at once (384 states, aligned fp32
+    pool): invalid rows, a false flag and untouched rows as in the small
+    cases; three tokens per sequence."""
+    N, H, T, rows = 48, 8, 3, 64
+    cfg = KdaConfig("decode_many", B=N, T=T, H=H, dk=dk, dv=dv, dtype="bf16", beta_sigmoid=True,
+                    gate_in_kernel=True, seed=dk + 5)
+    inp = make(cfg)
+    base, pool = _pool(rows, H, dk, dv, torch.float32, gap=0, seed=9)
+    before = base.clone()
+    perm = torch.randperm(rows, generator=torch.Generator().manual_seed(4))[:N].to(torch.int32)
+    idx = perm.clone()
+    idx[5] = -1
+    idx[17] = rows  # past the pool: invalid
+    flags = torch.ones(N, dtype=torch.bool)
+    flags[9] = False
+    S0 = torch.zeros(N, H, dk, dv, dtype=torch.float64)
+    for i in range(N):
+        r = int(idx[i])
+        if 0 <= r < rows and flags[i]:
+            S0[i] = pool[r].double().cpu()
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v", "g", "beta", "a_log", "dt_bias")}
+    out = cuda_lib.kda_recurrent_step(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], pool,
+                                      idx.cuda(), flags.cuda(), scale=scale_of(cfg),
+                                      a_log=dev["a_log"], dt_bias=dev["dt_bias"], l2norm_qk=True,
+                                      beta_sigmoid=True, gate_in_kernel=True)
+    torch.cuda.synchronize()
+    o_ref, f_ref = oracle.chunk_fwd(oracle_problem(cfg, inp), S0)
+    check(out.reshape(o_ref.shape), o_ref, "bf16", "o")
+    written = set()
+    for i in range(N):
+        r = int(idx[i])
+        if 0 <= r < rows:
+            check(pool[r], f_ref[i], "bf16", f"pool row {r}")
+            written.add(r)
+    for r in range(rows):
+        if r not in written:
+            assert torch.equal(base[r], before[r]), f"row {r} changed"
