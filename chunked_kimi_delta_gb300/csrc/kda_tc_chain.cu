@@ -128,20 +128,17 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
 #pragma unroll
     for (int x = 0; x < 64; ++x) hr[x] = 0.f;
   }
-  // h (bf16) -> the MMA operand tile; with h_img also the tile's byte image
-  // for chunk ci (the state entering it), for the backward
-  auto store_hb = [&](int64_t ci) {
-    uint8_t *img = (a.h_img && ci < nch) ? a.h_img + (size_t)((c0 + ci) * H + h) * 32768 : nullptr;
+  // h (bf16) -> the MMA operand tile (with h_img, the tile itself is copied
+  // out as the byte image of the state entering the chunk, for the backward)
+  auto store_hb = [&]() {
 #pragma unroll
     for (int x = 0; x < 64; x += 8) {
       const uint4 v = make_uint4(pack_bf16(hr[x], hr[x + 1]), pack_bf16(hr[x + 2], hr[x + 3]),
                                  pack_bf16(hr[x + 4], hr[x + 5]), pack_bf16(hr[x + 6], hr[x + 7]));
-      const uint32_t off = mnmaj_off(128, kr, 64 * hf + x);
-      *reinterpret_cast<uint4 *>(sm + S_HB + off) = v;
-      if (img) *reinterpret_cast<uint4 *>(img + off) = v;
+      *reinterpret_cast<uint4 *>(sm + S_HB + mnmaj_off(128, kr, 64 * hf + x)) = v;
     }
   };
-  store_hb(0);
+  store_hb();
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -250,6 +247,15 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
 
     // ---- [qg; w] h -> P (this chunk's buffer)
     if (tid == LEAD) {
+      if (a.h_img || a.vn_img) {
+        // the previous chunk's v_new image has been read out of S_VN before
+        // this chunk's v_new replaces it; the h tile goes out as its image
+        bulk_wait_read();
+        if (a.h_img) {
+          bulk_store(a.h_img + (size_t)((c0 + c) * H + h) * 32768, sm + S_HB, 32768);
+          bulk_commit();
+        }
+      }
       tc::tc_fence_after();
       const uint32_t idesc = tc::idesc_bf16_f32(128, 128, false, true);
       const uint32_t a0 = tc::smem_u32(buf + PK_WQ), b0 = tc::smem_u32(sm + S_HB);
@@ -319,11 +325,6 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
                                     pack_bf16(vn[12], vn[13]), pack_bf16(vn[14], vn[15]));
         *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col)) = v0;
         *reinterpret_cast<uint4 *>(sm + S_VN + mnmaj_off(64, r, col + 8)) = v1;
-        if (a.vn_img) {  // the tile's byte image, for the backward
-          uint8_t *img = a.vn_img + (size_t)((c0 + c) * H + h) * 16384;
-          *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col)) = v0;
-          *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col + 8)) = v1;
-        }
         if (a.v_new_out && r < len && col < dv) {
           float4 *dst = reinterpret_cast<float4 *>(a.v_new_out + ((tc0 + r) * H + h) * dv + col);
 #pragma unroll
@@ -355,6 +356,8 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
       if (!go) *abort_flag = 1;
     }
     if (go) {
+      // the h image has been read out of S_HB before the update below rewrites it
+      if (a.h_img) bulk_wait_read();
       tc::tc_fence_after();
       const uint32_t vn0 = tc::smem_u32(sm + S_VN);
       const uint32_t idc = tc::idesc_bf16_f32(128, 128, true, true);
@@ -377,6 +380,10 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
         mb_issued = true;
         mb_par = (uint32_t)(c & 1);
       }
+      if (a.vn_img) {  // the v_new tile goes out as its image, for the backward
+        bulk_store(a.vn_img + (size_t)((c0 + c) * H + h) * 16384, sm + S_VN, 16384);
+        bulk_commit();
+      }
     }
     __syncwarp();
     ok = __all_sync(0xffffffffu, wait_or_flag(bar_mc, (uint32_t)(c & 1), a.err));
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
 #pragma unroll
         for (int x = 0; x < 16; ++x) hr[16 * cc + x] = fmaf(gcv, hr[16 * cc + x], d[x]);
       }
-      store_hb(c + 1);
+      store_hb();
     }
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();
@@ -421,7 +428,9 @@ __global__ void __launch_bounds__(NT, 1) tc_chain_kernel(const __grid_constant__
     for (int64_t c = a_done; c < a_issued; ++c) drain_wait(fullA + (c & 1), (uint32_t)((c >> 1) & 1));
     for (int64_t c = b_done; c < b_issued; ++c) drain_wait(fullB + (c & 1), (uint32_t)((c >> 1) & 1));
   }
-  if (tid == 0) bulk_wait_all();  // the TMA stores of o are complete before the CTA ends
+  // the TMA stores of o (thread 0) and the image copies (LEAD) are complete
+  // before the CTA ends
+  if (tid == 0 || tid == LEAD) bulk_wait_all();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
