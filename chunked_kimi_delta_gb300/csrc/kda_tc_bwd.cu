@@ -93,20 +93,18 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
 #pragma unroll
     for (int x = 0; x < 64; ++x) dh[x] = 0.f;
   }
-  // dh' (bf16) -> the MMA operand tile; with dh_img also its byte image for
-  // chunk ci (the gradient of the state leaving it)
-  auto store_hb = [&](int64_t ci) {
-    uint8_t *img = (a.dh_img && ci >= 0) ? a.dh_img + (size_t)((c0 + ci) * H + h) * 32768 : nullptr;
+  // dh' (bf16) -> the MMA operand tile (with dh_img, the tile itself is
+  // copied out as the byte image of the gradient of the state leaving the
+  // chunk it serves)
+  auto store_hb = [&]() {
 #pragma unroll
     for (int x = 0; x < 64; x += 8) {
       const uint4 v = make_uint4(pack_bf16(dh[x], dh[x + 1]), pack_bf16(dh[x + 2], dh[x + 3]),
                                  pack_bf16(dh[x + 4], dh[x + 5]), pack_bf16(dh[x + 6], dh[x + 7]));
-      const uint32_t off = mnmaj_off(128, kr, 64 * hf + x);
-      *reinterpret_cast<uint4 *>(sm + S_HB + off) = v;
-      if (img) *reinterpret_cast<uint4 *>(img + off) = v;
+      *reinterpret_cast<uint4 *>(sm + S_HB + mnmaj_off(128, kr, 64 * hf + x)) = v;
     }
   };
-  store_hb(nch - 1);
+  store_hb();
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -159,6 +157,15 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
     if (*abort_flag) break;
 
     if (tid == 0) {
+      if (a.dh_img || a.dv_img) {
+        // the previous step's -dv_new image has been read out of S_DV before
+        // this step's replaces it; the dh' tile goes out as its image
+        bulk_wait_read();
+        if (a.dh_img) {
+          bulk_store(a.dh_img + (size_t)((c0 + c) * H + h) * 32768, sm + S_HB, 32768);
+          bulk_commit();
+        }
+      }
       tc::tc_fence_after();
       // ---- D1 = kg dh' + Aqk^T dO   (M = 64 tokens)
       const uint32_t idk = tc::idesc_bf16_f32(64, 128, false, true);
@@ -216,11 +223,6 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
                                       pack_bf16(-d[12], -d[13]), pack_bf16(-d[14], -d[15]));
           *reinterpret_cast<uint4 *>(sm + S_DV + mnmaj_off(64, r, col)) = v0;
           *reinterpret_cast<uint4 *>(sm + S_DV + mnmaj_off(64, r, col + 8)) = v1;
-          if (a.dv_img) {
-            uint8_t *img = a.dv_img + (size_t)((c0 + c) * H + h) * 16384;
-            *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col)) = v0;
-            *reinterpret_cast<uint4 *>(img + mnmaj_off(64, r, col + 8)) = v1;
-          }
         }
       }
     }
@@ -236,6 +238,8 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
     if (tid == 0) {
       go = !*abort_flag && wait_or_flag(dv_ready, (uint32_t)(i & 1), a.err);
       if (go) {
+        // the dh' image has been read out of S_HB before the update below rewrites it
+        if (a.dh_img) bulk_wait_read();
         tc::tc_fence_after();
         const uint32_t idq = tc::idesc_bf16_f32(128, 128, true, true);
         const uint32_t w0 = tc::smem_u32(buf + B_WQ), v0 = tc::smem_u32(sm + S_DV);
@@ -247,6 +251,10 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
         d2_pending = true;
         d2_open = false;
         d2_par = (uint32_t)(i & 1);
+        if (a.dv_img) {  // the -dv_new tile goes out as its image
+          bulk_store(a.dv_img + (size_t)((c0 + c) * H + h) * 16384, sm + S_DV, 16384);
+          bulk_commit();
+        }
       } else {
         *abort_flag = 1;
         if (d2_open) {  // cover the qg^T dO MMAs already issued, for the drain
@@ -276,7 +284,7 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
 #pragma unroll
         for (int x = 0; x < 16; ++x) dh[16 * cc + x] = fmaf(gcv, dh[16 * cc + x], d[x]);
       }
-      store_hb(c - 1);
+      store_hb();
     }
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();
@@ -296,6 +304,7 @@ tc_bwd_dh_kernel(const __grid_constant__ CUtensorMap map_do, BwdChainArgs a, Seq
     if (d2_pending) drain_wait(bar_d2, d2_par);
     for (int64_t x = done; x < issued; ++x) drain_wait(full + (x & 1), (uint32_t)((x >> 1) & 1));
   }
+  if (tid == 0) bulk_wait_all();  // the image copies are complete before the CTA ends
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
