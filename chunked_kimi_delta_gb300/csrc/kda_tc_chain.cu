@@ -18,7 +18,10 @@
 // first MMA of chunk c + 1 runs.  Packages are double-buffered in two halves
 // that are refilled as soon as their last reader is done: WQ and U of chunk
 // c + 2 once v_new of chunk c is computed, KG, AQK and GC of chunk c + 1 once
-// the MMAs of chunk c - 1 have finished.
+// the MMAs of chunk c - 1 have finished.  o of a full chunk is staged in
+// shared memory and written by TMA tensor stores; the backward's bf16 tile
+// images of h and v_new are the shared-memory tiles themselves, copied out
+// by one bulk copy each per chunk.
 //
 #include <cuda_bf16.h>
 #include <string.h>
