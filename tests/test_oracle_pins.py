@@ -188,6 +188,41 @@ def test_chunked_form_equals_recurrence(BT, lens):
     assert _rel(fin2, fin) < 1e-12
 
 
+@pytest.mark.parametrize("pattern", ["a_log U(1,3)", "cliff", "fast uniform"])
+def test_chunked_form_equals_recurrence_under_strong_decay(pattern):
+    """Strong gate decay, the regime "Hyper-Parallel Chunk KDA current
+    implementation design" section 8.2 singles out: the chunked form takes
+    every decay as e^{G_r - G_j} of a difference, the token loop multiplies
+    the per-token decays in turn; both stay exact in fp64 whatever the decay,
+    so they agree.  Patterns: gate from a_log ~ U(1, 3) (about -2 to -60 nats
+    per token); a precomputed gate of -0.01 per token with a -80-nat cliff
+    inside a 16-token block on half the channels; -2.2 nats per token
+    everywhere (about 141 nats per 64-token chunk)."""
+    H, K, V = 2, 16, 12
+    lens = (1, 63, 65, 200)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    S0 = 0.3 * RNG.standard_normal((len(lens), H, K, V))
+    if pattern == "a_log U(1,3)":
+        p = _prob(T, H, K, V, cu=cu, a_log=RNG.uniform(1, 3, H), dt_bias=0.1 * RNG.standard_normal((H, K)),
+                  gate_in_kernel=True, beta_sigmoid=True, g=RNG.standard_normal((T, H, K)),
+                  beta=RNG.standard_normal((T, H)))
+    else:
+        g = np.full((T, H, K), -0.01)
+        if pattern == "cliff":
+            g[(np.arange(T) % 16) == 5, :, 1::2] = -80.0
+        else:
+            g[:] = -2.2
+        p = _prob(T, H, K, V, cu=cu, g=g)
+    qh, kh, b, gl = oracle.preprocess(p)
+    assert gl.min() < -2.0  # the case decays strongly somewhere
+    out, fin = oracle.chunk_fwd(p, S0)
+    for BT in (16, 64):
+        out2, fin2 = chunked.chunk_fwd(qh, kh, p.v, b, gl, cu, p.scale, BT=BT, initial_state=S0)
+        assert _rel(out2, out) < 1e-11
+        assert _rel(fin2, fin) < 1e-11
+
+
 def test_golden_varlen_chunk_map():
     """Worked example of the TPU design, section 3.8: B=1, T=12, BT=4 with two
     sequences of lengths 8 and 4 -> chunk segment ids [1, 1, 2]."""
