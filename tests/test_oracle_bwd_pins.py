@@ -105,6 +105,20 @@ def test_backward_matches_finite_differences(flags):
     _check(x, cu, {**flags, "use_exp2": False}, do, dfin)
 
 
+def test_backward_matches_finite_differences_under_strong_decay():
+    """Strong gate decay (a_log ~ U(1, 3): about -2 to -60 nats per token,
+    "Hyper-Parallel Chunk KDA current implementation design" section 8.2):
+    the backward still equals the derivative of the forward."""
+    cu = [0, 3, 7]
+    T, H, K, V = 7, 2, 4, 3
+    flags = dict(gate_in_kernel=True, beta_sigmoid=True, l2norm=True)
+    x = _inputs(T, H, K, V, n_seqs_cu=cu, **flags)
+    x["a_log"] = RNG.uniform(1.0, 3.0, H)
+    do = RNG.standard_normal((T, H, V))
+    dfin = RNG.standard_normal((2, H, K, V))
+    _check(x, cu, {**flags, "use_exp2": False}, do, dfin)
+
+
 def test_backward_through_checkpoint_blocks():
     """A sequence longer than the oracle's 64-token checkpoint block."""
     cu = [0, 70]
